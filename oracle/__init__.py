@@ -1,0 +1,219 @@
+"""CPU oracle for MLA latent-KV decode -- TEST INFRASTRUCTURE ONLY.
+
+A plain, slow fp64 statement of what the decode step computes (``mla_oracle.c``), loaded
+through ctypes.  Only the tests, ``__graft_entry__.smoke()`` and the bench's CPU-baseline leg
+use it.  The CUDA library never imports, links or calls anything here, and the two share no
+code: the only common module is the seeded input generator, which holds no attention math.
+
+Parity status of each function (what pins it, see ``tests/test_oracle_pins.py``):
+  e4m3 decode         -- all 256 codes against torch's float8_e4m3fn, plus printed values.
+  decode_naive        -- closed forms (S = 1, uniform weights, constructed scores), softmax
+                         rows summing to 1, permutation/NaN-tail invariance.
+  absorb_q, latent_attention, out_proj
+                      -- the absorption identity against decode_naive (page 1 section 4),
+                         single-row closed forms.
+  lse_combine         -- split-partition invariance against an unsplit latent_attention and
+                         equal-weight closed form.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mla_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_build", "libmla_oracle.so")
+
+NUM_HEADS, D_HC, D_C, D_R, D_ROW, PAGE = 128, 128, 512, 64, 576, 64
+
+_lib = None
+
+
+def build(force: bool = False, src: Optional[str] = None, out: Optional[str] = None) -> str:
+    """Compile the oracle with gcc (OpenMP if the toolchain has it). Returns the .so path."""
+    src = src or _SRC
+    out = out or _LIB_PATH
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
+        return out
+    base = ["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-fno-fast-math", "-ffp-contract=off", src, "-o", out, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    return out
+
+
+def _load(path: str):
+    L = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    i32, i64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double
+    L.oracle_e4m3_value.restype = f64
+    L.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+    L.oracle_e4m3_decode.argtypes = [P, i64, P]
+    L.oracle_set_threads.argtypes = [i32]
+    L.oracle_max_threads.restype = i32
+    L.oracle_decode_naive.restype = i32
+    L.oracle_decode_naive.argtypes = [i32, P, P, i32, i32, i32, P, P, P, P, P, P, P, P, f64, i32, P, P, P]
+    L.oracle_absorb_q.argtypes = [i32, P, P, P]
+    L.oracle_latent_attention.restype = i32
+    L.oracle_latent_attention.argtypes = [i32, P, P, P, P, i32, P, P, i32, i32, P, P, P, P, f64, i32, P, P, P]
+    L.oracle_out_proj.argtypes = [i32, P, P, P]
+    L.oracle_lse_combine.argtypes = [i32, i32, P, P, P, P]
+    return L
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        _lib = _load(build())
+    return _lib
+
+
+def _use_library(path: Optional[str]) -> None:
+    """Swap in another build of the oracle (the mutation tests load broken copies)."""
+    global _lib
+    _lib = None if path is None else _load(path)
+
+
+def _p(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _u16(t) -> np.ndarray:
+    """bf16 torch tensor (or uint16 array) → contiguous uint16 bit patterns."""
+    if isinstance(t, np.ndarray):
+        assert t.dtype == np.uint16
+        return np.ascontiguousarray(t)
+    import torch
+    assert t.dtype == torch.bfloat16
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def _arr(t, dtype) -> np.ndarray:
+    if t is None:
+        return None
+    if not isinstance(t, np.ndarray):
+        t = t.contiguous().numpy()
+    return np.ascontiguousarray(t, dtype=dtype)
+
+
+class _Cache:
+    """The paged cache of a ``synth.DecodeInputs`` as C arrays."""
+
+    def __init__(self, inp):
+        self.kv_fp8 = 1 if inp.kv_dtype == "fp8_e4m3" else 0
+        self.num_pages = int(inp.num_pool_pages)
+        self.pool = _u16(inp.pool) if inp.pool is not None else None
+        self.c8 = _arr(inp.c8, np.uint8) if inp.c8 is not None else None
+        self.scale = _arr(inp.kv_scale, np.float32) if inp.kv_scale is not None else None
+        self.kr = _u16(inp.kr) if inp.kr is not None else None
+
+    def args(self):
+        return [self.kv_fp8, self.num_pages, _p(self.pool), _p(self.c8), _p(self.scale), _p(self.kr)]
+
+
+def set_threads(n: int) -> None:
+    lib().oracle_set_threads(int(n))
+
+
+def max_threads() -> int:
+    return int(lib().oracle_max_threads())
+
+
+def e4m3_decode(codes: np.ndarray) -> np.ndarray:
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.empty(codes.shape, dtype=np.float64)
+    lib().oracle_e4m3_decode(_p(codes), codes.size, _p(out))
+    return out
+
+
+def _heads(heads: Optional[Sequence[int]]) -> np.ndarray:
+    h = np.arange(NUM_HEADS, dtype=np.int32) if heads is None else np.asarray(heads, dtype=np.int32)
+    assert h.ndim == 1 and h.size > 0 and (h >= 0).all() and (h < NUM_HEADS).all()
+    return np.ascontiguousarray(h)
+
+
+def decode_naive(inp, *, softmax_scale: float, heads=None, want_probs: bool = False):
+    """Decompressed-path decode. Returns out [B, n_heads, 128] (and probs if asked)."""
+    hs = _heads(heads)
+    B = inp.batch
+    out = np.empty((B, hs.size, D_HC), dtype=np.float64)
+    probs = np.empty((B, hs.size, inp.max_pages * PAGE), dtype=np.float64) if want_probs else None
+    sl = _arr(inp.seq_lens, np.int32)
+    bt = _arr(inp.block_table, np.int32)
+    qc, qr, wk, wv = _u16(inp.q_c), _u16(inp.q_r), _u16(inp.w_uk), _u16(inp.w_uv)
+    rc = lib().oracle_decode_naive(B, _p(sl), _p(bt), inp.max_pages, *_Cache(inp).args(),
+                                   _p(qc), _p(qr), _p(wk), _p(wv), float(softmax_scale),
+                                   hs.size, _p(hs), _p(out), _p(probs))
+    if rc != 0:
+        raise ValueError("block table entry out of range")
+    return (out, probs) if want_probs else out
+
+
+def absorb_q(q_c, w_uk) -> np.ndarray:
+    """q_abs [B, 128, 512] in float64."""
+    qc, wk = _u16(q_c), _u16(w_uk)
+    B = qc.shape[0]
+    out = np.empty((B, NUM_HEADS, D_C), dtype=np.float64)
+    lib().oracle_absorb_q(B, _p(qc), _p(wk), _p(out))
+    return out
+
+
+def latent_attention(inp, q_lat: np.ndarray, *, softmax_scale: float, heads=None,
+                     page_begin=None, page_end=None):
+    """Latent-space attention over a page range of each sequence. Returns (o_lat, lse)."""
+    hs = _heads(heads)
+    B = inp.batch
+    q_lat = np.ascontiguousarray(q_lat, dtype=np.float64)
+    assert q_lat.shape == (B, NUM_HEADS, D_C)
+    pages = (inp.seq_lens.astype(np.int64) + PAGE - 1) // PAGE
+    pb = np.zeros(B, np.int32) if page_begin is None else np.asarray(page_begin, np.int32)
+    pe = pages.astype(np.int32) if page_end is None else np.asarray(page_end, np.int32)
+    o = np.empty((B, hs.size, D_C), dtype=np.float64)
+    lse = np.empty((B, hs.size), dtype=np.float64)
+    sl = _arr(inp.seq_lens, np.int32)
+    bt = _arr(inp.block_table, np.int32)
+    qr = _u16(inp.q_r)
+    rc = lib().oracle_latent_attention(B, _p(q_lat), _p(qr), _p(sl), _p(bt), inp.max_pages,
+                                       _p(np.ascontiguousarray(pb)), _p(np.ascontiguousarray(pe)),
+                                       *_Cache(inp).args(), float(softmax_scale), hs.size, _p(hs),
+                                       _p(o), _p(lse))
+    if rc != 0:
+        raise ValueError("block table entry out of range")
+    return o, lse
+
+
+def out_proj(o_lat: np.ndarray, w_uv) -> np.ndarray:
+    """out [B, 128, 128] from o_lat [B, 128, 512] (float64) and W_UV (bf16)."""
+    o_lat = np.ascontiguousarray(o_lat, dtype=np.float64)
+    B = o_lat.shape[0]
+    assert o_lat.shape == (B, NUM_HEADS, D_C)
+    wv = _u16(w_uv)
+    out = np.empty((B, NUM_HEADS, D_HC), dtype=np.float64)
+    lib().oracle_out_proj(B, _p(o_lat), _p(wv), _p(out))
+    return out
+
+
+def lse_combine(lse_parts: np.ndarray, o_parts: np.ndarray):
+    """Merge n partial results: lse_parts [n, rows], o_parts [n, rows, 512]."""
+    lse_parts = np.ascontiguousarray(lse_parts, dtype=np.float64)
+    o_parts = np.ascontiguousarray(o_parts, dtype=np.float64)
+    n, rows = lse_parts.shape
+    assert o_parts.shape == (n, rows, D_C)
+    lse = np.empty(rows, dtype=np.float64)
+    o = np.empty((rows, D_C), dtype=np.float64)
+    lib().oracle_lse_combine(rows, n, _p(lse_parts), _p(o_parts), _p(lse), _p(o))
+    return lse, o
+
+
+def decode_absorbed(inp, *, softmax_scale: float):
+    """Absorbed path end to end in fp64: (q_abs, o_lat, lse, out)."""
+    q_abs = absorb_q(inp.q_c, inp.w_uk)
+    o_lat, lse = latent_attention(inp, q_abs, softmax_scale=softmax_scale)
+    out = out_proj(o_lat, inp.w_uv)
+    return q_abs, o_lat, lse, out

@@ -1,0 +1,346 @@
+"""Pins for the CPU oracle: facts fixed by the pages or by mathematics, not by the oracle.
+
+Each ``check_*`` raises AssertionError when the oracle disagrees.  They are plain functions
+so that ``test_oracle_pins.py`` can run them against the real oracle and
+``test_oracle_mutants.py`` can run them against deliberately broken builds of it.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import torch
+
+import oracle
+from mla_latent_kv_absorb_gb300 import synth
+
+SCALE = 1.0 / math.sqrt(synth.D_HC + synth.D_R)
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _f64(t: torch.Tensor) -> np.ndarray:
+    return t.to(torch.float64).numpy()
+
+
+def _cache_rows_f64(inp, b: int) -> tuple:
+    """(c [S, 512], k_R [S, 64]) of sequence b in logical order, widened to float64."""
+    S = int(inp.seq_lens[b])
+    rows_c, rows_r = [], []
+    for t in range(S):
+        page, slot = int(inp.block_table[b, t // 64]), t % 64
+        if inp.kv_dtype == "bf16":
+            row = inp.pool[page, slot].to(torch.float64).numpy()
+            rows_c.append(row[:512])
+            rows_r.append(row[512:])
+        else:
+            codes = inp.c8[page, slot].numpy()
+            deq = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+            rows_c.append(deq * float(inp.kv_scale[page, slot]))
+            rows_r.append(inp.kr[page, slot].to(torch.float64).numpy())
+    return np.stack(rows_c), np.stack(rows_r)
+
+
+def _rel(a: np.ndarray, b: np.ndarray) -> float:
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+
+
+def tiny_inputs(seq_lens=(1, 65, 130), seed=7, kv_dtype="bf16", poison=True):
+    return synth.make_inputs(list(seq_lens), seed=seed, shuffle_pages=True, kv_dtype=kv_dtype,
+                             poison_tail=poison)
+
+
+# ----------------------------------------------------------------------------- element decoding
+
+def check_e4m3_all_codes():
+    """All 256 e4m3 codes decode to what torch's float8_e4m3fn (a library routine) gives."""
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_decode(codes)
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan_ours, nan_ref = np.isnan(ours), np.isnan(ref)
+    assert (nan_ours == nan_ref).all(), "NaN codes differ"
+    assert nan_ref.sum() == 2 and nan_ref[0x7F] and nan_ref[0xFF]
+    assert np.array_equal(ours[~nan_ours], ref[~nan_ref]), "e4m3 values differ"
+    # values fixed by the format itself
+    assert ours[0x7E] == 448.0 and ours[0xFE] == -448.0          # largest finite
+    assert ours[0x01] == 2.0 ** -9 and ours[0x08] == 2.0 ** -6    # smallest subnormal / normal
+    assert ours[0x38] == 1.0 and ours[0x00] == 0.0
+
+
+# ----------------------------------------------------------------------------- naive path closed forms
+
+def check_single_token_is_projected_value(kv_dtype="bf16"):
+    """S = 1: the only weight is 1, so out[b,h] = W_UV[h] c_0 exactly (up to fp64 rounding).
+    For the fp8 cache c_0 is the stored code decoded by torch (a library routine) times the
+    token's scale."""
+    inp = synth.make_inputs([1, 1], seed=3, shuffle_pages=True, poison_tail=True, kv_dtype=kv_dtype)
+    heads = [0, 5, 127]
+    out = oracle.decode_naive(inp, softmax_scale=SCALE, heads=heads)
+    wv = _f64(inp.w_uv)
+    for b in range(2):
+        c, _ = _cache_rows_f64(inp, b)
+        for i, h in enumerate(heads):
+            ref = wv[h] @ c[0]
+            assert np.allclose(out[b, i], ref, rtol=1e-12, atol=1e-13), f"S=1 closed form b={b} h={h}"
+
+
+def check_single_token_is_projected_value_fp8():
+    check_single_token_is_projected_value("fp8_e4m3")
+
+
+def check_zero_query_gives_mean_value(kv_dtype="bf16"):
+    """q_c = q_R = 0: every score is 0, weights are 1/S, out = W_UV[h] mean_t c_t."""
+    inp = synth.make_inputs([70, 3], seed=4, shuffle_pages=True, poison_tail=True, kv_dtype=kv_dtype)
+    inp.q_c = torch.zeros_like(inp.q_c)
+    inp.q_r = torch.zeros_like(inp.q_r)
+    heads = [1, 64]
+    out = oracle.decode_naive(inp, softmax_scale=SCALE, heads=heads)
+    wv = _f64(inp.w_uv)
+    for b in range(2):
+        c, _ = _cache_rows_f64(inp, b)
+        for i, h in enumerate(heads):
+            ref = wv[h] @ c.mean(axis=0)
+            assert np.allclose(out[b, i], ref, rtol=1e-11, atol=1e-13), f"uniform weights b={b} h={h}"
+
+
+def check_zero_query_gives_mean_value_fp8():
+    check_zero_query_gives_mean_value("fp8_e4m3")
+
+
+def _constructed(seq_len=5, seed=11):
+    """Inputs whose scores are known in closed form.
+
+    W_UK[h] is zero except W_UK[h, d0, c0] = w (d0 != c0 so a swapped d/c index reads a zero);
+    q_c[b,h] = alpha e_d0, q_R[b,h] = gamma e_r0, cache row t has c[c0] = beta_t, k_R[r0] = delta_t
+    and random values elsewhere in c (which only the value path sees).  Then
+    s_t = (alpha w beta_t + gamma delta_t) / sqrt(192) and v_t = W_UV[h] c_t.
+    """
+    g = torch.Generator().manual_seed(seed)
+    inp = synth.make_inputs([seq_len], seed=seed, shuffle_pages=False, poison_tail=True)
+    d0, c0, r0 = 3, 200, 17
+    w, alpha, gamma = 0.5, 2.0, -1.5
+    w_uk = torch.zeros(128, 128, 512)
+    w_uk[:, d0, c0] = w
+    inp.w_uk = w_uk.to(torch.bfloat16)
+    q_c = torch.zeros(1, 128, 128)
+    q_c[0, :, d0] = alpha
+    inp.q_c = q_c.to(torch.bfloat16)
+    q_r = torch.zeros(1, 128, 64)
+    q_r[0, :, r0] = gamma
+    inp.q_r = q_r.to(torch.bfloat16)
+    beta = torch.tensor([4.0, -2.0, 1.0, 3.5, 0.25, -3.0, 2.0, 0.5])[:seq_len]
+    delta = torch.tensor([1.0, 2.0, -4.0, 0.5, 3.0, 1.0, -1.0, 2.5])[:seq_len]
+    pool = inp.pool.clone()
+    for t in range(seq_len):
+        page = int(inp.block_table[0, t // 64])
+        row = torch.randn(576, generator=g)
+        row[512:] = 0.0
+        row[c0] = beta[t]
+        row[512 + r0] = delta[t]
+        pool[page, t % 64] = row.to(torch.bfloat16)
+    inp.pool = pool
+    s = (alpha * w * beta.double() + gamma * delta.double()) / math.sqrt(192.0)
+    return inp, s.numpy()
+
+
+def check_constructed_scores():
+    """Scores built to be known: pins the scale 1/sqrt(d_hc + d_R), the W_UK index order, the
+    sign and presence of the RoPE term and the softmax itself."""
+    inp, s = _constructed()
+    heads = [0, 77]
+    out, probs = oracle.decode_naive(inp, softmax_scale=SCALE, heads=heads, want_probs=True)
+    S = len(s)
+    e = np.exp(s - s.max())
+    p_ref = e / e.sum()
+    c, _ = _cache_rows_f64(inp, 0)
+    wv = _f64(inp.w_uv)
+    for i, h in enumerate(heads):
+        assert np.allclose(probs[0, i, :S], p_ref, rtol=1e-12, atol=1e-15), "attention weights"
+        assert np.all(probs[0, i, S:] == 0.0)
+        ref = wv[h] @ (p_ref @ c)
+        assert np.allclose(out[0, i], ref, rtol=1e-11, atol=1e-13), "weighted value"
+
+
+def check_softmax_rows_sum_to_one():
+    inp = tiny_inputs((1, 65, 130), seed=5)
+    _, probs = oracle.decode_naive(inp, softmax_scale=SCALE, heads=[0, 9, 100], want_probs=True)
+    for b, S in enumerate(inp.seq_lens):
+        row = probs[b, :, :S]
+        assert np.all(row >= 0.0)
+        assert np.allclose(row.sum(axis=-1), 1.0, rtol=0, atol=1e-12), "softmax row sum"
+        assert np.all(probs[b, :, S:] == 0.0), "weights past S_b"
+
+
+# ----------------------------------------------------------------------------- absorption identity
+
+def check_absorbed_equals_naive(kv_dtype="bf16"):
+    """Page 1 section 4: q_c . (W_UK c) = (W_UK^T q_c) . c, and likewise on the value side, so
+    the absorbed path (absorb -> latent attention -> W_UV) equals the naive path up to fp64
+    rounding."""
+    inp = tiny_inputs((1, 65, 130), seed=6, kv_dtype=kv_dtype)
+    heads = list(range(0, 128, 9))
+    naive = oracle.decode_naive(inp, softmax_scale=SCALE, heads=heads)
+    _, _, _, out = oracle.decode_absorbed(inp, softmax_scale=SCALE)
+    got = out[:, heads, :]
+    assert _rel(got, naive) < 1e-12, f"absorbed vs naive rel {_rel(got, naive):.3e}"
+    assert np.max(np.abs(got - naive)) < 1e-12
+
+
+def check_absorbed_equals_naive_fp8():
+    check_absorbed_equals_naive("fp8_e4m3")
+
+
+def check_absorb_q_rows():
+    """q_abs[b,h] = q_c[b,h] @ W_UK[h] as a matrix-vector product (library routine)."""
+    inp = tiny_inputs((3, 3), seed=8)
+    q_abs = oracle.absorb_q(inp.q_c, inp.w_uk)
+    qc, wk = _f64(inp.q_c), _f64(inp.w_uk)
+    for b in range(2):
+        for h in (0, 31, 127):
+            assert np.allclose(q_abs[b, h], qc[b, h] @ wk[h], rtol=1e-12, atol=1e-14)
+
+
+def check_out_proj_rows():
+    """out[b,h] = W_UV[h] @ o_lat[b,h] as a matrix-vector product (library routine)."""
+    inp = tiny_inputs((3, 3), seed=9)
+    o = np.random.default_rng(0).standard_normal((2, 128, 512))
+    out = oracle.out_proj(o, inp.w_uv)
+    wv = _f64(inp.w_uv)
+    for b in range(2):
+        for h in (0, 64, 127):
+            assert np.allclose(out[b, h], wv[h] @ o[b, h], rtol=1e-12, atol=1e-14)
+
+
+# ----------------------------------------------------------------------------- invariances
+
+def check_page_permutation_invariance():
+    """Moving pages to other physical slots (block table updated) changes nothing, bit for bit."""
+    a = synth.make_inputs([100, 200], seed=12, shuffle_pages=False, poison_tail=True)
+    b = synth.make_inputs([100, 200], seed=12, shuffle_pages=False, poison_tail=True)
+    perm = np.random.default_rng(1).permutation(a.num_pool_pages)
+    pool = torch.empty_like(a.pool)
+    pool[torch.from_numpy(perm)] = a.pool
+    b.pool = pool
+    b.block_table = np.where(a.block_table >= 0, perm[np.maximum(a.block_table, 0)], -1).astype(np.int32)
+    heads = [2, 50]
+    na, nb = (oracle.decode_naive(x, softmax_scale=SCALE, heads=heads) for x in (a, b))
+    assert np.array_equal(na, nb), "naive path depends on physical placement"
+    qa = oracle.absorb_q(a.q_c, a.w_uk)
+    oa, la = oracle.latent_attention(a, qa, softmax_scale=SCALE)
+    ob, lb = oracle.latent_attention(b, qa, softmax_scale=SCALE)
+    assert np.array_equal(oa, ob) and np.array_equal(la, lb), "latent path depends on physical placement"
+
+
+def check_nan_tail_ignored():
+    """Slots past S_b (NaN-poisoned) have no effect: same output as with finite tails."""
+    clean = synth.make_inputs([70, 129], seed=13, shuffle_pages=True, poison_tail=False)
+    dirty = synth.make_inputs([70, 129], seed=13, shuffle_pages=True, poison_tail=True)
+    assert torch.isnan(dirty.pool).any()
+    nc = oracle.decode_naive(clean, softmax_scale=SCALE, heads=[0, 127])
+    nd = oracle.decode_naive(dirty, softmax_scale=SCALE, heads=[0, 127])
+    assert np.isfinite(nd).all() and np.array_equal(nc, nd)
+
+
+def check_split_combine_invariance(kv_dtype="bf16"):
+    """Any partition of a sequence's pages, merged by log-sum-exp, equals the unsplit result."""
+    inp = synth.make_inputs([64 * 7 + 5, 64 * 3], seed=14, kv_dtype=kv_dtype, poison_tail=True)
+    q = oracle.absorb_q(inp.q_c, inp.w_uk)
+    full_o, full_l = oracle.latent_attention(inp, q, softmax_scale=SCALE)
+    pages = (inp.seq_lens + 63) // 64
+    rng = np.random.default_rng(2)
+    for trial in range(3):
+        cuts = [sorted(set([0, int(p)] + list(rng.integers(1, max(int(p), 2), size=3)))) for p in pages]
+        n = max(len(c) - 1 for c in cuts)
+        lse_parts = np.full((n, inp.batch * 128), -np.inf)
+        o_parts = np.zeros((n, inp.batch * 128, 512))
+        for j in range(n):
+            pb = [c[j] if j < len(c) - 1 else c[-1] for c in cuts]
+            pe = [c[j + 1] if j < len(c) - 1 else c[-1] for c in cuts]
+            o, l = oracle.latent_attention(inp, q, softmax_scale=SCALE, page_begin=pb, page_end=pe)
+            lse_parts[j] = l.reshape(-1)
+            o_parts[j] = o.reshape(-1, 512)
+        lse, o = oracle.lse_combine(lse_parts, o_parts)
+        assert np.allclose(lse, full_l.reshape(-1), rtol=0, atol=1e-12), "split lse"
+        assert _rel(o, full_o.reshape(-1, 512)) < 1e-12, "split o_lat"
+
+
+def check_lse_combine_closed_forms():
+    rng = np.random.default_rng(3)
+    o = rng.standard_normal((4, 512))
+    lse = np.array([0.3, -2.0, 5.0, 1.0])
+    # two equal parts: lse + ln 2, output unchanged
+    l2, o2 = oracle.lse_combine(np.stack([lse, lse]), np.stack([o, o]))
+    assert np.allclose(l2, lse + math.log(2.0), atol=1e-15) and np.allclose(o2, o, atol=1e-15)
+    # an empty part (lse = -inf) carries no weight
+    l3, o3 = oracle.lse_combine(np.stack([lse, np.full(4, -np.inf)]), np.stack([o, 7 * o]))
+    assert np.allclose(l3, lse, atol=0) and np.allclose(o3, o, atol=1e-15)
+    # weights exp(lse_j - lse) for two different parts
+    la, lb = np.zeros(4), np.full(4, math.log(3.0))
+    l4, o4 = oracle.lse_combine(np.stack([la, lb]), np.stack([o, -o]))
+    assert np.allclose(l4, math.log(4.0), atol=1e-15)
+    assert np.allclose(o4, 0.25 * o - 0.75 * o, atol=1e-15)
+
+
+def check_latent_attention_rows():
+    """Latent attention of one row equals softmax(q . C^T * scale) @ C written with numpy."""
+    inp = tiny_inputs((130,), seed=15)
+    q = oracle.absorb_q(inp.q_c, inp.w_uk)
+    o, l = oracle.latent_attention(inp, q, softmax_scale=SCALE, heads=[0, 99])
+    c, r = _cache_rows_f64(inp, 0)
+    qr = _f64(inp.q_r)
+    for i, h in enumerate((0, 99)):
+        s = (c @ q[0, h] + r @ qr[0, h]) * SCALE
+        m = s.max()
+        ref_l = m + math.log(np.exp(s - m).sum())
+        assert abs(l[0, i] - ref_l) < 1e-12
+        assert _rel(o[0, i], np.exp(s - ref_l) @ c) < 1e-12
+
+
+# ----------------------------------------------------------------------------- printed figures
+
+def check_cache_geometry_golden():
+    """Cache figures printed on the pages, recomputed from the oracle's dimensions."""
+    g = json.load(open(os.path.join(GOLDEN, "cache_geometry.json")))
+    row = oracle.D_C + oracle.D_R
+    assert row == g["row_elements"]["value"]
+    row_bytes = row * 2
+    assert row_bytes / 1024 == g["row_bytes_bf16_kib"]["value"]
+    mha = oracle.NUM_HEADS * oracle.D_HC * 2 * 2
+    assert mha / 1024 == g["mha_row_bytes_kib"]["value"]
+    assert round(100 * (1 - row_bytes / mha), 2) == g["compression_percent"]["value"]
+    assert oracle.PAGE == g["page_tokens"]["value"]
+    page_bytes = oracle.PAGE * row_bytes
+    assert page_bytes == 73728 and round(page_bytes / 1024) == g["page_bytes_kib_approx"]["value"]
+    assert 16 * row_bytes / 1024 == g["page16_bytes_kib"]["value"]
+    m = g["mha_cache_tib_64k_b16"]
+    assert round(m["context_tokens"] * m["batch"] * m["layers"] * mha / 2 ** 40, 2) == m["value"]
+    k = g["h100_kernel_smem_bytes"]
+    smem = (k["tile_s"] * oracle.D_C + k["tile_s"] * oracle.D_R) * 2 * k["stages"]
+    assert smem == k["value"] and round(smem / 1024) == k["approx_kib"]
+    r = g["ridge_flop_per_byte_h100"]
+    assert round(r["tflops"] / r["tbps"]) == r["value"]
+    k3 = g["mla_kib_per_token_24_layers"]
+    assert round(k3["layers"] * row_bytes / 1024, 1) == k3["value"]
+    assert abs(g["softmax_scale"]["value"] - 1 / math.sqrt(oracle.D_HC + oracle.D_R)) < 1e-16
+
+
+ALL_CHECKS = [
+    check_e4m3_all_codes,
+    check_single_token_is_projected_value,
+    check_single_token_is_projected_value_fp8,
+    check_zero_query_gives_mean_value,
+    check_zero_query_gives_mean_value_fp8,
+    check_constructed_scores,
+    check_softmax_rows_sum_to_one,
+    check_absorbed_equals_naive,
+    check_absorbed_equals_naive_fp8,
+    check_absorb_q_rows,
+    check_out_proj_rows,
+    check_page_permutation_invariance,
+    check_nan_tail_ignored,
+    check_split_combine_invariance,
+    check_lse_combine_closed_forms,
+    check_latent_attention_rows,
+    check_cache_geometry_golden,
+]

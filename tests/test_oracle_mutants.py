@@ -1,0 +1,76 @@
+"""Plant plausible mistakes in copies of the oracle source and check that some pin fails.
+
+Each mutant is one textual change to ``oracle/mla_oracle.c`` (a dropped term, a flipped
+sign, a transposed or wrong operand, an off-by-one).  The copy is compiled into a temporary
+directory on the CPU and the pins of ``oracle_pins.py`` run against it; at least one must
+raise.  The real oracle source is never modified.
+"""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+import oracle  # noqa: E402
+import oracle_pins as pins  # noqa: E402
+
+MUTANTS = {
+    "naive_rope_term_dropped": (
+        "for (int r = 0; r < DR; ++r) dot += qr[r] * kvr[r];\n            s[t] = dot * softmax_scale;",
+        "s[t] = dot * softmax_scale;"),
+    "naive_w_uk_transposed": ("a += Wk[d * DC + c] * ckv[c];", "a += Wk[c * DHC + d] * ckv[c];"),
+    "naive_value_through_w_uk": ("a += Wv[d * DC + c] * ckv[c];", "a += Wk[d * DC + c] * ckv[c];"),
+    "naive_softmax_sign": ("double p = exp(s[t] - mx) / den;", "double p = exp(mx - s[t]) / den;"),
+    "naive_denominator_short": ("for (int64_t t = 0; t < S; ++t) den += exp(s[t] - mx);",
+                                "for (int64_t t = 0; t + 1 < S; ++t) den += exp(s[t] - mx);"),
+    "naive_scale_dropped": ("s[t] = dot * softmax_scale;", "s[t] = dot;"),
+    "gather_slot_shifted": ("slot = t % PG;", "slot = (t + 1) % PG;"),
+    "gather_ignores_block_table": ("int64_t page = bt_row[t / PG]", "int64_t page = t / PG"),
+    "e4m3_bias_off_by_one": ("mag = ldexp(1.0 + (double)m / 8.0, e - 7);", "mag = ldexp(1.0 + (double)m / 8.0, e - 8);"),
+    "fp8_scale_ignored": ("ckv[i] = oracle_e4m3_value(row[i]) * sigma;", "ckv[i] = oracle_e4m3_value(row[i]);"),
+    "latent_rope_term_dropped": (
+        "for (int r = 0; r < DR; ++r) dot += qr[r] * kvr[r];\n            s[i] = dot * softmax_scale;",
+        "s[i] = dot * softmax_scale;"),
+    "latent_lse_base2": ("const double l = n > 0 ? mx + log(den) : -INFINITY;",
+                         "const double l = n > 0 ? mx + log2(den) : -INFINITY;"),
+    "latent_last_token_dropped": ("if (t1 > seq_lens[b]) t1 = seq_lens[b];",
+                                  "if (t1 > seq_lens[b] - 1) t1 = seq_lens[b] - 1;"),
+    "absorb_w_uk_transposed": ("bf16_value(w_uk[((int64_t)h * DHC + d) * DC + c])",
+                               "bf16_value(w_uk[((int64_t)h * DC + c) * DHC + d])"),
+    "out_proj_wrong_head": ("bf16_value(w_uv[((int64_t)h * DHC + d) * DC + c])",
+                            "bf16_value(w_uv[((int64_t)(h ^ 1) * DHC + d) * DC + c])"),
+    "combine_unnormalised_weight": ("const double w = exp(lj - L);", "const double w = exp(lj - mx);"),
+    "bf16_widening_wrong": ("uint32_t u = (uint32_t)bits << 16;", "uint32_t u = ((uint32_t)bits << 16) | 0x8000u;"),
+}
+
+
+@pytest.fixture(scope="module")
+def mutant_dir(tmp_path_factory):
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    return tmp_path_factory.mktemp("oracle_mutants")
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, mutant_dir):
+    src = open(oracle._SRC).read()
+    old, new = MUTANTS[name]
+    assert src.count(old) == 1, f"mutation site for {name} not unique or missing"
+    path_c = os.path.join(mutant_dir, f"{name}.c")
+    with open(path_c, "w") as f:
+        f.write(src.replace(old, new))
+    so = oracle.build(force=True, src=path_c, out=os.path.join(mutant_dir, f"{name}.so"))
+    oracle._use_library(so)
+    try:
+        caught = None
+        for check in pins.ALL_CHECKS:
+            try:
+                check()
+            except (AssertionError, ValueError) as e:  # noqa: PERF203
+                caught = (check.__name__, e)
+                break
+        assert caught is not None, f"no pin caught mutant {name}"
+    finally:
+        oracle._use_library(None)
