@@ -1,0 +1,183 @@
+/*
+ * mla.h -- C ABI of libmla_gb300.so: Multi-Head Latent Attention decode over a paged latent
+ * KV cache with matrix absorption, for NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow "撕開 DeepSeek MLA 源碼：C++ 與 TensorRT-LLM 算子設計優化全景"
+ * (jh158.com/news/60867, "P1" below) and the split-KV decode of the Kimi K3 decode
+ * time-share page (jinnpan.com/sources/kimi-k3-kda-time-share.html, "P3" below).
+ *
+ * Fixed geometry (P1 section 1 and the mla_config.h block of section 3): 128 heads, content
+ * head dim d_hc = 128, latent dim d_c = 512, decoupled RoPE dim d_R = 64, so one cache row is
+ * 576 elements; pages hold 64 tokens (P1 section 3, page_size 64).
+ *
+ * Conventions shared by every entry point
+ *   - Pointers marked "device" are CUDA device pointers; "host" pointers are ordinary memory.
+ *   - bf16 tensors are passed as void* and are contiguous, row-major, in the shapes stated.
+ *   - The caller allocates and owns every buffer, workspaces included.  The library calls no
+ *     allocator and keeps no global mutable state; calls are safe from several host threads.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only enqueue work and
+ *     return; results are ready when the stream reaches them.
+ *   - Arguments, shapes, alignment and workspace sizes are checked on the host before any
+ *     launch; a failed check returns an error and enqueues nothing.  A failed launch returns
+ *     MLA_ERR_CUDA.  Problems only the GPU can see (a block-table entry outside the pool, a
+ *     wait that timed out) set bits in the caller's device word `dev_error`; the kernel then
+ *     ends early and never traps.  Read it with mla_read_device_error().
+ */
+#ifndef MLA_GB300_H
+#define MLA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MLA_API __attribute__((visibility("default")))
+#else
+#define MLA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MLA_NUM_HEADS 128
+#define MLA_HEAD_DIM 128   /* d_hc */
+#define MLA_LATENT_DIM 512 /* d_c  */
+#define MLA_ROPE_DIM 64    /* d_R  */
+#define MLA_ROW_DIM 576    /* d_c + d_R */
+#define MLA_PAGE_SIZE 64
+
+typedef enum mla_status {
+    MLA_OK = 0,
+    MLA_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, bad enum, inconsistent plan */
+    MLA_ERR_ALIGNMENT = 2,    /* a pointer is not 16-byte aligned (TMA and vector loads need it) */
+    MLA_ERR_UNSUPPORTED = 3,  /* a size the kernels do not handle (e.g. plan too large) */
+    MLA_ERR_WORKSPACE = 4,    /* a caller buffer is smaller than required */
+    MLA_ERR_CUDA = 5,         /* a CUDA runtime/driver call or a launch failed */
+    MLA_ERR_DEVICE_FAULT = 6  /* mla_read_device_error found a non-zero device error word */
+} mla_status;
+
+typedef enum mla_kv_dtype {
+    MLA_KV_BF16 = 0,     /* one bf16 pool [pages][64][576]: c_KV (512) then k_R (64) per row */
+    MLA_KV_FP8_E4M3 = 1  /* c_KV as e4m3 codes [pages][64][512], fp32 scale [pages][64], k_R bf16 [pages][64][64] */
+} mla_kv_dtype;
+
+/* Bits of the device error word. */
+#define MLA_DEVERR_BAD_PAGE 1u    /* a block-table entry outside [0, num_pool_pages): read as zeros */
+#define MLA_DEVERR_TIMEOUT 2u     /* a bounded wait ran out; the kernel stopped early */
+#define MLA_DEVERR_SMEM_ALIGN 4u  /* shared memory was not 1024-byte aligned; nothing computed */
+#define MLA_DEVERR_BAD_PLAN 8u    /* the device plan image failed its header check */
+
+MLA_API const char* mla_status_string(mla_status status);
+
+/* ---------------------------------------------------------------- a1: split planning (host only)
+ *
+ * P3 ("Inside the blocks") splits the decode KV scan over many workgroups and merges the
+ * pieces in a separate KV-split reduction.  Here each sequence's pages are cut into
+ * contiguous work items so that every CTA pair (two SMs) streams about the same number of
+ * pages; sequences cut into several items get a log-sum-exp merge (mla_combine_splits).
+ */
+typedef struct mla_plan_options {
+    int32_t min_pages_per_split; /* 0 = default 8: no item boundary closer than this to a sequence edge */
+    int32_t max_clusters;        /* 0 = num_sms / 2; otherwise at most this many CTA pairs */
+    int64_t wait_timeout_ns;     /* 0 = default 2e9: bound on every device-side wait */
+} mla_plan_options;
+
+typedef struct mla_plan_info {
+    int32_t batch;
+    int32_t num_clusters;    /* CTA pairs the decode launch uses (grid = 2 * num_clusters CTAs) */
+    int32_t num_items;       /* work items (sequence, page range) */
+    int32_t num_partials;    /* items that write a split partial into the workspace */
+    int32_t num_combine;     /* sequences with more than one item */
+    int32_t max_splits;      /* most items any one sequence has */
+    int32_t total_pages;     /* sum over sequences of ceil(S_b / 64) */
+    int32_t reserved;
+    int64_t plan_bytes;      /* bytes of the plan image written to plan_host */
+    int64_t workspace_bytes; /* bytes mla_decode_paged needs in `workspace` */
+    int64_t wait_timeout_ns;
+} mla_plan_info;
+
+/* Upper bound on the plan image size for `batch` sequences on `num_sms` SMs. */
+MLA_API size_t mla_plan_bytes_max(int32_t batch, int32_t num_sms);
+
+/* Builds the plan image in host memory.
+ *   seq_lens   host int32 [batch], each >= 1 (the context length S_b of sequence b)
+ *   num_sms    SMs of the device the decode runs on (>= 2)
+ *   opts       may be NULL (defaults)
+ *   plan_host  host buffer of plan_capacity bytes (>= mla_plan_bytes_max); the caller copies
+ *              info->plan_bytes of it to device memory (16-byte aligned) for the calls below.
+ * Pure host code: needs no GPU. */
+MLA_API mla_status mla_plan_splits(const int32_t* seq_lens, int32_t batch, int32_t num_sms,
+                           const mla_plan_options* opts, void* plan_host, size_t plan_capacity,
+                           mla_plan_info* info);
+
+/* ---------------------------------------------------------------- a2: absorb W_UK into the query
+ *
+ * P1 section 4, path B: q_abs[b,h,c] = sum_d q_c[b,h,d] * W_UK[h,d,c].
+ *   q_c   device bf16 [batch][128][128]
+ *   w_uk  device bf16 [128][128][512]   (heads, d_hc, d_c)
+ *   q_abs device bf16 [batch][128][512] (fp32 accumulation, rounded once to bf16)
+ * All three 16-byte aligned.  Tensor cores (tcgen05), one 128-row batch tile per CTA. */
+MLA_API mla_status mla_absorb_q(const void* q_c, const void* w_uk, void* q_abs, int32_t batch, void* stream);
+
+/* ---------------------------------------------------------------- a3-a8: paged decode
+ *
+ * For every work item of the plan: gather its pages through the block table, score all 128
+ * heads against each cached row, s = (q_abs . c_KV + q_R . k_R) * softmax_scale (P1 section 4),
+ * run an online softmax and accumulate P . c_KV in the 512-d latent space.
+ *   plan_dev        device copy of the plan image (16-byte aligned); info = its host header
+ *   q_abs           device bf16 [batch][128][512]   (from mla_absorb_q)
+ *   q_r             device bf16 [batch][128][64]    (already rotated)
+ *   kv_dtype        MLA_KV_BF16: kv_pool = bf16 [num_pool_pages][64][576]; kv_scale, kr_pool NULL
+ *                   MLA_KV_FP8_E4M3: kv_pool = e4m3 codes [num_pool_pages][64][512],
+ *                   kv_scale = fp32 [num_pool_pages][64] (the stored value times the scale is
+ *                   the latent), kr_pool = bf16 [num_pool_pages][64][64]
+ *   block_table     device int32 [batch][max_pages_per_seq]; entry p of row b is the physical
+ *                   page of tokens 64p..64p+63 of sequence b.  Only the first ceil(S_b/64)
+ *                   entries of a row are read.
+ *   softmax_scale   1/sqrt(d_hc + d_R) for the pages' model
+ *   workspace       device buffer of info->workspace_bytes (split partials), 16-byte aligned;
+ *                   may be NULL when info->workspace_bytes == 0
+ *   o_lat           device bf16 [batch][128][512]: normalised latent output of sequences that
+ *                   have a single item (the others are written by mla_combine_splits)
+ *   lse             device fp32 [batch][128]: natural-log sum of exp(scores), same rule
+ *   dev_error       device uint32 error word (MLA_DEVERR_* bits are OR-ed in), 4-byte aligned
+ * Slots past S_b in a sequence's last page may hold anything (NaN included): they are masked. */
+MLA_API mla_status mla_decode_paged(const mla_plan_info* info, const void* plan_dev,
+                            const void* q_abs, const void* q_r,
+                            mla_kv_dtype kv_dtype, const void* kv_pool, const float* kv_scale,
+                            const void* kr_pool, int32_t num_pool_pages,
+                            const int32_t* block_table, int32_t max_pages_per_seq,
+                            float softmax_scale, void* workspace, size_t workspace_bytes,
+                            void* o_lat, float* lse, uint32_t* dev_error, void* stream);
+
+/* ---------------------------------------------------------------- a9: merge split partials
+ *
+ * P3's KV-split reduction: for each sequence with several items,
+ *   lse = log sum_j exp(lse_j),  o_lat = sum_j exp(lse_j - lse) o_j,
+ * reading the partials mla_decode_paged left in `workspace`.  Writes o_lat (bf16) and lse
+ * (fp32) for those sequences only.  A plan with num_combine == 0 enqueues nothing. */
+MLA_API mla_status mla_combine_splits(const mla_plan_info* info, const void* plan_dev, const void* workspace,
+                              size_t workspace_bytes, void* o_lat, float* lse, void* stream);
+
+/* ---------------------------------------------------------------- a10: W_UV projection
+ *
+ * out[b,h,d] = sum_c o_lat[b,h,c] * W_UV[h,d,c]   (W_UV laid out like W_UK: heads, d_hc, d_c)
+ *   o_lat device bf16 [batch][128][512], w_uv device bf16 [128][128][512],
+ *   out   device bf16 [batch][128][128].  Tensor cores (tcgen05), fp32 accumulation. */
+MLA_API mla_status mla_out_proj(const void* o_lat, const void* w_uv, void* out, int32_t batch, void* stream);
+
+/* ---------------------------------------------------------------- device error word
+ *
+ * Waits for `stream`, copies the device word to *host_bits (may be NULL) and returns
+ * MLA_ERR_DEVICE_FAULT if any bit is set, MLA_OK otherwise.  Does not clear the word. */
+MLA_API mla_status mla_read_device_error(const uint32_t* dev_error, uint32_t* host_bits, void* stream);
+
+/* Test hook for the bounded waits: launches one CTA that waits on a barrier nothing will
+ * ever complete, giving up after timeout_ns (1 ms .. 10 s).  The kernel must set
+ * MLA_DEVERR_TIMEOUT in *dev_error and return; the context stays usable. */
+MLA_API mla_status mla_debug_wait_timeout(uint32_t* dev_error, int64_t timeout_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MLA_GB300_H */

@@ -1,0 +1,278 @@
+"""ctypes binding of libmla_gb300.so: the C ABI of include/mla.h under the same names.
+
+Argument marshalling only: torch tensors supply device memory and streams, every step of the
+decode runs in the library's CUDA kernels.  If the library has not been built this module
+raises; there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import D_C, D_HC, D_R, D_ROW, NUM_HEADS, PAGE
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmla_gb300.so")
+
+# mla_status
+MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_ALIGNMENT, MLA_ERR_UNSUPPORTED = 0, 1, 2, 3
+MLA_ERR_WORKSPACE, MLA_ERR_CUDA, MLA_ERR_DEVICE_FAULT = 4, 5, 6
+# mla_kv_dtype
+MLA_KV_BF16, MLA_KV_FP8_E4M3 = 0, 1
+# device error bits
+MLA_DEVERR_BAD_PAGE, MLA_DEVERR_TIMEOUT, MLA_DEVERR_SMEM_ALIGN, MLA_DEVERR_BAD_PLAN = 1, 2, 4, 8
+
+SOFTMAX_SCALE = 1.0 / math.sqrt(D_HC + D_R)
+
+
+class MlaError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn} failed: {msg} (status {status})")
+        self.status = status
+
+
+class PlanOptions(ctypes.Structure):
+    _fields_ = [("min_pages_per_split", ctypes.c_int32), ("max_clusters", ctypes.c_int32),
+                ("wait_timeout_ns", ctypes.c_int64)]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("num_clusters", ctypes.c_int32), ("num_items", ctypes.c_int32),
+                ("num_partials", ctypes.c_int32), ("num_combine", ctypes.c_int32), ("max_splits", ctypes.c_int32),
+                ("total_pages", ctypes.c_int32), ("reserved", ctypes.c_int32), ("plan_bytes", ctypes.c_int64),
+                ("workspace_bytes", ctypes.c_int64), ("wait_timeout_ns", ctypes.c_int64)]
+
+
+EXPORTS = ("mla_status_string", "mla_plan_bytes_max", "mla_plan_splits", "mla_absorb_q", "mla_decode_paged",
+           "mla_combine_splits", "mla_out_proj", "mla_read_device_error", "mla_debug_wait_timeout")
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Open libmla_gb300.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() or "
+                           "python -m mla_latent_kv_absorb_gb300.build")
+    L = ctypes.CDLL(LIB_PATH)
+    P, i32, i64, sz, u32p = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p
+    L.mla_status_string.restype = ctypes.c_char_p
+    L.mla_status_string.argtypes = [ctypes.c_int]
+    L.mla_plan_bytes_max.restype = sz
+    L.mla_plan_bytes_max.argtypes = [i32, i32]
+    L.mla_plan_splits.restype = ctypes.c_int
+    L.mla_plan_splits.argtypes = [P, i32, i32, ctypes.POINTER(PlanOptions), P, sz, ctypes.POINTER(PlanInfo)]
+    L.mla_absorb_q.restype = ctypes.c_int
+    L.mla_absorb_q.argtypes = [P, P, P, i32, P]
+    L.mla_decode_paged.restype = ctypes.c_int
+    L.mla_decode_paged.argtypes = [ctypes.POINTER(PlanInfo), P, P, P, ctypes.c_int, P, P, P, i32, P, i32,
+                                   ctypes.c_float, P, sz, P, P, u32p, P]
+    L.mla_combine_splits.restype = ctypes.c_int
+    L.mla_combine_splits.argtypes = [ctypes.POINTER(PlanInfo), P, P, sz, P, P, P]
+    L.mla_out_proj.restype = ctypes.c_int
+    L.mla_out_proj.argtypes = [P, P, P, i32, P]
+    L.mla_read_device_error.restype = ctypes.c_int
+    L.mla_read_device_error.argtypes = [u32p, ctypes.POINTER(ctypes.c_uint32), P]
+    L.mla_debug_wait_timeout.restype = ctypes.c_int
+    L.mla_debug_wait_timeout.argtypes = [u32p, i64, P]
+    _lib = L
+    return L
+
+
+def status_string(status: int) -> str:
+    return lib().mla_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int) -> None:
+    if status != MLA_OK:
+        raise MlaError(fn, status, status_string(status))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _need(t: torch.Tensor, name: str, dtype, shape=None, device=True):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if device and not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+# --------------------------------------------------------------------------- C ABI, same names
+
+def mla_plan_splits(seq_lens, num_sms: int, *, min_pages_per_split: int = 0, max_clusters: int = 0,
+                    wait_timeout_ns: int = 0):
+    """Host planning. Returns (plan image as an int32 numpy array, PlanInfo)."""
+    lens = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+    B = int(lens.size)
+    cap = int(lib().mla_plan_bytes_max(B, int(num_sms)))
+    if cap == 0:
+        raise MlaError("mla_plan_splits", MLA_ERR_INVALID_ARG, "bad batch or SM count")
+    buf = np.zeros(cap // 4, dtype=np.int32)
+    opts = PlanOptions(int(min_pages_per_split), int(max_clusters), int(wait_timeout_ns))
+    info = PlanInfo()
+    st = lib().mla_plan_splits(lens.ctypes.data_as(ctypes.c_void_p), B, int(num_sms), ctypes.byref(opts),
+                               buf.ctypes.data_as(ctypes.c_void_p), cap, ctypes.byref(info))
+    _check("mla_plan_splits", st)
+    return buf[: info.plan_bytes // 4].copy(), info
+
+
+def mla_absorb_q(q_c: torch.Tensor, w_uk: torch.Tensor, q_abs: torch.Tensor, stream=None) -> None:
+    B = q_c.shape[0]
+    _need(q_c, "q_c", torch.bfloat16, (B, NUM_HEADS, D_HC))
+    _need(w_uk, "w_uk", torch.bfloat16, (NUM_HEADS, D_HC, D_C))
+    _need(q_abs, "q_abs", torch.bfloat16, (B, NUM_HEADS, D_C))
+    _check("mla_absorb_q", lib().mla_absorb_q(_ptr(q_c), _ptr(w_uk), _ptr(q_abs), B, _stream(stream)))
+
+
+def mla_out_proj(o_lat: torch.Tensor, w_uv: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+    B = o_lat.shape[0]
+    _need(o_lat, "o_lat", torch.bfloat16, (B, NUM_HEADS, D_C))
+    _need(w_uv, "w_uv", torch.bfloat16, (NUM_HEADS, D_HC, D_C))
+    _need(out, "out", torch.bfloat16, (B, NUM_HEADS, D_HC))
+    _check("mla_out_proj", lib().mla_out_proj(_ptr(o_lat), _ptr(w_uv), _ptr(out), B, _stream(stream)))
+
+
+def mla_decode_paged(info: PlanInfo, plan_dev: torch.Tensor, q_abs: torch.Tensor, q_r: torch.Tensor, *,
+                     kv_pool: torch.Tensor, block_table: torch.Tensor, o_lat: torch.Tensor, lse: torch.Tensor,
+                     dev_error: torch.Tensor, workspace: Optional[torch.Tensor] = None,
+                     kv_scale: Optional[torch.Tensor] = None, kr_pool: Optional[torch.Tensor] = None,
+                     softmax_scale: float = SOFTMAX_SCALE, stream=None) -> None:
+    B = q_abs.shape[0]
+    _need(plan_dev, "plan_dev", torch.int32)
+    _need(q_abs, "q_abs", torch.bfloat16, (B, NUM_HEADS, D_C))
+    _need(q_r, "q_r", torch.bfloat16, (B, NUM_HEADS, D_R))
+    _need(block_table, "block_table", torch.int32)
+    _need(o_lat, "o_lat", torch.bfloat16, (B, NUM_HEADS, D_C))
+    _need(lse, "lse", torch.float32, (B, NUM_HEADS))
+    _need(dev_error, "dev_error", torch.int32, (1,))
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be [batch, max_pages]")
+    if kv_scale is None:
+        _need(kv_pool, "kv_pool", torch.bfloat16)
+        if kv_pool.dim() != 3 or tuple(kv_pool.shape[1:]) != (PAGE, D_ROW):
+            raise ValueError("bf16 kv_pool must be [pages, 64, 576]")
+        dtype = MLA_KV_BF16
+    else:
+        _need(kv_pool, "kv_pool (e4m3 codes)", torch.uint8)
+        if kv_pool.dim() != 3 or tuple(kv_pool.shape[1:]) != (PAGE, D_C):
+            raise ValueError("fp8 kv_pool must be [pages, 64, 512]")
+        _need(kv_scale, "kv_scale", torch.float32, (kv_pool.shape[0], PAGE))
+        _need(kr_pool, "kr_pool", torch.bfloat16, (kv_pool.shape[0], PAGE, D_R))
+        dtype = MLA_KV_FP8_E4M3
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().mla_decode_paged(ctypes.byref(info), _ptr(plan_dev), _ptr(q_abs), _ptr(q_r), dtype, _ptr(kv_pool),
+                                _ptr(kv_scale), _ptr(kr_pool), int(kv_pool.shape[0]), _ptr(block_table),
+                                int(block_table.shape[1]), float(softmax_scale), _ptr(workspace), ws_bytes,
+                                _ptr(o_lat), _ptr(lse), _ptr(dev_error), _stream(stream))
+    _check("mla_decode_paged", st)
+
+
+def mla_combine_splits(info: PlanInfo, plan_dev: torch.Tensor, workspace: Optional[torch.Tensor],
+                       o_lat: torch.Tensor, lse: torch.Tensor, stream=None) -> None:
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().mla_combine_splits(ctypes.byref(info), _ptr(plan_dev), _ptr(workspace), ws_bytes, _ptr(o_lat),
+                                  _ptr(lse), _stream(stream))
+    _check("mla_combine_splits", st)
+
+
+def mla_read_device_error(dev_error: torch.Tensor, stream=None) -> int:
+    """Device error bits (0 = none); waits for the stream."""
+    bits = ctypes.c_uint32(0)
+    st = lib().mla_read_device_error(_ptr(dev_error), ctypes.byref(bits), _stream(stream))
+    if st not in (MLA_OK, MLA_ERR_DEVICE_FAULT):
+        _check("mla_read_device_error", st)
+    return int(bits.value)
+
+
+def mla_debug_wait_timeout(dev_error: torch.Tensor, timeout_ns: int, stream=None) -> None:
+    _check("mla_debug_wait_timeout", lib().mla_debug_wait_timeout(_ptr(dev_error), int(timeout_ns), _stream(stream)))
+
+
+# --------------------------------------------------------------------------- one decode step
+
+def num_sms(device=None) -> int:
+    return torch.cuda.get_device_properties(device if device is not None else torch.cuda.current_device()).multi_processor_count
+
+
+class DecodeStep:
+    """Device buffers and plan for one batch shape; ``run`` enqueues the four kernels.
+
+    absorb (q_c -> q_abs) -> paged decode (-> o_lat, lse, split partials) -> split merge ->
+    W_UV projection (-> out).  All buffers are allocated here, by torch, once.
+    """
+
+    def __init__(self, seq_lens, *, w_uk: torch.Tensor, w_uv: torch.Tensor, kv_pool: torch.Tensor,
+                 block_table: torch.Tensor, kv_scale: Optional[torch.Tensor] = None,
+                 kr_pool: Optional[torch.Tensor] = None, device=None, min_pages_per_split: int = 0,
+                 max_clusters: int = 0, wait_timeout_ns: int = 0, softmax_scale: float = SOFTMAX_SCALE):
+        self.device = torch.device(device if device is not None else "cuda")
+        self.seq_lens = np.asarray(seq_lens, dtype=np.int32)
+        self.batch = int(self.seq_lens.size)
+        self.plan_host, self.info = mla_plan_splits(self.seq_lens, num_sms(self.device),
+                                                    min_pages_per_split=min_pages_per_split,
+                                                    max_clusters=max_clusters, wait_timeout_ns=wait_timeout_ns)
+        self.plan_dev = torch.from_numpy(self.plan_host).to(self.device)
+        self.w_uk, self.w_uv = w_uk, w_uv
+        self.kv_pool, self.kv_scale, self.kr_pool = kv_pool, kv_scale, kr_pool
+        self.block_table = block_table
+        self.softmax_scale = softmax_scale
+        B = self.batch
+        ws = int(self.info.workspace_bytes)
+        self.workspace = torch.empty(max(ws // 4, 4), dtype=torch.float32, device=self.device) if ws else None
+        self.q_abs = torch.empty(B, NUM_HEADS, D_C, dtype=torch.bfloat16, device=self.device)
+        self.o_lat = torch.empty(B, NUM_HEADS, D_C, dtype=torch.bfloat16, device=self.device)
+        self.lse = torch.empty(B, NUM_HEADS, dtype=torch.float32, device=self.device)
+        self.out = torch.empty(B, NUM_HEADS, D_HC, dtype=torch.bfloat16, device=self.device)
+        self.dev_error = torch.zeros(1, dtype=torch.int32, device=self.device)
+
+    def run(self, q_c: torch.Tensor, q_r: torch.Tensor, stream=None) -> torch.Tensor:
+        mla_absorb_q(q_c, self.w_uk, self.q_abs, stream)
+        mla_decode_paged(self.info, self.plan_dev, self.q_abs, q_r, kv_pool=self.kv_pool,
+                         block_table=self.block_table, o_lat=self.o_lat, lse=self.lse, dev_error=self.dev_error,
+                         workspace=self.workspace, kv_scale=self.kv_scale, kr_pool=self.kr_pool,
+                         softmax_scale=self.softmax_scale, stream=stream)
+        mla_combine_splits(self.info, self.plan_dev, self.workspace, self.o_lat, self.lse, stream)
+        mla_out_proj(self.o_lat, self.w_uv, self.out, stream)
+        return self.out
+
+    def device_error(self, stream=None) -> int:
+        return mla_read_device_error(self.dev_error, stream)
+
+    @property
+    def launches_per_step(self) -> int:
+        return 3 + (1 if self.info.num_combine > 0 else 0)
+
+
+def inputs_to_device(inp, device="cuda"):
+    """Move a synth.DecodeInputs to the device: (q_c, q_r, w_uk, w_uv, kv dict, block_table)."""
+    dev = torch.device(device)
+    kv = {}
+    if inp.kv_dtype == "bf16":
+        kv["kv_pool"] = inp.pool.to(dev)
+    else:
+        kv["kv_pool"] = inp.c8.to(dev)
+        kv["kv_scale"] = inp.kv_scale.to(dev)
+        kv["kr_pool"] = inp.kr.to(dev)
+    bt = torch.from_numpy(np.ascontiguousarray(inp.block_table)).to(dev)
+    return inp.q_c.to(dev), inp.q_r.to(dev), inp.w_uk.to(dev), inp.w_uv.to(dev), kv, bt

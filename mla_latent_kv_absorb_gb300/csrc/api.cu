@@ -1,0 +1,228 @@
+// api.cu -- the C ABI of libmla_gb300.so (declared in include/mla.h): host-side argument
+// checks, TMA tensor-map encoding and kernel launches.  No allocation, no global mutable state
+// (the driver entry point for tensor-map encoding is looked up once, thread-safely).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/mla.h"
+#include "combine.cuh"
+#include "decode.cuh"
+#include "head_gemm.cuh"
+#include "plan.h"
+
+namespace {
+
+using mla::gemm::Cfg;
+
+// absorb: K = 128 (d_hc), N tile 128 of 512 (d_c), W_UK is MN-major for the MMA
+constexpr int kAbsorbN = 128;
+using AbsorbCfg = Cfg<128, kAbsorbN, true, 2>;
+// out-proj: K = 512 (d_c), N tile 64 of 128 (d_hc), W_UV is K-major for the MMA
+constexpr int kOutN = 64;
+using OutCfg = Cfg<512, kOutN, false, 4>;
+
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = []() -> EncodeTiledFn {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// bf16 tensor map with 128-byte swizzle.  dims/strides innermost first; strides in bytes for
+// dims 1.. (rank - 1 entries).
+bool make_map_bf16(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                   const cuuint32_t* box)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+template <typename K>
+bool set_smem(K kernel, int bytes)
+{
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
+}
+
+mla_status launch_status()
+{
+    return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+// Shared by absorb and out-proj: activations [batch][128][K] (K-major rows of 128*K), weights
+// [128][128][512].
+template <int K_TOTAL, int N_TILE, bool W_MN, int STAGES>
+mla_status launch_head_gemm(const void* act, const void* weight, void* out, int32_t batch, int n_total,
+                            cuuint32_t w_box_rows, void* stream)
+{
+    using C = Cfg<K_TOTAL, N_TILE, W_MN, STAGES>;
+    CUtensorMap tm_a, tm_w;
+    const cuuint64_t a_dims[2] = {(cuuint64_t)128 * K_TOTAL, (cuuint64_t)batch};
+    const cuuint64_t a_str[1] = {(cuuint64_t)128 * K_TOTAL * 2};
+    const cuuint32_t a_box[2] = {64, 128};
+    const cuuint64_t w_dims[2] = {512, 128 * 128};
+    const cuuint64_t w_str[1] = {512 * 2};
+    const cuuint32_t w_box[2] = {64, w_box_rows};
+    if (!make_map_bf16(&tm_a, act, 2, a_dims, a_str, a_box) || !make_map_bf16(&tm_w, weight, 2, w_dims, w_str, w_box))
+        return MLA_ERR_CUDA;
+    auto kernel = mla::gemm::head_gemm_kernel<K_TOTAL, N_TILE, W_MN, STAGES>;
+    if (!set_smem(kernel, C::kSmemBytes)) return MLA_ERR_CUDA;
+    mla::gemm::Args args;
+    args.out = static_cast<__nv_bfloat16*>(out);
+    args.batch = batch;
+    args.out_row_stride = (int64_t)128 * n_total;
+    args.n_total = n_total;
+    args.dev_error = nullptr;
+    args.timeout_ns = kDefaultTimeoutNs;
+    const dim3 grid(n_total / N_TILE, 128, (batch + 127) / 128);
+    kernel<<<grid, 192, C::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(tm_a, tm_w, args);
+    return launch_status();
+}
+
+bool plan_header_ok(const mla_plan_info* info)
+{
+    return info && info->batch > 0 && info->num_clusters > 0 && info->num_items > 0 && info->num_partials >= 0 &&
+           info->num_combine >= 0 && info->plan_bytes > 0 && info->workspace_bytes >= 0 && info->wait_timeout_ns > 0;
+}
+
+__global__ void wait_timeout_kernel(uint32_t* dev_error, uint64_t timeout_ns)
+{
+    using namespace mla::dev;
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);  // nothing will ever arrive
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const WaitCtx w{timeout_ns, &abort_flag, dev_error};
+        wait_phase(smem_u32(&bar), 0, w);
+    }
+    __syncthreads();
+}
+
+}  // namespace
+
+extern "C" mla_status mla_absorb_q(const void* q_c, const void* w_uk, void* q_abs, int32_t batch, void* stream)
+{
+    if (!q_c || !w_uk || !q_abs || batch <= 0) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(q_c) || !aligned16(w_uk) || !aligned16(q_abs)) return MLA_ERR_ALIGNMENT;
+    return launch_head_gemm<128, kAbsorbN, true, 2>(q_c, w_uk, q_abs, batch, 512, 64, stream);
+}
+
+extern "C" mla_status mla_out_proj(const void* o_lat, const void* w_uv, void* out, int32_t batch, void* stream)
+{
+    if (!o_lat || !w_uv || !out || batch <= 0) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(o_lat) || !aligned16(w_uv) || !aligned16(out)) return MLA_ERR_ALIGNMENT;
+    return launch_head_gemm<512, kOutN, false, 4>(o_lat, w_uv, out, batch, 128, kOutN, stream);
+}
+
+extern "C" mla_status mla_decode_paged(const mla_plan_info* info, const void* plan_dev, const void* q_abs,
+                                       const void* q_r, mla_kv_dtype kv_dtype, const void* kv_pool,
+                                       const float* kv_scale, const void* kr_pool, int32_t num_pool_pages,
+                                       const int32_t* block_table, int32_t max_pages_per_seq, float softmax_scale,
+                                       void* workspace, size_t workspace_bytes, void* o_lat, float* lse,
+                                       uint32_t* dev_error, void* stream)
+{
+    if (!plan_header_ok(info) || !plan_dev || !q_abs || !q_r || !kv_pool || !block_table || !o_lat || !lse ||
+        !dev_error)
+        return MLA_ERR_INVALID_ARG;
+    if (num_pool_pages <= 0 || max_pages_per_seq <= 0 || !(softmax_scale > 0.f) || !std::isfinite(softmax_scale))
+        return MLA_ERR_INVALID_ARG;
+    if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_INVALID_ARG;
+    if (kv_dtype == MLA_KV_FP8_E4M3 && (!kv_scale || !kr_pool)) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(plan_dev) || !aligned16(q_abs) || !aligned16(q_r) || !aligned16(kv_pool) || !aligned16(o_lat) ||
+        !aligned16(lse) || (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(dev_error) & 3u))
+        return MLA_ERR_ALIGNMENT;
+    if (info->workspace_bytes > 0) {
+        if (!workspace || workspace_bytes < (size_t)info->workspace_bytes) return MLA_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return MLA_ERR_ALIGNMENT;
+    }
+    if (kv_dtype == MLA_KV_FP8_E4M3) return MLA_ERR_UNSUPPORTED;  // fp8 gather: separate kernel
+
+    CUtensorMap tm_pool;
+    const cuuint64_t dims[3] = {576, 64, (cuuint64_t)num_pool_pages};
+    const cuuint64_t strides[2] = {576 * 2, 64 * 576 * 2};
+    const cuuint32_t box[3] = {64, 64, 1};
+    if (!make_map_bf16(&tm_pool, kv_pool, 3, dims, strides, box)) return MLA_ERR_CUDA;
+
+    mla::decode::Params p;
+    p.plan = static_cast<const int32_t*>(plan_dev);
+    p.q_abs = static_cast<const __nv_bfloat16*>(q_abs);
+    p.q_r = static_cast<const __nv_bfloat16*>(q_r);
+    p.block_table = block_table;
+    p.max_pages = max_pages_per_seq;
+    p.num_pool_pages = num_pool_pages;
+    p.scale_log2 = softmax_scale * 1.4426950408889634f;
+    p.o_lat = static_cast<__nv_bfloat16*>(o_lat);
+    p.lse = lse;
+    p.ws_o = static_cast<float*>(workspace);
+    p.ws_lse = workspace ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                    (size_t)info->num_partials * mla::kPartialOBytes)
+                         : nullptr;
+    p.dev_error = dev_error;
+    p.timeout_ns = (uint64_t)info->wait_timeout_ns;
+
+    if (!set_smem(mla::decode::decode_bf16_kernel, mla::decode::kSmemBytes)) return MLA_ERR_CUDA;
+    mla::decode::decode_bf16_kernel<<<2 * info->num_clusters, mla::decode::kThreads, mla::decode::kSmemBytes,
+                                      static_cast<cudaStream_t>(stream)>>>(tm_pool, p);
+    return launch_status();
+}
+
+extern "C" mla_status mla_combine_splits(const mla_plan_info* info, const void* plan_dev, const void* workspace,
+                                         size_t workspace_bytes, void* o_lat, float* lse, void* stream)
+{
+    if (!plan_header_ok(info) || !plan_dev || !o_lat || !lse) return MLA_ERR_INVALID_ARG;
+    if (info->num_combine == 0) return MLA_OK;
+    if (!workspace || workspace_bytes < (size_t)info->workspace_bytes) return MLA_ERR_WORKSPACE;
+    if (!aligned16(plan_dev) || !aligned16(workspace) || !aligned16(o_lat) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return MLA_ERR_ALIGNMENT;
+    const float* ws_o = static_cast<const float*>(workspace);
+    const float* ws_lse = reinterpret_cast<const float*>(static_cast<const char*>(workspace) +
+                                                         (size_t)info->num_partials * mla::kPartialOBytes);
+    const dim3 grid(info->num_combine, 128 / mla::combine::kHeadsPerCta);
+    mla::combine::combine_kernel<<<grid, 32 * mla::combine::kHeadsPerCta, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const int32_t*>(plan_dev), ws_o, ws_lse, static_cast<__nv_bfloat16*>(o_lat), lse);
+    return launch_status();
+}
+
+extern "C" mla_status mla_read_device_error(const uint32_t* dev_error, uint32_t* host_bits, void* stream)
+{
+    if (!dev_error) return MLA_ERR_INVALID_ARG;
+    uint32_t bits = 0;
+    if (cudaMemcpyAsync(&bits, dev_error, sizeof bits, cudaMemcpyDeviceToHost, static_cast<cudaStream_t>(stream)) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return MLA_ERR_CUDA;
+    if (host_bits) *host_bits = bits;
+    return bits ? MLA_ERR_DEVICE_FAULT : MLA_OK;
+}
+
+extern "C" mla_status mla_debug_wait_timeout(uint32_t* dev_error, int64_t timeout_ns, void* stream)
+{
+    if (!dev_error || timeout_ns < 1000000 || timeout_ns > 10000000000LL) return MLA_ERR_INVALID_ARG;
+    wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(dev_error, (uint64_t)timeout_ns);
+    return launch_status();
+}

@@ -1,0 +1,127 @@
+"""The C ABI library without a GPU: it loads, exports what include/mla.h declares, and its
+host-side checks reject bad arguments before anything is launched.
+
+Every call below fails host validation by construction (null, misaligned or inconsistent
+arguments), so none of them reaches a kernel launch even where a GPU is present.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from mla_latent_kv_absorb_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build_library()
+    return binding.lib()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "mla.h")).read()
+    return sorted(set(re.findall(r"MLA_API\s+[\w\s\*]+?\b(mla_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for n in ("mla_plan_splits", "mla_absorb_q", "mla_decode_paged", "mla_combine_splits", "mla_out_proj"):
+        assert n in names
+    assert set(names) == set(binding.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_symbols():
+        assert hasattr(L, name), f"{name} not exported"
+
+
+def test_status_strings(L):
+    for s in range(7):
+        assert binding.status_string(s) not in ("", "unknown status")
+    assert binding.status_string(99) == "unknown status"
+
+
+def _p(v):
+    return ctypes.c_void_p(v)
+
+
+def test_absorb_and_out_proj_reject_bad_args(L):
+    assert L.mla_absorb_q(None, _p(4096), _p(8192), 1, None) == binding.MLA_ERR_INVALID_ARG
+    assert L.mla_absorb_q(_p(4096), _p(8192), _p(12288), 0, None) == binding.MLA_ERR_INVALID_ARG
+    assert L.mla_absorb_q(_p(4097), _p(8192), _p(12288), 1, None) == binding.MLA_ERR_ALIGNMENT
+    assert L.mla_out_proj(_p(4096), None, _p(8192), 1, None) == binding.MLA_ERR_INVALID_ARG
+    assert L.mla_out_proj(_p(4096), _p(8200), _p(12288), 1, None) == binding.MLA_ERR_ALIGNMENT
+
+
+def _info(**kw):
+    lens = kw.pop("lens", [100, 5000])
+    plan, info = binding.mla_plan_splits(lens, 152, min_pages_per_split=2)
+    for k, v in kw.items():
+        setattr(info, k, v)
+    return plan, info
+
+
+def _decode(L, info, *, ws=None, ws_bytes=0, q_abs=0x10000, dtype=binding.MLA_KV_BF16, scale=0.07,
+            kv_scale=None, kr=None, dev_error=0x50000):
+    return L.mla_decode_paged(ctypes.byref(info), _p(0x20000), _p(q_abs), _p(0x30000), dtype, _p(0x40000),
+                              _p(kv_scale) if kv_scale else None, _p(kr) if kr else None, 100, _p(0x60000), 80,
+                              ctypes.c_float(scale), _p(ws) if ws else None, ws_bytes, _p(0x70000), _p(0x80000),
+                              _p(dev_error) if dev_error else None, None)
+
+
+def test_decode_rejects_bad_args(L):
+    _, info = _info()
+    assert info.workspace_bytes > 0
+    # inconsistent plan header
+    _, bad = _info(num_clusters=0)
+    assert _decode(L, bad, ws=0x90000, ws_bytes=info.workspace_bytes) == binding.MLA_ERR_INVALID_ARG
+    # missing pointers / bad scale / bad dtype
+    assert _decode(L, info, ws=0x90000, ws_bytes=info.workspace_bytes, q_abs=0) == binding.MLA_ERR_INVALID_ARG
+    assert _decode(L, info, ws=0x90000, ws_bytes=info.workspace_bytes, dev_error=0) == binding.MLA_ERR_INVALID_ARG
+    assert _decode(L, info, ws=0x90000, ws_bytes=info.workspace_bytes, scale=0.0) == binding.MLA_ERR_INVALID_ARG
+    assert _decode(L, info, ws=0x90000, ws_bytes=info.workspace_bytes, scale=float("nan")) == binding.MLA_ERR_INVALID_ARG
+    assert _decode(L, info, ws=0x90000, ws_bytes=info.workspace_bytes, dtype=7) == binding.MLA_ERR_INVALID_ARG
+    # fp8 without its scale / k_R pools
+    assert _decode(L, info, ws=0x90000, ws_bytes=info.workspace_bytes,
+                   dtype=binding.MLA_KV_FP8_E4M3) == binding.MLA_ERR_INVALID_ARG
+    # misaligned query
+    assert _decode(L, info, ws=0x90000, ws_bytes=info.workspace_bytes, q_abs=0x10008) == binding.MLA_ERR_ALIGNMENT
+    # workspace missing or too small
+    assert _decode(L, info, ws=None, ws_bytes=0) == binding.MLA_ERR_WORKSPACE
+    assert _decode(L, info, ws=0x90000, ws_bytes=info.workspace_bytes - 1) == binding.MLA_ERR_WORKSPACE
+
+
+def test_combine_rejects_bad_args(L):
+    plan, info = _info()
+    assert info.num_combine > 0
+    assert L.mla_combine_splits(ctypes.byref(info), _p(0x20000), None, 0, _p(0x70000), _p(0x80000),
+                                None) == binding.MLA_ERR_WORKSPACE
+    assert L.mla_combine_splits(ctypes.byref(info), None, _p(0x90000), info.workspace_bytes, _p(0x70000),
+                                _p(0x80000), None) == binding.MLA_ERR_INVALID_ARG
+    assert L.mla_combine_splits(ctypes.byref(info), _p(0x20000), _p(0x90004), info.workspace_bytes, _p(0x70000),
+                                _p(0x80000), None) == binding.MLA_ERR_ALIGNMENT
+
+
+def test_debug_and_error_reader_reject_bad_args(L):
+    assert L.mla_debug_wait_timeout(None, 10 ** 8, None) == binding.MLA_ERR_INVALID_ARG
+    assert L.mla_debug_wait_timeout(_p(0x50000), 10, None) == binding.MLA_ERR_INVALID_ARG
+    assert L.mla_read_device_error(None, None, None) == binding.MLA_ERR_INVALID_ARG
+
+
+def test_plan_rejects_bad_args(L):
+    with pytest.raises(binding.MlaError):
+        binding.mla_plan_splits([10, 0, 5], 152)            # S = 0
+    with pytest.raises(binding.MlaError):
+        binding.mla_plan_splits([10], 1)                    # fewer than 2 SMs
+    with pytest.raises(binding.MlaError):
+        binding.mla_plan_splits([10], 152, min_pages_per_split=-1)
+    lens = np.array([100], dtype=np.int32)
+    info = binding.PlanInfo()
+    buf = np.zeros(4, dtype=np.int32)  # too small
+    st = L.mla_plan_splits(lens.ctypes.data_as(ctypes.c_void_p), 1, 152, None, buf.ctypes.data_as(ctypes.c_void_p),
+                           buf.nbytes, ctypes.byref(info))
+    assert st == binding.MLA_ERR_WORKSPACE

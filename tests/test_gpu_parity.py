@@ -1,0 +1,196 @@
+"""GPU parity: every kernel of the decode step, through the C ABI, against the CPU oracle.
+
+All inputs come from the seeded generator; every expected value comes from ``oracle/``.
+Tails of last pages are NaN-poisoned, so a kernel that reads past S_b fails.
+"""
+import os
+import sys
+
+import numpy as np
+import pytest
+import torch
+
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+import oracle  # noqa: E402
+from parity_util import SCALE, TOL_BF16, assert_close, bf16_round  # noqa: E402
+
+from mla_latent_kv_absorb_gb300 import binding, synth  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+def _sync_err(step_or_err):
+    torch.cuda.synchronize()
+    bits = binding.mla_read_device_error(step_or_err)
+    assert bits == 0, f"device error bits {bits:#x}"
+
+
+# ------------------------------------------------------------------------------------ absorb
+
+@pytest.mark.parametrize("batch", [1, 16, 128, 130])
+def test_absorb_q(batch):
+    inp = synth.make_inputs([1] * batch, seed=100 + batch)
+    q_abs = torch.empty(batch, 128, 512, dtype=torch.bfloat16, device=DEV)
+    binding.mla_absorb_q(inp.q_c.to(DEV), inp.w_uk.to(DEV), q_abs)
+    torch.cuda.synchronize()
+    ref = oracle.absorb_q(inp.q_c, inp.w_uk)
+    assert_close(q_abs, ref, TOL_BF16, f"q_abs B={batch}")
+
+
+# ------------------------------------------------------------------------------------ out-proj
+
+@pytest.mark.parametrize("batch", [1, 16, 129])
+def test_out_proj(batch):
+    inp = synth.make_inputs([1] * batch, seed=200 + batch)
+    g = torch.Generator().manual_seed(batch)
+    o_lat = (torch.randn(batch, 128, 512, generator=g) * 0.05).to(torch.bfloat16)
+    out = torch.empty(batch, 128, 128, dtype=torch.bfloat16, device=DEV)
+    binding.mla_out_proj(o_lat.to(DEV), inp.w_uv.to(DEV), out)
+    torch.cuda.synchronize()
+    ref = oracle.out_proj(o_lat.double().numpy(), inp.w_uv)
+    assert_close(out, ref, TOL_BF16, f"out B={batch}")
+
+
+# ------------------------------------------------------------------------------------ decode kernel alone
+
+def _decode_only(inp, *, min_pages=0, max_clusters=0):
+    """Run mla_decode_paged (+ merge) on bf16-rounded oracle q_abs; return (o_lat, lse, info, q_abs_bf16)."""
+    q_abs_bf16 = bf16_round(oracle.absorb_q(inp.q_c, inp.w_uk))
+    _, q_r, _, _, kv, bt = binding.inputs_to_device(inp, DEV)
+    plan, info = binding.mla_plan_splits(inp.seq_lens, binding.num_sms(), min_pages_per_split=min_pages,
+                                         max_clusters=max_clusters)
+    plan_dev = torch.from_numpy(plan).to(DEV)
+    B = inp.batch
+    o_lat = torch.full((B, 128, 512), float("nan"), dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((B, 128), float("nan"), dtype=torch.float32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ws = torch.empty(max(info.workspace_bytes // 4, 4), dtype=torch.float32, device=DEV)
+    binding.mla_decode_paged(info, plan_dev, q_abs_bf16.to(DEV), q_r, block_table=bt, o_lat=o_lat, lse=lse,
+                             dev_error=err, workspace=ws, **kv)
+    binding.mla_combine_splits(info, plan_dev, ws, o_lat, lse)
+    _sync_err(err)
+    return o_lat, lse, info, q_abs_bf16
+
+
+def _check_latent(inp, o_lat, lse, q_abs_bf16, heads=None):
+    ref_o, ref_l = oracle.latent_attention(inp, q_abs_bf16.double().numpy(), softmax_scale=SCALE, heads=heads)
+    hs = slice(None) if heads is None else list(heads)
+    assert_close(o_lat[:, hs] if heads is None else o_lat[:, hs, :], ref_o, TOL_BF16, "o_lat")
+    assert_close(lse[:, hs] if heads is None else lse[:, hs], ref_l, TOL_BF16, "lse")
+
+
+@pytest.mark.parametrize("lens", [[1], [64], [65], [700], [100, 37, 64 * 5], [129, 1, 2000, 63]])
+def test_decode_single_item(lens):
+    """One item per sequence (no merge): the decode kernel's own o_lat and lse."""
+    inp = synth.make_inputs(lens, seed=300 + len(lens), poison_tail=True)
+    o_lat, lse, info, q = _decode_only(inp, min_pages=10 ** 6)
+    assert info.num_combine == 0
+    _check_latent(inp, o_lat, lse, q)
+
+
+@pytest.mark.parametrize("lens,min_pages", [([4000], 1), ([64 * 40 + 5, 1, 9000], 2), ([3000] * 8, 4),
+                                            ([100] * 200, 1)])
+def test_decode_split_and_merge(lens, min_pages):
+    """Sequences cut into several items: partials + the log-sum-exp merge kernel."""
+    inp = synth.make_inputs(lens, seed=400 + len(lens), poison_tail=True)
+    o_lat, lse, info, q = _decode_only(inp, min_pages=min_pages)
+    assert info.num_combine > 0 or len(lens) > 76
+    _check_latent(inp, o_lat, lse, q)
+
+
+def test_decode_few_clusters_many_items():
+    """Two CTA pairs walk many items each (item boundaries inside the pipelines)."""
+    lens = [70, 1, 640, 129, 3, 64, 2000, 65]
+    inp = synth.make_inputs(lens, seed=501, poison_tail=True)
+    o_lat, lse, info, q = _decode_only(inp, min_pages=1, max_clusters=2)
+    assert info.num_clusters == 2 and info.num_items >= len(lens)
+    _check_latent(inp, o_lat, lse, q)
+
+
+def test_decode_large_scores_rescale():
+    """Large query norms make the running max jump between pages: exercises the rescale path."""
+    inp = synth.make_inputs([64 * 30 + 7, 900], seed=502, poison_tail=True)
+    g = torch.Generator().manual_seed(5)
+    # scale the queries up by a page-dependent amount so later pages see higher scores
+    inp.q_c = (inp.q_c.float() * 6.0).to(torch.bfloat16)
+    inp.q_r = (torch.randn(2, 128, 64, generator=g) * 6.0).to(torch.bfloat16)
+    pool = inp.pool.float()
+    for b in range(2):
+        for j in range((int(inp.seq_lens[b]) + 63) // 64):
+            pg = int(inp.block_table[b, j])
+            pool[pg] *= 0.25 + 0.08 * j
+    inp.pool = pool.to(torch.bfloat16)
+    o_lat, lse, info, q = _decode_only(inp, min_pages=10 ** 6)
+    _check_latent(inp, o_lat, lse, q)
+
+
+# ------------------------------------------------------------------------------------ end to end
+
+def _run_step(inp, **kw):
+    q_c, q_r, w_uk, w_uv, kv, bt = binding.inputs_to_device(inp, DEV)
+    step = binding.DecodeStep(inp.seq_lens, w_uk=w_uk, w_uv=w_uv, block_table=bt, **kv, **kw)
+    out = step.run(q_c, q_r)
+    torch.cuda.synchronize()
+    assert step.device_error() == 0
+    return out, step
+
+
+def test_end_to_end_b1_s2048_naive():
+    """B=1, S=2048, identity block table: the whole step against the naive (decompressed) oracle."""
+    inp = synth.make_workload("b1_s2048", poison_tail=True)
+    out, step = _run_step(inp)
+    ref = oracle.decode_naive(inp, softmax_scale=SCALE)
+    assert_close(out, ref, TOL_BF16, "out vs naive oracle")
+
+
+def test_end_to_end_b16_s4096():
+    """B=16, S=4096, shuffled pool: absorbed oracle on all heads, naive oracle on three heads."""
+    inp = synth.make_workload("b16_s4096", poison_tail=True)
+    out, step = _run_step(inp)
+    _, _, _, ref = oracle.decode_absorbed(inp, softmax_scale=SCALE)
+    assert_close(out, ref, TOL_BF16, "out vs absorbed oracle")
+    heads = [0, 61, 127]
+    ref_n = oracle.decode_naive(inp, softmax_scale=SCALE, heads=heads)
+    assert_close(out[:, heads, :], ref_n, TOL_BF16, "out vs naive oracle (3 heads)")
+
+
+def test_end_to_end_ragged_b64():
+    """B=64 ragged lengths in [128, 32768] (seed 42): split planning and merge at full size;
+    the oracle computes every 8th head."""
+    inp = synth.make_workload("b64_ragged", poison_tail=True)
+    out, step = _run_step(inp)
+    assert step.info.num_combine > 0
+    heads = list(range(0, 128, 8))
+    q_abs = oracle.absorb_q(inp.q_c, inp.w_uk)
+    o, _ = oracle.latent_attention(inp, q_abs, softmax_scale=SCALE, heads=heads)
+    full = np.zeros((inp.batch, 128, 512))
+    full[:, heads, :] = o
+    ref = oracle.out_proj(full, inp.w_uv)[:, heads, :]
+    assert_close(out[:, heads, :], ref, TOL_BF16, "out (every 8th head)")
+
+
+def test_end_to_end_b16_s65536_sampled():
+    """B=16, S=65536 (1.2 GB cache): the launch configuration the bench times; the oracle
+    computes three heads of every sequence."""
+    inp = synth.make_workload("b16_s65536", poison_tail=False)
+    out, step = _run_step(inp)
+    assert step.info.num_clusters == binding.num_sms() // 2
+    heads = [0, 77, 127]
+    q_abs = oracle.absorb_q(inp.q_c, inp.w_uk)
+    o, _ = oracle.latent_attention(inp, q_abs, softmax_scale=SCALE, heads=heads)
+    full = np.zeros((inp.batch, 128, 512))
+    full[:, heads, :] = o
+    ref = oracle.out_proj(full, inp.w_uv)[:, heads, :]
+    assert_close(out[:, heads, :], ref, TOL_BF16, "out (3 heads)")
+
+
+def test_step_is_deterministic():
+    inp = synth.make_inputs([5000, 300, 64], seed=7, poison_tail=True)
+    q_c, q_r, w_uk, w_uv, kv, bt = binding.inputs_to_device(inp, DEV)
+    step = binding.DecodeStep(inp.seq_lens, w_uk=w_uk, w_uv=w_uv, block_table=bt, min_pages_per_split=2, **kv)
+    a = step.run(q_c, q_r).clone()
+    b = step.run(q_c, q_r).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)

@@ -1,0 +1,113 @@
+"""Host split planner (mla_plan_splits): the plan image covers every page exactly once, in
+order, balanced over CTA pairs, with consistent partial slots and merge entries."""
+import numpy as np
+import pytest
+import torch
+
+from mla_latent_kv_absorb_gb300 import binding, synth
+
+HDR = dict(magic=0, version=1, batch=2, clusters=3, items=4, partials=5, combine=6, cl_off=7, it_off=8, cb_off=9,
+           total=10, max_splits=11)
+
+
+def decode_plan(plan):
+    h = {k: int(plan[v]) for k, v in HDR.items()}
+    cl = plan[h["cl_off"]: h["cl_off"] + h["clusters"] + 1]
+    items = plan[h["it_off"]: h["it_off"] + 8 * h["items"]].reshape(-1, 8)[:, :5]
+    comb = plan[h["cb_off"]: h["cb_off"] + 4 * h["combine"]].reshape(-1, 4)[:, :3]
+    return h, cl, items, comb
+
+
+def check_plan(lens, num_sms=152, **kw):
+    lens = np.asarray(lens, dtype=np.int32)
+    plan, info = binding.mla_plan_splits(lens, num_sms, **kw)
+    h, cl, items, comb = decode_plan(plan)
+    B = lens.size
+    pages = (lens.astype(np.int64) + 63) // 64
+    assert h["magic"] == 0x504C4D41 and h["version"] == 1 and h["batch"] == B
+    assert h["total"] == pages.sum() == info.total_pages
+    assert 1 <= h["clusters"] <= num_sms // 2 and h["clusters"] == info.num_clusters
+    assert cl[0] == 0 and cl[-1] == h["items"] and np.all(np.diff(cl) >= 0)
+    # coverage: items in order tile every sequence's pages exactly once
+    covered = {b: [] for b in range(B)}
+    for seq, pb, pe, slen, slot in items:
+        assert 0 <= seq < B and 0 <= pb < pe <= pages[seq] and slen == lens[seq]
+        covered[seq].append((pb, pe))
+    for b in range(B):
+        rng = covered[b]
+        assert rng[0][0] == 0 and rng[-1][1] == pages[b]
+        assert all(rng[i][1] == rng[i + 1][0] for i in range(len(rng) - 1))
+    # partial slots: -1 for single-item sequences, consecutive per sequence otherwise
+    n_items = np.bincount(items[:, 0], minlength=B)
+    assert info.max_splits == n_items.max()
+    slots = items[:, 4]
+    assert np.all(slots[n_items[items[:, 0]] == 1] == -1)
+    multi = slots[n_items[items[:, 0]] > 1]
+    assert sorted(multi.tolist()) == list(range(info.num_partials))
+    assert info.num_combine == (n_items > 1).sum() == h["combine"]
+    for seq, first, n in comb:
+        assert n == n_items[seq] > 1
+        own = items[items[:, 0] == seq]
+        assert own[:, 4].tolist() == list(range(first, first + n))
+    assert info.workspace_bytes == info.num_partials * (128 * 512 * 4 + 128 * 4)
+    # balance: no CTA pair has more than its share plus one sequence edge's slack
+    per = np.zeros(h["clusters"], dtype=np.int64)
+    for k in range(h["clusters"]):
+        for seq, pb, pe, _, _ in items[cl[k]:cl[k + 1]]:
+            per[k] += pe - pb
+    assert per.sum() == pages.sum()
+    return info, per, items
+
+
+def test_single_long_sequence_is_split_evenly():
+    info, per, _ = check_plan([65536])
+    assert info.num_clusters == 76 and info.num_combine == 1 and info.max_splits == 76
+    assert per.max() - per.min() <= 1
+
+
+def test_64k_workload_balance():
+    info, per, _ = check_plan([65536] * 16)
+    assert info.num_clusters == 76
+    share = 16384 / 76
+    assert per.max() <= share + 8 + 1  # min-split snapping moves an edge by < 8 pages
+
+
+def test_short_sequences_stay_whole():
+    info, per, items = check_plan([2048])
+    # 32 pages with the default minimum of 8 pages per item: 4 pairs
+    assert info.num_clusters == 4 and info.num_items == 4 and info.num_combine == 1
+
+
+def test_ragged_workload():
+    g = torch.Generator().manual_seed(42)
+    lens = synth.ragged_lengths(64, 128, 32768, g)
+    info, per, _ = check_plan(lens)
+    assert info.total_pages == 17480
+    assert per.max() <= 17480 / 76 + 8 + 1
+
+
+@pytest.mark.parametrize("lens", [[1], [1, 1, 1], [64], [65], [63, 64, 65, 129], [1] * 300, [5000, 1, 70000, 3]])
+def test_edge_lengths(lens):
+    check_plan(lens)
+
+
+@pytest.mark.parametrize("min_pages,max_clusters", [(1, 0), (2, 3), (64, 0), (8, 1)])
+def test_options(min_pages, max_clusters):
+    info, per, items = check_plan([100, 3000, 9000, 64 * 7], min_pages_per_split=min_pages, max_clusters=max_clusters)
+    if max_clusters:
+        assert info.num_clusters <= max_clusters
+
+
+def test_randomised_plans():
+    rng = np.random.default_rng(0)
+    for _ in range(200):
+        B = int(rng.integers(1, 200))
+        lens = rng.integers(1, 70000, size=B)
+        sms = int(rng.choice([2, 16, 148, 152]))
+        check_plan(lens, num_sms=sms, min_pages_per_split=int(rng.integers(0, 20)))
+
+
+def test_timeout_option_recorded():
+    plan, info = binding.mla_plan_splits([100], 152, wait_timeout_ns=123456789)
+    assert info.wait_timeout_ns == 123456789
+    assert int(plan[12]) + (int(plan[13]) << 32) == 123456789
