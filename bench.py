@@ -1,0 +1,446 @@
+#!/usr/bin/env python3
+"""Benchmark of the MLA decode step on GB300: one JSON line on stdout (rank 0).
+
+A step is one pass of the whole decode path over one batch: absorb W_UK into q, paged
+split-KV decode, log-sum-exp merge of split partials, W_UV projection.  The default workload
+is 16 sequences of 65,536 tokens (a 1.21 GB bf16 latent cache, shuffled 64-token pages),
+the configuration the 70 %-of-roofline target is stated on.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-cpu-baseline]
+
+Timing: W warm-up steps, then exactly K timed steps between a barrier + synchronize on both
+sides.  Each step is bracketed by CUDA events on the launch stream, with events between its
+kernels so each kernel's duration is measured live; a 512 MB buffer is rewritten before every
+step (outside the events) so L2 starts cold, and the 1.2 GB cache is itself larger than L2.
+`value` is the mean device time per step (microseconds, lower is better); with N ranks every
+rank runs its own replica of the workload and the slowest rank is reported.
+
+`e2e` times the same step through the public API with host buffers: per step the queries come
+from pinned host memory, the split plan is rebuilt on the host and copied over with the block
+table, and the output is read back; wall clock around all of it.
+
+`--impl reference` times the CPU oracle (plain fp64 C, the definition of the result) on the
+host cores, on a bounded sample of the same workload per step, scaled to a full step.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import ctypes.util
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mla_latent_kv_absorb_gb300 import synth  # noqa: E402
+
+METRIC = "MLA decode us/step (KV TB/s & TFLOP/s as fraction of GB300 roofline)"
+UNIT = "us/step"
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_PATH = os.path.join(ROOT, "profiles", "decode_traffic.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+KERNEL_SOURCES = ["mla_latent_kv_absorb_gb300/csrc/decode.cuh", "mla_latent_kv_absorb_gb300/csrc/ptx.cuh"]
+
+
+# ----------------------------------------------------------------------------- distributed helpers
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def dist_barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def dist_max(value: float, world: int, device="cpu") -> float:
+    """Max of a per-rank float over all ranks (the slowest rank sets the step time)."""
+    if world <= 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- clocks (NVML, read only)
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML in a thread (reads only)."""
+
+    HW_SLOWDOWN, SW_POWER_CAP, HW_THERMAL, SW_THERMAL = 0x8, 0x4, 0x40, 0x20
+
+    def __init__(self, index: int, period_s: float = 0.002):
+        self.samples, self.reasons_seen = [], set()
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._period = period_s
+        self._ok = False
+        try:
+            name = ctypes.util.find_library("nvidia-ml") or "libnvidia-ml.so.1"
+            self.nvml = ctypes.CDLL(name)
+            if self.nvml.nvmlInit_v2() != 0:
+                return
+            self.handle = ctypes.c_void_p()
+            if self.nvml.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(self.handle)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx)) == 0:  # 1 = SM
+                self.max_mhz = int(mx.value)
+            self._ok = True
+        except OSError:
+            pass
+
+    def _read(self):
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(clk)) == 0:
+            self.samples.append(int(clk.value))
+        fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        if fn(self.handle, ctypes.byref(rs)) == 0:
+            v = int(rs.value)
+            for bit, name in ((self.HW_SLOWDOWN, "hw_slowdown"), (self.SW_POWER_CAP, "sw_power_cap"),
+                              (self.HW_THERMAL, "hw_thermal_slowdown"), (self.SW_THERMAL, "sw_thermal_slowdown")):
+                if v & bit:
+                    self.reasons_seen.add(name)
+
+    def _loop(self):
+        while not self._stop.is_set():
+            self._read()
+            time.sleep(self._period)
+
+    def __enter__(self):
+        if self._ok:
+            self._t = threading.Thread(target=self._loop, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self._ok:
+            self._stop.set()
+            self._t.join()
+            self._read()
+
+    def summary(self):
+        if not self._ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0, "source": "unavailable"}
+        return {"sm_mhz": int(statistics.median(self.samples)), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons_seen), "samples": len(self.samples), "source": "nvml"}
+
+
+# ----------------------------------------------------------------------------- accounting
+
+def workload_accounting(inp):
+    """Algorithmic bytes and FLOPs of one step (no partial-output traffic, no decompression)."""
+    B, T = inp.batch, inp.num_tokens
+    row_bytes = 1152 if inp.kv_dtype == "bf16" else 512 + 4 + 128
+    kv_bytes = T * row_bytes
+    w_bytes = 2 * 128 * 128 * 512 * 2
+    q_bytes = B * 128 * (128 + 64) * 2
+    out_bytes = B * 128 * 128 * 2
+    decode_bytes = kv_bytes + B * 128 * (512 + 64) * 2 + B * 128 * (512 * 2 + 4)
+    attn_flop = T * 128 * 2 * (576 + 512)
+    proj_flop = 2 * B * 128 * (2 * 128 * 512)
+    return dict(tokens=T, kv_bytes=kv_bytes, step_bytes=kv_bytes + w_bytes + q_bytes + out_bytes,
+                decode_bytes=decode_bytes, step_flop=attn_flop + proj_flop, decode_flop=attn_flop)
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_PATH) as f:
+            p = json.load(f)
+        p["source"] = "measured"
+        return p
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS)
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, tokens: int):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was taken on the
+    current kernel source; scaled to this workload's tokens when captured on a smaller case."""
+    try:
+        with open(TRAFFIC_PATH) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if t.get("kernel_hash") != kernel_hash():
+        return None
+    per_token = t["dram_bytes_per_launch"] / t["tokens"]
+    return per_token * tokens
+
+
+# ----------------------------------------------------------------------------- the GPU arm
+
+def run_ours(args, rank, world, local):
+    from mla_latent_kv_absorb_gb300 import binding
+
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    dist_init(world, "nccl")
+    binding.lib()
+    inp = synth.make_workload(args.workload, seed=synth.DEFAULT_SEED + rank, poison_tail=False)
+    q_c, q_r, w_uk, w_uv, kv, bt = binding.inputs_to_device(inp, device)
+    step = binding.DecodeStep(inp.seq_lens, w_uk=w_uk, w_uv=w_uv, block_table=bt, **kv)
+    acc = workload_accounting(inp)
+    peaks = load_peaks()
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def one_step(evs=None):
+        if evs is None:
+            return step.run(q_c, q_r, stream)
+        evs[0].record(stream)
+        binding.mla_absorb_q(q_c, step.w_uk, step.q_abs, stream)
+        evs[1].record(stream)
+        binding.mla_decode_paged(step.info, step.plan_dev, step.q_abs, q_r, kv_pool=step.kv_pool,
+                                 block_table=step.block_table, o_lat=step.o_lat, lse=step.lse,
+                                 dev_error=step.dev_error, workspace=step.workspace, kv_scale=step.kv_scale,
+                                 kr_pool=step.kr_pool, softmax_scale=step.softmax_scale, stream=stream)
+        evs[2].record(stream)
+        binding.mla_combine_splits(step.info, step.plan_dev, step.workspace, step.o_lat, step.lse, stream)
+        evs[3].record(stream)
+        binding.mla_out_proj(step.o_lat, step.w_uv, step.out, stream)
+        evs[4].record(stream)
+
+    # warm-up: at least W steps and at least half a second of work so clocks settle
+    t0 = time.perf_counter()
+    n = 0
+    while n < args.warmup or time.perf_counter() - t0 < 0.5:
+        flush.fill_(n & 0xFF)
+        one_step()
+        n += 1
+        if n % 16 == 0:
+            torch.cuda.synchronize(device)
+    torch.cuda.synchronize(device)
+    if step.device_error() != 0:
+        raise RuntimeError(f"device error bits {step.device_error():#x} during warm-up")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    dist_barrier(world)
+    torch.cuda.synchronize(device)
+    with ClockSampler(local) as clocks:
+        wall0 = time.perf_counter()
+        for i in range(K):
+            flush.fill_(i & 0xFF)
+            one_step(evs[i])
+        torch.cuda.synchronize(device)
+        wall = time.perf_counter() - wall0
+    dist_barrier(world)
+    err = step.device_error()
+    if err != 0:
+        raise RuntimeError(f"device error bits {err:#x} in the timed region")
+
+    step_ms = [e[0].elapsed_time(e[4]) for e in evs]
+    k_ms = {name: [e[i].elapsed_time(e[i + 1]) for e in evs]
+            for i, name in enumerate(["absorb", "decode", "combine", "out_proj"])}
+    ms = statistics.mean(step_ms)
+    ms_max = dist_max(ms, world, device)
+    decode_ms = statistics.mean(k_ms["decode"])
+
+    # sampled parity against the oracle at full size (three heads of every sequence)
+    parity = None
+    if args.parity and rank == 0:
+        parity = sampled_parity(inp, step.out)
+
+    e2e = run_e2e(args, inp, step, binding, device, stream) if args.e2e else None
+
+    bw = peaks.get("hbm_gbs")
+    tf = peaks.get("bf16_tflops")
+    achieved_gbs = acc["decode_bytes"] / (decode_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(args.workload, acc["tokens"])
+    step_roof_us = max(acc["step_bytes"] / (bw * 1e9), acc["step_flop"] / (tf * 1e12)) * 1e6
+    decode_roof_us = max(acc["decode_bytes"] / (bw * 1e9), acc["decode_flop"] / (tf * 1e12)) * 1e6
+    res = {
+        "metric": METRIC,
+        "value": round(ms_max * 1e3, 2),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_max, 5),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if inp.kv_dtype == "bf16" else "fp8_e4m3+bf16",
+        "data": "synthetic (seeded N(0,1) cache/queries, N(0,1/512) weights)",
+        "config": {"workload": args.workload, "desc": synth.WORKLOADS[args.workload]["desc"],
+                   "global_batch": inp.batch * world, "seq_len": int(inp.seq_lens.max()),
+                   "tokens_per_replica": acc["tokens"], "parallelism": f"replicas x{world}",
+                   "l2": "512 MB buffer rewritten before every timed step; cache (1.2 GB) > L2",
+                   "plan": {"clusters": step.info.num_clusters, "items": step.info.num_items,
+                            "combine_seqs": step.info.num_combine, "max_splits": step.info.max_splits}},
+        "kernels_us": {k: round(statistics.mean(v) * 1e3, 2) for k, v in k_ms.items()},
+        "kv_tbps": round(acc["kv_bytes"] / (ms_max * 1e-3) / 1e12, 3),
+        "step_tflops": round(acc["step_flop"] / (ms_max * 1e-3) / 1e12, 1),
+        "decode_tflops": round(acc["decode_flop"] / (decode_ms * 1e-3) / 1e12, 1),
+        "roofline": {"bound": "hbm", "kernel": "decode_bf16_kernel", "achieved": round(achieved_gbs, 1),
+                     "peak": bw, "unit": "GB/s", "frac": round(achieved_gbs / bw, 4),
+                     "traffic": None if traffic is None else int(traffic),
+                     "algorithmic_bytes": acc["decode_bytes"], "peak_source": peaks.get("source"),
+                     "tensor_frac": round(acc["decode_flop"] / (decode_ms * 1e-3) / 1e12 / tf, 4)},
+        "step_roofline_frac": round(step_roof_us / (ms_max * 1e3), 4),
+        "decode_roofline_frac": round(decode_roof_us / (decode_ms * 1e3), 4),
+        "clocks": clocks.summary(),
+        "wall_s_timed": round(wall, 4),
+        "gpu_launches": K * step.launches_per_step,
+        "e2e": e2e,
+        "parity": parity,
+    }
+    if rank == 0 and args.cpu_baseline and world >= 1:
+        res["cpu_baseline"] = cpu_baseline(inp, samples=1)
+    return res
+
+
+def sampled_parity(inp, out_dev):
+    import oracle
+    from mla_latent_kv_absorb_gb300 import binding
+
+    heads = [0, 77, 127]
+    q_abs = oracle.absorb_q(inp.q_c, inp.w_uk)
+    o, _ = oracle.latent_attention(inp, q_abs, softmax_scale=binding.SOFTMAX_SCALE, heads=heads)
+    full = np.zeros((inp.batch, 128, 512))
+    full[:, heads, :] = o
+    ref = oracle.out_proj(full, inp.w_uv)[:, heads, :]
+    got = out_dev[:, heads, :].double().cpu().numpy()
+    d = got - ref
+    return {"heads": heads, "max_abs": float(np.abs(d).max()),
+            "rel_l2": float(np.linalg.norm(d) / np.linalg.norm(ref)), "tol": {"max_abs": 2e-2, "rel_l2": 1e-2}}
+
+
+def run_e2e(args, inp, step, binding, device, stream):
+    """Through the public API with host buffers: H2D queries/plan/table, D2H output."""
+    q_c_h = inp.q_c.pin_memory()
+    q_r_h = inp.q_r.pin_memory()
+    bt_h = torch.from_numpy(np.ascontiguousarray(inp.block_table)).pin_memory()
+    out_h = torch.empty_like(step.out, device="cpu").pin_memory()
+    q_c_d = torch.empty_like(q_c_h, device=device)
+    q_r_d = torch.empty_like(q_r_h, device=device)
+    n_sm = binding.num_sms(device)
+    times = []
+    h2d = d2h = 0
+    for i in range(args.warmup + args.steps):
+        torch.cuda.synchronize(device)
+        t0 = time.perf_counter()
+        plan, info = binding.mla_plan_splits(inp.seq_lens, n_sm)
+        plan_h = torch.from_numpy(plan).pin_memory()
+        step.plan_dev.copy_(plan_h, non_blocking=True)
+        step.block_table.copy_(bt_h, non_blocking=True)
+        q_c_d.copy_(q_c_h, non_blocking=True)
+        q_r_d.copy_(q_r_h, non_blocking=True)
+        step.info = info
+        step.run(q_c_d, q_r_d, stream)
+        out_h.copy_(step.out, non_blocking=True)
+        torch.cuda.synchronize(device)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+        h2d = plan_h.numel() * 4 + bt_h.numel() * 4 + q_c_h.numel() * 2 + q_r_h.numel() * 2
+        d2h = out_h.numel() * 2
+    return {"value": round(statistics.mean(times) * 1e6, 2), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h)}
+
+
+# ----------------------------------------------------------------------------- the CPU oracle
+
+def cpu_baseline(inp, samples=1, tokens=None):
+    """Time the naive oracle on one sequence x 16 heads (every 8th) on all host cores; scale to
+    a full step (all sequences, all heads; the oracle is linear in tokens)."""
+    import oracle
+
+    cores = len(os.sched_getaffinity(0))
+    oracle.set_threads(cores)
+    heads = list(range(0, 128, 8))
+    sub = synth.DecodeInputs(seq_lens=inp.seq_lens[:1].copy(), block_table=inp.block_table[:1].copy(),
+                             num_pool_pages=inp.num_pool_pages, q_c=inp.q_c[:1], q_r=inp.q_r[:1], w_uk=inp.w_uk,
+                             w_uv=inp.w_uv, kv_dtype=inp.kv_dtype, pool=inp.pool, c8=inp.c8, kv_scale=inp.kv_scale,
+                             kr=inp.kr)
+    if tokens is not None:
+        sub.seq_lens[0] = min(int(sub.seq_lens[0]), tokens)
+    from mla_latent_kv_absorb_gb300.binding import SOFTMAX_SCALE
+
+    dts = []
+    for _ in range(samples):
+        t0 = time.perf_counter()
+        oracle.decode_naive(sub, softmax_scale=SOFTMAX_SCALE, heads=heads)
+        dts.append(time.perf_counter() - t0)
+    dt = statistics.mean(dts)
+    scale = (inp.num_tokens * 128) / (int(sub.seq_lens[0]) * len(heads))
+    return {"value": round(dt * scale * 1e6, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"naive fp64 oracle, sequence 0 ({int(sub.seq_lens[0])} tokens) x heads 0,8,..,120; "
+                      f"{dt:.2f} s measured, scaled x{scale:.0f} to the full step"}
+
+
+def run_reference(args, rank, world, local):
+    """The CPU oracle as the reference arm: rank 0 only."""
+    if rank != 0:
+        return None
+    inp = synth.make_workload(args.workload, poison_tail=False)
+    per_step = []
+    tokens = 8192
+    for i in range(args.warmup + args.steps):
+        r = cpu_baseline(inp, samples=1, tokens=tokens)
+        if i >= args.warmup:
+            per_step.append(r["value"])
+    v = statistics.mean(per_step)
+    cb = dict(r)
+    cb["value"] = round(v, 1)
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(v / 1e3, 3), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "desc": synth.WORKLOADS[args.workload]["desc"]},
+            "cpu_baseline": cb, "e2e": {"value": round(v, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                                        "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default="b16_s65536")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--no-parity", dest="parity", action="store_false")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, rank, world, local)
+    else:
+        res = run_ours(args, rank, world, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1 and torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

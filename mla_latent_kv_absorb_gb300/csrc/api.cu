@@ -26,6 +26,10 @@ using OutCfg = Cfg<512, kOutN, false, 4>;
 
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 
+#ifdef MLA_DECODE_TRACE
+long long* g_trace = nullptr;  // wait-cycle accounting buffer, instrumented builds only
+#endif
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -125,6 +129,20 @@ __global__ void wait_timeout_kernel(uint32_t* dev_error, uint64_t timeout_ns)
 
 }  // namespace
 
+#ifdef MLA_DECODE_TRACE
+extern "C" __attribute__((visibility("default"))) void mla_debug_set_trace(long long* trace) { g_trace = trace; }
+extern "C" __attribute__((visibility("default"))) int mla_debug_timeout_sites(unsigned long long* host, int n, int clear)
+{
+    if (n > 1024) n = 1024;
+    if (cudaMemcpyFromSymbol(host, mla::dev::g_timeout_site, sizeof(unsigned long long) * n) != cudaSuccess) return -1;
+    if (clear) {
+        static unsigned long long zeros[1024];
+        cudaMemcpyToSymbol(mla::dev::g_timeout_site, zeros, sizeof zeros);
+    }
+    return 0;
+}
+#endif
+
 extern "C" mla_status mla_absorb_q(const void* q_c, const void* w_uk, void* q_abs, int32_t batch, void* stream)
 {
     if (!q_c || !w_uk || !q_abs || batch <= 0) return MLA_ERR_INVALID_ARG;
@@ -184,6 +202,11 @@ extern "C" mla_status mla_decode_paged(const mla_plan_info* info, const void* pl
                          : nullptr;
     p.dev_error = dev_error;
     p.timeout_ns = (uint64_t)info->wait_timeout_ns;
+#ifdef MLA_DECODE_TRACE
+    p.trace = g_trace;
+#else
+    p.trace = nullptr;
+#endif
 
     if (!set_smem(mla::decode::decode_bf16_kernel, mla::decode::kSmemBytes)) return MLA_ERR_CUDA;
     mla::decode::decode_bf16_kernel<<<2 * info->num_clusters, mla::decode::kThreads, mla::decode::kSmemBytes,

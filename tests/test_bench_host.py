@@ -1,0 +1,80 @@
+"""Host logic of bench.py without a GPU: the multi-rank reduction over gloo (world size 2),
+the reference arm's rank rule, and the algorithmic byte / FLOP accounting."""
+import multiprocessing as mp
+import os
+import socket
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    import torch
+
+    import bench
+
+    r, w, _ = bench.dist_env()
+    bench.dist_init(w, "gloo")
+    slowest = bench.dist_max(1.5 * (r + 1), w)
+    bench.dist_barrier(w)
+    q.put((r, slowest))
+    torch.distributed.destroy_process_group()
+
+
+def test_max_over_ranks_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert got == [(0, 3.0), (1, 3.0)]
+
+
+def test_reference_arm_only_rank0(monkeypatch):
+    import bench
+
+    class A:
+        workload, steps, warmup = "b1_s2048", 1, 3
+
+    assert bench.run_reference(A(), rank=1, world=2, local=1) is None
+
+
+def test_accounting_matches_roofline_table():
+    import bench
+    from mla_latent_kv_absorb_gb300 import synth
+
+    class Fake:
+        kv_dtype = "bf16"
+        batch = 16
+        num_tokens = 16 * 65536
+
+    acc = bench.workload_accounting(Fake())
+    assert acc["kv_bytes"] == 1_207_959_552          # 16 x 1024 pages x 73,728 B
+    assert abs(acc["step_flop"] / 1e9 - 292.6) < 0.5   # QK + PV + absorb + out-proj
+    assert abs(acc["step_bytes"] / 1e6 - 1242.8) < 1.0
+    Fake.kv_dtype, Fake.batch, Fake.num_tokens = "fp8_e4m3", 128, 128 * 8192
+    acc = bench.workload_accounting(Fake())
+    assert acc["kv_bytes"] == 128 * 8192 * 644         # e4m3 latent + fp32 scale + bf16 k_R
+
+
+def test_warmup_floor():
+    import bench
+
+    with pytest.raises(SystemExit):
+        bench.main(["--warmup", "2"])
