@@ -69,6 +69,9 @@ typedef enum mla_kv_dtype {
 
 MLA_API const char* mla_status_string(mla_status status);
 
+/* Text of the last CUDA runtime failure (MLA_ERR_CUDA) seen by the calling host thread. */
+MLA_API const char* mla_last_error_string(void);
+
 /* ---------------------------------------------------------------- a1: split planning (host only)
  *
  * P3 ("Inside the blocks") splits the decode KV scan over many workgroups and merges the

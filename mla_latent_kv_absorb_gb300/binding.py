@@ -47,7 +47,7 @@ class PlanInfo(ctypes.Structure):
                 ("workspace_bytes", ctypes.c_int64), ("wait_timeout_ns", ctypes.c_int64)]
 
 
-EXPORTS = ("mla_status_string", "mla_plan_bytes_max", "mla_plan_splits", "mla_absorb_q", "mla_decode_paged",
+EXPORTS = ("mla_status_string", "mla_last_error_string", "mla_plan_bytes_max", "mla_plan_splits", "mla_absorb_q", "mla_decode_paged",
            "mla_combine_splits", "mla_out_proj", "mla_read_device_error", "mla_debug_wait_timeout")
 
 _lib = None
@@ -65,6 +65,8 @@ def lib() -> ctypes.CDLL:
     P, i32, i64, sz, u32p = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p
     L.mla_status_string.restype = ctypes.c_char_p
     L.mla_status_string.argtypes = [ctypes.c_int]
+    L.mla_last_error_string.restype = ctypes.c_char_p
+    L.mla_last_error_string.argtypes = []
     L.mla_plan_bytes_max.restype = sz
     L.mla_plan_bytes_max.argtypes = [i32, i32]
     L.mla_plan_splits.restype = ctypes.c_int
@@ -92,7 +94,10 @@ def status_string(status: int) -> str:
 
 def _check(fn: str, status: int) -> None:
     if status != MLA_OK:
-        raise MlaError(fn, status, status_string(status))
+        msg = status_string(status)
+        if status == MLA_ERR_CUDA:
+            msg += ": " + lib().mla_last_error_string().decode()
+        raise MlaError(fn, status, msg)
 
 
 def _ptr(t: Optional[torch.Tensor]):

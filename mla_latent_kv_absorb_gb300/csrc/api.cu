@@ -6,6 +6,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
 
 #include "../../include/mla.h"
 #include "combine.cuh"
@@ -60,17 +61,28 @@ bool make_map_bf16(CUtensorMap* m, const void* base, int rank, const cuuint64_t*
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Text of the last CUDA failure seen by this host thread (thread-local: no shared state).
+thread_local char t_last_error[256] = "no error";
+
+mla_status record_cuda(cudaError_t e, const char* where)
+{
+    if (e == cudaSuccess) return MLA_OK;
+    snprintf(t_last_error, sizeof t_last_error, "%s: %s (%s)", where, cudaGetErrorString(e), cudaGetErrorName(e));
+    return MLA_ERR_CUDA;
+}
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 template <typename K>
 bool set_smem(K kernel, int bytes)
 {
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
+    return record_cuda(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes),
+                       "cudaFuncSetAttribute(max dynamic shared memory)") == MLA_OK;
 }
 
 mla_status launch_status()
 {
-    return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+    return record_cuda(cudaGetLastError(), "kernel launch");
 }
 
 // Shared by absorb and out-proj: activations [batch][128][K] (K-major rows of 128*K), weights
@@ -230,6 +242,8 @@ extern "C" mla_status mla_combine_splits(const mla_plan_info* info, const void* 
         static_cast<const int32_t*>(plan_dev), ws_o, ws_lse, static_cast<__nv_bfloat16*>(o_lat), lse);
     return launch_status();
 }
+
+extern "C" const char* mla_last_error_string(void) { return t_last_error; }
 
 extern "C" mla_status mla_read_device_error(const uint32_t* dev_error, uint32_t* host_bits, void* stream)
 {

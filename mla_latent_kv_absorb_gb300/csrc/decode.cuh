@@ -11,12 +11,16 @@
 // memory, and the scores need 64 more; the bf16 query [128 x 576] is 144 KB.  So a cluster of
 // two CTAs on two SMs splits the work by role instead of recomputing anything:
 //   rank 0, the score CTA: q_abs lives in TMEM (256 columns, the A operand of "TS" MMAs) and
-//     q_R in shared memory (16 KB); the scores of two pages at a time go to one of two
-//     128-column TMEM buffers (one N=128 MMA covers both pages, which halves the MMA count:
-//     a tcgen05.mma costs about the same to issue at N=64 as at N=128).  Pages stream through
-//     a ring of K-chunks (one 64-column box of both pages, 16 KB).  Four warps run the softmax,
-//     write P (bf16, 16 KB per page) into local shared memory, and ship it to the value CTA
-//     with asynchronous bulk copies that complete the peer's barrier by byte count.
+//     q_R in shared memory (16 KB); the scores of four pages at a time go to the other 256
+//     TMEM columns, one N=256 MMA per K step.  At N=256 each MMA carries 128 cycles of tensor
+//     work, which hides the issuing thread's own overhead (its warp shares an SM sub-partition
+//     with softmax warps); at N=64 the single issuing thread, not the tensor pipe, was the limit.
+//     Pages stream through a ring of K-chunks (one 64-column box of four pages, 32 KB).  Eight
+//     softmax warps in two sets (pages 0-1 and 2-3 of a group) each pull two pages of scores
+//     into registers, free the score buffer at once, agree on the group's running max through
+//     shared memory, write P (bf16, 16 KB per page) into local shared memory, and ship it to
+//     the value CTA with asynchronous bulk copies that complete the peer's barrier by byte
+//     count.
 //   rank 1, the value CTA: O lives in TMEM (512 columns); per page it runs PV from P and its
 //     own copy of the page's 512 latent columns; four warps apply the (rare) rescales, zero
 //     the unused slots of a sequence's last page, and write the normalised output.
@@ -28,14 +32,19 @@
 // P values stay <= 2^8, and the final division by l makes the result exact whatever m is.
 //
 // Pipelines (all waits bounded; see ptx.cuh):
-//   kv_full/kv_empty[S]   TMA rings: 10 K-chunk stages in the score CTA, 3 page stages in the
+//   kv_full/kv_empty[S]   TMA rings: 5 K-chunk stages in the score CTA, 3 page stages in the
 //                         value CTA
-//   s_full/s_free[2]      two-page score buffers (score CTA)
+//   s_full/s_free         the four-page score buffer (score CTA)
 //   q_ready               query loaded into TMEM for an item (score CTA)
+//   stg_ready[4]          a staged P message is complete (four softmax warps of one set)
+//   stg_freed             counter, not a barrier: messages whose staging slot may be reused
+//                         (published by the shipper warp, which alone waits on msg_free)
 //   msg_full[2]           P + per-row statistics landed in the value CTA (bulk copies; armed
 //                         by the value CTA's MMA thread)
 //   msg_free[2]           PV using that P finished (value CTA's MMA commit, multicast to rank 0)
-//                         and the value CTA's four correction warps have read the statistics
+//                         and the value CTA's four correction warps have read the statistics.
+//   A parity wait is valid only while the awaited phase is the current one or the last
+//   completed one, so every barrier has waiters that follow all of its phases in order.
 //   o_drain[2]            every PV issued before a flagged tile has finished (value CTA's MMA
 //                         commit right before it waits o_ready)
 //   o_ready[2]            value CTA's correction warps finished a flagged tile (rescale O, zero
@@ -48,14 +57,16 @@
 namespace mla {
 namespace decode {
 
-constexpr int kThreads = 192;
-constexpr int kChunkStages = 10;
+constexpr int kThreads = 352;                     // producer, MMA, 8 softmax / 4 correction, shipper
+constexpr int kShipperWarp = 10;
+constexpr int kChunkStages = 4;
 constexpr int kValueStages = 3;
-constexpr int kMaxStages = 10;
+constexpr int kMaxStages = 4;
+constexpr int kStagingSlots = 4;                  // score CTA: P messages staged ahead of the peer
 constexpr int kBoxBytes = 64 * 128;               // 64 tokens x 64 bf16 columns
 constexpr int kBoxesPerRow = 9;                   // c_KV: 8 boxes, k_R: 1 box
-constexpr int kGroupPages = 2;                    // pages per score MMA (N = 128)
-constexpr int kChunkBytes = kGroupPages * kBoxBytes;  // one box column of a two-page group
+constexpr int kGroupPages = 4;                    // pages per score MMA (N = 256)
+constexpr int kChunkBytes = kGroupPages * kBoxBytes;  // one box column of a four-page group
 constexpr int kValueStageBytes = 8 * kBoxBytes;   // 65,536: c_KV only
 constexpr int kPBytes = 128 * 128;                // P: 128 heads x 64 tokens bf16
 // Per message statistics, one 272-byte block per softmax warp (32 heads): factor[32] (rescale
@@ -66,10 +77,14 @@ constexpr int kStatsWarpBytes = 128 + 128 + 16;
 constexpr int kStatsBytes = 4 * kStatsWarpBytes;
 constexpr int kPWarpBytes = kPBytes / 4;
 constexpr int kMsgBytes = kPBytes + kStatsBytes;
-// score CTA: q_R (K-major, 128-byte swizzle), the K-chunk ring, two local P staging buffers
+// score CTA: q_R (K-major, 128-byte swizzle), the K-chunk ring, the staging ring of P messages
+// and their statistics blocks
 constexpr int kOffQR = 0;
 constexpr int kOffChunks = kOffQR + 128 * 128;
 constexpr int kOffScoreStaging = kOffChunks + kChunkStages * kChunkBytes;
+constexpr int kOffStatsStaging = kOffScoreStaging + kStagingSlots * kPBytes;
+// score CTA: the two softmax sets exchange row maxima and partial sums here (double-buffered)
+constexpr int kOffXchg = kOffStatsStaging + kStagingSlots * kStatsBytes;
 // value CTA: stages, then two P buffers (1024-aligned, the MMA reads them)
 constexpr int kOffP = kValueStages * kValueStageBytes;
 // both CTAs: statistics (staging in the score CTA, destination in the value CTA)
@@ -87,13 +102,15 @@ enum Bar : int {
     kOReady0 = kMsgFull0 + 2,
     kODrain0 = kOReady0 + 2,
     kDrain = kODrain0 + 2,
-    kNumBars = kDrain + 1
+    kStgReady0 = kDrain + 1,
+    kNumBars = kStgReady0 + kStagingSlots
 };
 
 constexpr int kOffTmemHolder = kOffBars + 8 * kNumBars;
 constexpr int kOffAbort = kOffTmemHolder + 4;
-constexpr int kSmemBytes = ((kOffAbort + 4 + 127) / 128) * 128;
-static_assert(kOffScoreStaging + 2 * kPBytes <= kOffStats, "score staging overlaps the statistics");
+constexpr int kOffStgFreed = kOffAbort + 4;  // score CTA: messages whose staging slot may be reused
+constexpr int kSmemBytes = ((kOffStgFreed + 4 + 127) / 128) * 128;
+static_assert(kOffXchg + 4 * 2 * 128 * 4 <= kOffStats, "score staging overlaps the value CTA's statistics");
 static_assert(kChunkStages <= kMaxStages && kValueStages <= kMaxStages, "barrier slots per ring");
 static_assert(kOffBars % 8 == 0, "barriers need 8-byte alignment");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -101,10 +118,11 @@ static_assert(kStatsWarpBytes % 16 == 0 && kPWarpBytes % 16 == 0, "bulk copies m
 
 // TMEM columns
 constexpr uint32_t kQCol = 0;      // score CTA: q_abs, 256 columns (512 bf16 per lane)
-constexpr uint32_t kSCol = 256;    // score CTA: two 128-column score buffers (two pages each)
+constexpr uint32_t kSCol = 256;    // score CTA: the 256-column score buffer (four pages)
 constexpr uint32_t kTmemCols = 512;
 
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when the max grows by > 2^8
+constexpr uint32_t kSoftmaxBarrier = 1;    // named barrier of the eight softmax warps
 
 // Wait-cycle accounting for performance work, compiled only with MLA_DECODE_TRACE: each role
 // adds the SM cycles it spends in each wait to a local array and writes it to
@@ -214,8 +232,8 @@ __device__ __forceinline__ void run_producer(const CUtensorMap* tm, const Params
 
 // ---------------------------------------------------------------------------- score CTA
 
-// Streams this cluster's pages as K-chunks: chunk j of a two-page group holds 64-column box j
-// (boxes 0-7: c_KV, box 8: k_R) of the first page in rows 0-63 and of the second in rows 64-127.
+// Streams this cluster's pages as K-chunks: chunk j of a four-page group holds 64-column box j
+// (boxes 0-7: c_KV, box 8: k_R) of the group's pages in rows 0-63, 64-127, 128-191, 192-255.
 __device__ __forceinline__ void score_producer(const CUtensorMap* tm, const Params& p, int item_begin, int item_end,
                                                int items_off, uint32_t sbase, uint32_t bars, const dev::WaitCtx& w,
                                                int lane)
@@ -224,13 +242,13 @@ __device__ __forceinline__ void score_producer(const CUtensorMap* tm, const Para
     MLA_TRACE_DECL;
     const uint64_t policy = l2_policy_evict_normal();  // the value CTA reads these pages next
     if (lane == 0) tma_prefetch_desc(tm);
-    int c = 0;
+    int s = 0, phase = 0, c = 0;
     bool ok = true;
     for (int i = item_begin; i < item_end && ok; ++i) {
         const Item it = load_item(p.plan, items_off, i);
         const int32_t* bt = p.block_table + (int64_t)it.seq * p.max_pages;
         for (int pg0 = it.page_begin; pg0 < it.page_end && ok; pg0 += 32) {
-            const int n = min(32, it.page_end - pg0);  // even unless it ends the item
+            const int n = min(32, it.page_end - pg0);  // a multiple of 4 unless it ends the item
             int page = 0;
             if (lane < n) {
                 page = __ldg(bt + pg0 + lane);
@@ -238,20 +256,23 @@ __device__ __forceinline__ void score_producer(const CUtensorMap* tm, const Para
             }
             for (int j = 0; j < n && ok; j += kGroupPages) {
                 const int npg = min(kGroupPages, n - j);
-                const int pa = __shfl_sync(0xffffffffu, page, j);
-                const int pb = __shfl_sync(0xffffffffu, page, min(j + 1, 31));
+                int pages[kGroupPages];
+#pragma unroll
+                for (int q = 0; q < kGroupPages; ++q) pages[q] = __shfl_sync(0xffffffffu, page, min(j + q, 31));
                 if (lane == 0) {
                     for (int box = 0; box < kBoxesPerRow && ok; ++box, ++c) {
-                        const int s = c % kChunkStages;
                         if (c >= kChunkStages)
-                            ok = MLA_TIMED(1, wait_phase(bars + 8 * (kEmpty0 + s), c / kChunkStages - 1, w));
+                            ok = MLA_TIMED(1, wait_phase(bars + 8 * (kEmpty0 + s), phase - 1, w));
                         if (!ok) break;
                         const uint32_t full = bars + 8 * (kFull0 + s);
                         const uint32_t dst = sbase + kOffChunks + s * kChunkBytes;
                         mbar_arrive_expect_tx(full, npg * kBoxBytes);
                         // an out-of-range page id reads as zeros (TMA fills outside the tensor)
-                        tma_load_3d(dst, tm, full, 64 * box, 0, pa, policy);
-                        if (npg == 2) tma_load_3d(dst + kBoxBytes, tm, full, 64 * box, 0, pb, policy);
+                        for (int q = 0; q < npg; ++q) tma_load_3d(dst + q * kBoxBytes, tm, full, 64 * box, 0, pages[q], policy);
+                        if (++s == kChunkStages) {
+                            s = 0;
+                            ++phase;
+                        }
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -265,20 +286,19 @@ __device__ __forceinline__ void score_producer(const CUtensorMap* tm, const Para
     if (lane == 0) MLA_TRACE_FLUSH(0, 1, 0);
 }
 
-// QK of a two-page group: S[128 heads x N tokens] (N = 64 per page) accumulated over the nine
-// K-chunks: chunks 0-7 take q_abs from TMEM ("TS"), chunk 8 takes q_R from shared memory.
-// One thread issues everything, so the loop is kept to a handful of instructions per MMA:
-// descriptors are built once and advanced by constants (16-byte units in the low bits),
-// the ring position is a wrapping counter, and the nine chunks are unrolled.
+// QK of a four-page group: S[128 heads x N tokens] (N = 64 per page, 256 for a full group)
+// accumulated over the nine K-chunks: chunks 0-7 take q_abs from TMEM ("TS"), chunk 8 takes
+// q_R from shared memory.  Descriptors are built once and advanced by constants (16-byte
+// units in the low bits) and the ring position is a wrapping counter, so the one issuing
+// thread spends few instructions per MMA.
 __device__ __forceinline__ void score_mma(const Params& p, int item_begin, int item_end, int items_off, uint32_t sbase,
                                           uint32_t bars, uint32_t tmem, const dev::WaitCtx& w)
 {
     using namespace dev;
-    constexpr uint32_t idesc2 = idesc_bf16(128, 128, false, false);
-    constexpr uint32_t idesc1 = idesc_bf16(128, 64, false, false);
     const uint64_t chunk_desc0 = smem_desc(sbase + kOffChunks, 16, 1024);
     const uint64_t qr_desc = smem_desc(sbase + kOffQR, 16, 1024);
     const uint32_t full0 = bars + 8 * kFull0, empty0 = bars + 8 * kEmpty0;
+    const uint32_t d = tmem + kSCol;
     MLA_TRACE_DECL;
     int s = 0, phase = 0, G = 0, n_item = 0;
     for (int i = item_begin; i < item_end; ++i, ++n_item) {
@@ -286,10 +306,9 @@ __device__ __forceinline__ void score_mma(const Params& p, int item_begin, int i
         if (!MLA_TIMED(5, wait_phase(bars + 8 * kQReady, n_item, w))) goto out;
         tc_fence_after();
         for (int pg = it.page_begin; pg < it.page_end; pg += kGroupPages, ++G) {
-            const uint32_t idesc = (it.page_end - pg >= 2) ? idesc2 : idesc1;
-            const int buf = G & 1;
-            if (G >= 2 && !MLA_TIMED(4, wait_phase(bars + 8 * (kSFree0 + buf), (G >> 1) - 1, w))) goto out;
-            const uint32_t d = tmem + kSCol + 128 * buf;
+            const int npg = min(kGroupPages, it.page_end - pg);
+            const uint32_t idesc = idesc_bf16(128, 64 * npg, false, false);
+            if (G >= 1 && !MLA_TIMED(4, wait_phase(bars + 8 * kSFree0, G - 1, w))) goto out;
 #pragma unroll
             for (int box = 0; box < kBoxesPerRow; ++box) {
                 if (!MLA_TIMED(3, wait_phase(full0 + 8 * s, phase, w))) goto out;
@@ -313,7 +332,7 @@ __device__ __forceinline__ void score_mma(const Params& p, int item_begin, int i
                     ++phase;
                 }
             }
-            mma_commit(bars + 8 * (kSFull0 + buf));
+            mma_commit(bars + 8 * kSFull0);
         }
     }
 out:
@@ -324,18 +343,16 @@ out:
     MLA_TRACE_FLUSH(12, 12, 2);
 }
 
-// Query row of this thread: q_abs -> TMEM lane `row`, columns 0..255 (two bf16 per column, K
-// order); q_R -> row `row` of the K-major, 128-byte-swizzled q_R tile in shared memory.
-__device__ __forceinline__ void load_query(const Params& p, int seq, int row, uint32_t taddr, uint8_t* qr_smem)
+// The query of row `row`: softmax set 0 writes q_abs dims 0..255 to TMEM columns 0..127 of lane
+// `row` and q_R to row `row` of the K-major, 128-byte-swizzled q_R tile in shared memory; set 1
+// writes q_abs dims 256..511 to columns 128..255.
+__device__ __forceinline__ void load_query(const Params& p, int seq, int row, int set, uint32_t taddr,
+                                           uint8_t* qr_smem)
 {
     using namespace dev;
-    const uint4* qa = reinterpret_cast<const uint4*>(p.q_abs + ((int64_t)seq * 128 + row) * 512);
-    const uint4* qr = reinterpret_cast<const uint4*>(p.q_r + ((int64_t)seq * 128 + row) * 64);
-    uint4 r8[8];
+    const uint4* qa = reinterpret_cast<const uint4*>(p.q_abs + ((int64_t)seq * 128 + row) * 512) + 32 * set;
 #pragma unroll
-    for (int v = 0; v < 8; ++v) r8[v] = __ldg(qr + v);
-#pragma unroll
-    for (int c0 = 0; c0 < 8; c0 += 2) {
+    for (int c0 = 0; c0 < 4; c0 += 2) {
         uint4 x[16];
 #pragma unroll
         for (int v = 0; v < 16; ++v) x[v] = __ldg(qa + 8 * c0 + v);
@@ -349,14 +366,130 @@ __device__ __forceinline__ void load_query(const Params& p, int seq, int row, ui
                 r[4 * v + 2] = x[8 * cc + v].z;
                 r[4 * v + 3] = x[8 * cc + v].w;
             }
-            tmem_st32(taddr + kQCol + 32 * (c0 + cc), r);
+            tmem_st32(taddr + kQCol + 128 * set + 32 * (c0 + cc), r);
         }
     }
-    uint8_t* dst = qr_smem + (row >> 3) * 1024 + (row & 7) * 128;
+    if (set == 0) {
+        const uint4* qr = reinterpret_cast<const uint4*>(p.q_r + ((int64_t)seq * 128 + row) * 64);
+        uint8_t* dst = qr_smem + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
-    for (int v = 0; v < 8; ++v) *reinterpret_cast<uint4*>(dst + ((v ^ (row & 7)) << 4)) = r8[v];
-    fence_proxy_async_cta();  // read by the MMA (async proxy)
+        for (int v = 0; v < 8; ++v) *reinterpret_cast<uint4*>(dst + ((v ^ (row & 7)) << 4)) = __ldg(qr + v);
+        fence_proxy_async_cta();  // read by the MMA (async proxy)
+    }
     tmem_wait_st();
+}
+
+// Softmax of one page held in registers: masks slots past the sequence end, p = 2^(s * scale *
+// log2(e) - m) (one FMA and one MUFU.EX2 per score), and writes P as bf16 straight into this
+// thread's row of the swizzled staging tile (16-byte chunk c of the row goes to chunk c ^ (row
+// & 7)).  Returns the row sum of p.
+__device__ __forceinline__ float page_softmax(uint32_t (&sr)[64], int valid, float scale_log2, float m_used,
+                                              uint8_t* stage_row, int row)
+{
+    using namespace dev;
+    if (valid < 64) {
+#pragma unroll
+        for (int j = 0; j < 64; ++j)
+            if (j >= valid) sr[j] = __float_as_uint(-INFINITY);
+    }
+    float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int j = 8 * c + 2 * q;
+            const float p0 = ex2_approx(fmaf(__uint_as_float(sr[j]), scale_log2, -m_used));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(sr[j + 1]), scale_log2, -m_used));
+            pk[q] = pack_bf16x2(p0, p1);
+            l8[(2 * q) & 7] += p0;
+            l8[(2 * q + 1) & 7] += p1;
+        }
+        *reinterpret_cast<uint4*>(stage_row + ((c ^ (row & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+    return ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+}
+
+// Row max of a page's raw scores (slots past the sequence end excluded), 8-way tree.
+__device__ __forceinline__ float page_max(const uint32_t (&sr)[64], int valid)
+{
+    float m8[8];
+#pragma unroll
+    for (int a = 0; a < 8; ++a) m8[a] = (a < valid) ? __uint_as_float(sr[a]) : -INFINITY;
+#pragma unroll
+    for (int j = 8; j < 64; ++j) m8[j & 7] = fmaxf(m8[j & 7], (j < valid) ? __uint_as_float(sr[j]) : -INFINITY);
+    return fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+}
+
+// Finish this warp's part of staged message `slot`: its statistics block (per-row O rescale
+// factor, 1/l on the item's last page, flags), then mark the warp's share ready for the shipper.
+__device__ __forceinline__ void stage_message(uint8_t* smem, uint32_t bars, int slot, int q4, int lane, float factor,
+                                              float inv_l, bool last, bool tail)
+{
+    using namespace dev;
+    float* stats = reinterpret_cast<float*>(smem + kOffStatsStaging + slot * kStatsBytes + q4 * kStatsWarpBytes);
+    stats[lane] = factor;
+    if (last) stats[32 + lane] = inv_l;
+    const bool any_rescale = __any_sync(0xffffffffu, factor != 1.f);
+    if (lane == 0) reinterpret_cast<uint32_t*>(stats)[64] = (any_rescale ? 1u : 0u) | (tail ? 2u : 0u);
+    fence_proxy_async_cta();  // the staged P and statistics are read by the shipper's bulk copies
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars + 8 * (kStgReady0 + slot));
+}
+
+// Shipper (one thread): sends the staged messages in order to the value CTA, two bulk copies
+// each (P, statistics) that complete the peer's msg_full barrier by byte count.  It alone waits
+// on msg_free, follows all of its phases, and publishes how many messages the value CTA has
+// consumed, which frees their staging slots for the softmax warps.
+__device__ __forceinline__ void score_shipper(const Params& p, int item_begin, int item_end, int items_off,
+                                              uint8_t* smem, uint32_t sbase, uint32_t bars, const dev::WaitCtx& w)
+{
+    using namespace dev;
+    const uint32_t r_p = map_to_cta(sbase + kOffP, 1);
+    const uint32_t r_stats = map_to_cta(sbase + kOffStats, 1);
+    const uint32_t r_msg_full = map_to_cta(bars + 8 * kMsgFull0, 1);
+    uint32_t* freed = reinterpret_cast<uint32_t*>(smem + kOffStgFreed);
+    int m = 0;
+    for (int i = item_begin; i < item_end; ++i) {
+        const Item it = load_item(p.plan, items_off, i);
+        for (int t = it.page_begin; t < it.page_end; ++t, ++m) {
+            const int slot = m % kStagingSlots, buf = m & 1;
+            if (!wait_phase(bars + 8 * (kStgReady0 + slot), m / kStagingSlots, w)) goto out;
+            if (m >= 2) {
+                if (!wait_phase<true>(bars + 8 * (kMsgFree0 + buf), (m >> 1) - 1, w)) goto out;
+                st_release_u32(freed, (uint32_t)(m - 1));  // messages 0 .. m-2 consumed
+            }
+            const uint32_t bar = r_msg_full + 8 * buf;
+            bulk_copy_to_cta(r_p + buf * kPBytes, sbase + kOffScoreStaging + slot * kPBytes, kPBytes, bar);
+            bulk_copy_to_cta(r_stats + buf * kStatsBytes, sbase + kOffStatsStaging + slot * kStatsBytes,
+                             kStatsBytes, bar);
+        }
+    }
+    // the value CTA's last commits and arrivals land in this CTA: wait for them before it ends
+    for (int k = (m > 2 ? m - 2 : 0); k < m; ++k)
+        if (!wait_phase<true>(bars + 8 * (kMsgFree0 + (k & 1)), k >> 1, w)) break;
+out:
+    return;
+}
+
+// Wait (bounded) until at least `target` staged messages have been consumed; warp-uniform.
+__device__ __forceinline__ bool wait_freed(const uint32_t* freed, uint32_t target, const dev::WaitCtx& w)
+{
+    using namespace dev;
+    bool ok = ld_acquire_u32(freed) >= target;
+    if (!ok && !*w.abort) {
+        const uint64_t t0 = globaltimer_ns();
+        while (true) {
+            if (ld_acquire_u32(freed) >= target) { ok = true; break; }
+            if (*w.abort) break;
+            if (globaltimer_ns() - t0 > w.timeout_ns) {
+                *w.abort = 1;
+                raise_error(w.dev_error, MLA_DEVERR_TIMEOUT);
+                break;
+            }
+        }
+    }
+    return __all_sync(0xffffffffu, ok);
 }
 
 __device__ __forceinline__ void score_softmax(const Params& p, int item_begin, int item_end, int items_off,
@@ -365,120 +498,112 @@ __device__ __forceinline__ void score_softmax(const Params& p, int item_begin, i
 {
     using namespace dev;
     const int q4 = warp & 3, row = 32 * q4 + lane;
+    const int set = (warp - 2) >> 2;               // 0: pages 0-1 of a group, 1: pages 2-3
     const bool leader = (warp == 2 && lane == 0);  // writes the wait-cycle trace, if enabled
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
-    // addresses in the value CTA (rank 1)
-    const uint32_t r_p = map_to_cta(sbase + kOffP, 1);
-    const uint32_t r_stats = map_to_cta(sbase + kOffStats, 1);
-    const uint32_t r_msg_full = map_to_cta(bars + 8 * kMsgFull0, 1);
     const uint32_t p_row_off = (uint32_t)((row >> 3) * 1024 + (row & 7) * 128);
+    const uint32_t* freed = reinterpret_cast<const uint32_t*>(smem + kOffStgFreed);
+    float* xchg = reinterpret_cast<float*>(smem + kOffXchg);  // [slot 2][kind 2: max, l][set 2][128]
     MLA_TRACE_DECL;
-    int g = 0, G = 0;  // pages (messages) and two-page groups
+    int g = 0, G = 0;  // pages (messages) and four-page groups
     for (int i = item_begin; i < item_end; ++i) {
         const Item it = load_item(p.plan, items_off, i);
         [[maybe_unused]] const long long tq0 = MLA_TRACE_NOW();
-        load_query(p, it.seq, row, tmem + lane_off, smem + kOffQR);
+        load_query(p, it.seq, row, set, tmem + lane_off, smem + kOffQR);
         tc_fence_before();
-        mbar_arrive(bars + 8 * kQReady);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars + 8 * kQReady);
         MLA_TRACE_ADD(9, MLA_TRACE_NOW() - tq0);
-        float m_used = -INFINITY, l = 0.f;
+        float m_used = -INFINITY, l_mine = 0.f, l_total = 0.f;
         for (int pg = it.page_begin; pg < it.page_end; pg += kGroupPages, ++G) {
             const int npg = min(kGroupPages, it.page_end - pg);
-            const int sbuf = G & 1;
-            if (!MLA_TIMED(7, wait_warp(bars + 8 * (kSFull0 + sbuf), G >> 1, w))) return;
-            tc_fence_after();
-            for (int pp = 0; pp < npg; ++pp, ++g) {
-                const int t = pg + pp;
-                const int buf = g & 1;
-                const int valid = min(64, it.seq_len - 64 * t);
-                const bool last = (t == it.page_end - 1);
-                [[maybe_unused]] const long long tc0 = MLA_TRACE_NOW();
-                uint32_t sr[64];
-                const uint32_t scol = tmem + lane_off + kSCol + 128 * sbuf + 64 * pp;
-                tmem_ld32(scol, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-                tmem_ld32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-                tmem_wait_ld();
-                MLA_TRACE_ADD(11, MLA_TRACE_NOW() - tc0);
-                if (pp == npg - 1) {  // both pages of the group are in registers or done
-                    [[maybe_unused]] const long long ta0 = MLA_TRACE_NOW();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bars + 8 * (kSFree0 + sbuf));
-                    MLA_TRACE_ADD(13, MLA_TRACE_NOW() - ta0);
-                }
-
-                // slots past the sequence end score -inf (their p is exactly 0)
-                if (valid < 64) {
-#pragma unroll
-                    for (int j = 0; j < 64; ++j)
-                        if (j >= valid) sr[j] = __float_as_uint(-INFINITY);
-                }
-                // row max of the raw scores (softmax_scale > 0 commutes with max), 8-way tree
-                float m8[8];
-#pragma unroll
-                for (int a = 0; a < 8; ++a) m8[a] = __uint_as_float(sr[a]);
-#pragma unroll
-                for (int j = 8; j < 64; ++j) m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(sr[j]));
-                const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * p.scale_log2;
-                float factor = 1.f;
-                if (mx > m_used + kRescaleThreshold) {
-                    if (t != it.page_begin) {
-                        factor = ex2_approx(m_used - mx);
-                        l *= factor;
+            const int n_mine = max(0, min(2, npg - 2 * set));
+            const bool last_group = (pg + kGroupPages >= it.page_end);
+            float* xs = xchg + (G & 1) * 2 * 2 * 128;
+            // Both sets must reach every named barrier below the same number of times: a failed
+            // (timed-out) wait only clears `ok`, and each barrier ORs the abort state so that the
+            // two sets leave together.
+            bool ok = MLA_TIMED(7, wait_warp(bars + 8 * kSFull0, G, w));
+            [[maybe_unused]] const long long tc0 = MLA_TRACE_NOW();
+            uint32_t sr[2][64];
+            const int t0 = pg + 2 * set;
+            const int valid0 = min(64, it.seq_len - 64 * t0), valid1 = min(64, it.seq_len - 64 * (t0 + 1));
+            float mx = -INFINITY;
+            if (ok) {
+                tc_fence_after();
+                if (n_mine > 0) {
+                    const uint32_t scol = tmem + lane_off + kSCol + 128 * set;
+                    tmem_ld32(scol, *reinterpret_cast<uint32_t(*)[32]>(&sr[0][0]));
+                    tmem_ld32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[0][32]));
+                    if (n_mine > 1) {
+                        tmem_ld32(scol + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[1][0]));
+                        tmem_ld32(scol + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[1][32]));
                     }
-                    m_used = mx;
+                    tmem_wait_ld();
                 }
-                // p = 2^(s * scale * log2(e) - m): one FMA and one MUFU.EX2 per score
-                uint32_t pk[32];
-                float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * j]), p.scale_log2, -m_used));
-                    const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * j + 1]), p.scale_log2, -m_used));
-                    pk[j] = pack_bf16x2(p0, p1);
-                    l8[j & 7] += p0 + p1;
-                }
-                l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
-                MLA_TRACE_ADD(14, MLA_TRACE_NOW() - tc0);
-
-                // the staging buffer and the peer's P buffer `buf` are free once PV(g-2) finished
-                if (g >= 2 && !MLA_TIMED(8, wait_warp<true>(bars + 8 * (kMsgFree0 + buf), (g >> 1) - 1, w))) return;
-                [[maybe_unused]] const long long tw0 = MLA_TRACE_NOW();
-                uint8_t* stage_p = smem + kOffScoreStaging + buf * kPBytes + p_row_off;
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<uint4*>(stage_p + ((c ^ (row & 7)) << 4)) =
-                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                const uint32_t stats_off = kOffStats + buf * kStatsBytes + q4 * kStatsWarpBytes;
-                float* stats = reinterpret_cast<float*>(smem + stats_off);
-                stats[lane] = factor;
-                if (last) stats[32 + lane] = 1.f / l;
-                const bool any_rescale = __any_sync(0xffffffffu, factor != 1.f);
-                if (lane == 0)
-                    reinterpret_cast<uint32_t*>(stats)[64] = (any_rescale ? 1u : 0u) | (valid < 64 ? 2u : 0u);
-                fence_proxy_async_cta();  // these generic writes are read by the bulk copies
+                tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    const uint32_t bar = r_msg_full + 8 * buf;
-                    // rows 32*q4 .. 32*q4+31 of P are one contiguous 4 KB slice of the swizzled tile
-                    bulk_copy_to_cta(r_p + buf * kPBytes + q4 * kPWarpBytes,
-                                     sbase + kOffScoreStaging + buf * kPBytes + q4 * kPWarpBytes, kPWarpBytes, bar);
-                    bulk_copy_to_cta(r_stats + (stats_off - kOffStats), sbase + stats_off, kStatsWarpBytes, bar);
-                }
+                if (lane == 0) mbar_arrive(bars + 8 * kSFree0);  // the next group's QK may start
+                MLA_TRACE_ADD(14, MLA_TRACE_NOW() - tc0);
+                if (n_mine > 0) mx = page_max(sr[0], valid0);
+                if (n_mine > 1) mx = fmaxf(mx, page_max(sr[1], valid1));
+            }
+            MLA_TRACE_ADD(11, MLA_TRACE_NOW() - tc0);
+
+            // group max, agreed between the two sets, drives the lazy rescale
+            xs[set * 128 + row] = mx * p.scale_log2;
+            if (MLA_TIMED(13, named_barrier_or(kSoftmaxBarrier, 256, !ok || *w.abort))) return;
+            const float gm = fmaxf(xs[row], xs[128 + row]);
+            float factor = 1.f;
+            if (gm > m_used + kRescaleThreshold) {
+                if (pg != it.page_begin) factor = ex2_approx(m_used - gm);
+                m_used = gm;
+            }
+            l_mine *= factor;
+
+            // P of my pages goes into staging slot (message % 4), free once the value CTA has
+            // consumed the message four before; every page but the item's last is handed to the
+            // shipper at once, the last waits for 1/l below
+            bool hold_last = false;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                if (j >= n_mine || !ok) break;
+                const int gg = g + 2 * set + j;
+                const int slot = gg % kStagingSlots;
+                if (gg >= kStagingSlots)
+                    ok = MLA_TIMED(8, wait_freed(freed, (uint32_t)(gg - kStagingSlots + 1), w));
+                if (!ok) break;
+                [[maybe_unused]] const long long tw0 = MLA_TRACE_NOW();
+                l_mine += page_softmax(sr[j], j ? valid1 : valid0, p.scale_log2, m_used,
+                                       smem + kOffScoreStaging + slot * kPBytes + p_row_off, row);
+                const float f_page = (set == 0 && j == 0) ? factor : 1.f;  // O rescale precedes page 0
+                if (t0 + j == it.page_end - 1)
+                    hold_last = true;
+                else
+                    stage_message(smem, bars, slot, q4, lane, f_page, 0.f, false, (j ? valid1 : valid0) < 64);
                 MLA_TRACE_ADD(10, MLA_TRACE_NOW() - tw0);
             }
+            if (last_group) {  // 1/l for the item's last page needs both sets' sums
+                xs[256 + set * 128 + row] = l_mine;
+                if (MLA_TIMED(13, named_barrier_or(kSoftmaxBarrier, 256, !ok || *w.abort))) return;
+                l_total = xs[256 + row] + xs[256 + 128 + row];
+                if (hold_last) {
+                    const int j = n_mine - 1;
+                    const int slot = (g + 2 * set + j) % kStagingSlots;
+                    const float f_page = (set == 0 && j == 0) ? factor : 1.f;
+                    stage_message(smem, bars, slot, q4, lane, f_page, 1.f / l_total, true, (j ? valid1 : valid0) < 64);
+                }
+            }
+            g += npg;
         }
-        const float lse_val = (m_used + log2f(l)) * 0.69314718055994531f;
-        if (it.slot < 0)
-            p.lse[(int64_t)it.seq * 128 + row] = lse_val;
-        else
-            p.ws_lse[(int64_t)it.slot * 128 + row] = lse_val;
+        if (set == 0) {
+            const float lse_val = (m_used + log2f(l_total)) * 0.69314718055994531f;
+            if (it.slot < 0)
+                p.lse[(int64_t)it.seq * 128 + row] = lse_val;
+            else
+                p.ws_lse[(int64_t)it.slot * 128 + row] = lse_val;
+        }
     }
-    // the value CTA's last commits arrive here, and the last bulk copies read this CTA's
-    // staging buffers: wait for both before this CTA can finish
-    for (int k = (g > 2 ? g - 2 : 0); k < g; ++k)
-        if (!wait_warp<true>(bars + 8 * (kMsgFree0 + (k & 1)), k >> 1, w)) return;
     if (leader) MLA_TRACE_FLUSH(6, 11, 6);
     if (leader) MLA_TRACE_FLUSH(13, 14, 6);
 }
@@ -669,7 +794,9 @@ done:
 
 // ---------------------------------------------------------------------------- kernel
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+// 11 warps: three SM sub-partitions hold three of them, and a sub-partition's 16K registers then
+// allow at most 3 x 32 x 168.
+__global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
 decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_pool, const Params p)
 {
     using namespace dev;
@@ -690,13 +817,15 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_pool, const Params p)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bars + 8 * (kSFull0 + b), 1);
-            mbar_init(bars + 8 * (kSFree0 + b), 4);        // one arrive per softmax warp
+            mbar_init(bars + 8 * (kSFree0 + b), 8);        // one arrive per softmax warp
             mbar_init(bars + 8 * (kMsgFree0 + b), 1 + 4);  // PV commit + four correction warps
             mbar_init(bars + 8 * (kMsgFull0 + b), 1);      // the MMA thread's arm + the copies' bytes
             mbar_init(bars + 8 * (kOReady0 + b), 128);
             mbar_init(bars + 8 * (kODrain0 + b), 1);
         }
-        mbar_init(bars + 8 * kQReady, 128);
+        mbar_init(bars + 8 * kQReady, 8);                  // one arrive per softmax warp
+        for (int s = 0; s < kStagingSlots; ++s) mbar_init(bars + 8 * (kStgReady0 + s), 4);  // one set's warps
+        *reinterpret_cast<volatile uint32_t*>(smem + kOffStgFreed) = 0;
         mbar_init(bars + 8 * kDrain, 1);
         int bad = misaligned ? 1 : 0;
         if (misaligned) raise_error(p.dev_error, MLA_DEVERR_SMEM_ALIGN);
@@ -728,6 +857,8 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_pool, const Params p)
                 score_producer(&tm_pool, p, item_begin, item_end, items_off, sbase, bars, w, lane);
             else if (warp == 1) {
                 if (lane == 0) score_mma(p, item_begin, item_end, items_off, sbase, bars, tmem, w);
+            } else if (warp == kShipperWarp) {
+                if (lane == 0) score_shipper(p, item_begin, item_end, items_off, smem, sbase, bars, w);
             } else
                 score_softmax(p, item_begin, item_end, items_off, smem, sbase, bars, tmem, w, warp, lane);
         } else {
@@ -736,7 +867,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_pool, const Params p)
                              kValueStageBytes, l2_policy_evict_first(), w, lane);
             else if (warp == 1) {
                 if (lane == 0) value_mma(p, item_begin, item_end, items_off, smem, sbase, bars, tmem, w);
-            } else
+            } else if (warp < 6)
                 value_correction(p, item_begin, item_end, items_off, smem, bars, tmem, w, warp, lane,
                                  threadIdx.x - 64);
         }
