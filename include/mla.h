@@ -169,6 +169,39 @@ MLA_API mla_status mla_combine_splits(const mla_plan_info* info, const void* pla
  *   out   device bf16 [batch][128][128].  Tensor cores (tcgen05), fp32 accumulation. */
 MLA_API mla_status mla_out_proj(const void* o_lat, const void* w_uv, void* out, int32_t batch, void* stream);
 
+/* ---------------------------------------------------------------- decode + merge, no allocation
+ *
+ * The pages describe no counterpart of this call: it is a convenience of this library.
+ * mla_decode_paged followed by mla_combine_splits, with the split-partial workspace taken from
+ * a fixed device array inside the library instead of from the caller.  The call allocates no
+ * device memory itself.  It is meant for callers that cannot allocate at the point of the call:
+ * code running inside a custom allocator's own callbacks (allocating there would re-enter the
+ * allocator), runtimes that reserve all device memory up front and forbid later allocation,
+ * and embedders with no caching allocator to take a workspace from.
+ *
+ * Arguments, layouts and results are those of mla_decode_paged (o_lat and lse end up final for
+ * every sequence, as after mla_combine_splits).
+ * Limit: the array holds MLA_STATIC_WS_MAX_PARTIALS split partials (MLA_STATIC_WS_BYTES bytes,
+ * about 33.6 MB, per device); a plan with more partials is rejected with MLA_ERR_WORKSPACE and
+ * the reason in mla_last_error_string().  Plan with fewer clusters, or use mla_decode_paged.
+ * Nothing in the array needs to start at zero: each call's decode launch writes every partial
+ * that its merge launch reads.
+ * Set-up: the first call on each device (with that device current) looks up the array's device
+ * address and, through it, loads the library module that holds the array; make that first call
+ * before any stream capture.
+ * One array per device: calls whose kernels may overlap (different streams, or several host
+ * threads on one device) race on it and corrupt each other's results.  Calls in order on one
+ * stream are safe. */
+#define MLA_STATIC_WS_MAX_PARTIALS 128
+#define MLA_STATIC_WS_BYTES ((size_t)MLA_STATIC_WS_MAX_PARTIALS * (128u * 512u * 4u + 128u * 4u))
+MLA_API mla_status mla_decode_paged_static_ws(const mla_plan_info* info, const void* plan_dev,
+                            const void* q_abs, const void* q_r,
+                            mla_kv_dtype kv_dtype, const void* kv_pool, const float* kv_scale,
+                            const void* kr_pool, int32_t num_pool_pages,
+                            const int32_t* block_table, int32_t max_pages_per_seq,
+                            float softmax_scale, void* o_lat, float* lse, uint32_t* dev_error,
+                            void* stream);
+
 /* ---------------------------------------------------------------- device error word
  *
  * Waits for `stream`, copies the device word to *host_bits (may be NULL) and returns

@@ -48,7 +48,11 @@ class PlanInfo(ctypes.Structure):
 
 
 EXPORTS = ("mla_status_string", "mla_last_error_string", "mla_plan_bytes_max", "mla_plan_splits", "mla_absorb_q", "mla_decode_paged",
-           "mla_combine_splits", "mla_out_proj", "mla_read_device_error", "mla_debug_wait_timeout")
+           "mla_combine_splits", "mla_out_proj", "mla_read_device_error", "mla_debug_wait_timeout",
+           "mla_decode_paged_static_ws")
+
+# capacity of the library's fixed split-partial array (mla_decode_paged_static_ws)
+MLA_STATIC_WS_MAX_PARTIALS = 128
 
 _lib = None
 
@@ -76,6 +80,9 @@ def lib() -> ctypes.CDLL:
     L.mla_decode_paged.restype = ctypes.c_int
     L.mla_decode_paged.argtypes = [ctypes.POINTER(PlanInfo), P, P, P, ctypes.c_int, P, P, P, i32, P, i32,
                                    ctypes.c_float, P, sz, P, P, u32p, P]
+    L.mla_decode_paged_static_ws.restype = ctypes.c_int
+    L.mla_decode_paged_static_ws.argtypes = [ctypes.POINTER(PlanInfo), P, P, P, ctypes.c_int, P, P, P, i32, P, i32,
+                                             ctypes.c_float, P, P, u32p, P]
     L.mla_combine_splits.restype = ctypes.c_int
     L.mla_combine_splits.argtypes = [ctypes.POINTER(PlanInfo), P, P, sz, P, P, P]
     L.mla_out_proj.restype = ctypes.c_int
@@ -95,7 +102,7 @@ def status_string(status: int) -> str:
 def _check(fn: str, status: int) -> None:
     if status != MLA_OK:
         msg = status_string(status)
-        if status == MLA_ERR_CUDA:
+        if status == MLA_ERR_CUDA or (status == MLA_ERR_WORKSPACE and fn == "mla_decode_paged_static_ws"):
             msg += ": " + lib().mla_last_error_string().decode()
         raise MlaError(fn, status, msg)
 
@@ -191,6 +198,45 @@ def mla_decode_paged(info: PlanInfo, plan_dev: torch.Tensor, q_abs: torch.Tensor
                                 int(block_table.shape[1]), float(softmax_scale), _ptr(workspace), ws_bytes,
                                 _ptr(o_lat), _ptr(lse), _ptr(dev_error), _stream(stream))
     _check("mla_decode_paged", st)
+
+
+def mla_decode_paged_static_ws(info: PlanInfo, plan_dev: torch.Tensor, q_abs: torch.Tensor, q_r: torch.Tensor, *,
+                               kv_pool: torch.Tensor, block_table: torch.Tensor, o_lat: torch.Tensor,
+                               lse: torch.Tensor, dev_error: torch.Tensor, kv_scale: Optional[torch.Tensor] = None,
+                               kr_pool: Optional[torch.Tensor] = None, softmax_scale: float = SOFTMAX_SCALE,
+                               stream=None) -> None:
+    """Decode plus split merge with the library's fixed scratch array: allocates nothing.
+    Calls that may overlap on one device race on that array (see include/mla.h)."""
+    B = q_abs.shape[0]
+    _need(plan_dev, "plan_dev", torch.int32)
+    _need(q_abs, "q_abs", torch.bfloat16, (B, NUM_HEADS, D_C))
+    _need(q_r, "q_r", torch.bfloat16, (B, NUM_HEADS, D_R))
+    _need(block_table, "block_table", torch.int32)
+    _need(o_lat, "o_lat", torch.bfloat16, (B, NUM_HEADS, D_C))
+    _need(lse, "lse", torch.float32, (B, NUM_HEADS))
+    _need(dev_error, "dev_error", torch.int32, (1,))
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be [batch, max_pages]")
+    dtype = _kv_dtype(kv_pool, kv_scale, kr_pool)
+    st = lib().mla_decode_paged_static_ws(ctypes.byref(info), _ptr(plan_dev), _ptr(q_abs), _ptr(q_r), dtype,
+                                          _ptr(kv_pool), _ptr(kv_scale), _ptr(kr_pool), int(kv_pool.shape[0]),
+                                          _ptr(block_table), int(block_table.shape[1]), float(softmax_scale),
+                                          _ptr(o_lat), _ptr(lse), _ptr(dev_error), _stream(stream))
+    _check("mla_decode_paged_static_ws", st)
+
+
+def _kv_dtype(kv_pool, kv_scale, kr_pool) -> int:
+    if kv_scale is None:
+        _need(kv_pool, "kv_pool", torch.bfloat16)
+        if kv_pool.dim() != 3 or tuple(kv_pool.shape[1:]) != (PAGE, D_ROW):
+            raise ValueError("bf16 kv_pool must be [pages, 64, 576]")
+        return MLA_KV_BF16
+    _need(kv_pool, "kv_pool (e4m3 codes)", torch.uint8)
+    if kv_pool.dim() != 3 or tuple(kv_pool.shape[1:]) != (PAGE, D_C):
+        raise ValueError("fp8 kv_pool must be [pages, 64, 512]")
+    _need(kv_scale, "kv_scale", torch.float32, (kv_pool.shape[0], PAGE))
+    _need(kr_pool, "kr_pool", torch.bfloat16, (kv_pool.shape[0], PAGE, D_R))
+    return MLA_KV_FP8_E4M3
 
 
 def mla_combine_splits(info: PlanInfo, plan_dev: torch.Tensor, workspace: Optional[torch.Tensor],

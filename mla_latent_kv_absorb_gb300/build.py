@@ -1,6 +1,6 @@
 """Build libmla_gb300.so in place with nvcc (sm_103a only).
 
-Run ``python -m mla_latent_kv_absorb_gb300.build`` or call ``build_library()``.  The two
+Run ``python -m mla_latent_kv_absorb_gb300.build`` or call ``build_library()``.  The
 translation units compile in parallel; the library links the CUDA runtime statically so it
 loads without a CUDA install on the library path (the driver is found at first use).
 """
@@ -30,7 +30,7 @@ def _nvcc() -> str:
 
 
 def _sources():
-    return [os.path.join(CSRC, "api.cu"), os.path.join(CSRC, "plan.cpp")]
+    return [os.path.join(CSRC, "api.cu"), os.path.join(CSRC, "static_ws.cu"), os.path.join(CSRC, "plan.cpp")]
 
 
 def _deps():

@@ -245,6 +245,11 @@ extern "C" mla_status mla_combine_splits(const mla_plan_info* info, const void* 
 
 extern "C" const char* mla_last_error_string(void) { return t_last_error; }
 
+namespace mla {
+// For the library's other translation units: replace this thread's last-error text.
+void set_last_error_text(const char* text) { snprintf(t_last_error, sizeof t_last_error, "%s", text); }
+}  // namespace mla
+
 extern "C" mla_status mla_read_device_error(const uint32_t* dev_error, uint32_t* host_bits, void* stream)
 {
     if (!dev_error) return MLA_ERR_INVALID_ARG;
