@@ -228,10 +228,10 @@ def run_ours(args, rank, world, local):
         binding.mla_out_proj(step.o_lat, step.w_uv, step.out, stream)
         evs[4].record(stream)
 
-    # warm-up: at least W steps and at least half a second of work so clocks settle
+    # warm-up: at least W steps and at least --min-warmup-s seconds of work so clocks settle
     t0 = time.perf_counter()
     n = 0
-    while n < args.warmup or time.perf_counter() - t0 < 0.5:
+    while n < args.warmup or time.perf_counter() - t0 < args.min_warmup_s:
         flush.fill_(n & 0xFF)
         one_step()
         n += 1
@@ -425,6 +425,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(synth.WORKLOADS), default="b16_s65536")
+    ap.add_argument("--min-warmup-s", type=float, default=0.5,
+                    help="keep warming up for at least this long (0: exactly --warmup steps, for profilers)")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-parity", dest="parity", action="store_false")

@@ -351,23 +351,18 @@ __device__ __forceinline__ void load_query(const Params& p, int seq, int row, in
 {
     using namespace dev;
     const uint4* qa = reinterpret_cast<const uint4*>(p.q_abs + ((int64_t)seq * 128 + row) * 512) + 32 * set;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
 #pragma unroll
-    for (int c0 = 0; c0 < 4; c0 += 2) {
-        uint4 x[16];
-#pragma unroll
-        for (int v = 0; v < 16; ++v) x[v] = __ldg(qa + 8 * c0 + v);
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-            uint32_t r[32];
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-                r[4 * v + 0] = x[8 * cc + v].x;
-                r[4 * v + 1] = x[8 * cc + v].y;
-                r[4 * v + 2] = x[8 * cc + v].z;
-                r[4 * v + 3] = x[8 * cc + v].w;
-            }
-            tmem_st32(taddr + kQCol + 128 * set + 32 * (c0 + cc), r);
+        for (int v = 0; v < 8; ++v) {
+            const uint4 x = __ldg(qa + 8 * c + v);
+            r[4 * v + 0] = x.x;
+            r[4 * v + 1] = x.y;
+            r[4 * v + 2] = x.z;
+            r[4 * v + 3] = x.w;
         }
+        tmem_st32(taddr + kQCol + 128 * set + 32 * c, r);
     }
     if (set == 0) {
         const uint4* qr = reinterpret_cast<const uint4*>(p.q_r + ((int64_t)seq * 128 + row) * 64);
@@ -449,14 +444,15 @@ __device__ __forceinline__ void score_shipper(const Params& p, int item_begin, i
     const uint32_t r_stats = map_to_cta(sbase + kOffStats, 1);
     const uint32_t r_msg_full = map_to_cta(bars + 8 * kMsgFull0, 1);
     uint32_t* freed = reinterpret_cast<uint32_t*>(smem + kOffStgFreed);
+    MLA_TRACE_DECL;
     int m = 0;
     for (int i = item_begin; i < item_end; ++i) {
         const Item it = load_item(p.plan, items_off, i);
         for (int t = it.page_begin; t < it.page_end; ++t, ++m) {
             const int slot = m % kStagingSlots, buf = m & 1;
-            if (!wait_phase(bars + 8 * (kStgReady0 + slot), m / kStagingSlots, w)) goto out;
+            if (!MLA_TIMED(14, wait_phase(bars + 8 * (kStgReady0 + slot), m / kStagingSlots, w))) goto out;
             if (m >= 2) {
-                if (!wait_phase<true>(bars + 8 * (kMsgFree0 + buf), (m >> 1) - 1, w)) goto out;
+                if (!MLA_TIMED(15, wait_phase<true>(bars + 8 * (kMsgFree0 + buf), (m >> 1) - 1, w))) goto out;
                 st_release_u32(freed, (uint32_t)(m - 1));  // messages 0 .. m-2 consumed
             }
             const uint32_t bar = r_msg_full + 8 * buf;
@@ -469,7 +465,7 @@ __device__ __forceinline__ void score_shipper(const Params& p, int item_begin, i
     for (int k = (m > 2 ? m - 2 : 0); k < m; ++k)
         if (!wait_phase<true>(bars + 8 * (kMsgFree0 + (k & 1)), k >> 1, w)) break;
 out:
-    return;
+    MLA_TRACE_FLUSH(14, 15, 0);
 }
 
 // Wait (bounded) until at least `target` staged messages have been consumed; warp-uniform.
@@ -605,7 +601,7 @@ __device__ __forceinline__ void score_softmax(const Params& p, int item_begin, i
         }
     }
     if (leader) MLA_TRACE_FLUSH(6, 11, 6);
-    if (leader) MLA_TRACE_FLUSH(13, 14, 6);
+    if (leader) MLA_TRACE_FLUSH(13, 13, 6);
 }
 
 // ---------------------------------------------------------------------------- value CTA
@@ -859,7 +855,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_pool, const Params p)
                 if (lane == 0) score_mma(p, item_begin, item_end, items_off, sbase, bars, tmem, w);
             } else if (warp == kShipperWarp) {
                 if (lane == 0) score_shipper(p, item_begin, item_end, items_off, smem, sbase, bars, w);
-            } else
+            } else if (warp >= 2 && warp < 10)
                 score_softmax(p, item_begin, item_end, items_off, smem, sbase, bars, tmem, w, warp, lane);
         } else {
             if (warp == 0)
