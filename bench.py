@@ -50,7 +50,10 @@ UNIT = "us/step"
 PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_PATH = os.path.join(ROOT, "profiles", "decode_traffic.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
-KERNEL_SOURCES = ["mla_latent_kv_absorb_gb300/csrc/decode.cuh", "mla_latent_kv_absorb_gb300/csrc/ptx.cuh"]
+KERNEL_SOURCES = {
+    "decode_bf16_kernel": ["mla_latent_kv_absorb_gb300/csrc/decode.cuh", "mla_latent_kv_absorb_gb300/csrc/ptx.cuh"],
+    "decode_fp8_kernel": ["mla_latent_kv_absorb_gb300/csrc/decode_fp8.cuh", "mla_latent_kv_absorb_gb300/csrc/ptx.cuh"],
+}
 
 
 # ----------------------------------------------------------------------------- distributed helpers
@@ -173,26 +176,29 @@ def load_peaks():
         return dict(FALLBACK_PEAKS)
 
 
-def kernel_hash() -> str:
+def kernel_hash(kernel: str = "decode_bf16_kernel") -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str, tokens: int):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was taken on the
-    current kernel source; scaled to this workload's tokens when captured on a smaller case."""
+def recorded_traffic(kernel: str, workload: str, tokens: int):
+    """DRAM bytes per decode launch from the committed ncu record of this kernel, if it was taken
+    on the current kernel source; scaled to this workload's tokens when captured on a smaller
+    case of the same kernel."""
     try:
         with open(TRAFFIC_PATH) as f:
-            t = json.load(f)
+            records = json.load(f)
     except (OSError, ValueError):
         return None
-    if t.get("kernel_hash") != kernel_hash():
-        return None
-    per_token = t["dram_bytes_per_launch"] / t["tokens"]
-    return per_token * tokens
+    if isinstance(records, dict):
+        records = [records]
+    for t in records:
+        if t.get("kernel") == kernel and t.get("kernel_hash") == kernel_hash(kernel):
+            return t["dram_bytes_per_launch"] / t["tokens"] * tokens
+    return None
 
 
 # ----------------------------------------------------------------------------- the GPU arm
@@ -274,7 +280,23 @@ def run_ours(args, rank, world, local):
     bw = peaks.get("hbm_gbs")
     tf = peaks.get("bf16_tflops")
     achieved_gbs = acc["decode_bytes"] / (decode_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(args.workload, acc["tokens"])
+    achieved_tfs = acc["decode_flop"] / (decode_ms * 1e-3) / 1e12
+    kernel_name = "decode_bf16_kernel" if inp.kv_dtype == "bf16" else "decode_fp8_kernel"
+    traffic = recorded_traffic(kernel_name, args.workload, acc["tokens"])
+    # the decode kernel's bound: whichever of its bytes and its (bf16 tensor-core) FLOPs takes
+    # longer at the measured peaks
+    if acc["decode_flop"] / (tf * 1e12) > acc["decode_bytes"] / (bw * 1e9):
+        roofline = {"bound": "tensor", "kernel": kernel_name, "achieved": round(achieved_tfs, 1), "peak": tf,
+                    "unit": "TFLOP/s", "frac": round(achieved_tfs / tf, 4),
+                    "traffic": None if traffic is None else int(traffic),
+                    "algorithmic_flop": acc["decode_flop"], "algorithmic_bytes": acc["decode_bytes"],
+                    "peak_source": peaks.get("source"), "hbm_frac": round(achieved_gbs / bw, 4)}
+    else:
+        roofline = {"bound": "hbm", "kernel": kernel_name, "achieved": round(achieved_gbs, 1), "peak": bw,
+                    "unit": "GB/s", "frac": round(achieved_gbs / bw, 4),
+                    "traffic": None if traffic is None else int(traffic),
+                    "algorithmic_bytes": acc["decode_bytes"], "peak_source": peaks.get("source"),
+                    "tensor_frac": round(achieved_tfs / tf, 4)}
     step_roof_us = max(acc["step_bytes"] / (bw * 1e9), acc["step_flop"] / (tf * 1e12)) * 1e6
     decode_roof_us = max(acc["decode_bytes"] / (bw * 1e9), acc["decode_flop"] / (tf * 1e12)) * 1e6
     res = {
@@ -300,11 +322,7 @@ def run_ours(args, rank, world, local):
         "kv_tbps": round(acc["kv_bytes"] / (ms_max * 1e-3) / 1e12, 3),
         "step_tflops": round(acc["step_flop"] / (ms_max * 1e-3) / 1e12, 1),
         "decode_tflops": round(acc["decode_flop"] / (decode_ms * 1e-3) / 1e12, 1),
-        "roofline": {"bound": "hbm", "kernel": "decode_bf16_kernel", "achieved": round(achieved_gbs, 1),
-                     "peak": bw, "unit": "GB/s", "frac": round(achieved_gbs / bw, 4),
-                     "traffic": None if traffic is None else int(traffic),
-                     "algorithmic_bytes": acc["decode_bytes"], "peak_source": peaks.get("source"),
-                     "tensor_frac": round(acc["decode_flop"] / (decode_ms * 1e-3) / 1e12 / tf, 4)},
+        "roofline": roofline,
         "step_roofline_frac": round(step_roof_us / (ms_max * 1e3), 4),
         "decode_roofline_frac": round(decode_roof_us / (decode_ms * 1e3), 4),
         "clocks": clocks.summary(),
@@ -330,8 +348,10 @@ def sampled_parity(inp, out_dev):
     ref = oracle.out_proj(full, inp.w_uv)[:, heads, :]
     got = out_dev[:, heads, :].double().cpu().numpy()
     d = got - ref
-    return {"heads": heads, "max_abs": float(np.abs(d).max()),
-            "rel_l2": float(np.linalg.norm(d) / np.linalg.norm(ref)), "tol": {"max_abs": 2e-2, "rel_l2": 1e-2}}
+    tol = {"max_abs": 2e-2, "rel_l2": 1e-2} if inp.kv_dtype == "bf16" else {"max_abs": 5e-2, "rel_l2": 5e-2}
+    max_abs, rel = float(np.abs(d).max()), float(np.linalg.norm(d) / np.linalg.norm(ref))
+    return {"heads": heads, "max_abs": max_abs, "rel_l2": rel, "tol": tol,
+            "ok": bool(np.isfinite(got).all() and max_abs <= tol["max_abs"] and rel <= tol["rel_l2"])}
 
 
 def run_e2e(args, inp, step, binding, device, stream):

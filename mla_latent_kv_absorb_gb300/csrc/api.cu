@@ -11,6 +11,7 @@
 #include "../../include/mla.h"
 #include "combine.cuh"
 #include "decode.cuh"
+#include "decode_fp8.cuh"
 #include "head_gemm.cuh"
 #include "plan.h"
 
@@ -48,17 +49,24 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// bf16 tensor map with 128-byte swizzle.  dims/strides innermost first; strides in bytes for
-// dims 1.. (rank - 1 entries).
-bool make_map_bf16(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-                   const cuuint32_t* box)
+// Tiled tensor map.  dims/strides innermost first; strides in bytes for dims 1.. (rank - 1
+// entries).
+bool make_map(CUtensorMap* m, CUtensorMapDataType type, CUtensorMapSwizzle swizzle, const void* base, int rank,
+              const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return enc(m, type, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// bf16 tensor map with 128-byte swizzle.
+bool make_map_bf16(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                   const cuuint32_t* box)
+{
+    return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, CU_TENSOR_MAP_SWIZZLE_128B, base, rank, dims, strides, box);
 }
 
 // Text of the last CUDA failure seen by this host thread (thread-local: no shared state).
@@ -155,6 +163,52 @@ extern "C" __attribute__((visibility("default"))) int mla_debug_timeout_sites(un
 }
 #endif
 
+// The e4m3 cache: c8 [pages][64][512] bytes (64x64 boxes, no swizzle: the converter warps read
+// it), kr_pool [pages][64][64] bf16 (64x64 boxes, 128-byte swizzle: the MMA reads it), one fp32
+// scale per token.
+mla_status launch_decode_fp8(const mla_plan_info* info, const void* plan_dev, const void* q_abs, const void* q_r,
+                             const void* kv_pool, const float* kv_scale, const void* kr_pool, int32_t num_pool_pages,
+                             const int32_t* block_table, int32_t max_pages_per_seq, float softmax_scale,
+                             void* workspace, void* o_lat, float* lse, uint32_t* dev_error, void* stream)
+{
+    if (!aligned16(kr_pool) || (reinterpret_cast<uintptr_t>(kv_scale) & 3u)) return MLA_ERR_ALIGNMENT;
+    CUtensorMap tm_c8, tm_kr;
+    const cuuint64_t c_dims[3] = {512, 64, (cuuint64_t)num_pool_pages};
+    const cuuint64_t c_strides[2] = {512, 64 * 512};
+    const cuuint32_t c_box[3] = {64, 64, 1};
+    const cuuint64_t r_dims[3] = {64, 64, (cuuint64_t)num_pool_pages};
+    const cuuint64_t r_strides[2] = {64 * 2, 64 * 64 * 2};
+    const cuuint32_t r_box[3] = {64, 64, 1};
+    if (!make_map(&tm_c8, CU_TENSOR_MAP_DATA_TYPE_UINT8, CU_TENSOR_MAP_SWIZZLE_NONE, kv_pool, 3, c_dims, c_strides,
+                  c_box) ||
+        !make_map_bf16(&tm_kr, kr_pool, 3, r_dims, r_strides, r_box))
+        return MLA_ERR_CUDA;
+
+    mla::decode_fp8::Params p;
+    p.plan = static_cast<const int32_t*>(plan_dev);
+    p.q_abs = static_cast<const __nv_bfloat16*>(q_abs);
+    p.q_r = static_cast<const __nv_bfloat16*>(q_r);
+    p.block_table = block_table;
+    p.max_pages = max_pages_per_seq;
+    p.num_pool_pages = num_pool_pages;
+    p.scale_log2 = softmax_scale * 1.4426950408889634f;
+    p.o_lat = static_cast<__nv_bfloat16*>(o_lat);
+    p.lse = lse;
+    p.ws_o = static_cast<float*>(workspace);
+    p.ws_lse = workspace ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                    (size_t)info->num_partials * mla::kPartialOBytes)
+                         : nullptr;
+    p.dev_error = dev_error;
+    p.timeout_ns = (uint64_t)info->wait_timeout_ns;
+    p.kv_scale = kv_scale;
+
+    if (!set_smem(mla::decode_fp8::decode_fp8_kernel, mla::decode_fp8::kSmemBytes)) return MLA_ERR_CUDA;
+    mla::decode_fp8::decode_fp8_kernel<<<2 * info->num_clusters, mla::decode_fp8::kThreads,
+                                         mla::decode_fp8::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(tm_c8, tm_kr,
+                                                                                                            p);
+    return launch_status();
+}
+
 extern "C" mla_status mla_absorb_q(const void* q_c, const void* w_uk, void* q_abs, int32_t batch, void* stream)
 {
     if (!q_c || !w_uk || !q_abs || batch <= 0) return MLA_ERR_INVALID_ARG;
@@ -190,7 +244,9 @@ extern "C" mla_status mla_decode_paged(const mla_plan_info* info, const void* pl
         if (!workspace || workspace_bytes < (size_t)info->workspace_bytes) return MLA_ERR_WORKSPACE;
         if (!aligned16(workspace)) return MLA_ERR_ALIGNMENT;
     }
-    if (kv_dtype == MLA_KV_FP8_E4M3) return MLA_ERR_UNSUPPORTED;  // fp8 gather: separate kernel
+    if (kv_dtype == MLA_KV_FP8_E4M3)
+        return launch_decode_fp8(info, plan_dev, q_abs, q_r, kv_pool, kv_scale, kr_pool, num_pool_pages, block_table,
+                                 max_pages_per_seq, softmax_scale, workspace, o_lat, lse, dev_error, stream);
 
     CUtensorMap tm_pool;
     const cuuint64_t dims[3] = {576, 64, (cuuint64_t)num_pool_pages};

@@ -88,6 +88,11 @@ def test_decode_rejects_bad_args(L):
     # fp8 without its scale / k_R pools
     assert _decode(L, info, ws=0x90000, ws_bytes=info.workspace_bytes,
                    dtype=binding.MLA_KV_FP8_E4M3) == binding.MLA_ERR_INVALID_ARG
+    # fp8 with a misaligned k_R pool or scale array
+    assert _decode(L, info, ws=0x90000, ws_bytes=info.workspace_bytes, dtype=binding.MLA_KV_FP8_E4M3,
+                   kv_scale=0xA0000, kr=0xB0008) == binding.MLA_ERR_ALIGNMENT
+    assert _decode(L, info, ws=0x90000, ws_bytes=info.workspace_bytes, dtype=binding.MLA_KV_FP8_E4M3,
+                   kv_scale=0xA0002, kr=0xB0000) == binding.MLA_ERR_ALIGNMENT
     # misaligned query
     assert _decode(L, info, ws=0x90000, ws_bytes=info.workspace_bytes, q_abs=0x10008) == binding.MLA_ERR_ALIGNMENT
     # workspace missing or too small

@@ -1,0 +1,100 @@
+"""GPU parity of the FP8 e4m3 latent cache (per-token fp32 scale, k_R in bf16) against the oracle.
+
+The oracle reads the dequantised cache, float(c8) * sigma, in fp64; the GPU rounds that
+product to bf16 before the tensor cores, so the FP8 tolerance (5e-2 max-abs and rel-L2)
+applies.  Tails of last pages are poisoned: e4m3 NaN codes, NaN scales, NaN k_R.
+"""
+import os
+import sys
+
+import numpy as np
+import pytest
+import torch
+
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+import oracle  # noqa: E402
+from parity_util import SCALE, TOL_FP8, assert_close, bf16_round  # noqa: E402
+
+from mla_latent_kv_absorb_gb300 import binding, synth  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+def _decode_only(inp, *, min_pages=0, max_clusters=0):
+    q_abs_bf16 = bf16_round(oracle.absorb_q(inp.q_c, inp.w_uk))
+    _, q_r, _, _, kv, bt = binding.inputs_to_device(inp, DEV)
+    plan, info = binding.mla_plan_splits(inp.seq_lens, binding.num_sms(), min_pages_per_split=min_pages,
+                                         max_clusters=max_clusters)
+    plan_dev = torch.from_numpy(plan).to(DEV)
+    B = inp.batch
+    o_lat = torch.full((B, 128, 512), float("nan"), dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((B, 128), float("nan"), dtype=torch.float32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ws = torch.empty(max(info.workspace_bytes // 4, 4), dtype=torch.float32, device=DEV)
+    binding.mla_decode_paged(info, plan_dev, q_abs_bf16.to(DEV), q_r, block_table=bt, o_lat=o_lat, lse=lse,
+                             dev_error=err, workspace=ws, **kv)
+    binding.mla_combine_splits(info, plan_dev, ws, o_lat, lse)
+    torch.cuda.synchronize()
+    assert binding.mla_read_device_error(err) == 0
+    return o_lat, lse, info, q_abs_bf16
+
+
+def _check_latent(inp, o_lat, lse, q_abs_bf16):
+    ref_o, ref_l = oracle.latent_attention(inp, q_abs_bf16.double().numpy(), softmax_scale=SCALE)
+    assert_close(o_lat, ref_o, TOL_FP8, "o_lat (fp8 cache)")
+    assert_close(lse, ref_l, TOL_FP8, "lse (fp8 cache)")
+
+
+@pytest.mark.parametrize("lens", [[1], [65], [700], [100, 37, 64 * 5], [129, 1, 2000, 63]])
+def test_fp8_decode_single_item(lens):
+    inp = synth.make_inputs(lens, seed=600 + len(lens), kv_dtype="fp8_e4m3", poison_tail=True)
+    o_lat, lse, info, q = _decode_only(inp, min_pages=10 ** 6)
+    assert info.num_combine == 0
+    _check_latent(inp, o_lat, lse, q)
+
+
+@pytest.mark.parametrize("lens,min_pages", [([4000], 1), ([64 * 40 + 5, 1, 9000], 2), ([100] * 200, 1)])
+def test_fp8_decode_split_and_merge(lens, min_pages):
+    inp = synth.make_inputs(lens, seed=700 + len(lens), kv_dtype="fp8_e4m3", poison_tail=True)
+    o_lat, lse, info, q = _decode_only(inp, min_pages=min_pages)
+    _check_latent(inp, o_lat, lse, q)
+
+
+def test_fp8_few_clusters_many_items():
+    lens = [70, 1, 640, 129, 3, 64, 2000, 65]
+    inp = synth.make_inputs(lens, seed=801, kv_dtype="fp8_e4m3", poison_tail=True)
+    o_lat, lse, info, q = _decode_only(inp, min_pages=1, max_clusters=2)
+    assert info.num_clusters == 2 and info.num_items >= len(lens)
+    _check_latent(inp, o_lat, lse, q)
+
+
+def test_fp8_end_to_end_naive_small():
+    """B=3 mixed lengths, the whole step against the naive (decompressed) oracle."""
+    inp = synth.make_inputs([300, 2048, 77], seed=802, kv_dtype="fp8_e4m3", poison_tail=True)
+    q_c, q_r, w_uk, w_uv, kv, bt = binding.inputs_to_device(inp, DEV)
+    step = binding.DecodeStep(inp.seq_lens, w_uk=w_uk, w_uv=w_uv, block_table=bt, min_pages_per_split=4, **kv)
+    out = step.run(q_c, q_r)
+    torch.cuda.synchronize()
+    assert step.device_error() == 0
+    ref = oracle.decode_naive(inp, softmax_scale=SCALE)
+    assert_close(out, ref, TOL_FP8, "out vs naive oracle (fp8 cache)")
+
+
+def test_fp8_end_to_end_b128_s8192_sampled():
+    """B=128, S=8192, e4m3 cache: the FP8 workload at full size; the oracle computes three heads
+    of every sequence."""
+    inp = synth.make_workload("b128_s8192_fp8")
+    q_c, q_r, w_uk, w_uv, kv, bt = binding.inputs_to_device(inp, DEV)
+    step = binding.DecodeStep(inp.seq_lens, w_uk=w_uk, w_uv=w_uv, block_table=bt, **kv)
+    out = step.run(q_c, q_r)
+    torch.cuda.synchronize()
+    assert step.device_error() == 0
+    heads = [0, 64, 127]
+    q_abs = oracle.absorb_q(inp.q_c, inp.w_uk)
+    o, _ = oracle.latent_attention(inp, q_abs, softmax_scale=SCALE, heads=heads)
+    full = np.zeros((inp.batch, 128, 512))
+    full[:, heads, :] = o
+    ref = oracle.out_proj(full, inp.w_uv)[:, heads, :]
+    assert_close(out[:, heads, :], ref, TOL_FP8, "out (3 heads, fp8 cache)")
