@@ -32,17 +32,21 @@
 // P values stay <= 2^8, and the final division by l makes the result exact whatever m is.
 //
 // Pipelines (all waits bounded; see ptx.cuh):
-//   kv_full/kv_empty[S]   TMA rings: 5 K-chunk stages in the score CTA, 3 page stages in the
+//   kv_full/kv_empty[S]   TMA rings: 4 K-chunk stages in the score CTA, 2 page stages in the
 //                         value CTA
 //   s_full/s_free         the four-page score buffer (score CTA)
 //   q_ready               query loaded into TMEM for an item (score CTA)
 //   stg_ready[4]          a staged P message is complete (four softmax warps of one set)
 //   stg_freed             counter, not a barrier: messages whose staging slot may be reused
-//                         (published by the shipper warp, which alone waits on msg_free)
-//   msg_full[2]           P + per-row statistics landed in the value CTA (bulk copies; armed
-//                         by the value CTA's MMA thread)
-//   msg_free[2]           PV using that P finished (value CTA's MMA commit, multicast to rank 0)
-//                         and the value CTA's four correction warps have read the statistics.
+//                         (published by the tracker thread, which alone waits on copied)
+//   msg_full[4]           P + per-row statistics landed in the value CTA (bulk copies; armed
+//                         by the value CTA's acknowledgement thread)
+//   copied[4]             (score CTA) message m has landed in the value CTA (acknowledgement
+//                         thread): its staging slot may be reused before PV has consumed it
+//   msg_free[4]           PV using that P finished (value CTA's MMA commit, multicast to rank 0)
+//                         and the value CTA's four correction warps have read the statistics:
+//                         the value CTA's buffer may take a new message.  Four message buffers
+//                         keep the DSMEM copy and PV round trip off the critical path.
 //   A parity wait is valid only while the awaited phase is the current one or the last
 //   completed one, so every barrier has waiters that follow all of its phases in order.
 //   o_drain[2]            every PV issued before a flagged tile has finished (value CTA's MMA
@@ -59,10 +63,12 @@ namespace decode {
 
 constexpr int kThreads = 352;                     // producer, MMA, 8 softmax / 4 correction, shipper
 constexpr int kShipperWarp = 10;
+constexpr int kAckWarp = 6;                       // value CTA: message acknowledgements
 constexpr int kChunkStages = 4;
-constexpr int kValueStages = 3;
+constexpr int kValueStages = 2;
 constexpr int kMaxStages = 4;
 constexpr int kStagingSlots = 4;                  // score CTA: P messages staged ahead of the peer
+constexpr int kMsgSlots = 4;                      // value CTA: P messages it can hold
 constexpr int kBoxBytes = 64 * 128;               // 64 tokens x 64 bf16 columns
 constexpr int kBoxesPerRow = 9;                   // c_KV: 8 boxes, k_R: 1 box
 constexpr int kGroupPages = 4;                    // pages per score MMA (N = 256)
@@ -85,11 +91,12 @@ constexpr int kOffScoreStaging = kOffChunks + kChunkStages * kChunkBytes;
 constexpr int kOffStatsStaging = kOffScoreStaging + kStagingSlots * kPBytes;
 // score CTA: the two softmax sets exchange row maxima and partial sums here (double-buffered)
 constexpr int kOffXchg = kOffStatsStaging + kStagingSlots * kStatsBytes;
-// value CTA: stages, then two P buffers (1024-aligned, the MMA reads them)
+// value CTA: stages, then the P buffers (1024-aligned, the MMA reads them) and their statistics
 constexpr int kOffP = kValueStages * kValueStageBytes;
-// both CTAs: statistics (staging in the score CTA, destination in the value CTA)
-constexpr int kOffStats = kOffP + 2 * kPBytes;
-constexpr int kOffBars = kOffStats + 2 * kStatsBytes;
+constexpr int kOffStats = kOffP + kMsgSlots * kPBytes;
+constexpr int kScoreEnd = kOffXchg + 4 * 2 * 128 * 4;
+constexpr int kValueEnd = kOffStats + kMsgSlots * kStatsBytes;
+constexpr int kOffBars = ((kScoreEnd > kValueEnd ? kScoreEnd : kValueEnd) + 7) / 8 * 8;
 
 enum Bar : int {
     kFull0 = 0,
@@ -98,8 +105,9 @@ enum Bar : int {
     kSFree0 = kSFull0 + 2,
     kQReady = kSFree0 + 2,
     kMsgFree0 = kQReady + 1,
-    kMsgFull0 = kMsgFree0 + 2,
-    kOReady0 = kMsgFull0 + 2,
+    kMsgFull0 = kMsgFree0 + kMsgSlots,
+    kCopied0 = kMsgFull0 + kMsgSlots,
+    kOReady0 = kCopied0 + kMsgSlots,
     kODrain0 = kOReady0 + 2,
     kDrain = kODrain0 + 2,
     kStgReady0 = kDrain + 1,
@@ -110,7 +118,7 @@ constexpr int kOffTmemHolder = kOffBars + 8 * kNumBars;
 constexpr int kOffAbort = kOffTmemHolder + 4;
 constexpr int kOffStgFreed = kOffAbort + 4;  // score CTA: messages whose staging slot may be reused
 constexpr int kSmemBytes = ((kOffStgFreed + 4 + 127) / 128) * 128;
-static_assert(kOffXchg + 4 * 2 * 128 * 4 <= kOffStats, "score staging overlaps the value CTA's statistics");
+static_assert(kOffP % 1024 == 0, "P buffers are MMA operands (1024-byte aligned)");
 static_assert(kChunkStages <= kMaxStages && kValueStages <= kMaxStages, "barrier slots per ring");
 static_assert(kOffBars % 8 == 0, "barriers need 8-byte alignment");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -432,10 +440,28 @@ __device__ __forceinline__ void stage_message(uint8_t* smem, uint32_t bars, int 
     if (lane == 0) mbar_arrive(bars + 8 * (kStgReady0 + slot));
 }
 
+// Staging tracker (one thread): follows every phase of copied, in message order, and publishes
+// how many messages have landed in the value CTA, which frees their staging slots for the
+// softmax warps.
+__device__ __forceinline__ void score_tracker(const Params& p, int item_begin, int item_end, int items_off,
+                                              uint8_t* smem, uint32_t bars, const dev::WaitCtx& w)
+{
+    using namespace dev;
+    uint32_t* freed = reinterpret_cast<uint32_t*>(smem + kOffStgFreed);
+    int k = 0;
+    for (int i = item_begin; i < item_end; ++i) {
+        const Item it = load_item(p.plan, items_off, i);
+        for (int t = it.page_begin; t < it.page_end; ++t, ++k) {
+            if (!wait_phase<true>(bars + 8 * (kCopied0 + k % kMsgSlots), k / kMsgSlots, w)) return;
+            st_release_u32(freed, (uint32_t)(k + 1));  // messages 0 .. k copied
+        }
+    }
+}
+
 // Shipper (one thread): sends the staged messages in order to the value CTA, two bulk copies
-// each (P, statistics) that complete the peer's msg_full barrier by byte count.  It alone waits
-// on msg_free, follows all of its phases, and publishes how many messages the value CTA has
-// consumed, which frees their staging slots for the softmax warps.
+// each (P, statistics) that complete the peer's msg_full barrier by byte count, once the value
+// CTA has finished with the message that last used the same buffer.  It alone waits on
+// msg_free and follows all of its phases.
 __device__ __forceinline__ void score_shipper(const Params& p, int item_begin, int item_end, int items_off,
                                               uint8_t* smem, uint32_t sbase, uint32_t bars, const dev::WaitCtx& w)
 {
@@ -443,18 +469,16 @@ __device__ __forceinline__ void score_shipper(const Params& p, int item_begin, i
     const uint32_t r_p = map_to_cta(sbase + kOffP, 1);
     const uint32_t r_stats = map_to_cta(sbase + kOffStats, 1);
     const uint32_t r_msg_full = map_to_cta(bars + 8 * kMsgFull0, 1);
-    uint32_t* freed = reinterpret_cast<uint32_t*>(smem + kOffStgFreed);
     MLA_TRACE_DECL;
     int m = 0;
     for (int i = item_begin; i < item_end; ++i) {
         const Item it = load_item(p.plan, items_off, i);
         for (int t = it.page_begin; t < it.page_end; ++t, ++m) {
-            const int slot = m % kStagingSlots, buf = m & 1;
+            const int slot = m % kStagingSlots, buf = m % kMsgSlots;
             if (!MLA_TIMED(14, wait_phase(bars + 8 * (kStgReady0 + slot), m / kStagingSlots, w))) goto out;
-            if (m >= 2) {
-                if (!MLA_TIMED(15, wait_phase<true>(bars + 8 * (kMsgFree0 + buf), (m >> 1) - 1, w))) goto out;
-                st_release_u32(freed, (uint32_t)(m - 1));  // messages 0 .. m-2 consumed
-            }
+            if (m >= kMsgSlots &&  // the value CTA is done with the message that last used buffer buf
+                !MLA_TIMED(15, wait_phase<true>(bars + 8 * (kMsgFree0 + buf), m / kMsgSlots - 1, w)))
+                goto out;
             const uint32_t bar = r_msg_full + 8 * buf;
             bulk_copy_to_cta(r_p + buf * kPBytes, sbase + kOffScoreStaging + slot * kPBytes, kPBytes, bar);
             bulk_copy_to_cta(r_stats + buf * kStatsBytes, sbase + kOffStatsStaging + slot * kStatsBytes,
@@ -462,8 +486,8 @@ __device__ __forceinline__ void score_shipper(const Params& p, int item_begin, i
         }
     }
     // the value CTA's last commits and arrivals land in this CTA: wait for them before it ends
-    for (int k = (m > 2 ? m - 2 : 0); k < m; ++k)
-        if (!wait_phase<true>(bars + 8 * (kMsgFree0 + (k & 1)), k >> 1, w)) break;
+    for (int k = (m > kMsgSlots ? m - kMsgSlots : 0); k < m; ++k)
+        if (!wait_phase<true>(bars + 8 * (kMsgFree0 + k % kMsgSlots), k / kMsgSlots, w)) break;
 out:
     MLA_TRACE_FLUSH(14, 15, 0);
 }
@@ -613,6 +637,27 @@ __device__ __forceinline__ uint32_t msg_flags(const uint8_t* smem, int buf)
     return f[64] | f[w + 64] | f[2 * w + 64] | f[3 * w + 64];
 }
 
+// Message acknowledgement (one thread of the value CTA): arms msg_full for each message in
+// order (expected bytes; the copies may land before or after) and, as soon as the message has
+// landed, tells the score CTA that its staging slot is free (copied).  Keeping this off the MMA
+// thread lets the score CTA reuse staging slots without waiting for PV.
+__device__ __forceinline__ void value_ack(const Params& p, int item_begin, int item_end, int items_off,
+                                          uint32_t bars, const dev::WaitCtx& w)
+{
+    using namespace dev;
+    const uint32_t r_copied = map_to_cta(bars + 8 * kCopied0, 0);
+    int g = 0;
+    for (int i = item_begin; i < item_end; ++i) {
+        const Item it = load_item(p.plan, items_off, i);
+        for (int t = it.page_begin; t < it.page_end; ++t, ++g) {
+            const int buf = g % kMsgSlots;
+            mbar_arrive_expect_tx(bars + 8 * (kMsgFull0 + buf), kMsgBytes);
+            if (!wait_phase<true>(bars + 8 * (kMsgFull0 + buf), g / kMsgSlots, w)) return;
+            mbar_arrive_remote(r_copied + 8 * buf);
+        }
+    }
+}
+
 __device__ __forceinline__ void value_mma(const Params& p, int item_begin, int item_end, int items_off,
                                           const uint8_t* smem, uint32_t sbase, uint32_t bars, uint32_t tmem,
                                           const dev::WaitCtx& w)
@@ -626,11 +671,9 @@ __device__ __forceinline__ void value_mma(const Params& p, int item_begin, int i
     for (int i = item_begin; i < item_end; ++i) {
         const Item it = load_item(p.plan, items_off, i);
         for (int t = it.page_begin; t < it.page_end; ++t, ++g) {
-            const int s = g % kValueStages, buf = g & 1;
+            const int s = g % kValueStages, buf = g % kMsgSlots;
             if (!MLA_TIMED(3, wait_phase(bars + 8 * (kFull0 + s), g / kValueStages, w))) goto out;
-            // expect this message's bytes (the copies may land before or after this)
-            mbar_arrive_expect_tx(bars + 8 * (kMsgFull0 + buf), kMsgBytes);
-            if (!MLA_TIMED(4, wait_phase<true>(bars + 8 * (kMsgFull0 + buf), g >> 1, w))) goto out;
+            if (!MLA_TIMED(4, wait_phase<true>(bars + 8 * (kMsgFull0 + buf), g / kMsgSlots, w))) goto out;
             // The correction warps go first on flagged tiles (rescale O, zero a tail) and on the
             // first tile of every item after the first (their epilogue still reads O, which this
             // PV overwrites).  Both sides apply the same rule, so o_ready phases stay paired.
@@ -716,8 +759,8 @@ __device__ __forceinline__ void value_correction(const Params& p, int item_begin
         const Item it = load_item(p.plan, items_off, i);
         float inv_l = 0.f;
         for (int t = it.page_begin; t < it.page_end; ++t, ++g) {
-            const int buf = g & 1;
-            if (!MLA_TIMED(7, wait_warp<true>(bars + 8 * (kMsgFull0 + buf), g >> 1, w))) goto done;
+            const int buf = g % kMsgSlots;
+            if (!MLA_TIMED(7, wait_warp<true>(bars + 8 * (kMsgFull0 + buf), g / kMsgSlots, w))) goto done;
             const float* stats =
                 reinterpret_cast<const float*>(smem + kOffStats + buf * kStatsBytes + q4 * kStatsWarpBytes);
             if (t == it.page_end - 1) inv_l = stats[32 + lane];
@@ -814,10 +857,13 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_pool, const Params p)
         for (int b = 0; b < 2; ++b) {
             mbar_init(bars + 8 * (kSFull0 + b), 1);
             mbar_init(bars + 8 * (kSFree0 + b), 8);        // one arrive per softmax warp
-            mbar_init(bars + 8 * (kMsgFree0 + b), 1 + 4);  // PV commit + four correction warps
-            mbar_init(bars + 8 * (kMsgFull0 + b), 1);      // the MMA thread's arm + the copies' bytes
             mbar_init(bars + 8 * (kOReady0 + b), 128);
             mbar_init(bars + 8 * (kODrain0 + b), 1);
+        }
+        for (int b = 0; b < kMsgSlots; ++b) {
+            mbar_init(bars + 8 * (kMsgFree0 + b), 1 + 4);  // PV commit + four correction warps
+            mbar_init(bars + 8 * (kMsgFull0 + b), 1);      // the MMA thread's arm + the copies' bytes
+            mbar_init(bars + 8 * (kCopied0 + b), 1);       // the value MMA thread saw the message land
         }
         mbar_init(bars + 8 * kQReady, 8);                  // one arrive per softmax warp
         for (int s = 0; s < kStagingSlots; ++s) mbar_init(bars + 8 * (kStgReady0 + s), 4);  // one set's warps
@@ -855,6 +901,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_pool, const Params p)
                 if (lane == 0) score_mma(p, item_begin, item_end, items_off, sbase, bars, tmem, w);
             } else if (warp == kShipperWarp) {
                 if (lane == 0) score_shipper(p, item_begin, item_end, items_off, smem, sbase, bars, w);
+                else if (lane == 1) score_tracker(p, item_begin, item_end, items_off, smem, bars, w);
             } else if (warp >= 2 && warp < 10)
                 score_softmax(p, item_begin, item_end, items_off, smem, sbase, bars, tmem, w, warp, lane);
         } else {
@@ -863,7 +910,9 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_pool, const Params p)
                              kValueStageBytes, l2_policy_evict_first(), w, lane);
             else if (warp == 1) {
                 if (lane == 0) value_mma(p, item_begin, item_end, items_off, smem, sbase, bars, tmem, w);
-            } else if (warp < 6)
+            } else if (warp == kAckWarp) {
+                if (lane == 0) value_ack(p, item_begin, item_end, items_off, bars, w);
+            } else if (warp >= 2 && warp < 6)
                 value_correction(p, item_begin, item_end, items_off, smem, bars, tmem, w, warp, lane,
                                  threadIdx.x - 64);
         }
