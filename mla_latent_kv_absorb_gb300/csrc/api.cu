@@ -19,12 +19,16 @@ namespace {
 
 using mla::gemm::Cfg;
 
-// absorb: K = 128 (d_hc), N tile 128 of 512 (d_c), W_UK is MN-major for the MMA
-constexpr int kAbsorbN = 128;
-using AbsorbCfg = Cfg<128, kAbsorbN, true, 2>;
-// out-proj: K = 512 (d_c), N tile 64 of 128 (d_hc), W_UV is K-major for the MMA
-constexpr int kOutN = 64;
-using OutCfg = Cfg<512, kOutN, false, 4>;
+// absorb: K = 128 (d_hc), N tile 256 of 512 (d_c), W_UK is MN-major for the MMA; 256 CTAs of
+// 96 KB (two per SM) run as one wave
+constexpr int kAbsorbN = 256;
+constexpr int kAbsorbStages = 2;
+using AbsorbCfg = Cfg<128, kAbsorbN, true, kAbsorbStages>;
+// out-proj: K = 512 (d_c), the whole head's N = 128 (d_hc) per CTA, W_UV is K-major for the MMA;
+// six of the eight K-chunks in flight, 128 CTAs of 192 KB (one wave)
+constexpr int kOutN = 128;
+constexpr int kOutStages = 6;
+using OutCfg = Cfg<512, kOutN, false, kOutStages>;
 
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 
@@ -213,14 +217,14 @@ extern "C" mla_status mla_absorb_q(const void* q_c, const void* w_uk, void* q_ab
 {
     if (!q_c || !w_uk || !q_abs || batch <= 0) return MLA_ERR_INVALID_ARG;
     if (!aligned16(q_c) || !aligned16(w_uk) || !aligned16(q_abs)) return MLA_ERR_ALIGNMENT;
-    return launch_head_gemm<128, kAbsorbN, true, 2>(q_c, w_uk, q_abs, batch, 512, 64, stream);
+    return launch_head_gemm<128, kAbsorbN, true, kAbsorbStages>(q_c, w_uk, q_abs, batch, 512, 64, stream);
 }
 
 extern "C" mla_status mla_out_proj(const void* o_lat, const void* w_uv, void* out, int32_t batch, void* stream)
 {
     if (!o_lat || !w_uv || !out || batch <= 0) return MLA_ERR_INVALID_ARG;
     if (!aligned16(o_lat) || !aligned16(w_uv) || !aligned16(out)) return MLA_ERR_ALIGNMENT;
-    return launch_head_gemm<512, kOutN, false, 4>(o_lat, w_uv, out, batch, 128, kOutN, stream);
+    return launch_head_gemm<512, kOutN, false, kOutStages>(o_lat, w_uv, out, batch, 128, kOutN, stream);
 }
 
 extern "C" mla_status mla_decode_paged(const mla_plan_info* info, const void* plan_dev, const void* q_abs,

@@ -4,8 +4,10 @@
 // Partial j of head h carries a normalised latent output o_j (512 fp32) and lse_j (natural
 // log).  The merge is the log-sum-exp identity:
 //   lse = log sum_j exp(lse_j),   o_lat = sum_j exp(lse_j - lse) * o_j.
-// One warp per (sequence, head): the lanes split the 512 dims 16 each, so every partial row is
-// read as 2 KB of coalesced float4 loads.  HBM/L2 bound: n_parts * 2 KB per (sequence, head).
+// One warp per (sequence, head): lane j holds partial j's log-sum-exp and merge weight (32
+// partials per pass), the lanes split the 512 dims 16 each, and the partial rows are read as
+// 2 KB of coalesced float4 loads, four partials at a time so the loads overlap.  HBM/L2 bound:
+// n_parts * 2 KB per (sequence, head).
 #pragma once
 #include "plan.h"
 #include "ptx.cuh"
@@ -37,16 +39,40 @@ combine_kernel(const int32_t* __restrict__ plan, const float* __restrict__ ws_o,
     float4 acc[4];
 #pragma unroll
     for (int v = 0; v < 4; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < n; ++j) {
-        const float wgt = expf(ws_lse[(int64_t)(first + j) * 128 + h] - L);
-        const float4* src = reinterpret_cast<const float4*>(ws_o + ((int64_t)(first + j) * 128 + h) * 512) + lane;
+    const float4* rows = reinterpret_cast<const float4*>(ws_o + ((int64_t)first * 128 + h) * 512) + lane;
+    constexpr int64_t kPartStride = 128 * 512 / 4;  // float4s between partial j and j + 1
+    for (int j0 = 0; j0 < n; j0 += 32) {
+        const int cnt = min(32, n - j0);
+        const float wj = lane < cnt ? expf(ws_lse[(int64_t)(first + j0 + lane) * 128 + h] - L) : 0.f;
+        int j = 0;
+        for (; j + 4 <= cnt; j += 4) {
+            float4 x[4][4];
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-            const float4 x = src[32 * v];
-            acc[v].x += wgt * x.x;
-            acc[v].y += wgt * x.y;
-            acc[v].z += wgt * x.z;
-            acc[v].w += wgt * x.w;
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int v = 0; v < 4; ++v) x[u][v] = rows[(j0 + j + u) * kPartStride + 32 * v];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float wgt = __shfl_sync(0xffffffffu, wj, j + u);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    acc[v].x += wgt * x[u][v].x;
+                    acc[v].y += wgt * x[u][v].y;
+                    acc[v].z += wgt * x[u][v].z;
+                    acc[v].w += wgt * x[u][v].w;
+                }
+            }
+        }
+        for (; j < cnt; ++j) {
+            const float wgt = __shfl_sync(0xffffffffu, wj, j);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const float4 x = rows[(j0 + j) * kPartStride + 32 * v];
+                acc[v].x += wgt * x.x;
+                acc[v].y += wgt * x.y;
+                acc[v].z += wgt * x.z;
+                acc[v].w += wgt * x.w;
+            }
         }
     }
     uint2* dst = reinterpret_cast<uint2*>(o_lat + ((int64_t)seq * 128 + h) * 512) + lane;

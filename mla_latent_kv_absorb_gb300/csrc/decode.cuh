@@ -147,6 +147,13 @@ constexpr int kTraceSlots = 16;
 #define MLA_TRACE_DECL long long tr_[kTraceSlots] = {0}; const long long tstart_ = clock64()
 #define MLA_TRACE_ADD(slot, v) (tr_[(slot)] += (v))
 #define MLA_TRACE_NOW() clock64()
+// Event timeline of cluster 0 (global timer, ns): trace[kEvBase + kind * kEvSlots + index].
+constexpr int kEvBase = 4096, kEvSlots = 512;
+#define MLA_EV(kind, idx)                                                                              \
+    do {                                                                                               \
+        if (p.trace && (blockIdx.x >> 1) == 0 && (idx) < kEvSlots)                                    \
+            p.trace[kEvBase + (kind) * kEvSlots + (idx)] = (long long)dev::globaltimer_ns();           \
+    } while (0)
 #define MLA_TRACE_FLUSH(first, last, total_slot)                                                    \
     do {                                                                                            \
         tr_[(total_slot)] = clock64() - tstart_;                                                    \
@@ -155,6 +162,7 @@ constexpr int kTraceSlots = 16;
     } while (0)
 #else
 #define MLA_TIMED(slot, expr) (expr)
+#define MLA_EV(kind, idx) do { } while (0)
 #define MLA_TRACE_DECL do { } while (0)
 #define MLA_TRACE_ADD(slot, v) do { } while (0)
 #define MLA_TRACE_NOW() 0LL
@@ -223,6 +231,7 @@ __device__ __forceinline__ void run_producer(const CUtensorMap* tm, const Params
                         mbar_arrive_expect_tx(full, boxes * kBoxBytes);
                         // an out-of-range page id reads as zeros (TMA fills outside the tensor)
                         for (int x = 0; x < boxes; ++x) tma_load_3d(dst + x * kBoxBytes, tm, full, 64 * x, 0, pj, policy);
+                        MLA_EV(13, g);
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -277,6 +286,7 @@ __device__ __forceinline__ void score_producer(const CUtensorMap* tm, const Para
                         mbar_arrive_expect_tx(full, npg * kBoxBytes);
                         // an out-of-range page id reads as zeros (TMA fills outside the tensor)
                         for (int q = 0; q < npg; ++q) tma_load_3d(dst + q * kBoxBytes, tm, full, 64 * box, 0, pages[q], policy);
+                        MLA_EV(0, c);
                         if (++s == kChunkStages) {
                             s = 0;
                             ++phase;
@@ -317,9 +327,11 @@ __device__ __forceinline__ void score_mma(const Params& p, int item_begin, int i
             const int npg = min(kGroupPages, it.page_end - pg);
             const uint32_t idesc = idesc_bf16(128, 64 * npg, false, false);
             if (G >= 1 && !MLA_TIMED(4, wait_phase(bars + 8 * kSFree0, G - 1, w))) goto out;
+            MLA_EV(3, G);
 #pragma unroll
             for (int box = 0; box < kBoxesPerRow; ++box) {
                 if (!MLA_TIMED(3, wait_phase(full0 + 8 * s, phase, w))) goto out;
+                MLA_EV(1, 9 * G + box);
                 tc_fence_after();
                 const uint64_t b0 = chunk_desc0 + (uint64_t)(s * (kChunkBytes >> 4));
                 if (box < 8) {
@@ -341,6 +353,7 @@ __device__ __forceinline__ void score_mma(const Params& p, int item_begin, int i
                 }
             }
             mma_commit(bars + 8 * kSFull0);
+            MLA_EV(2, G);
         }
     }
 out:
@@ -417,10 +430,17 @@ __device__ __forceinline__ float page_softmax(uint32_t (&sr)[64], int valid, flo
 __device__ __forceinline__ float page_max(const uint32_t (&sr)[64], int valid)
 {
     float m8[8];
+    if (valid >= 64) {  // every page but a sequence's last: no masking
 #pragma unroll
-    for (int a = 0; a < 8; ++a) m8[a] = (a < valid) ? __uint_as_float(sr[a]) : -INFINITY;
+        for (int a = 0; a < 8; ++a) m8[a] = __uint_as_float(sr[a]);
 #pragma unroll
-    for (int j = 8; j < 64; ++j) m8[j & 7] = fmaxf(m8[j & 7], (j < valid) ? __uint_as_float(sr[j]) : -INFINITY);
+        for (int j = 8; j < 64; ++j) m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(sr[j]));
+    } else {
+#pragma unroll
+        for (int a = 0; a < 8; ++a) m8[a] = (a < valid) ? __uint_as_float(sr[a]) : -INFINITY;
+#pragma unroll
+        for (int j = 8; j < 64; ++j) m8[j & 7] = fmaxf(m8[j & 7], (j < valid) ? __uint_as_float(sr[j]) : -INFINITY);
+    }
     return fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
 }
 
@@ -453,6 +473,7 @@ __device__ __forceinline__ void score_tracker(const Params& p, int item_begin, i
         const Item it = load_item(p.plan, items_off, i);
         for (int t = it.page_begin; t < it.page_end; ++t, ++k) {
             if (!wait_phase<true>(bars + 8 * (kCopied0 + k % kMsgSlots), k / kMsgSlots, w)) return;
+            MLA_EV(9, k);
             st_release_u32(freed, (uint32_t)(k + 1));  // messages 0 .. k copied
         }
     }
@@ -483,6 +504,7 @@ __device__ __forceinline__ void score_shipper(const Params& p, int item_begin, i
             bulk_copy_to_cta(r_p + buf * kPBytes, sbase + kOffScoreStaging + slot * kPBytes, kPBytes, bar);
             bulk_copy_to_cta(r_stats + buf * kStatsBytes, sbase + kOffStatsStaging + slot * kStatsBytes,
                              kStatsBytes, bar);
+            MLA_EV(8, m);
         }
     }
     // the value CTA's last commits and arrivals land in this CTA: wait for them before it ends
@@ -544,6 +566,7 @@ __device__ __forceinline__ void score_softmax(const Params& p, int item_begin, i
             // (timed-out) wait only clears `ok`, and each barrier ORs the abort state so that the
             // two sets leave together.
             bool ok = MLA_TIMED(7, wait_warp(bars + 8 * kSFull0, G, w));
+            if (lane == 0 && (warp == 2 || warp == 6)) MLA_EV(warp == 2 ? 4 : 15, G);
             [[maybe_unused]] const long long tc0 = MLA_TRACE_NOW();
             uint32_t sr[2][64];
             const int t0 = pg + 2 * set;
@@ -564,6 +587,7 @@ __device__ __forceinline__ void score_softmax(const Params& p, int item_begin, i
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bars + 8 * kSFree0);  // the next group's QK may start
+                if (lane == 0 && warp == 2) MLA_EV(5, G);
                 MLA_TRACE_ADD(14, MLA_TRACE_NOW() - tc0);
                 if (n_mine > 0) mx = page_max(sr[0], valid0);
                 if (n_mine > 1) mx = fmaxf(mx, page_max(sr[1], valid1));
@@ -573,6 +597,7 @@ __device__ __forceinline__ void score_softmax(const Params& p, int item_begin, i
             // group max, agreed between the two sets, drives the lazy rescale
             xs[set * 128 + row] = mx * p.scale_log2;
             if (MLA_TIMED(13, named_barrier_or(kSoftmaxBarrier, 256, !ok || *w.abort))) return;
+            if (lane == 0 && warp == 2) MLA_EV(6, G);
             const float gm = fmaxf(xs[row], xs[128 + row]);
             float factor = 1.f;
             if (gm > m_used + kRescaleThreshold) {
@@ -614,6 +639,7 @@ __device__ __forceinline__ void score_softmax(const Params& p, int item_begin, i
                     stage_message(smem, bars, slot, q4, lane, f_page, 1.f / l_total, true, (j ? valid1 : valid0) < 64);
                 }
             }
+            if (lane == 0 && (warp == 2 || warp == 6)) MLA_EV(warp == 2 ? 7 : 14, G);
             g += npg;
         }
         if (set == 0) {
@@ -673,7 +699,9 @@ __device__ __forceinline__ void value_mma(const Params& p, int item_begin, int i
         for (int t = it.page_begin; t < it.page_end; ++t, ++g) {
             const int s = g % kValueStages, buf = g % kMsgSlots;
             if (!MLA_TIMED(3, wait_phase(bars + 8 * (kFull0 + s), g / kValueStages, w))) goto out;
+            MLA_EV(12, g);
             if (!MLA_TIMED(4, wait_phase<true>(bars + 8 * (kMsgFull0 + buf), g / kMsgSlots, w))) goto out;
+            MLA_EV(10, g);
             // The correction warps go first on flagged tiles (rescale O, zero a tail) and on the
             // first tile of every item after the first (their epilogue still reads O, which this
             // PV overwrites).  Both sides apply the same rule, so o_ready phases stay paired.
@@ -700,6 +728,7 @@ __device__ __forceinline__ void value_mma(const Params& p, int item_begin, int i
             }
             mma_commit(bars + 8 * (kEmpty0 + s));
             mma_commit_multicast(bars + 8 * (kMsgFree0 + buf), 0x1);
+            MLA_EV(11, g);
         }
     }
 out:
