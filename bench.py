@@ -16,9 +16,9 @@ step (outside the events) so L2 starts cold, and the 1.2 GB cache is itself larg
 `value` is the mean device time per step (microseconds, lower is better); with N ranks every
 rank runs its own replica of the workload and the slowest rank is reported.
 
-`e2e` times the same step through the public API with host buffers: per step the queries come
-from pinned host memory, the split plan is rebuilt on the host and copied over with the block
-table, and the output is read back; wall clock around all of it.
+`e2e` times the same step through the public API with host buffers (DecodeStep.run_host): per
+step the split plan is rebuilt on the host, plan, block table and queries go over in one pinned
+transfer, and the output is read back; wall clock around all of it.
 
 `--impl reference` times the CPU oracle (plain fp64 C, the definition of the result) on the
 host cores, on a bounded sample of the same workload per step, scaled to a full step.
@@ -355,33 +355,22 @@ def sampled_parity(inp, out_dev):
 
 
 def run_e2e(args, inp, step, binding, device, stream):
-    """Through the public API with host buffers: H2D queries/plan/table, D2H output."""
+    """Through the public API with host buffers (DecodeStep.run_host): every step re-plans for
+    the sequence lengths, uploads plan, block table and queries from pinned memory in one
+    transfer, runs the kernels and reads the output back."""
     q_c_h = inp.q_c.pin_memory()
     q_r_h = inp.q_r.pin_memory()
     bt_h = torch.from_numpy(np.ascontiguousarray(inp.block_table)).pin_memory()
-    out_h = torch.empty_like(step.out, device="cpu").pin_memory()
-    q_c_d = torch.empty_like(q_c_h, device=device)
-    q_r_d = torch.empty_like(q_r_h, device=device)
-    n_sm = binding.num_sms(device)
+    out_h = torch.empty(tuple(step.out.shape), dtype=step.out.dtype).pin_memory()
     times = []
-    h2d = d2h = 0
     for i in range(args.warmup + args.steps):
         torch.cuda.synchronize(device)
         t0 = time.perf_counter()
-        plan, info = binding.mla_plan_splits(inp.seq_lens, n_sm)
-        plan_h = torch.from_numpy(plan).pin_memory()
-        step.plan_dev.copy_(plan_h, non_blocking=True)
-        step.block_table.copy_(bt_h, non_blocking=True)
-        q_c_d.copy_(q_c_h, non_blocking=True)
-        q_r_d.copy_(q_r_h, non_blocking=True)
-        step.info = info
-        step.run(q_c_d, q_r_d, stream)
-        out_h.copy_(step.out, non_blocking=True)
-        torch.cuda.synchronize(device)
+        step.run_host(q_c_h, q_r_h, block_table=bt_h, seq_lens=inp.seq_lens, out=out_h, stream=stream)
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
-        h2d = plan_h.numel() * 4 + bt_h.numel() * 4 + q_c_h.numel() * 2 + q_r_h.numel() * 2
-        d2h = out_h.numel() * 2
+    h2d = step.plan_host.nbytes + bt_h.numel() * 4 + q_c_h.numel() * 2 + q_r_h.numel() * 2
+    d2h = out_h.numel() * 2
     return {"value": round(statistics.mean(times) * 1e6, 2), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h)}
 

@@ -280,9 +280,10 @@ class DecodeStep:
         self.device = torch.device(device if device is not None else "cuda")
         self.seq_lens = np.asarray(seq_lens, dtype=np.int32)
         self.batch = int(self.seq_lens.size)
-        self.plan_host, self.info = mla_plan_splits(self.seq_lens, num_sms(self.device),
-                                                    min_pages_per_split=min_pages_per_split,
-                                                    max_clusters=max_clusters, wait_timeout_ns=wait_timeout_ns)
+        self._plan_opts = dict(min_pages_per_split=min_pages_per_split, max_clusters=max_clusters,
+                               wait_timeout_ns=wait_timeout_ns)
+        self._num_sms = num_sms(self.device)
+        self.plan_host, self.info = mla_plan_splits(self.seq_lens, self._num_sms, **self._plan_opts)
         self.plan_dev = torch.from_numpy(self.plan_host).to(self.device)
         self.w_uk, self.w_uv = w_uk, w_uv
         self.kv_pool, self.kv_scale, self.kr_pool = kv_pool, kv_scale, kr_pool
@@ -296,6 +297,7 @@ class DecodeStep:
         self.lse = torch.empty(B, NUM_HEADS, dtype=torch.float32, device=self.device)
         self.out = torch.empty(B, NUM_HEADS, D_HC, dtype=torch.bfloat16, device=self.device)
         self.dev_error = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self._h_stage = self._d_stage = None  # pinned host / device staging of run_host
 
     def run(self, q_c: torch.Tensor, q_r: torch.Tensor, stream=None) -> torch.Tensor:
         mla_absorb_q(q_c, self.w_uk, self.q_abs, stream)
@@ -306,6 +308,68 @@ class DecodeStep:
         mla_combine_splits(self.info, self.plan_dev, self.workspace, self.o_lat, self.lse, stream)
         mla_out_proj(self.o_lat, self.w_uv, self.out, stream)
         return self.out
+
+    def run_host(self, q_c: torch.Tensor, q_r: torch.Tensor, *, block_table: Optional[torch.Tensor] = None,
+                 seq_lens=None, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        """One decode step from host (CPU) tensors, end to end.
+
+        If ``seq_lens`` is given the step is re-planned for those lengths (same batch size).
+        The plan image goes to the GPU through a pinned buffer kept by this object; the block
+        table (a CPU int32 [batch, max_pages] tensor, when given; otherwise the device table
+        given at construction is used) and the queries are copied straight from the caller's
+        tensors (asynchronous DMA when they are pinned); the four kernels run; ``out`` (a pinned
+        CPU bf16 [batch, 128, 128] tensor, allocated once if not given) receives the result.
+        Waits for the stream before returning ``out``."""
+        B = self.batch
+        _need(q_c, "q_c", torch.bfloat16, (B, NUM_HEADS, D_HC), device=False)
+        _need(q_r, "q_r", torch.bfloat16, (B, NUM_HEADS, D_R), device=False)
+        if seq_lens is not None:
+            lens = np.asarray(seq_lens, dtype=np.int32)
+            if lens.size != B:
+                raise ValueError("run_host: seq_lens must keep the batch size")
+            self.seq_lens = lens
+            self.plan_host, self.info = mla_plan_splits(lens, self._num_sms, **self._plan_opts)
+            ws = int(self.info.workspace_bytes)
+            if ws and (self.workspace is None or self.workspace.numel() * 4 < ws):
+                self.workspace = torch.empty(ws // 4, dtype=torch.float32, device=self.device)
+        if block_table is not None:
+            _need(block_table, "block_table", torch.int32, device=False)
+            if block_table.dim() != 2 or block_table.shape[0] != B:
+                raise ValueError("block_table must be [batch, max_pages]")
+
+        st = torch.cuda.current_stream(self.device) if stream is None else stream
+        plan = torch.from_numpy(self.plan_host)
+        if self._h_stage is None or self._h_stage.numel() < plan.numel():
+            self._h_stage = torch.empty(max(plan.numel(), 4096), dtype=torch.int32).pin_memory()
+            self._d_stage = torch.empty(self._h_stage.numel(), dtype=torch.int32, device=self.device)
+        self._h_stage[:plan.numel()].copy_(plan)  # a few KB
+        if not hasattr(self, "_q_c_dev"):
+            self._q_c_dev = torch.empty(B, NUM_HEADS, D_HC, dtype=torch.bfloat16, device=self.device)
+            self._q_r_dev = torch.empty(B, NUM_HEADS, D_R, dtype=torch.bfloat16, device=self.device)
+        with torch.cuda.stream(st):
+            self._d_stage[:plan.numel()].copy_(self._h_stage[:plan.numel()], non_blocking=True)
+            if block_table is not None:
+                if getattr(self, "_bt_dev", None) is None or tuple(self._bt_dev.shape) != tuple(block_table.shape):
+                    self._bt_dev = torch.empty(tuple(block_table.shape), dtype=torch.int32, device=self.device)
+                self._bt_dev.copy_(block_table, non_blocking=True)  # DMA straight from pinned memory
+            self._q_c_dev.copy_(q_c, non_blocking=True)
+            self._q_r_dev.copy_(q_r, non_blocking=True)
+        plan_dev = self._d_stage[:plan.numel()]
+        bt_dev = self._bt_dev if block_table is not None else self.block_table
+        q_c_dev, q_r_dev = self._q_c_dev, self._q_r_dev
+
+        mla_absorb_q(q_c_dev, self.w_uk, self.q_abs, st)
+        mla_decode_paged(self.info, plan_dev, self.q_abs, q_r_dev, kv_pool=self.kv_pool, block_table=bt_dev,
+                         o_lat=self.o_lat, lse=self.lse, dev_error=self.dev_error, workspace=self.workspace,
+                         kv_scale=self.kv_scale, kr_pool=self.kr_pool, softmax_scale=self.softmax_scale, stream=st)
+        mla_combine_splits(self.info, plan_dev, self.workspace, self.o_lat, self.lse, st)
+        mla_out_proj(self.o_lat, self.w_uv, self.out, st)
+        if out is None:
+            out = torch.empty(B, NUM_HEADS, D_HC, dtype=torch.bfloat16).pin_memory()
+        with torch.cuda.stream(st):
+            out.copy_(self.out, non_blocking=True)
+        st.synchronize()
+        return out
 
     def device_error(self, stream=None) -> int:
         return mla_read_device_error(self.dev_error, stream)

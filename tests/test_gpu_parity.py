@@ -195,3 +195,18 @@ def test_step_is_deterministic():
     b = step.run(q_c, q_r).clone()
     torch.cuda.synchronize()
     assert torch.equal(a, b)
+
+
+def test_run_host_matches_device_run():
+    """DecodeStep.run_host (host tensors in, one staged upload, re-plan) gives the same bits as
+    run() on device tensors, twice in a row."""
+    inp = synth.make_inputs([3000, 700, 64 * 9 + 1], seed=11, poison_tail=True)
+    q_c, q_r, w_uk, w_uv, kv, bt = binding.inputs_to_device(inp, DEV)
+    step = binding.DecodeStep(inp.seq_lens, w_uk=w_uk, w_uv=w_uv, block_table=bt, min_pages_per_split=2, **kv)
+    ref = step.run(q_c, q_r).clone()
+    torch.cuda.synchronize()
+    bt_h = torch.from_numpy(np.ascontiguousarray(inp.block_table))
+    for _ in range(2):
+        out = step.run_host(inp.q_c, inp.q_r, block_table=bt_h, seq_lens=inp.seq_lens)
+        assert step.device_error() == 0
+        assert torch.equal(out, ref.cpu())
