@@ -134,9 +134,10 @@ MLA_API mla_status mla_absorb_q(const void* q_c, const void* w_uk, void* q_abs, 
  *                   MLA_KV_FP8_E4M3: kv_pool = e4m3 codes [num_pool_pages][64][512],
  *                   kv_scale = fp32 [num_pool_pages][64] (the stored value times the scale is
  *                   the latent), kr_pool = bf16 [num_pool_pages][64][64]; kv_pool and
- *                   kr_pool 16-byte aligned, kv_scale 4-byte aligned.  The kernel forms
- *                   bf16(float(code) * scale) in shared memory and runs the bf16 tensor-core
- *                   path on it (relative rounding 2^-9 against the exact dequantised value).
+ *                   kr_pool 16-byte aligned, kv_scale 4-byte aligned.  The codes feed e4m3
+ *                   tensor-core MMAs as loaded; q_abs and P enter them as e4m3 pairs (hi +
+ *                   lo, about 2^-8 relative), the scales are applied to the scores and to P
+ *                   per token, and k_R / scale is formed in bf16 for the RoPE MMA.
  *   block_table     device int32 [batch][max_pages_per_seq]; entry p of row b is the physical
  *                   page of tokens 64p..64p+63 of sequence b.  Only the first ceil(S_b/64)
  *                   entries of a row are read.

@@ -167,9 +167,9 @@ extern "C" __attribute__((visibility("default"))) int mla_debug_timeout_sites(un
 }
 #endif
 
-// The e4m3 cache: c8 [pages][64][512] bytes (64x64 boxes, no swizzle: the converter warps read
-// it), kr_pool [pages][64][64] bf16 (64x64 boxes, 128-byte swizzle: the MMA reads it), one fp32
-// scale per token.
+// The e4m3 cache: c8 [pages][64][512] bytes (boxes of 128 columns x 64 tokens, 128-byte
+// swizzle: the e4m3 MMAs read them as they land), kr_pool [pages][64][64] bf16 (64x64 boxes,
+// 128-byte swizzle), one fp32 scale per token (read with plain loads).
 mla_status launch_decode_fp8(const mla_plan_info* info, const void* plan_dev, const void* q_abs, const void* q_r,
                              const void* kv_pool, const float* kv_scale, const void* kr_pool, int32_t num_pool_pages,
                              const int32_t* block_table, int32_t max_pages_per_seq, float softmax_scale,
@@ -179,11 +179,11 @@ mla_status launch_decode_fp8(const mla_plan_info* info, const void* plan_dev, co
     CUtensorMap tm_c8, tm_kr;
     const cuuint64_t c_dims[3] = {512, 64, (cuuint64_t)num_pool_pages};
     const cuuint64_t c_strides[2] = {512, 64 * 512};
-    const cuuint32_t c_box[3] = {64, 64, 1};
+    const cuuint32_t c_box[3] = {128, 64, 1};
     const cuuint64_t r_dims[3] = {64, 64, (cuuint64_t)num_pool_pages};
     const cuuint64_t r_strides[2] = {64 * 2, 64 * 64 * 2};
     const cuuint32_t r_box[3] = {64, 64, 1};
-    if (!make_map(&tm_c8, CU_TENSOR_MAP_DATA_TYPE_UINT8, CU_TENSOR_MAP_SWIZZLE_NONE, kv_pool, 3, c_dims, c_strides,
+    if (!make_map(&tm_c8, CU_TENSOR_MAP_DATA_TYPE_UINT8, CU_TENSOR_MAP_SWIZZLE_128B, kv_pool, 3, c_dims, c_strides,
                   c_box) ||
         !make_map_bf16(&tm_kr, kr_pool, 3, r_dims, r_strides, r_box))
         return MLA_ERR_CUDA;
@@ -205,6 +205,11 @@ mla_status launch_decode_fp8(const mla_plan_info* info, const void* plan_dev, co
     p.dev_error = dev_error;
     p.timeout_ns = (uint64_t)info->wait_timeout_ns;
     p.kv_scale = kv_scale;
+#ifdef MLA_DECODE_TRACE
+    p.trace = g_trace;
+#else
+    p.trace = nullptr;
+#endif
 
     if (!set_smem(mla::decode_fp8::decode_fp8_kernel, mla::decode_fp8::kSmemBytes)) return MLA_ERR_CUDA;
     mla::decode_fp8::decode_fp8_kernel<<<2 * info->num_clusters, mla::decode_fp8::kThreads,
