@@ -18,7 +18,8 @@
 // Output.  o[h] = sum_t p[h,t] sigma_t c8_t / l[h].  The PV operand is P~ = p * sigma_t * g,
 // with g a power of two per item chosen from the item's largest sigma so that P~ <= 448, split
 // the same way into e4m3 hi + lo and packed into one 128-byte row per head (bytes 0-63: hi of
-// the page's 64 tokens, bytes 64-127: lo).  PV runs e4m3 MMAs on the raw c8 page (B operand
+// the page's 64 tokens, bytes 64-127: lo).  The score CTA ships p as bf16 (with sigma_t g per
+// token); four warps of the value CTA form P~ in place before PV.  PV runs e4m3 MMAs on the raw c8 page (B operand
 // MN-major) and the last page's 1/(g l) normalises.  The lazy-rescale threshold is 4 (log2
 // units), so p <= 16 and the typical P~ stays above 1/4, where the pair is exact to 2^-8; below
 // that its absolute error is at most 2^-10, against a running maximum of at least 14.
@@ -28,16 +29,18 @@
 // Layout of the pair (sm_103a), as decode.cuh:
 //   rank 0, the score CTA: q_hi and q_lo in TMEM (128 columns each, four e4m3 per 32-bit
 //     column), the scores of four pages in the other 256 columns.  Five K-chunks per four-page
-//     group: the four 128-column boxes of c8 (8 KB per page) and the k_R box (8 KB per page),
+//     group: the k_R box (8 KB per page) and the four 128-column boxes of c8 (8 KB per page),
 //     32 KB each, through a four-slot ring.  Eight softmax warps, the shipper and tracker as in
 //     the bf16 kernel; warp 11 turns k_R into k_R / sigma and writes the per-token factors the
 //     softmax needs (sigma * scale * log2(e), sigma * g).
-//   rank 1, the value CTA: O in TMEM (512 columns), four 32 KB c8 page stages, PV from P~.
+//   rank 1, the value CTA: O in TMEM (512 columns), four 32 KB c8 page stages, PV from P~;
+//     warps 7-10 form P~ from the shipped p.
 //
 // Pipelines: those of decode.cuh, plus
 //   kr_landed             the group's k_R box has landed (TMA bytes; waited by warp 11, which
 //                         then arrives on the slot's kv_full for the MMA)
 //   sig_ready             counter: groups whose token factors are written (warp 11)
+//   p_ready[4]            the value CTA's P~ of a message is written (its four converter warps)
 #pragma once
 #include "decode.cuh"
 
@@ -57,6 +60,7 @@ constexpr int kThreads = 384;                     // 12 warps, roles in the kern
 constexpr int kShipperWarp = 10;
 constexpr int kKrWarp = 11;                       // score CTA: k_R / sigma, token factors
 constexpr int kAckWarp = 6;                       // value CTA: message acknowledgements
+constexpr int kPConvWarp0 = 7;                    // value CTA: warps 7-10 turn P into P~ (e4m3 pair)
 constexpr int kChunkStages = 4;
 constexpr int kValueStages = 4;
 constexpr int kMaxStages = 4;
@@ -64,12 +68,15 @@ constexpr int kStagingSlots = 4;
 constexpr int kMsgSlots = 4;
 constexpr int kBoxBytes = 64 * 128;               // 64 tokens x 128 bytes (128 e4m3 or 64 bf16)
 constexpr int kC8Boxes = 4;                       // a c8 row: four 128-column boxes
-constexpr int kChunksPerGroup = kC8Boxes + 1;     // then the k_R box
+constexpr int kChunksPerGroup = kC8Boxes + 1;     // the k_R box, then the c8 boxes
 constexpr int kGroupPages = 4;                    // pages per score MMA (N = 256)
 constexpr int kChunkBytes = kGroupPages * kBoxBytes;    // 32 KB
 constexpr int kValueStageBytes = kC8Boxes * kBoxBytes;  // 32 KB: one page of c8
 constexpr int kPBytes = 128 * 128;                // P~: 128 heads x (64 hi + 64 lo) e4m3
-constexpr int kStatsWarpBytes = 128 + 128 + 16;   // factor[32], inv_l[32], flags (as decode.cuh)
+// Per message statistics, one block per softmax warp: factor[32], inv_l[32], a 16-byte flags
+// slot (as decode.cuh), then sig_p of 16 of the page's tokens (warp k: tokens 16k..16k+15).
+constexpr int kStatsWarpBytes = 128 + 128 + 16 + 64;
+constexpr int kSigPWord = 68;                     // float index of sig_p in a warp's block
 constexpr int kStatsBytes = 4 * kStatsWarpBytes;
 constexpr int kPWarpBytes = kPBytes / 4;
 constexpr int kMsgBytes = kPBytes + kStatsBytes;
@@ -103,7 +110,8 @@ enum Bar : int {
     kDrain = kODrain0 + 2,
     kStgReady0 = kDrain + 1,
     kKrLanded = kStgReady0 + kStagingSlots,
-    kNumBars = kKrLanded + 1
+    kPReady0 = kKrLanded + 1,
+    kNumBars = kPReady0 + kMsgSlots
 };
 
 constexpr int kOffTmemHolder = kOffBars + 8 * kNumBars;
@@ -240,7 +248,7 @@ __device__ __forceinline__ void value_producer(const CUtensorMap* tm_c8, const P
                 const int pj = __shfl_sync(0xffffffffu, page, j);
                 if (lane == 0) {
                     const int s = g % kValueStages;
-                    if (g >= kValueStages) ok = wait_phase(bars + 8 * (kEmpty0 + s), g / kValueStages - 1, w);
+                    if (g >= kValueStages) ok = wait_phase_ool(bars + 8 * (kEmpty0 + s), g / kValueStages - 1, w);
                     if (ok) {
                         const uint32_t full = bars + 8 * (kFull0 + s);
                         const uint32_t dst = sbase + s * kValueStageBytes;
@@ -248,6 +256,7 @@ __device__ __forceinline__ void value_producer(const CUtensorMap* tm_c8, const P
                         // an out-of-range page id reads as zeros (TMA fills outside the tensor)
                         for (int x = 0; x < kC8Boxes; ++x)
                             tma_load_3d(dst + x * kBoxBytes, tm_c8, full, 128 * x, 0, pj, policy);
+                        MLA_EV(16, g);
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -262,9 +271,11 @@ __device__ __forceinline__ void value_producer(const CUtensorMap* tm_c8, const P
     }
 }
 
-// Score CTA: chunk j of a four-page group holds box j of the group's pages in rows 0-63,
-// 64-127, 128-191, 192-255: j = 0..3 the 128-column c8 boxes (their bytes complete kv_full),
-// j = 4 the k_R box (its bytes complete kr_landed; warp 11 completes kv_full after the divide).
+// Score CTA: chunk j of a four-page group holds one box of the group's pages in rows 0-63,
+// 64-127, 128-191, 192-255: j = 0 the k_R box (its bytes complete kr_landed; warp 11 completes
+// kv_full after the divide), j = 1..4 the 128-column c8 boxes j - 1 (their bytes complete
+// kv_full).  k_R goes first so that it lands, and is divided, while the MMA still works on the
+// group before.
 __device__ __forceinline__ void score_producer(const CUtensorMap* tm_c8, const CUtensorMap* tm_kr, const Params& p,
                                                int item_begin, int item_end, int items_off, uint32_t sbase,
                                                uint32_t bars, const dev::WaitCtx& w, int lane)
@@ -293,15 +304,16 @@ __device__ __forceinline__ void score_producer(const CUtensorMap* tm_c8, const C
 #pragma unroll
                 for (int q = 0; q < kGroupPages; ++q) pages[q] = __shfl_sync(0xffffffffu, page, min(j + q, 31));
                 if (lane == 0) {
+#pragma unroll 1
                     for (int box = 0; box < kChunksPerGroup && ok; ++box, ++c) {
-                        if (c >= kChunkStages) ok = wait_phase(bars + 8 * (kEmpty0 + s), phase - 1, w);
+                        if (c >= kChunkStages) ok = wait_phase_ool(bars + 8 * (kEmpty0 + s), phase - 1, w);
                         if (!ok) break;
                         const uint32_t dst = sbase + kOffChunks + s * kChunkBytes;
-                        if (box < kC8Boxes) {
+                        if (box > 0) {
                             const uint32_t full = bars + 8 * (kFull0 + s);
                             mbar_arrive_expect_tx(full, npg * kBoxBytes);
                             for (int q = 0; q < npg; ++q)
-                                tma_load_3d(dst + q * kBoxBytes, tm_c8, full, 128 * box, 0, pages[q], policy);
+                                tma_load_3d(dst + q * kBoxBytes, tm_c8, full, 128 * (box - 1), 0, pages[q], policy);
                         } else {
                             const uint32_t landed = bars + 8 * kKrLanded;
                             mbar_arrive_expect_tx(landed, npg * kBoxBytes);
@@ -323,7 +335,7 @@ __device__ __forceinline__ void score_producer(const CUtensorMap* tm_c8, const C
         // Loads still in flight must land before the CTA exits: the last kChunkStages chunks,
         // at most one of them a k_R chunk (its bytes complete kr_landed, the latest phase).
         for (int k = (c > kChunkStages ? c - kChunkStages : 0); k < c; ++k) {
-            if (k % kChunksPerGroup == kC8Boxes)
+            if (k % kChunksPerGroup == 0)
                 drain_phase(bars + 8 * kKrLanded, k / kChunksPerGroup, w.timeout_ns);
             else
                 drain_phase(bars + 8 * (kFull0 + k % kChunkStages), k / kChunkStages, w.timeout_ns);
@@ -338,9 +350,10 @@ __device__ __forceinline__ void score_producer(const CUtensorMap* tm_c8, const C
 // factors for the softmax (sig_s = sigma * scale * log2(e) and sig_p = sigma * g, both 0 past
 // the sequence end, and g) into factor slot G % 4, and every k_R row divided by its token's
 // sigma in place; then kv_full for the MMA.  Factor slot G % 4 is free when warp 11 writes it:
-// warp 11 finished group G - 1 after its k_R box landed, which the producer loaded once the MMA
-// had consumed group G - 1's first chunk, which it issued after s_free of group G - 2; so every
-// softmax warp had finished group G - 3, and slot G % 4 last held group G - 4.
+// warp 11 finished group G - 1 after its k_R box (chunk 5(G-1)) landed, which the producer
+// loaded once the MMA had consumed chunk 5(G-1) - 4, the second chunk of group G - 2, which it
+// issued after s_free of group G - 3; so every softmax warp had finished group G - 4, the last
+// group in slot G % 4.
 __device__ __forceinline__ void kr_convert(const Params& p, int item_begin, int item_end, int items_off,
                                            uint8_t* smem, uint32_t bars, const dev::WaitCtx& w, int lane)
 {
@@ -376,44 +389,53 @@ __device__ __forceinline__ void kr_convert(const Params& p, int item_begin, int 
         }
         for (int pg = it.page_begin; pg < it.page_end; pg += kGroupPages, ++G) {
             const int npg = min(kGroupPages, it.page_end - pg);
-            const int c = kChunksPerGroup * G + kC8Boxes, s = c % kChunkStages;
+            const int c = kChunksPerGroup * G, s = c % kChunkStages;  // the group's k_R chunk
             float* sig = reinterpret_cast<float*>(smem + kOffSig + (G % kSigSlots) * kSigGroupBytes);
-            // token t of the group (row t of the k_R chunk) is lane + 32 k: page t / 64
-            float inv[8];
+            // Token t = lane + 32 k of the group (row t of the k_R chunk) sits in page k / 2 at
+            // slot lane + 32 (k & 1).  All page ids, then all eight scales, are loaded before any
+            // is used, so the group costs two memory round trips.
+            int page_mine = 0;
+            if (lane < npg) {
+                page_mine = __ldg(bt + pg + lane);
+                if (page_mine < 0 || page_mine >= p.num_pool_pages) page_mine = -1;  // reported by the producers
+            }
+            float sigma[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                const int t = lane + 32 * k, q = t >> 6, r = t & 63;
-                float sigma = 0.f;
-                bool valid = false;
-                if (q < npg && 64 * (pg + q) + r < it.seq_len) {
-                    const int page = __ldg(bt + pg + q);
-                    if (page >= 0 && page < p.num_pool_pages) {
-                        sigma = __ldg(p.kv_scale + (int64_t)page * 64 + r);
-                        valid = true;
-                    }
-                }
-                sig[t] = valid ? sigma * p.scale_log2 : 0.f;
-                sig[256 + t] = valid ? sigma * g : 0.f;
-                inv[k] = valid ? 1.f / fmaxf(sigma, 5.421011e-20f) : 0.f;  // sigma >= 2^-64
+                const int page = __shfl_sync(0xffffffffu, page_mine, k >> 1);
+                sigma[k] = __ldg(p.kv_scale + (int64_t)max(page, 0) * 64 + lane + 32 * (k & 1));
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int t = lane + 32 * k, q = k >> 1;
+                const int page = __shfl_sync(0xffffffffu, page_mine, q);  // every lane, before any branch
+                const bool valid = q < npg && page >= 0 && 64 * (pg + q) + (t & 63) < it.seq_len;
+                sig[t] = valid ? sigma[k] * p.scale_log2 : 0.f;
+                sig[256 + t] = valid ? sigma[k] * g : 0.f;
             }
             if (lane == 0) sig[512] = g;
-            if (!wait_warp(bars + 8 * kKrLanded, G, w)) return;
+            if (lane == 0) MLA_EV(18, G);
+            if (!wait_warp_ool(bars + 8 * kKrLanded, G, w)) return;
+            if (lane == 0) MLA_EV(19, G);
             uint8_t* rows = smem + kOffChunks + s * kChunkBytes;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int t = lane + 32 * k;
-                if (t >= 64 * npg) break;
-                const uint32_t inv2 = pack_bf16x2(inv[k], inv[k]);
+            const float inv_scale = 1.f / p.scale_log2;
+#pragma unroll 1
+            for (int t = lane; t < 64 * npg; t += 32) {
+                // 1 / sigma_t (sigma >= 2^-64); a slot past the sequence end gets 0 (its score is masked)
+                const float ss = sig[t];
+                const float inv = ss > 0.f ? 1.f / fmaxf(ss * inv_scale, 5.421011e-20f) : 0.f;
+                const uint32_t inv2 = pack_bf16x2(inv, inv);
                 uint8_t* row = rows + t * 128;  // 16-byte chunks in any order: the divide is per element
+                uint4 v[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[j] = *reinterpret_cast<const uint4*>(row + (((j + lane) & 7) << 4));
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    uint4* ch = reinterpret_cast<uint4*>(row + (((j + lane) & 7) << 4));  // no bank conflicts
-                    uint4 v = *ch;
-                    v.x = mul_bf16x2(v.x, inv2);
-                    v.y = mul_bf16x2(v.y, inv2);
-                    v.z = mul_bf16x2(v.z, inv2);
-                    v.w = mul_bf16x2(v.w, inv2);
-                    *ch = v;
+                    v[j].x = mul_bf16x2(v[j].x, inv2);
+                    v[j].y = mul_bf16x2(v[j].y, inv2);
+                    v[j].z = mul_bf16x2(v[j].z, inv2);
+                    v[j].w = mul_bf16x2(v[j].w, inv2);
+                    *reinterpret_cast<uint4*>(row + (((j + lane) & 7) << 4)) = v[j];
                 }
             }
             fence_proxy_async_cta();  // the k_R rows are read by the MMA (async proxy)
@@ -427,9 +449,9 @@ __device__ __forceinline__ void kr_convert(const Params& p, int item_begin, int 
     }
 }
 
-// QK of a four-page group: S[128 heads x N tokens] accumulated over the five K-chunks: chunks
-// 0-3 run q_hi and q_lo (TMEM, "TS") against the 128-column c8 box, eight e4m3 MMAs of K = 32;
-// chunk 4 runs q_R 2^e (shared memory) against k_R / sigma, four bf16 MMAs of K = 16.
+// QK of a four-page group: S[128 heads x N tokens] accumulated over the five K-chunks: chunk 0
+// runs q_R 2^e (shared memory) against k_R / sigma, four bf16 MMAs of K = 16; chunks 1-4 run
+// q_hi and q_lo (TMEM, "TS") against a 128-column c8 box, eight e4m3 MMAs of K = 32.
 __device__ __forceinline__ void score_mma(const Params& p, int item_begin, int item_end, int items_off, uint32_t sbase,
                                           uint32_t bars, uint32_t tmem, const dev::WaitCtx& w)
 {
@@ -441,34 +463,34 @@ __device__ __forceinline__ void score_mma(const Params& p, int item_begin, int i
     int s = 0, phase = 0, G = 0, n_item = 0;
     for (int i = item_begin; i < item_end; ++i, ++n_item) {
         const Item it = load_item(p.plan, items_off, i);
-        if (!wait_phase(bars + 8 * kQReady, n_item, w)) goto out;
+        if (!wait_phase_ool(bars + 8 * kQReady, n_item, w)) goto out;
         tc_fence_after();
         for (int pg = it.page_begin; pg < it.page_end; pg += kGroupPages, ++G) {
             const int npg = min(kGroupPages, it.page_end - pg);
             const uint32_t idesc8 = idesc_e4m3(128, 64 * npg, false, false);
             const uint32_t idesc16 = idesc_bf16(128, 64 * npg, false, false);
-            if (G >= 1 && !wait_phase(bars + 8 * kSFree0, G - 1, w)) goto out;
+            if (G >= 1 && !wait_phase_ool(bars + 8 * kSFree0, G - 1, w)) goto out;
             MLA_EV(3, G);
-#pragma unroll
+#pragma unroll 1
             for (int box = 0; box < kChunksPerGroup; ++box) {
-                if (!wait_phase(full0 + 8 * s, phase, w)) goto out;
+                if (!wait_phase_ool(full0 + 8 * s, phase, w)) goto out;
                 MLA_EV(1, kChunksPerGroup * G + box);
                 tc_fence_after();
                 const uint64_t b0 = chunk_desc0 + (uint64_t)(s * (kChunkBytes >> 4));
-                if (box < kC8Boxes) {
+                if (box == 0) {
+                    mma_ss(d, qr_desc, b0, idesc16, 0u);
+                    mma_ss(d, qr_desc + 2, b0 + 2, idesc16, 1u);
+                    mma_ss(d, qr_desc + 4, b0 + 4, idesc16, 1u);
+                    mma_ss(d, qr_desc + 6, b0 + 6, idesc16, 1u);
+                } else {
 #pragma unroll
                     for (int part = 0; part < 2; ++part) {
-                        const uint32_t a0 = tmem + (part ? kQLoCol : kQHiCol) + 32 * box;
-                        mma_ts_e4m3(d, a0, b0, idesc8, (box | part) != 0 ? 1u : 0u);
+                        const uint32_t a0 = tmem + (part ? kQLoCol : kQHiCol) + 32 * (box - 1);
+                        mma_ts_e4m3(d, a0, b0, idesc8, 1u);
                         mma_ts_e4m3(d, a0 + 8, b0 + 2, idesc8, 1u);
                         mma_ts_e4m3(d, a0 + 16, b0 + 4, idesc8, 1u);
                         mma_ts_e4m3(d, a0 + 24, b0 + 6, idesc8, 1u);
                     }
-                } else {
-                    mma_ss(d, qr_desc, b0, idesc16, 1u);
-                    mma_ss(d, qr_desc + 2, b0 + 2, idesc16, 1u);
-                    mma_ss(d, qr_desc + 4, b0 + 4, idesc16, 1u);
-                    mma_ss(d, qr_desc + 6, b0 + 6, idesc16, 1u);
                 }
                 mma_commit(empty0 + 8 * s);
                 if (++s == kChunkStages) {
@@ -490,8 +512,8 @@ out:
 // 256k..256k+255, times 2^e, into the e4m3 pair and writes it to TMEM columns 64k.. of q_hi and
 // of q_lo in lane `row`; set 0 writes q_R 2^e (exact) to row `row` of the K-major,
 // 128-byte-swizzled q_R tile.  Returns 2^-e.
-__device__ __forceinline__ float load_query(const Params& p, int seq, int row, int set, uint32_t taddr,
-                                            uint8_t* qr_smem)
+__device__ __noinline__ float load_query(const Params& p, int seq, int row, int set, uint32_t taddr,
+                                        uint8_t* qr_smem)
 {
     using namespace dev;
     const uint4* qrow = reinterpret_cast<const uint4*>(p.q_abs + ((int64_t)seq * 128 + row) * 512);
@@ -553,8 +575,7 @@ __device__ __forceinline__ float page_scale_max(uint32_t (&sr)[64], const float*
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int j = 4 * v + u;
-            float y = __uint_as_float(sr[j]) * fs[u];
-            if (j >= valid) y = -INFINITY;
+            const float y = j < valid ? __uint_as_float(sr[j]) * fs[u] : -INFINITY;
             sr[j] = __float_as_uint(y);
             m8[j & 7] = fmaxf(m8[j & 7], y);
         }
@@ -562,47 +583,43 @@ __device__ __forceinline__ float page_scale_max(uint32_t (&sr)[64], const float*
     return fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
 }
 
-// Softmax of one page: p = 2^(y 2^-e - m) (one FMA and one MUFU.EX2 per score), P~ = p * sig_p[t]
-// as the e4m3 pair, written into this thread's row of the swizzled staging tile (16-byte chunk
-// c goes to chunk c ^ (row & 7); chunks 0-3 hold hi of tokens 0-63, chunks 4-7 lo).  Returns the
-// row sum of p.
-__device__ __forceinline__ float page_softmax(const uint32_t (&sr)[64], float r_h, float m_used, const float* sig_p,
-                                              uint8_t* stage_row, int row)
+// Softmax of one page: p = 2^(y 2^-e - m) (one FMA and one MUFU.EX2 per score), written as bf16
+// into this thread's row of the swizzled staging tile (16-byte chunk c of the row goes to chunk
+// c ^ (row & 7)), the layout of the bf16 kernel.  The value CTA scales it by sigma_t g and
+// splits it into the e4m3 pair.  Returns the row sum of p.
+__device__ __forceinline__ float page_softmax(const uint32_t (&sr)[64], float r_h, float m_used, uint8_t* stage_row,
+                                              int row)
 {
     using namespace dev;
     float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        uint32_t hi[4], lo[4];
+    for (int c = 0; c < 8; ++c) {
+        uint32_t pk[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const int j = 16 * c + 4 * q;
-            const float4 f = *reinterpret_cast<const float4*>(sig_p + j);
+            const int j = 8 * c + 2 * q;
             const float p0 = ex2_approx(fmaf(__uint_as_float(sr[j]), r_h, -m_used));
             const float p1 = ex2_approx(fmaf(__uint_as_float(sr[j + 1]), r_h, -m_used));
-            const float p2 = ex2_approx(fmaf(__uint_as_float(sr[j + 2]), r_h, -m_used));
-            const float p3 = ex2_approx(fmaf(__uint_as_float(sr[j + 3]), r_h, -m_used));
-            l8[(4 * q) & 7] += p0;
-            l8[(4 * q + 1) & 7] += p1;
-            l8[(4 * q + 2) & 7] += p2;
-            l8[(4 * q + 3) & 7] += p3;
-            split_e4m3x4(p0 * f.x, p1 * f.y, p2 * f.z, p3 * f.w, hi[q], lo[q]);
+            pk[q] = pack_bf16x2(p0, p1);
+            l8[(2 * q) & 7] += p0;
+            l8[(2 * q + 1) & 7] += p1;
         }
-        *reinterpret_cast<uint4*>(stage_row + ((c ^ (row & 7)) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(stage_row + (((c + 4) ^ (row & 7)) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        *reinterpret_cast<uint4*>(stage_row + ((c ^ (row & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
     }
     return ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
 }
 
 // Finish this warp's part of staged message `slot`: its statistics block (per-row O rescale
-// factor, 1/(g l) on the item's last page, flags), then mark the warp's share ready.
+// factor, 1/(g l) on the item's last page, flags, sig_p of tokens 16 q4..16 q4 + 15 of the
+// page), then mark the warp's share ready.
 __device__ __forceinline__ void stage_message(uint8_t* smem, uint32_t bars, int slot, int q4, int lane, float factor,
-                                              float inv_l, bool last, bool tail)
+                                              float inv_l, bool last, bool tail, const float* sig_p_page)
 {
     using namespace dev;
     float* stats = reinterpret_cast<float*>(smem + kOffStatsStaging + slot * kStatsBytes + q4 * kStatsWarpBytes);
     stats[lane] = factor;
     if (last) stats[32 + lane] = inv_l;
+    if (lane < 16) stats[kSigPWord + lane] = sig_p_page[16 * q4 + lane];
     const bool any_rescale = __any_sync(0xffffffffu, factor != 1.f);
     if (lane == 0) reinterpret_cast<uint32_t*>(stats)[64] = (any_rescale ? 1u : 0u) | (tail ? 2u : 0u);
     fence_proxy_async_cta();  // the staged P~ and statistics are read by the shipper's bulk copies
@@ -611,7 +628,9 @@ __device__ __forceinline__ void stage_message(uint8_t* smem, uint32_t bars, int 
 }
 
 // Staging tracker (one thread): follows every phase of copied and publishes how many messages
-// have landed in the value CTA (their staging slots are free).
+// have landed in the value CTA (their staging slots are free).  It shares warp 10 with the
+// shipper, so both poll with the inline wait: spinning inside an out-of-line call, one of the two
+// lanes could hold the warp while the other starved.
 __device__ __forceinline__ void score_tracker(const Params& p, int item_begin, int item_end, int items_off,
                                               uint8_t* smem, uint32_t bars, const dev::WaitCtx& w)
 {
@@ -622,6 +641,7 @@ __device__ __forceinline__ void score_tracker(const Params& p, int item_begin, i
         const Item it = load_item(p.plan, items_off, i);
         for (int t = it.page_begin; t < it.page_end; ++t, ++k) {
             if (!wait_phase<true>(bars + 8 * (kCopied0 + k % kMsgSlots), k / kMsgSlots, w)) return;
+            MLA_EV(9, k);
             st_release_u32(freed, (uint32_t)(k + 1));
         }
     }
@@ -684,7 +704,7 @@ __device__ __forceinline__ void score_softmax(const Params& p, int item_begin, i
             const float* sig = reinterpret_cast<const float*>(smem + kOffSig + (G % kSigSlots) * kSigGroupBytes);
             // Both sets reach every named barrier below the same number of times: a failed wait
             // only clears `ok`, and each barrier ORs the abort state so the sets leave together.
-            bool ok = wait_warp(bars + 8 * kSFull0, G, w);
+            bool ok = wait_warp_ool(bars + 8 * kSFull0, G, w);
             if (lane == 0 && warp == 2) MLA_EV(4, G);
             uint32_t sr[2][64];
             const int t0 = pg + 2 * set;
@@ -711,11 +731,13 @@ __device__ __forceinline__ void score_softmax(const Params& p, int item_begin, i
                     if (n_mine > 1) mx = fmaxf(mx, page_scale_max(sr[1], sig + 64 * (2 * set + 1), valid1));
                     g_item = sig[512];
                 }
+                if (lane == 0 && warp == 2) MLA_EV(5, G);
             }
 
             // group max (log2 units), agreed between the two sets, drives the lazy rescale
             xs[set * 128 + row] = mx * r_h;
             if (named_barrier_or(kSoftmaxBarrier, 256, !ok || *w.abort)) return;
+            if (lane == 0 && warp == 2) MLA_EV(6, G);
             const float gm = fmaxf(xs[row], xs[128 + row]);
             float factor = 1.f;
             if (gm > m_used + kRescaleThreshold) {
@@ -734,13 +756,13 @@ __device__ __forceinline__ void score_softmax(const Params& p, int item_begin, i
                 const int slot = gg % kStagingSlots;
                 if (gg >= kStagingSlots) ok = wait_freed(freed, (uint32_t)(gg - kStagingSlots + 1), w);
                 if (!ok) break;
-                l_mine += page_softmax(sr[j], r_h, m_used, sig + 256 + 64 * (2 * set + j),
-                                       smem + kOffScoreStaging + slot * kPBytes + p_row_off, row);
+                l_mine += page_softmax(sr[j], r_h, m_used, smem + kOffScoreStaging + slot * kPBytes + p_row_off, row);
                 const float f_page = (set == 0 && j == 0) ? factor : 1.f;  // O rescale precedes page 0
                 if (t0 + j == it.page_end - 1)
                     hold_last = true;
                 else
-                    stage_message(smem, bars, slot, q4, lane, f_page, 0.f, false, (j ? valid1 : valid0) < 64);
+                    stage_message(smem, bars, slot, q4, lane, f_page, 0.f, false, (j ? valid1 : valid0) < 64,
+                                  sig + 256 + 64 * (2 * set + j));
             }
             if (last_group) {  // 1/(g l) for the item's last page needs both sets' sums
                 xs[256 + set * 128 + row] = l_mine;
@@ -751,7 +773,7 @@ __device__ __forceinline__ void score_softmax(const Params& p, int item_begin, i
                     const int slot = (g + 2 * set + j) % kStagingSlots;
                     const float f_page = (set == 0 && j == 0) ? factor : 1.f;
                     stage_message(smem, bars, slot, q4, lane, f_page, 1.f / (g_item * l_total), true,
-                                  (j ? valid1 : valid0) < 64);
+                                  (j ? valid1 : valid0) < 64, sig + 256 + 64 * (2 * set + j));
                 }
             }
             if (lane == 0 && warp == 2) MLA_EV(7, G);
@@ -789,7 +811,7 @@ __device__ __forceinline__ void value_ack(const Params& p, int item_begin, int i
         for (int t = it.page_begin; t < it.page_end; ++t, ++g) {
             const int buf = g % kMsgSlots;
             mbar_arrive_expect_tx(bars + 8 * (kMsgFull0 + buf), kMsgBytes);
-            if (!wait_phase<true>(bars + 8 * (kMsgFull0 + buf), g / kMsgSlots, w)) return;
+            if (!wait_phase_ool<true>(bars + 8 * (kMsgFull0 + buf), g / kMsgSlots, w)) return;
             mbar_arrive_remote(r_copied + 8 * buf);
         }
     }
@@ -811,15 +833,17 @@ __device__ __forceinline__ void value_mma(const Params& p, int item_begin, int i
         const Item it = load_item(p.plan, items_off, i);
         for (int t = it.page_begin; t < it.page_end; ++t, ++g) {
             const int s = g % kValueStages, buf = g % kMsgSlots;
-            if (!wait_phase(bars + 8 * (kFull0 + s), g / kValueStages, w)) goto out;
-            if (!wait_phase<true>(bars + 8 * (kMsgFull0 + buf), g / kMsgSlots, w)) goto out;
+            if (!wait_phase_ool(bars + 8 * (kFull0 + s), g / kValueStages, w)) goto out;
+            MLA_EV(15, g);
+            if (!wait_phase_ool<true>(bars + 8 * (kMsgFull0 + buf), g / kMsgSlots, w)) goto out;
+            if (!wait_phase_ool(bars + 8 * (kPReady0 + buf), g / kMsgSlots, w)) goto out;  // P~ written
             MLA_EV(10, g);
             // The correction warps go first on flagged tiles and on the first tile of every item
             // after the first; both sides apply the same rule, so o_ready phases stay paired.
             if (msg_flags(smem, buf) != 0 || (t == it.page_begin && i != item_begin)) {
                 const int e = n_flagged & 1;
                 mma_commit(bars + 8 * (kODrain0 + e));  // arrives once every earlier PV is done
-                if (!wait_phase(bars + 8 * (kOReady0 + e), n_flagged >> 1, w)) goto out;
+                if (!wait_phase_ool(bars + 8 * (kOReady0 + e), n_flagged >> 1, w)) goto out;
                 ++n_flagged;
             }
             tc_fence_after();
@@ -845,6 +869,52 @@ __device__ __forceinline__ void value_mma(const Params& p, int item_begin, int i
 out:
     mma_commit(bars + 8 * kDrain);
     drain_phase(bars + 8 * kDrain, 0, w.timeout_ns);
+}
+
+// P -> P~ (four warps, thread = head row, in place in the message buffer): row h's 64 bf16 p
+// times sig_p[t] = sigma_t g (0 past the sequence end) from the message's statistics, split into
+// the e4m3 pair: 16-byte chunks 0-3 of the row take hi of tokens 0-63, chunks 4-7 lo (chunk c
+// at c ^ (h & 7), the 128-byte swizzle the MMA reads).  The whole row is read before any of it
+// is written.  p <= 16 and sig_p <= 28 keep P~ <= 448.
+__device__ __forceinline__ void value_pconvert(const Params& p, int item_begin, int item_end, int items_off,
+                                            uint8_t* smem, uint32_t bars, const dev::WaitCtx& w, int row, int lane)
+{
+    using namespace dev;
+    int g = 0;
+    for (int i = item_begin; i < item_end; ++i) {
+        const Item it = load_item(p.plan, items_off, i);
+        for (int t = it.page_begin; t < it.page_end; ++t, ++g) {
+            const int buf = g % kMsgSlots;
+            if (!wait_warp_ool<true>(bars + 8 * (kMsgFull0 + buf), g / kMsgSlots, w)) return;
+            if (lane == 0 && row == 0) MLA_EV(12, g);
+            const uint8_t* stats = smem + kOffStats + buf * kStatsBytes;
+            uint8_t* prow = smem + kOffP + buf * kPBytes + (row >> 3) * 1024 + (row & 7) * 128;
+            uint4 x[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) x[c] = *reinterpret_cast<const uint4*>(prow + ((c ^ (row & 7)) << 4));
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {  // tokens 16k..16k+15: chunks 2k, 2k+1 of p
+                const float* sp = reinterpret_cast<const float*>(stats + k * kStatsWarpBytes) + kSigPWord;
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint4 v = x[2 * k + h];
+                    const float4 f0 = *reinterpret_cast<const float4*>(sp + 8 * h);
+                    const float4 f1 = *reinterpret_cast<const float4*>(sp + 8 * h + 4);
+                    split_e4m3x4(bf16_lo(v.x) * f0.x, bf16_hi(v.x) * f0.y, bf16_lo(v.y) * f0.z, bf16_hi(v.y) * f0.w,
+                                 hi[2 * h], lo[2 * h]);
+                    split_e4m3x4(bf16_lo(v.z) * f1.x, bf16_hi(v.z) * f1.y, bf16_lo(v.w) * f1.z, bf16_hi(v.w) * f1.w,
+                                 hi[2 * h + 1], lo[2 * h + 1]);
+                }
+                *reinterpret_cast<uint4*>(prow + ((k ^ (row & 7)) << 4)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4*>(prow + (((k + 4) ^ (row & 7)) << 4)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+            fence_proxy_async_cta();  // read by the MMA (async proxy)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars + 8 * (kPReady0 + buf));
+            if (lane == 0 && row == 0) MLA_EV(14, g);
+        }
+    }
 }
 
 // Normalised output of an item: O / (g l) to o_lat (bf16, sole item of its sequence) or to the
@@ -896,7 +966,7 @@ __device__ __forceinline__ void value_correction(const Params& p, int item_begin
         float inv_l = 0.f;
         for (int t = it.page_begin; t < it.page_end; ++t, ++g) {
             const int buf = g % kMsgSlots;
-            if (!wait_warp<true>(bars + 8 * (kMsgFull0 + buf), g / kMsgSlots, w)) goto done;
+            if (!wait_warp_ool<true>(bars + 8 * (kMsgFull0 + buf), g / kMsgSlots, w)) goto done;
             const float* stats =
                 reinterpret_cast<const float*>(smem + kOffStats + buf * kStatsBytes + q4 * kStatsWarpBytes);
             if (t == it.page_end - 1) inv_l = stats[32 + lane];
@@ -910,7 +980,7 @@ __device__ __forceinline__ void value_correction(const Params& p, int item_begin
 
             // flagged tile: the MMA thread committed o_drain and waits o_ready before this PV
             const int e = n_flagged & 1;
-            if (!wait_warp(bars + 8 * (kODrain0 + e), n_flagged >> 1, w)) goto done;
+            if (!wait_warp_ool(bars + 8 * (kODrain0 + e), n_flagged >> 1, w)) goto done;
             tc_fence_after();
             if (boundary) {  // the previous item's output leaves TMEM before this PV overwrites it
                 write_output(p, prev, prev_inv_l, tmem, lane_off, row);
@@ -921,7 +991,7 @@ __device__ __forceinline__ void value_correction(const Params& p, int item_begin
                 // P~ = 0 times them stays 0 in the PV contraction
                 const int valid = min(64, it.seq_len - 64 * t);
                 const int s = g % kValueStages;
-                if (!wait_warp(bars + 8 * (kFull0 + s), g / kValueStages, w)) goto done;
+                if (!wait_warp_ool(bars + 8 * (kFull0 + s), g / kValueStages, w)) goto done;
                 uint8_t* stage = smem + s * kValueStageBytes;
                 const int chunks = (64 - valid) * 32;  // rows x (4 boxes x 8 chunks of 16 B)
                 for (int c = tid128; c < chunks; c += 128) {
@@ -952,7 +1022,7 @@ __device__ __forceinline__ void value_correction(const Params& p, int item_begin
     }
     if (have_prev) {
         // last item: every PV is done when the MMA thread's final commit lands
-        if (!wait_warp(bars + 8 * kDrain, 0, w)) goto done;
+        if (!wait_warp_ool(bars + 8 * kDrain, 0, w)) goto done;
         tc_fence_after();
         write_output(p, prev, prev_inv_l, tmem, lane_off, row);
     }
@@ -962,6 +1032,10 @@ done:
 
 // ---------------------------------------------------------------------------- kernel
 
+// Code size matters here: twelve warps run different roles, and when their hot loops do not fit
+// in the instruction caches every role slows down (instruction-fetch stalls led the profile of
+// a 163 KB build).  So the per-chunk and per-row loops stay rolled, barrier polling runs out of
+// line, and the query load (once per item) is a separate function.
 // 12 warps: each SM sub-partition holds three, and its 16K registers allow 3 x 32 x 168.
 __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
 decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_c8, const __grid_constant__ CUtensorMap tm_kr,
@@ -990,6 +1064,7 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_c8, const __grid_consta
             mbar_init(bars + 8 * (kODrain0 + b), 1);
         }
         for (int b = 0; b < kMsgSlots; ++b) {
+            mbar_init(bars + 8 * (kPReady0 + b), 4);       // the four P converter warps
             mbar_init(bars + 8 * (kMsgFree0 + b), 1 + 4);  // PV commit + four correction warps
             mbar_init(bars + 8 * (kMsgFull0 + b), 1);      // the acknowledgement thread's arm + the bytes
             mbar_init(bars + 8 * (kCopied0 + b), 1);       // the message landed in the value CTA
@@ -1047,8 +1122,10 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_c8, const __grid_consta
                                  threadIdx.x - 64);
             else if (warp == kAckWarp) {
                 if (lane == 0) value_ack(p, item_begin, item_end, items_off, bars, w);
-            }
-            // warps 7-11 of the value CTA have no role
+            } else if (warp >= kPConvWarp0 && warp < kPConvWarp0 + 4)
+                value_pconvert(p, item_begin, item_end, items_off, smem, bars, w, 32 * (warp - kPConvWarp0) + lane,
+                               lane);
+            // warp 11 of the value CTA has no role
         }
     }
     tc_fence_before();

@@ -140,6 +140,30 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t phase, const Wa
     return __all_sync(0xffffffffu, wait_phase<kCluster>(bar, phase, w));
 }
 
+// The same waits with the polling loop out of line, for kernels whose instruction footprint
+// matters more than the call: the loop runs only when the barrier is not ready yet, and one
+// shared copy keeps every wait site small in the instruction cache.
+template <bool kCluster>
+__device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t phase, volatile int* abort, uint64_t timeout_ns,
+                                             uint32_t* dev_error)
+{
+    const WaitCtx w{timeout_ns, abort, dev_error};
+    return wait_phase<kCluster>(bar, phase, w);
+}
+
+template <bool kCluster = false>
+__device__ __forceinline__ bool wait_phase_ool(uint32_t bar, uint32_t phase, const WaitCtx& w)
+{
+    if (kCluster ? mbar_try_wait_cluster(bar, phase & 1u) : mbar_try_wait(bar, phase & 1u)) return true;
+    return wait_phase_slow<kCluster>(bar, phase, w.abort, w.timeout_ns, w.dev_error);
+}
+
+template <bool kCluster = false>
+__device__ __forceinline__ bool wait_warp_ool(uint32_t bar, uint32_t phase, const WaitCtx& w)
+{
+    return __all_sync(0xffffffffu, wait_phase_ool<kCluster>(bar, phase, w));
+}
+
 // Drain wait used on the way out after an abort: ignores the abort flag, own deadline.
 __device__ __forceinline__ bool drain_phase(uint32_t bar, uint32_t phase, uint64_t timeout_ns)
 {
