@@ -277,6 +277,7 @@ __device__ __forceinline__ void score_producer(const CUtensorMap* tm, const Para
 #pragma unroll
                 for (int q = 0; q < kGroupPages; ++q) pages[q] = __shfl_sync(0xffffffffu, page, min(j + q, 31));
                 if (lane == 0) {
+#pragma unroll 1
                     for (int box = 0; box < kBoxesPerRow && ok; ++box, ++c) {
                         if (c >= kChunkStages)
                             ok = MLA_TIMED(1, wait_phase(bars + 8 * (kEmpty0 + s), phase - 1, w));
@@ -328,8 +329,8 @@ __device__ __forceinline__ void score_mma(const Params& p, int item_begin, int i
             const uint32_t idesc = idesc_bf16(128, 64 * npg, false, false);
             if (G >= 1 && !MLA_TIMED(4, wait_phase(bars + 8 * kSFree0, G - 1, w))) goto out;
             MLA_EV(3, G);
-#pragma unroll
-            for (int box = 0; box < kBoxesPerRow; ++box) {
+#pragma unroll 1
+            for (int box = 0; box < kBoxesPerRow; ++box) {  // rolled: a small loop stays in the instruction cache
                 if (!MLA_TIMED(3, wait_phase(full0 + 8 * s, phase, w))) goto out;
                 MLA_EV(1, 9 * G + box);
                 tc_fence_after();
