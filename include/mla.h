@@ -134,7 +134,8 @@ MLA_API mla_status mla_absorb_q(const void* q_c, const void* w_uk, void* q_abs, 
  *                   MLA_KV_FP8_E4M3: kv_pool = e4m3 codes [num_pool_pages][64][512],
  *                   kv_scale = fp32 [num_pool_pages][64] (the stored value times the scale is
  *                   the latent), kr_pool = bf16 [num_pool_pages][64][64]; kv_pool and
- *                   kr_pool 16-byte aligned, kv_scale 4-byte aligned.  The codes feed e4m3
+ *                   kr_pool 16-byte aligned, kv_scale 4-byte aligned; scales finite and >= 0
+ *                   (absmax / 448 per token; 0 marks an all-zero latent row).  The codes feed e4m3
  *                   tensor-core MMAs as loaded; q_abs and P enter them as e4m3 pairs (hi +
  *                   lo, about 2^-8 relative), the scales are applied to the scores and to P
  *                   per token, and k_R / scale is formed in bf16 for the RoPE MMA.

@@ -11,7 +11,7 @@
 // [128, 256).  q~ is held as a pair of e4m3 matrices q_hi = e4m3(q~), q_lo = e4m3(q~ - q_hi),
 // exact to about 2^-8 relative wherever |q~| >= 1/4; QK runs one e4m3 MMA for each, which at
 // twice the bf16 rate costs the tensor time of one bf16 MMA.  A converter warp divides each
-// page's k_R rows by sigma_t in shared memory (packed bf16 multiplies), so that the RoPE MMA
+// page's k_R rows by sigma_t in shared memory (fp32 products, one bf16 rounding), so that the RoPE MMA
 // (bf16, q_R 2^e_h) accumulates into the same fp32 scores; the softmax then scales column t
 // by sigma_t and row h by 2^-e_h.
 //
@@ -206,13 +206,6 @@ __device__ __forceinline__ void split_e4m3x4(float x0, float x1, float x2, float
         "mov.b32 %1, {l01, l23};\n\t}"
         : "=r"(hi), "=r"(lo)
         : "f"(x0), "f"(x1), "f"(x2), "f"(x3));
-}
-
-__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b)
-{
-    uint32_t d;
-    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
 }
 
 // 2^e as a float, e clamped to [-64, 64].
@@ -410,7 +403,9 @@ __device__ __forceinline__ void kr_convert(const Params& p, int item_begin, int 
                 const int t = lane + 32 * k, q = k >> 1;
                 const int page = __shfl_sync(0xffffffffu, page_mine, q);  // every lane, before any branch
                 const bool valid = q < npg && page >= 0 && 64 * (pg + q) + (t & 63) < it.seq_len;
-                sig[t] = valid ? sigma[k] * p.scale_log2 : 0.f;
+                // a zero scale (a zero latent row) enters the score side as 2^-64, so that k_R /
+                // sigma stays finite and sigma (q . c8 + q_R . k_R / sigma) is still q_R . k_R
+                sig[t] = valid ? fmaxf(sigma[k], 5.421011e-20f) * p.scale_log2 : 0.f;
                 sig[256 + t] = valid ? sigma[k] * g : 0.f;
             }
             if (lane == 0) sig[512] = g;
@@ -423,18 +418,17 @@ __device__ __forceinline__ void kr_convert(const Params& p, int item_begin, int 
             for (int t = lane; t < 64 * npg; t += 32) {
                 // 1 / sigma_t (sigma >= 2^-64); a slot past the sequence end gets 0 (its score is masked)
                 const float ss = sig[t];
-                const float inv = ss > 0.f ? 1.f / fmaxf(ss * inv_scale, 5.421011e-20f) : 0.f;
-                const uint32_t inv2 = pack_bf16x2(inv, inv);
+                const float inv = ss > 0.f ? 1.f / (ss * inv_scale) : 0.f;
                 uint8_t* row = rows + t * 128;  // 16-byte chunks in any order: the divide is per element
                 uint4 v[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) v[j] = *reinterpret_cast<const uint4*>(row + (((j + lane) & 7) << 4));
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    v[j].x = mul_bf16x2(v[j].x, inv2);
-                    v[j].y = mul_bf16x2(v[j].y, inv2);
-                    v[j].z = mul_bf16x2(v[j].z, inv2);
-                    v[j].w = mul_bf16x2(v[j].w, inv2);
+                for (int j = 0; j < 8; ++j) {  // fp32 product, one bf16 rounding per value
+                    v[j].x = pack_bf16x2(bf16_lo(v[j].x) * inv, bf16_hi(v[j].x) * inv);
+                    v[j].y = pack_bf16x2(bf16_lo(v[j].y) * inv, bf16_hi(v[j].y) * inv);
+                    v[j].z = pack_bf16x2(bf16_lo(v[j].z) * inv, bf16_hi(v[j].z) * inv);
+                    v[j].w = pack_bf16x2(bf16_lo(v[j].w) * inv, bf16_hi(v[j].w) * inv);
                     *reinterpret_cast<uint4*>(row + (((j + lane) & 7) << 4)) = v[j];
                 }
             }

@@ -98,3 +98,29 @@ def test_fp8_end_to_end_b128_s8192_sampled():
     full[:, heads, :] = o
     ref = oracle.out_proj(full, inp.w_uv)[:, heads, :]
     assert_close(out[:, heads, :], ref, TOL_FP8, "out (3 heads, fp8 cache)")
+
+
+def test_fp8_zero_and_wide_scales():
+    """Per-token scales spread over 2^-8 .. 2^0 of their absmax value within each sequence (the
+    latents stay O(1), so the absolute bound keeps its meaning), and some tokens with a zero scale
+    (an all-zero latent row: its score is q_R . k_R alone, and it adds nothing to o)."""
+    lens = [700, 2000, 65]
+    inp = synth.make_inputs(lens, seed=811, kv_dtype="fp8_e4m3", poison_tail=True)
+    gen = torch.Generator().manual_seed(812)
+    spread = torch.pow(2.0, torch.randint(-8, 1, inp.kv_scale.shape, generator=gen).float())
+    zero = torch.rand(inp.kv_scale.shape, generator=gen) < 0.05
+    inp.kv_scale = torch.where(zero, torch.zeros_like(inp.kv_scale), inp.kv_scale * spread).contiguous()
+    o_lat, lse, info, q = _decode_only(inp, min_pages=3)
+    _check_latent(inp, o_lat, lse, q)
+
+
+def test_fp8_sharp_softmax_rescales():
+    """Queries scaled by 8: scores with a spread of about 8 nats, so the running max moves past the
+    rescale threshold often and P~ spans the whole e4m3 range.  (The error grows with the spread:
+    k_R / sigma is rounded to bf16 for the RoPE MMA, 2^-9 per value; at a spread of 16 nats the
+    largest output error reaches about 0.06.)"""
+    inp = synth.make_inputs([1500, 300], seed=813, kv_dtype="fp8_e4m3", poison_tail=True)
+    inp.q_c = (inp.q_c.float() * 8).to(torch.bfloat16)
+    inp.q_r = (inp.q_r.float() * 8).to(torch.bfloat16)
+    o_lat, lse, info, q = _decode_only(inp, min_pages=4)
+    _check_latent(inp, o_lat, lse, q)
