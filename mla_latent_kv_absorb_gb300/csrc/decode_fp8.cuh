@@ -11,7 +11,8 @@
 // [128, 256).  q~ is held as a pair of e4m3 matrices q_hi = e4m3(q~), q_lo = e4m3(q~ - q_hi),
 // exact to about 2^-8 relative wherever |q~| >= 1/4; QK runs one e4m3 MMA for each, which at
 // twice the bf16 rate costs the tensor time of one bf16 MMA.  A converter warp divides each
-// page's k_R rows by sigma_t in shared memory (fp32 products, one bf16 rounding), so that the RoPE MMA
+// page's k_R rows by sigma_t in shared memory (bf16x2 fused multiply-adds by a two-part 1/sigma,
+// one rounding), so that the RoPE MMA
 // (bf16, q_R 2^e_h) accumulates into the same fp32 scores; the softmax then scales column t
 // by sigma_t and row h by 2^-e_h.
 //
@@ -206,6 +207,20 @@ __device__ __forceinline__ void split_e4m3x4(float x0, float x1, float x2, float
         "mov.b32 %1, {l01, l23};\n\t}"
         : "=r"(hi), "=r"(lo)
         : "f"(x0), "f"(x1), "f"(x2), "f"(x3));
+}
+
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t fma_bf16x2(uint32_t a, uint32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
 }
 
 // 2^e as a float, e clamped to [-64, 64].
@@ -419,16 +434,22 @@ __device__ __forceinline__ void kr_convert(const Params& p, int item_begin, int 
                 // 1 / sigma_t (sigma >= 2^-64); a slot past the sequence end gets 0 (its score is masked)
                 const float ss = sig[t];
                 const float inv = ss > 0.f ? 1.f / (ss * inv_scale) : 0.f;
+                // 1/sigma as a bf16 pair inv_hi + inv_lo; k * inv_hi + (k * inv_lo) in one fused
+                // bf16x2 multiply-add rounds once (the inner product is 2^-8 smaller, so its own
+                // rounding is below 2^-16 of the result)
+                const float inv_hi_f = __bfloat162float(__float2bfloat16_rn(inv));
+                const uint32_t inv_hi = pack_bf16x2(inv_hi_f, inv_hi_f);
+                const uint32_t inv_lo = pack_bf16x2(inv - inv_hi_f, inv - inv_hi_f);
                 uint8_t* row = rows + t * 128;  // 16-byte chunks in any order: the divide is per element
                 uint4 v[8];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) v[j] = *reinterpret_cast<const uint4*>(row + (((j + lane) & 7) << 4));
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {  // fp32 product, one bf16 rounding per value
-                    v[j].x = pack_bf16x2(bf16_lo(v[j].x) * inv, bf16_hi(v[j].x) * inv);
-                    v[j].y = pack_bf16x2(bf16_lo(v[j].y) * inv, bf16_hi(v[j].y) * inv);
-                    v[j].z = pack_bf16x2(bf16_lo(v[j].z) * inv, bf16_hi(v[j].z) * inv);
-                    v[j].w = pack_bf16x2(bf16_lo(v[j].w) * inv, bf16_hi(v[j].w) * inv);
+                for (int j = 0; j < 8; ++j) {
+                    v[j].x = fma_bf16x2(v[j].x, inv_hi, mul_bf16x2(v[j].x, inv_lo));
+                    v[j].y = fma_bf16x2(v[j].y, inv_hi, mul_bf16x2(v[j].y, inv_lo));
+                    v[j].z = fma_bf16x2(v[j].z, inv_hi, mul_bf16x2(v[j].z, inv_lo));
+                    v[j].w = fma_bf16x2(v[j].w, inv_hi, mul_bf16x2(v[j].w, inv_lo));
                     *reinterpret_cast<uint4*>(row + (((j + lane) & 7) << 4)) = v[j];
                 }
             }
