@@ -29,17 +29,18 @@
 //
 // Layout of the pair (sm_103a), as decode.cuh:
 //   rank 0, the score CTA: q_hi and q_lo in TMEM (128 columns each, four e4m3 per 32-bit
-//     column), the scores of four pages in the other 256 columns.  Five K-chunks per four-page
-//     group: the k_R box (8 KB per page) and the four 128-column boxes of c8 (8 KB per page),
-//     32 KB each, through a four-slot ring.  Eight softmax warps, the shipper and tracker as in
+//     column), the scores of four pages in the other 256 columns.  Per four-page group the four
+//     128-column boxes of c8 (8 KB per page, 32 KB per K-chunk) stream through a three-slot
+//     ring, and the k_R boxes (8 KB per page) through a buffer of their own.  Eight softmax warps, the shipper and tracker as in
 //     the bf16 kernel; warp 11 turns k_R into k_R / sigma and writes the per-token factors the
 //     softmax needs (sigma * scale * log2(e), sigma * g).
 //   rank 1, the value CTA: O in TMEM (512 columns), four 32 KB c8 page stages, PV from P~;
 //     warps 7-10 form P~ from the shipped p.
 //
 // Pipelines: those of decode.cuh, plus
-//   kr_landed             the group's k_R box has landed (TMA bytes; waited by warp 11, which
-//                         then arrives on the slot's kv_full for the MMA)
+//   kr_landed             the group's k_R boxes have landed in the k_R buffer (TMA bytes;
+//                         waited by warp 11, which loads them)
+//   kr_full / kr_empty    k_R / sigma is in place (warp 11) / the MMA has read it (commit)
 //   sig_ready             counter: groups whose token factors are written (warp 11)
 //   p_ready[4]            the value CTA's P~ of a message is written (its four converter warps)
 #pragma once
@@ -62,14 +63,14 @@ constexpr int kShipperWarp = 10;
 constexpr int kKrWarp = 11;                       // score CTA: k_R / sigma, token factors
 constexpr int kAckWarp = 6;                       // value CTA: message acknowledgements
 constexpr int kPConvWarp0 = 7;                    // value CTA: warps 7-10 turn P into P~ (e4m3 pair)
-constexpr int kChunkStages = 4;
+constexpr int kChunkStages = 3;                   // score CTA: c8 K-chunk ring
 constexpr int kValueStages = 4;
 constexpr int kMaxStages = 4;
 constexpr int kStagingSlots = 4;
 constexpr int kMsgSlots = 4;
 constexpr int kBoxBytes = 64 * 128;               // 64 tokens x 128 bytes (128 e4m3 or 64 bf16)
 constexpr int kC8Boxes = 4;                       // a c8 row: four 128-column boxes
-constexpr int kChunksPerGroup = kC8Boxes + 1;     // the k_R box, then the c8 boxes
+constexpr int kChunksPerGroup = kC8Boxes;         // c8 K-chunks per group (k_R has its own buffer)
 constexpr int kGroupPages = 4;                    // pages per score MMA (N = 256)
 constexpr int kChunkBytes = kGroupPages * kBoxBytes;    // 32 KB
 constexpr int kValueStageBytes = kC8Boxes * kBoxBytes;  // 32 KB: one page of c8
@@ -86,7 +87,8 @@ constexpr int kSigGroupBytes = 2 * 256 * 4 + 16;  // sig_s[256], sig_p[256], g
 // score CTA
 constexpr int kOffQR = 0;
 constexpr int kOffChunks = kOffQR + 128 * 128;
-constexpr int kOffScoreStaging = kOffChunks + kChunkStages * kChunkBytes;
+constexpr int kOffKr = kOffChunks + kChunkStages * kChunkBytes;   // k_R of one group (32 KB)
+constexpr int kOffScoreStaging = kOffKr + kChunkBytes;
 constexpr int kOffStatsStaging = kOffScoreStaging + kStagingSlots * kPBytes;
 constexpr int kOffXchg = kOffStatsStaging + kStagingSlots * kStatsBytes;
 constexpr int kOffSig = kOffXchg + 4 * 2 * 128 * 4;
@@ -111,7 +113,9 @@ enum Bar : int {
     kDrain = kODrain0 + 2,
     kStgReady0 = kDrain + 1,
     kKrLanded = kStgReady0 + kStagingSlots,
-    kPReady0 = kKrLanded + 1,
+    kKrFull = kKrLanded + 1,
+    kKrEmpty = kKrFull + 1,
+    kPReady0 = kKrEmpty + 1,
     kNumBars = kPReady0 + kMsgSlots
 };
 
@@ -120,11 +124,10 @@ constexpr int kOffAbort = kOffTmemHolder + 4;
 constexpr int kOffStgFreed = kOffAbort + 4;     // score CTA: messages whose staging slot may be reused
 constexpr int kOffSigReady = kOffStgFreed + 4;  // score CTA: groups whose token factors are written
 constexpr int kSmemBytes = ((kOffSigReady + 4 + 127) / 128) * 128;
-static_assert(kOffChunks % 1024 == 0 && kOffP % 1024 == 0 && kOffScoreStaging % 1024 == 0,
+static_assert(kOffChunks % 1024 == 0 && kOffKr % 1024 == 0 && kOffP % 1024 == 0 && kOffScoreStaging % 1024 == 0,
               "swizzled tiles need 1024-byte alignment");
 static_assert(kOffSig % 16 == 0 && kSigGroupBytes % 16 == 0, "token factors are read as float4");
 static_assert(kChunkStages <= kMaxStages && kValueStages <= kMaxStages, "barrier slots per ring");
-static_assert(kChunkStages < kChunksPerGroup, "at most one k_R chunk in flight at a time");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kStatsWarpBytes % 16 == 0 && kPWarpBytes % 16 == 0, "bulk copies move multiples of 16 bytes");
 
@@ -279,21 +282,16 @@ __device__ __forceinline__ void value_producer(const CUtensorMap* tm_c8, const P
     }
 }
 
-// Score CTA: chunk j of a four-page group holds one box of the group's pages in rows 0-63,
-// 64-127, 128-191, 192-255: j = 0 the k_R box (its bytes complete kr_landed; warp 11 completes
-// kv_full after the divide), j = 1..4 the 128-column c8 boxes j - 1 (their bytes complete
-// kv_full).  k_R goes first so that it lands, and is divided, while the MMA still works on the
-// group before.
-__device__ __forceinline__ void score_producer(const CUtensorMap* tm_c8, const CUtensorMap* tm_kr, const Params& p,
-                                               int item_begin, int item_end, int items_off, uint32_t sbase,
-                                               uint32_t bars, const dev::WaitCtx& w, int lane)
+// Score CTA: chunk j of a four-page group holds c8 box j (128 columns) of the group's pages in
+// rows 0-63, 64-127, 128-191, 192-255, through a three-slot ring; the k_R box has a buffer of
+// its own that warp 11 fills (see kr_convert).
+__device__ __forceinline__ void score_producer(const CUtensorMap* tm_c8, const Params& p, int item_begin,
+                                               int item_end, int items_off, uint32_t sbase, uint32_t bars,
+                                               const dev::WaitCtx& w, int lane)
 {
     using namespace dev;
     const uint64_t policy = l2_policy_evict_normal();  // the value CTA reads these pages next
-    if (lane == 0) {
-        tma_prefetch_desc(tm_c8);
-        tma_prefetch_desc(tm_kr);
-    }
+    if (lane == 0) tma_prefetch_desc(tm_c8);
     int s = 0, phase = 0, c = 0;
     bool ok = true;
     for (int i = item_begin; i < item_end && ok; ++i) {
@@ -317,17 +315,10 @@ __device__ __forceinline__ void score_producer(const CUtensorMap* tm_c8, const C
                         if (c >= kChunkStages) ok = wait_phase_ool(bars + 8 * (kEmpty0 + s), phase - 1, w);
                         if (!ok) break;
                         const uint32_t dst = sbase + kOffChunks + s * kChunkBytes;
-                        if (box > 0) {
-                            const uint32_t full = bars + 8 * (kFull0 + s);
-                            mbar_arrive_expect_tx(full, npg * kBoxBytes);
-                            for (int q = 0; q < npg; ++q)
-                                tma_load_3d(dst + q * kBoxBytes, tm_c8, full, 128 * (box - 1), 0, pages[q], policy);
-                        } else {
-                            const uint32_t landed = bars + 8 * kKrLanded;
-                            mbar_arrive_expect_tx(landed, npg * kBoxBytes);
-                            for (int q = 0; q < npg; ++q)
-                                tma_load_3d(dst + q * kBoxBytes, tm_kr, landed, 0, 0, pages[q], policy);
-                        }
+                        const uint32_t full = bars + 8 * (kFull0 + s);
+                        mbar_arrive_expect_tx(full, npg * kBoxBytes);
+                        for (int q = 0; q < npg; ++q)
+                            tma_load_3d(dst + q * kBoxBytes, tm_c8, full, 128 * box, 0, pages[q], policy);
                         MLA_EV(0, c);
                         if (++s == kChunkStages) {
                             s = 0;
@@ -339,34 +330,32 @@ __device__ __forceinline__ void score_producer(const CUtensorMap* tm_c8, const C
             }
         }
     }
-    if (lane == 0 && *w.abort) {
-        // Loads still in flight must land before the CTA exits: the last kChunkStages chunks,
-        // at most one of them a k_R chunk (its bytes complete kr_landed, the latest phase).
-        for (int k = (c > kChunkStages ? c - kChunkStages : 0); k < c; ++k) {
-            if (k % kChunksPerGroup == 0)
-                drain_phase(bars + 8 * kKrLanded, k / kChunksPerGroup, w.timeout_ns);
-            else
-                drain_phase(bars + 8 * (kFull0 + k % kChunkStages), k / kChunkStages, w.timeout_ns);
-        }
+    if (lane == 0 && *w.abort) {  // loads still in flight must land before the CTA exits
+        for (int k = (c > kChunkStages ? c - kChunkStages : 0); k < c; ++k)
+            drain_phase(bars + 8 * (kFull0 + k % kChunkStages), k / kChunkStages, w.timeout_ns);
     }
 }
 
 // ---------------------------------------------------------------------------- score CTA
 
 // Warp 11.  Per item, g = 2^floor(log2(28 / max sigma)) over the item's tokens (so that P~ =
-// p sigma g <= 16 * 28 = 448).  Per four-page group, once the k_R box has landed: the token
-// factors for the softmax (sig_s = sigma * scale * log2(e) and sig_p = sigma * g, both 0 past
-// the sequence end, and g) into factor slot G % 4, and every k_R row divided by its token's
-// sigma in place; then kv_full for the MMA.  Factor slot G % 4 is free when warp 11 writes it:
-// warp 11 finished group G - 1 after its k_R box (chunk 5(G-1)) landed, which the producer
-// loaded once the MMA had consumed chunk 5(G-1) - 4, the second chunk of group G - 2, which it
-// issued after s_free of group G - 3; so every softmax warp had finished group G - 4, the last
-// group in slot G % 4.
-__device__ __forceinline__ void kr_convert(const Params& p, int item_begin, int item_end, int items_off,
-                                           uint8_t* smem, uint32_t bars, const dev::WaitCtx& w, int lane)
+// p sigma g <= 16 * 28 = 448).  Per four-page group: once the MMA has read the previous group's
+// k_R (kr_empty), load this group's k_R boxes into the k_R buffer (TMA, kr_landed); meanwhile
+// write the token factors for the softmax (sig_s = sigma * scale * log2(e) and sig_p = sigma *
+// g, both 0 past the sequence end, and g) into factor slot G % 4; then divide every k_R row by
+// its token's sigma in place and arrive on kr_full for the MMA.  Factor slot G % 4 is free when
+// it is written: the MMA had read k_R of group G - 1, so it had started group G - 1, which it
+// does after s_free of group G - 2; every softmax warp had finished group G - 3 then, and slot
+// G % 4 last held group G - 4.  Owning the k_R loads keeps them off the c8 ring: the load for
+// group G + 1 starts as soon as the MMA has taken group G's k_R.
+__device__ __forceinline__ void kr_convert(const CUtensorMap* tm_kr, const Params& p, int item_begin, int item_end,
+                                           int items_off, uint8_t* smem, uint32_t sbase, uint32_t bars,
+                                           const dev::WaitCtx& w, int lane)
 {
     using namespace dev;
     uint32_t* sig_ready = reinterpret_cast<uint32_t*>(smem + kOffSigReady);
+    const uint64_t policy = l2_policy_evict_first();  // nobody else reads k_R
+    if (lane == 0) tma_prefetch_desc(tm_kr);
     int G = 0;
     for (int i = item_begin; i < item_end; ++i) {
         const Item it = load_item(p.plan, items_off, i);
@@ -397,9 +386,8 @@ __device__ __forceinline__ void kr_convert(const Params& p, int item_begin, int 
         }
         for (int pg = it.page_begin; pg < it.page_end; pg += kGroupPages, ++G) {
             const int npg = min(kGroupPages, it.page_end - pg);
-            const int c = kChunksPerGroup * G, s = c % kChunkStages;  // the group's k_R chunk
             float* sig = reinterpret_cast<float*>(smem + kOffSig + (G % kSigSlots) * kSigGroupBytes);
-            // Token t = lane + 32 k of the group (row t of the k_R chunk) sits in page k / 2 at
+            // Token t = lane + 32 k of the group (row t of the k_R buffer) sits in page k / 2 at
             // slot lane + 32 (k & 1).  All page ids, then all eight scales, are loaded before any
             // is used, so the group costs two memory round trips.
             int page_mine = 0;
@@ -407,17 +395,26 @@ __device__ __forceinline__ void kr_convert(const Params& p, int item_begin, int 
                 page_mine = __ldg(bt + pg + lane);
                 if (page_mine < 0 || page_mine >= p.num_pool_pages) page_mine = -1;  // reported by the producers
             }
+            int pages[kGroupPages];
+#pragma unroll
+            for (int q = 0; q < kGroupPages; ++q) pages[q] = __shfl_sync(0xffffffffu, page_mine, q);
+            // the MMA has read the previous group's k_R: load this group's (a bad page id, -1 here,
+            // reads zeros: TMA fills outside the tensor)
+            if (G >= 1 && !wait_warp_ool(bars + 8 * kKrEmpty, G - 1, w)) return;
+            if (lane == 0) {
+                const uint32_t landed = bars + 8 * kKrLanded;
+                mbar_arrive_expect_tx(landed, npg * kBoxBytes);
+                for (int q = 0; q < npg; ++q)
+                    tma_load_3d(sbase + kOffKr + q * kBoxBytes, tm_kr, landed, 0, 0, pages[q], policy);
+            }
             float sigma[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int page = __shfl_sync(0xffffffffu, page_mine, k >> 1);
-                sigma[k] = __ldg(p.kv_scale + (int64_t)max(page, 0) * 64 + lane + 32 * (k & 1));
-            }
+            for (int k = 0; k < 8; ++k)
+                sigma[k] = __ldg(p.kv_scale + (int64_t)max(pages[k >> 1], 0) * 64 + lane + 32 * (k & 1));
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const int t = lane + 32 * k, q = k >> 1;
-                const int page = __shfl_sync(0xffffffffu, page_mine, q);  // every lane, before any branch
-                const bool valid = q < npg && page >= 0 && 64 * (pg + q) + (t & 63) < it.seq_len;
+                const bool valid = q < npg && pages[q] >= 0 && 64 * (pg + q) + (t & 63) < it.seq_len;
                 // a zero scale (a zero latent row) enters the score side as 2^-64, so that k_R /
                 // sigma stays finite and sigma (q . c8 + q_R . k_R / sigma) is still q_R . k_R
                 sig[t] = valid ? fmaxf(sigma[k], 5.421011e-20f) * p.scale_log2 : 0.f;
@@ -425,9 +422,12 @@ __device__ __forceinline__ void kr_convert(const Params& p, int item_begin, int 
             }
             if (lane == 0) sig[512] = g;
             if (lane == 0) MLA_EV(18, G);
-            if (!wait_warp_ool(bars + 8 * kKrLanded, G, w)) return;
+            if (!wait_warp_ool(bars + 8 * kKrLanded, G, w)) {
+                if (lane == 0) drain_phase(bars + 8 * kKrLanded, G, w.timeout_ns);  // the load in flight
+                return;
+            }
             if (lane == 0) MLA_EV(19, G);
-            uint8_t* rows = smem + kOffChunks + s * kChunkBytes;
+            uint8_t* rows = smem + kOffKr;
             const float inv_scale = 1.f / p.scale_log2;
 #pragma unroll 1
             for (int t = lane; t < 64 * npg; t += 32) {
@@ -457,21 +457,22 @@ __device__ __forceinline__ void kr_convert(const Params& p, int item_begin, int 
             __syncwarp();
             if (lane == 0) {
                 st_release_u32(sig_ready, (uint32_t)(G + 1));
-                mbar_arrive(bars + 8 * (kFull0 + s));
+                mbar_arrive(bars + 8 * kKrFull);
                 MLA_EV(13, G);
             }
         }
     }
 }
 
-// QK of a four-page group: S[128 heads x N tokens] accumulated over the five K-chunks: chunk 0
-// runs q_R 2^e (shared memory) against k_R / sigma, four bf16 MMAs of K = 16; chunks 1-4 run
-// q_hi and q_lo (TMEM, "TS") against a 128-column c8 box, eight e4m3 MMAs of K = 32.
+// QK of a four-page group: S[128 heads x N tokens] accumulated over k_R and the four c8
+// K-chunks: k_R / sigma (its own buffer) against q_R 2^e (shared memory), four bf16 MMAs of K =
+// 16; then each c8 chunk against q_hi and q_lo (TMEM, "TS"), eight e4m3 MMAs of K = 32.
 __device__ __forceinline__ void score_mma(const Params& p, int item_begin, int item_end, int items_off, uint32_t sbase,
                                           uint32_t bars, uint32_t tmem, const dev::WaitCtx& w)
 {
     using namespace dev;
     const uint64_t chunk_desc0 = smem_desc(sbase + kOffChunks, 16, 1024);
+    const uint64_t kr_desc = smem_desc(sbase + kOffKr, 16, 1024);
     const uint64_t qr_desc = smem_desc(sbase + kOffQR, 16, 1024);
     const uint32_t full0 = bars + 8 * kFull0, empty0 = bars + 8 * kEmpty0;
     const uint32_t d = tmem + kSCol;
@@ -486,26 +487,27 @@ __device__ __forceinline__ void score_mma(const Params& p, int item_begin, int i
             const uint32_t idesc16 = idesc_bf16(128, 64 * npg, false, false);
             if (G >= 1 && !wait_phase_ool(bars + 8 * kSFree0, G - 1, w)) goto out;
             MLA_EV(3, G);
+            if (!wait_phase_ool(bars + 8 * kKrFull, G, w)) goto out;
+            MLA_EV(1, 5 * G);
+            tc_fence_after();
+            mma_ss(d, qr_desc, kr_desc, idesc16, 0u);
+            mma_ss(d, qr_desc + 2, kr_desc + 2, idesc16, 1u);
+            mma_ss(d, qr_desc + 4, kr_desc + 4, idesc16, 1u);
+            mma_ss(d, qr_desc + 6, kr_desc + 6, idesc16, 1u);
+            mma_commit(bars + 8 * kKrEmpty);
 #pragma unroll 1
             for (int box = 0; box < kChunksPerGroup; ++box) {
                 if (!wait_phase_ool(full0 + 8 * s, phase, w)) goto out;
-                MLA_EV(1, kChunksPerGroup * G + box);
+                MLA_EV(1, 5 * G + 1 + box);
                 tc_fence_after();
                 const uint64_t b0 = chunk_desc0 + (uint64_t)(s * (kChunkBytes >> 4));
-                if (box == 0) {
-                    mma_ss(d, qr_desc, b0, idesc16, 0u);
-                    mma_ss(d, qr_desc + 2, b0 + 2, idesc16, 1u);
-                    mma_ss(d, qr_desc + 4, b0 + 4, idesc16, 1u);
-                    mma_ss(d, qr_desc + 6, b0 + 6, idesc16, 1u);
-                } else {
 #pragma unroll
-                    for (int part = 0; part < 2; ++part) {
-                        const uint32_t a0 = tmem + (part ? kQLoCol : kQHiCol) + 32 * (box - 1);
-                        mma_ts_e4m3(d, a0, b0, idesc8, 1u);
-                        mma_ts_e4m3(d, a0 + 8, b0 + 2, idesc8, 1u);
-                        mma_ts_e4m3(d, a0 + 16, b0 + 4, idesc8, 1u);
-                        mma_ts_e4m3(d, a0 + 24, b0 + 6, idesc8, 1u);
-                    }
+                for (int part = 0; part < 2; ++part) {
+                    const uint32_t a0 = tmem + (part ? kQLoCol : kQHiCol) + 32 * box;
+                    mma_ts_e4m3(d, a0, b0, idesc8, 1u);
+                    mma_ts_e4m3(d, a0 + 8, b0 + 2, idesc8, 1u);
+                    mma_ts_e4m3(d, a0 + 16, b0 + 4, idesc8, 1u);
+                    mma_ts_e4m3(d, a0 + 24, b0 + 6, idesc8, 1u);
                 }
                 mma_commit(empty0 + 8 * s);
                 if (++s == kChunkStages) {
@@ -576,52 +578,53 @@ __device__ __noinline__ float load_query(const Params& p, int seq, int row, int 
     return exp2i(-e);
 }
 
-// One page of raw scores in registers -> y = S * sig_s[t] (sig_s = sigma_t * scale * log2(e)),
-// slots past the sequence end set to -inf (the raw score there may be NaN); returns max_t y.
-__device__ __forceinline__ float page_scale_max(uint32_t (&sr)[64], const float* sig_s, int valid)
+// Row max of one page of raw scores in registers, in log2 units before the row factor:
+// max_t S[t] * sig_s[t] (sig_s = sigma_t * scale * log2(e)) over the slots before the sequence
+// end (the raw score past it may be NaN).  The scores stay untouched in their registers.
+__device__ __forceinline__ float page_scale_max(const uint32_t (&sr)[64], const float* sig_s, int valid)
 {
-    float m8[8];
-#pragma unroll
-    for (int a = 0; a < 8; ++a) m8[a] = -INFINITY;
+    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
     for (int v = 0; v < 16; ++v) {
         const float4 f = *reinterpret_cast<const float4*>(sig_s + 4 * v);
-        const float fs[4] = {f.x, f.y, f.z, f.w};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int j = 4 * v + u;
-            const float y = j < valid ? __uint_as_float(sr[j]) * fs[u] : -INFINITY;
-            sr[j] = __float_as_uint(y);
-            m8[j & 7] = fmaxf(m8[j & 7], y);
-        }
+        const int j = 4 * v;
+        m4[0] = fmaxf(m4[0], j + 0 < valid ? __uint_as_float(sr[j + 0]) * f.x : -INFINITY);
+        m4[1] = fmaxf(m4[1], j + 1 < valid ? __uint_as_float(sr[j + 1]) * f.y : -INFINITY);
+        m4[2] = fmaxf(m4[2], j + 2 < valid ? __uint_as_float(sr[j + 2]) * f.z : -INFINITY);
+        m4[3] = fmaxf(m4[3], j + 3 < valid ? __uint_as_float(sr[j + 3]) * f.w : -INFINITY);
     }
-    return fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+    return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
 }
 
-// Softmax of one page: p = 2^(y 2^-e - m) (one FMA and one MUFU.EX2 per score), written as bf16
+// Softmax of one page: p = 2^(S sig_s[t] 2^-e - m) (0 past the sequence end), written as bf16
 // into this thread's row of the swizzled staging tile (16-byte chunk c of the row goes to chunk
 // c ^ (row & 7)), the layout of the bf16 kernel.  The value CTA scales it by sigma_t g and
 // splits it into the e4m3 pair.  Returns the row sum of p.
-__device__ __forceinline__ float page_softmax(const uint32_t (&sr)[64], float r_h, float m_used, uint8_t* stage_row,
-                                              int row)
+__device__ __forceinline__ float page_softmax(const uint32_t (&sr)[64], const float* sig_s, int valid, float r_h,
+                                              float m_used, uint8_t* stage_row, int row)
 {
     using namespace dev;
-    float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
+        const float4 f0 = *reinterpret_cast<const float4*>(sig_s + 8 * c);
+        const float4 f1 = *reinterpret_cast<const float4*>(sig_s + 8 * c + 4);
+        const float fs[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
         uint32_t pk[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int j = 8 * c + 2 * q;
-            const float p0 = ex2_approx(fmaf(__uint_as_float(sr[j]), r_h, -m_used));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(sr[j + 1]), r_h, -m_used));
+            float p0 = ex2_approx(fmaf(__uint_as_float(sr[j]) * fs[2 * q], r_h, -m_used));
+            float p1 = ex2_approx(fmaf(__uint_as_float(sr[j + 1]) * fs[2 * q + 1], r_h, -m_used));
+            p0 = j < valid ? p0 : 0.f;
+            p1 = j + 1 < valid ? p1 : 0.f;
             pk[q] = pack_bf16x2(p0, p1);
-            l8[(2 * q) & 7] += p0;
-            l8[(2 * q + 1) & 7] += p1;
+            l4[(2 * q) & 3] += p0;
+            l4[(2 * q + 1) & 3] += p1;
         }
         *reinterpret_cast<uint4*>(stage_row + ((c ^ (row & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
     }
-    return ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+    return (l4[0] + l4[1]) + (l4[2] + l4[3]);
 }
 
 // Finish this warp's part of staged message `slot`: its statistics block (per-row O rescale
@@ -721,31 +724,36 @@ __device__ __forceinline__ void score_softmax(const Params& p, int item_begin, i
             // only clears `ok`, and each barrier ORs the abort state so the sets leave together.
             bool ok = wait_warp_ool(bars + 8 * kSFull0, G, w);
             if (lane == 0 && warp == 2) MLA_EV(4, G);
-            uint32_t sr[2][64];
+            // One page of scores in registers at a time (a second one would spill into local
+            // memory, which the shared-memory carve-out leaves little L1 for): the first page
+            // stays, the second is read once for its max and again after the first page's P,
+            // and the score buffer is freed after that second read.
+            uint32_t sr[64];
+            const uint32_t scol = tmem + lane_off + kSCol + 128 * set;
             const int t0 = pg + 2 * set;
             const int valid0 = min(64, it.seq_len - 64 * t0), valid1 = min(64, it.seq_len - 64 * (t0 + 1));
             float mx = -INFINITY;
+            if (ok) ok = wait_freed(sig_ready, (uint32_t)(G + 1), w);  // this group's token factors
             if (ok) {
                 tc_fence_after();
-                if (n_mine > 0) {
-                    const uint32_t scol = tmem + lane_off + kSCol + 128 * set;
-                    tmem_ld32(scol, *reinterpret_cast<uint32_t(*)[32]>(&sr[0][0]));
-                    tmem_ld32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[0][32]));
-                    if (n_mine > 1) {
-                        tmem_ld32(scol + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[1][0]));
-                        tmem_ld32(scol + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[1][32]));
-                    }
+                if (n_mine > 1) {  // the second page: max only
+                    tmem_ld32(scol + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+                    tmem_ld32(scol + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
                     tmem_wait_ld();
+                    mx = page_scale_max(sr, sig + 64 * (2 * set + 1), valid1);
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bars + 8 * kSFree0);  // the next group's QK may start
-                ok = wait_freed(sig_ready, (uint32_t)(G + 1), w);  // this group's token factors
-                if (ok) {
-                    if (n_mine > 0) mx = page_scale_max(sr[0], sig + 64 * (2 * set), valid0);
-                    if (n_mine > 1) mx = fmaxf(mx, page_scale_max(sr[1], sig + 64 * (2 * set + 1), valid1));
-                    g_item = sig[512];
+                if (n_mine > 0) {
+                    tmem_ld32(scol, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+                    tmem_ld32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+                    tmem_wait_ld();
+                    mx = fmaxf(mx, page_scale_max(sr, sig + 64 * (2 * set), valid0));
                 }
+                if (n_mine < 2) {  // nothing left to read: the next group's QK may start
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bars + 8 * kSFree0);
+                }
+                g_item = sig[512];
                 if (lane == 0 && warp == 2) MLA_EV(5, G);
             }
 
@@ -764,14 +772,23 @@ __device__ __forceinline__ void score_softmax(const Params& p, int item_begin, i
             // P~ of my pages into staging slot (message % 4), free once the value CTA received
             // the message four before; the item's last page waits for 1/(g l) below
             bool hold_last = false;
-#pragma unroll
+#pragma unroll 1
             for (int j = 0; j < 2; ++j) {
                 if (j >= n_mine || !ok) break;
+                if (j == 1) {  // the second page again, then the score buffer is free
+                    tmem_ld32(scol + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+                    tmem_ld32(scol + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bars + 8 * kSFree0);
+                }
                 const int gg = g + 2 * set + j;
                 const int slot = gg % kStagingSlots;
                 if (gg >= kStagingSlots) ok = wait_freed(freed, (uint32_t)(gg - kStagingSlots + 1), w);
                 if (!ok) break;
-                l_mine += page_softmax(sr[j], r_h, m_used, smem + kOffScoreStaging + slot * kPBytes + p_row_off, row);
+                l_mine += page_softmax(sr, sig + 64 * (2 * set + j), j ? valid1 : valid0, r_h, m_used,
+                                       smem + kOffScoreStaging + slot * kPBytes + p_row_off, row);
                 const float f_page = (set == 0 && j == 0) ? factor : 1.f;  // O rescale precedes page 0
                 if (t0 + j == it.page_end - 1)
                     hold_last = true;
@@ -1087,6 +1104,8 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_c8, const __grid_consta
         mbar_init(bars + 8 * kQReady, 8);                  // one arrive per softmax warp
         for (int s = 0; s < kStagingSlots; ++s) mbar_init(bars + 8 * (kStgReady0 + s), 4);  // one set's warps
         mbar_init(bars + 8 * kKrLanded, 1);
+        mbar_init(bars + 8 * kKrFull, 1);   // warp 11: the group's k_R / sigma is in place
+        mbar_init(bars + 8 * kKrEmpty, 1);  // the MMA's commit after the k_R MMAs
         *reinterpret_cast<volatile uint32_t*>(smem + kOffStgFreed) = 0;
         *reinterpret_cast<volatile uint32_t*>(smem + kOffSigReady) = 0;
         mbar_init(bars + 8 * kDrain, 1);
@@ -1117,7 +1136,7 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_c8, const __grid_consta
         const int item_end = cluster < n_clusters ? p.plan[cl_off + cluster + 1] : 0;
         if (rank == 0) {
             if (warp == 0)
-                score_producer(&tm_c8, &tm_kr, p, item_begin, item_end, items_off, sbase, bars, w, lane);
+                score_producer(&tm_c8, p, item_begin, item_end, items_off, sbase, bars, w, lane);
             else if (warp == 1) {
                 if (lane == 0) score_mma(p, item_begin, item_end, items_off, sbase, bars, tmem, w);
             } else if (warp >= 2 && warp < 10)
@@ -1126,7 +1145,7 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_c8, const __grid_consta
                 if (lane == 0) score_shipper(p, item_begin, item_end, items_off, smem, sbase, bars, w);
                 else if (lane == 1) score_tracker(p, item_begin, item_end, items_off, smem, bars, w);
             } else if (warp == kKrWarp)
-                kr_convert(p, item_begin, item_end, items_off, smem, bars, w, lane);
+                kr_convert(&tm_kr, p, item_begin, item_end, items_off, smem, sbase, bars, w, lane);
         } else {
             if (warp == 0)
                 value_producer(&tm_c8, p, item_begin, item_end, items_off, sbase, bars, w, lane);
