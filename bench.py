@@ -355,9 +355,9 @@ def sampled_parity(inp, out_dev):
 
 
 def run_e2e(args, inp, step, binding, device, stream):
-    """Through the public API with host buffers (DecodeStep.run_host): every step re-plans for
-    the sequence lengths, uploads plan, block table and queries from pinned memory in one
-    transfer, runs the kernels and reads the output back."""
+    """Through the public API with host buffers (DecodeStep.run_host, one mla_decode_step_host
+    call): every step plans for the sequence lengths on the host, uploads plan, block table and
+    queries from pinned memory, runs the kernels and reads the output back."""
     q_c_h = inp.q_c.pin_memory()
     q_r_h = inp.q_r.pin_memory()
     bt_h = torch.from_numpy(np.ascontiguousarray(inp.block_table)).pin_memory()
@@ -369,7 +369,7 @@ def run_e2e(args, inp, step, binding, device, stream):
         step.run_host(q_c_h, q_r_h, block_table=bt_h, seq_lens=inp.seq_lens, out=out_h, stream=stream)
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
-    h2d = step.plan_host.nbytes + bt_h.numel() * 4 + q_c_h.numel() * 2 + q_r_h.numel() * 2
+    h2d = int(step.info.plan_bytes) + bt_h.numel() * 4 + q_c_h.numel() * 2 + q_r_h.numel() * 2
     d2h = out_h.numel() * 2
     return {"value": round(statistics.mean(times) * 1e6, 2), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h)}

@@ -207,6 +207,49 @@ MLA_API mla_status mla_decode_paged_static_ws(const mla_plan_info* info, const v
                             float softmax_scale, void* o_lat, float* lse, uint32_t* dev_error,
                             void* stream);
 
+/* ---- the whole step from host memory in one call ------------------------------------------
+ * For callers whose queries, block table and lengths live in host memory: plans the step for
+ * `seq_lens` on the host (as mla_plan_splits), copies the plan, the block table (when
+ * block_table_host is not NULL) and the queries to the device (one cudaMemcpyAsync each, from
+ * pinned memory for asynchronous DMA), runs absorb, decode, merge and out-proj on `stream`,
+ * copies `out` back to out_host and waits for the stream.  One library call instead of a dozen
+ * binding-level operations; it computes exactly what the four calls above compute.
+ *   bufs              the device buffers, owned by the caller and sized for `batch`:
+ *                       q_c, q_r, q_abs, o_lat, lse, out (as above), dev_error,
+ *                       block_table  int32 [batch][max_pages_per_seq] (written when a host table
+ *                                    is given, else read as it stands),
+ *                       plan         >= mla_plan_bytes_max(batch, num_sms) bytes, 16-byte aligned,
+ *                       workspace    workspace_bytes >= the plan's workspace_bytes (else
+ *                                    MLA_ERR_WORKSPACE before anything is copied or launched);
+ *                     and plan_host: pinned host memory of plan_capacity >= mla_plan_bytes_max.
+ *   q_c_host, q_r_host  host bf16 [batch][128][128] / [batch][128][64]
+ *   out_host          host bf16 [batch][128][128], receives out
+ *   info_out          may be NULL; receives the plan header
+ * Device-side errors land in bufs->dev_error as for mla_decode_paged (read it afterwards). */
+typedef struct mla_step_buffers {
+    void* q_c;
+    void* q_r;
+    void* q_abs;
+    int32_t* block_table;
+    void* plan;
+    void* workspace;
+    size_t workspace_bytes;
+    void* o_lat;
+    float* lse;
+    void* out;
+    uint32_t* dev_error;
+    void* plan_host;
+    size_t plan_capacity;
+} mla_step_buffers;
+
+MLA_API mla_status mla_decode_step_host(const int32_t* seq_lens, int32_t batch, int32_t num_sms,
+                                        const mla_plan_options* opts, const void* q_c_host, const void* q_r_host,
+                                        const int32_t* block_table_host, int32_t max_pages_per_seq,
+                                        const void* w_uk, const void* w_uv, mla_kv_dtype kv_dtype,
+                                        const void* kv_pool, const float* kv_scale, const void* kr_pool,
+                                        int32_t num_pool_pages, float softmax_scale, const mla_step_buffers* bufs,
+                                        void* out_host, mla_plan_info* info_out, void* stream);
+
 /* ---------------------------------------------------------------- device error word
  *
  * Waits for `stream`, copies the device word to *host_bits (may be NULL) and returns

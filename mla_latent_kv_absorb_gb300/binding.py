@@ -49,12 +49,21 @@ class PlanInfo(ctypes.Structure):
 
 EXPORTS = ("mla_status_string", "mla_last_error_string", "mla_plan_bytes_max", "mla_plan_splits", "mla_absorb_q", "mla_decode_paged",
            "mla_combine_splits", "mla_out_proj", "mla_read_device_error", "mla_debug_wait_timeout",
-           "mla_decode_paged_static_ws")
+           "mla_decode_paged_static_ws", "mla_decode_step_host")
 
 # capacity of the library's fixed split-partial array (mla_decode_paged_static_ws)
 MLA_STATIC_WS_MAX_PARTIALS = 128
 
 _lib = None
+
+
+class StepBuffers(ctypes.Structure):
+    """mla_step_buffers: the device buffers of mla_decode_step_host, plus its pinned plan staging."""
+    _fields_ = [("q_c", ctypes.c_void_p), ("q_r", ctypes.c_void_p), ("q_abs", ctypes.c_void_p),
+                ("block_table", ctypes.c_void_p), ("plan", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t), ("o_lat", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+                ("out", ctypes.c_void_p), ("dev_error", ctypes.c_void_p), ("plan_host", ctypes.c_void_p),
+                ("plan_capacity", ctypes.c_size_t)]
 
 
 def lib() -> ctypes.CDLL:
@@ -87,6 +96,10 @@ def lib() -> ctypes.CDLL:
     L.mla_combine_splits.argtypes = [ctypes.POINTER(PlanInfo), P, P, sz, P, P, P]
     L.mla_out_proj.restype = ctypes.c_int
     L.mla_out_proj.argtypes = [P, P, P, i32, P]
+    L.mla_decode_step_host.restype = ctypes.c_int
+    L.mla_decode_step_host.argtypes = [P, i32, i32, ctypes.POINTER(PlanOptions), P, P, P, i32, P, P, ctypes.c_int, P,
+                                       P, P, i32, ctypes.c_float, ctypes.POINTER(StepBuffers), P,
+                                       ctypes.POINTER(PlanInfo), P]
     L.mla_read_device_error.restype = ctypes.c_int
     L.mla_read_device_error.argtypes = [u32p, ctypes.POINTER(ctypes.c_uint32), P]
     L.mla_debug_wait_timeout.restype = ctypes.c_int
@@ -109,6 +122,10 @@ def _check(fn: str, status: int) -> None:
 
 def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _addr(t: Optional[torch.Tensor]) -> int:
+    return 0 if t is None else int(t.data_ptr())
 
 
 def _stream(stream) -> ctypes.c_void_p:
@@ -311,64 +328,60 @@ class DecodeStep:
 
     def run_host(self, q_c: torch.Tensor, q_r: torch.Tensor, *, block_table: Optional[torch.Tensor] = None,
                  seq_lens=None, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-        """One decode step from host (CPU) tensors, end to end.
-
-        If ``seq_lens`` is given the step is re-planned for those lengths (same batch size).
-        The plan image goes to the GPU through a pinned buffer kept by this object; the block
-        table (a CPU int32 [batch, max_pages] tensor, when given; otherwise the device table
-        given at construction is used) and the queries are copied straight from the caller's
-        tensors (asynchronous DMA when they are pinned); the four kernels run; ``out`` (a pinned
-        CPU bf16 [batch, 128, 128] tensor, allocated once if not given) receives the result.
-        Waits for the stream before returning ``out``."""
+        """One decode step from host (CPU) tensors, end to end, in one library call
+        (``mla_decode_step_host``): plan on the host for ``seq_lens`` (the lengths given at
+        construction when None; same batch size), copy the plan, the block table (a CPU int32
+        [batch, max_pages] tensor, when given; otherwise the device table given at construction
+        is used) and the queries to the device (asynchronous DMA when they are pinned), run the
+        four kernels, and copy the result into ``out`` (a CPU bf16 [batch, 128, 128] tensor,
+        pinned and allocated once if not given).  Returns ``out`` once the stream is done."""
         B = self.batch
         _need(q_c, "q_c", torch.bfloat16, (B, NUM_HEADS, D_HC), device=False)
         _need(q_r, "q_r", torch.bfloat16, (B, NUM_HEADS, D_R), device=False)
-        if seq_lens is not None:
-            lens = np.asarray(seq_lens, dtype=np.int32)
-            if lens.size != B:
-                raise ValueError("run_host: seq_lens must keep the batch size")
-            self.seq_lens = lens
-            self.plan_host, self.info = mla_plan_splits(lens, self._num_sms, **self._plan_opts)
-            ws = int(self.info.workspace_bytes)
-            if ws and (self.workspace is None or self.workspace.numel() * 4 < ws):
-                self.workspace = torch.empty(ws // 4, dtype=torch.float32, device=self.device)
+        lens = self.seq_lens if seq_lens is None else np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+        if lens.size != B:
+            raise ValueError("run_host: seq_lens must keep the batch size")
         if block_table is not None:
             _need(block_table, "block_table", torch.int32, device=False)
             if block_table.dim() != 2 or block_table.shape[0] != B:
                 raise ValueError("block_table must be [batch, max_pages]")
-
-        st = torch.cuda.current_stream(self.device) if stream is None else stream
-        plan = torch.from_numpy(self.plan_host)
-        if self._h_stage is None or self._h_stage.numel() < plan.numel():
-            self._h_stage = torch.empty(max(plan.numel(), 4096), dtype=torch.int32).pin_memory()
-            self._d_stage = torch.empty(self._h_stage.numel(), dtype=torch.int32, device=self.device)
-        self._h_stage[:plan.numel()].copy_(plan)  # a few KB
-        if not hasattr(self, "_q_c_dev"):
-            self._q_c_dev = torch.empty(B, NUM_HEADS, D_HC, dtype=torch.bfloat16, device=self.device)
-            self._q_r_dev = torch.empty(B, NUM_HEADS, D_R, dtype=torch.bfloat16, device=self.device)
-        with torch.cuda.stream(st):
-            self._d_stage[:plan.numel()].copy_(self._h_stage[:plan.numel()], non_blocking=True)
-            if block_table is not None:
-                if getattr(self, "_bt_dev", None) is None or tuple(self._bt_dev.shape) != tuple(block_table.shape):
-                    self._bt_dev = torch.empty(tuple(block_table.shape), dtype=torch.int32, device=self.device)
-                self._bt_dev.copy_(block_table, non_blocking=True)  # DMA straight from pinned memory
-            self._q_c_dev.copy_(q_c, non_blocking=True)
-            self._q_r_dev.copy_(q_r, non_blocking=True)
-        plan_dev = self._d_stage[:plan.numel()]
+        if not np.array_equal(lens, self.seq_lens) or self._h_stage is None:
+            # new lengths: size the workspace for their plan (the library plans again itself)
+            self.seq_lens = lens.copy()
+            _, info = mla_plan_splits(lens, self._num_sms, **self._plan_opts)
+            ws = int(info.workspace_bytes)
+            if ws and (self.workspace is None or self.workspace.numel() * 4 < ws):
+                self.workspace = torch.empty(ws // 4, dtype=torch.float32, device=self.device)
+            if self._h_stage is None:
+                cap = int(lib().mla_plan_bytes_max(B, self._num_sms))
+                self._h_stage = torch.empty(cap // 4, dtype=torch.int32).pin_memory()
+                self._d_stage = torch.empty(cap // 4, dtype=torch.int32, device=self.device)
+                self._q_c_dev = torch.empty(B, NUM_HEADS, D_HC, dtype=torch.bfloat16, device=self.device)
+                self._q_r_dev = torch.empty(B, NUM_HEADS, D_R, dtype=torch.bfloat16, device=self.device)
+        if block_table is not None and (getattr(self, "_bt_dev", None) is None or
+                                        tuple(self._bt_dev.shape) != tuple(block_table.shape)):
+            self._bt_dev = torch.empty(tuple(block_table.shape), dtype=torch.int32, device=self.device)
         bt_dev = self._bt_dev if block_table is not None else self.block_table
-        q_c_dev, q_r_dev = self._q_c_dev, self._q_r_dev
-
-        mla_absorb_q(q_c_dev, self.w_uk, self.q_abs, st)
-        mla_decode_paged(self.info, plan_dev, self.q_abs, q_r_dev, kv_pool=self.kv_pool, block_table=bt_dev,
-                         o_lat=self.o_lat, lse=self.lse, dev_error=self.dev_error, workspace=self.workspace,
-                         kv_scale=self.kv_scale, kr_pool=self.kr_pool, softmax_scale=self.softmax_scale, stream=st)
-        mla_combine_splits(self.info, plan_dev, self.workspace, self.o_lat, self.lse, st)
-        mla_out_proj(self.o_lat, self.w_uv, self.out, st)
         if out is None:
             out = torch.empty(B, NUM_HEADS, D_HC, dtype=torch.bfloat16).pin_memory()
-        with torch.cuda.stream(st):
-            out.copy_(self.out, non_blocking=True)
-        st.synchronize()
+        _need(out, "out", torch.bfloat16, (B, NUM_HEADS, D_HC), device=False)
+        dtype = MLA_KV_BF16 if self.kv_scale is None else MLA_KV_FP8_E4M3
+        bufs = StepBuffers(_addr(self._q_c_dev), _addr(self._q_r_dev), _addr(self.q_abs), _addr(bt_dev),
+                           _addr(self._d_stage), _addr(self.workspace),
+                           0 if self.workspace is None else self.workspace.numel() * 4, _addr(self.o_lat),
+                           _addr(self.lse), _addr(self.out), _addr(self.dev_error), _addr(self._h_stage),
+                           self._h_stage.numel() * 4)
+        opts = PlanOptions(int(self._plan_opts["min_pages_per_split"]), int(self._plan_opts["max_clusters"]),
+                           int(self._plan_opts["wait_timeout_ns"]))
+        info = PlanInfo()
+        st = lib().mla_decode_step_host(lens.ctypes.data_as(ctypes.c_void_p), B, self._num_sms, ctypes.byref(opts),
+                                        _ptr(q_c), _ptr(q_r), _ptr(block_table), int(bt_dev.shape[1]),
+                                        _ptr(self.w_uk), _ptr(self.w_uv), dtype, _ptr(self.kv_pool),
+                                        _ptr(self.kv_scale), _ptr(self.kr_pool), int(self.kv_pool.shape[0]),
+                                        float(self.softmax_scale), ctypes.byref(bufs), _ptr(out), ctypes.byref(info),
+                                        _stream(stream))
+        _check("mla_decode_step_host", st)
+        self.info = info
         return out
 
     def device_error(self, stream=None) -> int:

@@ -333,3 +333,55 @@ extern "C" mla_status mla_debug_wait_timeout(uint32_t* dev_error, int64_t timeou
     wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(dev_error, (uint64_t)timeout_ns);
     return launch_status();
 }
+
+// The whole step from host memory: plan on the host, one asynchronous copy per input, the four
+// kernels, the output copy back, one stream synchronisation.
+extern "C" mla_status mla_decode_step_host(const int32_t* seq_lens, int32_t batch, int32_t num_sms,
+                                           const mla_plan_options* opts, const void* q_c_host, const void* q_r_host,
+                                           const int32_t* block_table_host, int32_t max_pages_per_seq,
+                                           const void* w_uk, const void* w_uv, mla_kv_dtype kv_dtype,
+                                           const void* kv_pool, const float* kv_scale, const void* kr_pool,
+                                           int32_t num_pool_pages, float softmax_scale, const mla_step_buffers* bufs,
+                                           void* out_host, mla_plan_info* info_out, void* stream)
+{
+    if (!seq_lens || batch <= 0 || !q_c_host || !q_r_host || !bufs || !out_host || !bufs->plan_host ||
+        !bufs->plan || !bufs->block_table || max_pages_per_seq <= 0)
+        return MLA_ERR_INVALID_ARG;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    mla_plan_info info;
+    mla_status st = mla_plan_splits(seq_lens, batch, num_sms, opts, bufs->plan_host, bufs->plan_capacity, &info);
+    if (st != MLA_OK) return st;
+    if (info_out) *info_out = info;
+    if (info.workspace_bytes > 0 && (!bufs->workspace || bufs->workspace_bytes < (size_t)info.workspace_bytes))
+        return MLA_ERR_WORKSPACE;
+    const size_t q_c_bytes = (size_t)batch * 128 * 128 * 2, q_r_bytes = (size_t)batch * 128 * 64 * 2;
+    if (record_cuda(cudaMemcpyAsync(bufs->plan, bufs->plan_host, (size_t)info.plan_bytes, cudaMemcpyHostToDevice, s),
+                    "cudaMemcpyAsync(plan)") != MLA_OK)
+        return MLA_ERR_CUDA;
+    if (block_table_host &&
+        record_cuda(cudaMemcpyAsync(bufs->block_table, block_table_host,
+                                    (size_t)batch * (size_t)max_pages_per_seq * sizeof(int32_t),
+                                    cudaMemcpyHostToDevice, s),
+                    "cudaMemcpyAsync(block table)") != MLA_OK)
+        return MLA_ERR_CUDA;
+    if (record_cuda(cudaMemcpyAsync(bufs->q_c, q_c_host, q_c_bytes, cudaMemcpyHostToDevice, s),
+                    "cudaMemcpyAsync(q_c)") != MLA_OK ||
+        record_cuda(cudaMemcpyAsync(bufs->q_r, q_r_host, q_r_bytes, cudaMemcpyHostToDevice, s),
+                    "cudaMemcpyAsync(q_r)") != MLA_OK)
+        return MLA_ERR_CUDA;
+    if ((st = mla_absorb_q(bufs->q_c, w_uk, bufs->q_abs, batch, stream)) != MLA_OK) return st;
+    if ((st = mla_decode_paged(&info, bufs->plan, bufs->q_abs, bufs->q_r, kv_dtype, kv_pool, kv_scale, kr_pool,
+                               num_pool_pages, bufs->block_table, max_pages_per_seq, softmax_scale, bufs->workspace,
+                               bufs->workspace_bytes, bufs->o_lat, bufs->lse, bufs->dev_error, stream)) != MLA_OK)
+        return st;
+    if ((st = mla_combine_splits(&info, bufs->plan, bufs->workspace, bufs->workspace_bytes, bufs->o_lat, bufs->lse,
+                                 stream)) != MLA_OK)
+        return st;
+    if ((st = mla_out_proj(bufs->o_lat, w_uv, bufs->out, batch, stream)) != MLA_OK) return st;
+    const size_t out_bytes = (size_t)batch * 128 * 128 * 2;
+    if (record_cuda(cudaMemcpyAsync(out_host, bufs->out, out_bytes, cudaMemcpyDeviceToHost, s),
+                    "cudaMemcpyAsync(out)") != MLA_OK ||
+        record_cuda(cudaStreamSynchronize(s), "cudaStreamSynchronize") != MLA_OK)
+        return MLA_ERR_CUDA;
+    return MLA_OK;
+}

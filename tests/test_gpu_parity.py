@@ -210,3 +210,19 @@ def test_run_host_matches_device_run():
         out = step.run_host(inp.q_c, inp.q_r, block_table=bt_h, seq_lens=inp.seq_lens)
         assert step.device_error() == 0
         assert torch.equal(out, ref.cpu())
+
+
+def test_run_host_new_lengths_and_fp8():
+    """run_host re-plans when the lengths change (same batch, same buffers) and gives the bits of
+    a DecodeStep built for the new lengths; the same holds for an FP8 cache."""
+    for kv_dtype in ("bf16", "fp8_e4m3"):
+        inp = synth.make_inputs([3000, 700, 64 * 9 + 1], seed=12, poison_tail=False, kv_dtype=kv_dtype)
+        q_c, q_r, w_uk, w_uv, kv, bt = binding.inputs_to_device(inp, DEV)
+        step = binding.DecodeStep(inp.seq_lens, w_uk=w_uk, w_uv=w_uv, block_table=bt, min_pages_per_split=2, **kv)
+        short = np.array([1800, 65, 64 * 9 + 1], dtype=np.int32)
+        fresh = binding.DecodeStep(short, w_uk=w_uk, w_uv=w_uv, block_table=bt, min_pages_per_split=2, **kv)
+        ref = fresh.run(q_c, q_r).clone()
+        torch.cuda.synchronize()
+        out = step.run_host(inp.q_c.pin_memory(), inp.q_r.pin_memory(), seq_lens=short)
+        assert step.device_error() == 0
+        assert torch.equal(out, ref.cpu()), kv_dtype
