@@ -24,8 +24,8 @@
 //   rank 1, the value CTA: O lives in TMEM (512 columns); per page it runs PV from P and its
 //     own copy of the page's 512 latent columns; four warps apply the (rare) rescales, zero
 //     the unused slots of a sequence's last page, and write the normalised output.
-// Both CTAs stream the same pages with their own TMA ring; the score CTA reads first with
-// normal L2 priority and the value CTA second with evict-first, so HBM sees each page once.
+// Both CTAs stream the same pages with their own TMA ring; the score CTA reads first with an
+// evict-last hint and the value CTA second with evict-first, so HBM sees each page once.
 //
 // Online softmax with lazy rescaling: the running max m used for exp2 only moves when a tile's
 // max exceeds it by more than 8 (log2 units); then l and O are scaled by exp2(m_old - m_new).
@@ -257,7 +257,7 @@ __device__ __forceinline__ void score_producer(const CUtensorMap* tm, const Para
 {
     using namespace dev;
     MLA_TRACE_DECL;
-    const uint64_t policy = l2_policy_evict_normal();  // the value CTA reads these pages next
+    const uint64_t policy = l2_policy_evict_last();  // the value CTA reads these pages next
     if (lane == 0) tma_prefetch_desc(tm);
     int s = 0, phase = 0, c = 0;
     bool ok = true;

@@ -290,7 +290,7 @@ __device__ __forceinline__ void score_producer(const CUtensorMap* tm_c8, const P
                                                const dev::WaitCtx& w, int lane)
 {
     using namespace dev;
-    const uint64_t policy = l2_policy_evict_normal();  // the value CTA reads these pages next
+    const uint64_t policy = l2_policy_evict_last();  // the value CTA reads these pages next
     if (lane == 0) tma_prefetch_desc(tm_c8);
     int s = 0, phase = 0, c = 0;
     bool ok = true;

@@ -130,3 +130,39 @@ def test_plan_rejects_bad_args(L):
     st = L.mla_plan_splits(lens.ctypes.data_as(ctypes.c_void_p), 1, 152, None, buf.ctypes.data_as(ctypes.c_void_p),
                            buf.nbytes, ctypes.byref(info))
     assert st == binding.MLA_ERR_WORKSPACE
+
+
+def _step_host(L, bufs, *, lens=(100, 5000), q=0x1000, out=0x2000, opts=None):
+    arr = np.asarray(lens, dtype=np.int32)
+    o = opts if opts is not None else binding.PlanOptions(2, 0, 0)
+    info = binding.PlanInfo()
+    return L.mla_decode_step_host(arr.ctypes.data_as(ctypes.c_void_p), len(lens), 152, ctypes.byref(o), _p(q),
+                                  _p(q + 0x100), None, 80, _p(0x3000), _p(0x4000), binding.MLA_KV_BF16, _p(0x5000),
+                                  None, None, 100, ctypes.c_float(0.07),
+                                  ctypes.byref(bufs) if bufs is not None else None, _p(out), ctypes.byref(info),
+                                  None), info
+
+
+def test_step_host_rejects_bad_args(L):
+    """The host-step entry point plans on the host and checks its buffers before any copy or
+    launch: missing buffers are invalid arguments; a workspace smaller than the plan needs is a
+    workspace error (with the plan header still returned)."""
+    cap = int(L.mla_plan_bytes_max(2, 152))
+    plan_host = np.zeros(cap // 4, dtype=np.int32)
+    bufs = binding.StepBuffers(0x10000, 0x11000, 0x12000, 0x13000, 0x14000, 0x15000, 64, 0x16000, 0x17000,
+                               0x18000, 0x19000, plan_host.ctypes.data, cap)
+    st, _ = _step_host(L, None)
+    assert st == binding.MLA_ERR_INVALID_ARG
+    st, _ = _step_host(L, bufs, out=0)
+    assert st == binding.MLA_ERR_INVALID_ARG
+    no_plan = binding.StepBuffers(0x10000, 0x11000, 0x12000, 0x13000, 0x14000, 0x15000, 64, 0x16000, 0x17000,
+                                  0x18000, 0x19000, 0, cap)
+    st, _ = _step_host(L, no_plan)
+    assert st == binding.MLA_ERR_INVALID_ARG
+    st, info = _step_host(L, bufs)  # 5000 tokens over two pairs or more: split, so a workspace is due
+    assert st == binding.MLA_ERR_WORKSPACE
+    assert info.workspace_bytes > 64 and info.batch == 2
+    small_cap = binding.StepBuffers(0x10000, 0x11000, 0x12000, 0x13000, 0x14000, 0x15000, 1 << 30, 0x16000,
+                                    0x17000, 0x18000, 0x19000, plan_host.ctypes.data, 16)
+    st, _ = _step_host(L, small_cap)
+    assert st != binding.MLA_OK  # the plan does not fit its staging buffer
