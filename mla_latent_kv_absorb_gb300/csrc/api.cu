@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
+#include <utility>
 
 #include "../../include/mla.h"
 #include "combine.cuh"
@@ -97,11 +98,32 @@ mla_status launch_status()
     return record_cuda(cudaGetLastError(), "kernel launch");
 }
 
+// Launch with programmatic stream serialisation: the kernel may be scheduled before the kernel
+// ahead of it in the stream has finished (once that one allows it) and waits for that kernel's
+// output itself (griddepcontrol.wait), so its prologue and its independent loads overlap the
+// other's tail.  Every kernel of the step that reads the previous one's output does that wait.
+template <typename... KArgs, typename... Args>
+mla_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                      Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return record_cuda(cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...), "cudaLaunchKernelEx");
+}
+
 // Shared by absorb and out-proj: activations [batch][128][K] (K-major rows of 128*K), weights
 // [128][128][512].
 template <int K_TOTAL, int N_TILE, bool W_MN, int STAGES>
 mla_status launch_head_gemm(const void* act, const void* weight, void* out, int32_t batch, int n_total,
-                            cuuint32_t w_box_rows, void* stream)
+                            cuuint32_t w_box_rows, bool pdl, void* stream)
 {
     using C = Cfg<K_TOTAL, N_TILE, W_MN, STAGES>;
     CUtensorMap tm_a, tm_w;
@@ -123,6 +145,7 @@ mla_status launch_head_gemm(const void* act, const void* weight, void* out, int3
     args.dev_error = nullptr;
     args.timeout_ns = kDefaultTimeoutNs;
     const dim3 grid(n_total / N_TILE, 128, (batch + 127) / 128);
+    if (pdl) return launch_pdl(kernel, grid, dim3(192), C::kSmemBytes, static_cast<cudaStream_t>(stream), tm_a, tm_w, args);
     kernel<<<grid, 192, C::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(tm_a, tm_w, args);
     return launch_status();
 }
@@ -212,24 +235,24 @@ mla_status launch_decode_fp8(const mla_plan_info* info, const void* plan_dev, co
 #endif
 
     if (!set_smem(mla::decode_fp8::decode_fp8_kernel, mla::decode_fp8::kSmemBytes)) return MLA_ERR_CUDA;
-    mla::decode_fp8::decode_fp8_kernel<<<2 * info->num_clusters, mla::decode_fp8::kThreads,
-                                         mla::decode_fp8::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(tm_c8, tm_kr,
-                                                                                                            p);
-    return launch_status();
+    return launch_pdl(mla::decode_fp8::decode_fp8_kernel, dim3(2 * info->num_clusters), dim3(mla::decode_fp8::kThreads),
+                      mla::decode_fp8::kSmemBytes, static_cast<cudaStream_t>(stream), tm_c8, tm_kr, p);
 }
 
 extern "C" mla_status mla_absorb_q(const void* q_c, const void* w_uk, void* q_abs, int32_t batch, void* stream)
 {
     if (!q_c || !w_uk || !q_abs || batch <= 0) return MLA_ERR_INVALID_ARG;
     if (!aligned16(q_c) || !aligned16(w_uk) || !aligned16(q_abs)) return MLA_ERR_ALIGNMENT;
-    return launch_head_gemm<128, kAbsorbN, true, kAbsorbStages>(q_c, w_uk, q_abs, batch, 512, 64, stream);
+    // the step's first kernel: an ordinary launch (it allows the decode kernel to start early)
+    return launch_head_gemm<128, kAbsorbN, true, kAbsorbStages>(q_c, w_uk, q_abs, batch, 512, 64, false, stream);
 }
 
 extern "C" mla_status mla_out_proj(const void* o_lat, const void* w_uv, void* out, int32_t batch, void* stream)
 {
     if (!o_lat || !w_uv || !out || batch <= 0) return MLA_ERR_INVALID_ARG;
     if (!aligned16(o_lat) || !aligned16(w_uv) || !aligned16(out)) return MLA_ERR_ALIGNMENT;
-    return launch_head_gemm<512, kOutN, false, kOutStages>(o_lat, w_uv, out, batch, 128, kOutN, stream);
+    // streams W_UV while the merge (or the decode) before it finishes
+    return launch_head_gemm<512, kOutN, false, kOutStages>(o_lat, w_uv, out, batch, 128, kOutN, true, stream);
 }
 
 extern "C" mla_status mla_decode_paged(const mla_plan_info* info, const void* plan_dev, const void* q_abs,
@@ -286,9 +309,8 @@ extern "C" mla_status mla_decode_paged(const mla_plan_info* info, const void* pl
 #endif
 
     if (!set_smem(mla::decode::decode_bf16_kernel, mla::decode::kSmemBytes)) return MLA_ERR_CUDA;
-    mla::decode::decode_bf16_kernel<<<2 * info->num_clusters, mla::decode::kThreads, mla::decode::kSmemBytes,
-                                      static_cast<cudaStream_t>(stream)>>>(tm_pool, p);
-    return launch_status();
+    return launch_pdl(mla::decode::decode_bf16_kernel, dim3(2 * info->num_clusters), dim3(mla::decode::kThreads),
+                      mla::decode::kSmemBytes, static_cast<cudaStream_t>(stream), tm_pool, p);
 }
 
 extern "C" mla_status mla_combine_splits(const mla_plan_info* info, const void* plan_dev, const void* workspace,
@@ -303,9 +325,9 @@ extern "C" mla_status mla_combine_splits(const mla_plan_info* info, const void* 
     const float* ws_lse = reinterpret_cast<const float*>(static_cast<const char*>(workspace) +
                                                          (size_t)info->num_partials * mla::kPartialOBytes);
     const dim3 grid(info->num_combine, 128 / mla::combine::kHeadsPerCta);
-    mla::combine::combine_kernel<<<grid, 32 * mla::combine::kHeadsPerCta, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const int32_t*>(plan_dev), ws_o, ws_lse, static_cast<__nv_bfloat16*>(o_lat), lse);
-    return launch_status();
+    return launch_pdl(mla::combine::combine_kernel, grid, dim3(32 * mla::combine::kHeadsPerCta), 0,
+                      static_cast<cudaStream_t>(stream), static_cast<const int32_t*>(plan_dev), ws_o, ws_lse,
+                      static_cast<__nv_bfloat16*>(o_lat), lse);
 }
 
 extern "C" const char* mla_last_error_string(void) { return t_last_error; }

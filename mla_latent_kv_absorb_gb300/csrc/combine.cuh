@@ -22,6 +22,8 @@ combine_kernel(const int32_t* __restrict__ plan, const float* __restrict__ ws_o,
                __nv_bfloat16* __restrict__ o_lat, float* __restrict__ lse)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    dev::griddep_launch_dependents();  // the projection may start streaming its weights
+    dev::griddep_wait();               // the partials come from the decode kernel
     const int32_t* entry = plan + plan[kHdrCombineOff] + kCombineWords * blockIdx.x;
     const int seq = entry[0], first = entry[1], n = entry[2];
     const int h = blockIdx.y * kHeadsPerCta + warp;

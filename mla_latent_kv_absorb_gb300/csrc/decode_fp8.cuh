@@ -706,6 +706,7 @@ __device__ __forceinline__ void score_softmax(const Params& p, int item_begin, i
     const uint32_t* freed = reinterpret_cast<const uint32_t*>(smem + kOffStgFreed);
     const uint32_t* sig_ready = reinterpret_cast<const uint32_t*>(smem + kOffSigReady);
     float* xchg = reinterpret_cast<float*>(smem + kOffXchg);  // [slot 2][kind 2: max, l][set 2][128]
+    griddep_wait();  // q_abs comes from the kernel launched before this one
     int g = 0, G = 0;  // pages (messages) and four-page groups
     for (int i = item_begin; i < item_end; ++i) {
         const Item it = load_item(p.plan, items_off, i);

@@ -90,19 +90,15 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
     const uint32_t tmem = *tmem_holder;
     const WaitCtx w{args.timeout_ns, abort_flag, args.dev_error};
 
+    griddep_launch_dependents();  // the next kernel of the step may be scheduled
     if (warp == 0) {
         if (lane == 0) {
             tma_prefetch_desc(&tm_a);
             tma_prefetch_desc(&tm_w);
             const uint64_t pol_w = l2_policy_evict_first();  // weights: read once per step
             const uint64_t pol_a = l2_policy_evict_last();   // activations: re-read by other N tiles
-            int issued = 0;
-            for (int kc = 0; kc < C::kNK; ++kc) {
-                const int s = kc % STAGES;
-                if (kc >= STAGES && !wait_phase(bar_empty + 8 * s, kc / STAGES - 1, w)) break;
-                const uint32_t a_dst = sbase + s * C::kStageBytes, w_dst = a_dst + C::kABytes;
-                mbar_arrive_expect_tx(bar_full + 8 * s, C::kStageBytes);
-                tma_load_2d(a_dst, &tm_a, bar_full + 8 * s, h * K_TOTAL + kc * C::kKC, m0, pol_a);
+            const auto load_w = [&](int kc, int s) {
+                const uint32_t w_dst = sbase + s * C::kStageBytes + C::kABytes;
                 if (W_MN_MAJOR) {
 #pragma unroll
                     for (int i = 0; i < N_TILE / 64; ++i)
@@ -111,6 +107,24 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
                 } else {
                     tma_load_2d(w_dst, &tm_w, bar_full + 8 * s, kc * C::kKC, h * args.n_total + n0, pol_w);
                 }
+            };
+            // The weights do not depend on the kernel before this one: the first stages' weights
+            // are in flight before the wait for its output (the activations).
+            const int early = C::kNK < STAGES ? C::kNK : STAGES;
+            for (int kc = 0; kc < early; ++kc) {
+                mbar_arrive_expect_tx(bar_full + 8 * kc, C::kStageBytes);
+                load_w(kc, kc);
+            }
+            griddep_wait();
+            int issued = 0;
+            for (int kc = 0; kc < C::kNK; ++kc) {
+                const int s = kc % STAGES;
+                if (kc >= early) {
+                    if (!wait_phase(bar_empty + 8 * s, kc / STAGES - 1, w)) break;
+                    mbar_arrive_expect_tx(bar_full + 8 * s, C::kStageBytes);
+                    load_w(kc, s);
+                }
+                tma_load_2d(sbase + s * C::kStageBytes, &tm_a, bar_full + 8 * s, h * K_TOTAL + kc * C::kKC, m0, pol_a);
                 ++issued;
             }
             if (*abort_flag) {  // let loads already in flight land before the CTA can exit

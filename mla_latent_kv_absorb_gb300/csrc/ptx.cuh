@@ -436,6 +436,12 @@ __device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v)
     asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
 }
 
+// Programmatic dependent launch: wait until the grids this one depends on have completed and
+// their memory is visible (a no-op for a grid launched without the attribute), and allow the
+// grids that depend on this one to be scheduled.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
 // ------------------------------------------------------------------------------ misc
 
 // Two floats -> f16x2 (round to nearest even), `lo` in the low half.
