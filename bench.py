@@ -234,12 +234,27 @@ def run_ours(args, rank, world, local):
         binding.mla_out_proj(step.o_lat, step.w_uv, step.out, stream)
         evs[4].record(stream)
 
+    # the step as one CUDA graph (its kernels keep their programmatic dependencies)
+    graph, graph_note = None, "not used (--no-graph)"
+    if args.graph:
+        try:
+            graph = step.capture(q_c, q_r)
+            graph_note = "captured"
+        except Exception as e:  # noqa: BLE001 -- recorded in the JSON line; eager launches are timed instead
+            graph_note = f"capture failed, eager launches timed: {e}"[:240]
+
+    def whole_step():
+        if graph is not None:
+            graph.replay()
+        else:
+            one_step()
+
     # warm-up: at least W steps and at least --min-warmup-s seconds of work so clocks settle
     t0 = time.perf_counter()
     n = 0
     while n < args.warmup or time.perf_counter() - t0 < args.min_warmup_s:
         flush.fill_(n & 0xFF)
-        one_step()
+        whole_step()
         n += 1
         if n % 16 == 0:
             torch.cuda.synchronize(device)
@@ -249,20 +264,29 @@ def run_ours(args, rank, world, local):
 
     K = args.steps
     step_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    eager_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
     dist_barrier(world)
     torch.cuda.synchronize(device)
     with ClockSampler(local) as clocks:
-        # the metric: K whole steps, nothing recorded between their kernels, so each kernel may
-        # start under the previous one's tail (programmatic dependent launch)
+        # the metric: K whole steps (graph replays), nothing recorded between their kernels, so
+        # each kernel may start under the previous one's tail (programmatic dependent launch)
         wall0 = time.perf_counter()
         for i in range(K):
             flush.fill_(i & 0xFF)
             step_ev[i][0].record(stream)
-            one_step()
+            whole_step()
             step_ev[i][1].record(stream)
         torch.cuda.synchronize(device)
         wall = time.perf_counter() - wall0
+        dist_barrier(world)
+        # the same steps launched eagerly, for comparison
+        for i in range(K):
+            flush.fill_(i & 0xFF)
+            eager_ev[i][0].record(stream)
+            one_step()
+            eager_ev[i][1].record(stream)
+        torch.cuda.synchronize(device)
         dist_barrier(world)
         # the breakdown: K more steps with an event between kernels (events serialise them); the
         # per-kernel times and the decode kernel's roofline come from here
@@ -276,6 +300,7 @@ def run_ours(args, rank, world, local):
         raise RuntimeError(f"device error bits {err:#x} in the timed region")
 
     step_ms = [e[0].elapsed_time(e[1]) for e in step_ev]
+    eager_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in eager_ev)
     k_ms = {name: [e[i].elapsed_time(e[i + 1]) for e in evs]
             for i, name in enumerate(["absorb", "decode", "combine", "out_proj"])}
     ms = statistics.mean(step_ms)
@@ -328,10 +353,13 @@ def run_ours(args, rank, world, local):
                    "global_batch": inp.batch * world, "seq_len": int(inp.seq_lens.max()),
                    "tokens_per_replica": acc["tokens"], "parallelism": f"replicas x{world}",
                    "l2": "512 MB buffer rewritten before every timed step; cache (1.2 GB) > L2",
-                   "timing": "value: K whole steps between two events; kernels_us and roofline: a second "
-                             "pass of K steps with an event between kernels",
+                   "timing": "value: K replays of the step's CUDA graph, each between two events; "
+                             "step_us_eager: K eager launches of the same step; kernels_us and roofline: a "
+                             "third pass of K steps with an event between kernels",
+                   "graph": graph_note,
                    "plan": {"clusters": step.info.num_clusters, "items": step.info.num_items,
                             "combine_seqs": step.info.num_combine, "max_splits": step.info.max_splits}},
+        "step_us_eager": round(eager_ms * 1e3, 2),
         "kernels_us": {k: round(statistics.mean(v) * 1e3, 2) for k, v in k_ms.items()},
         "kv_tbps": round(acc["kv_bytes"] / (ms_max * 1e-3) / 1e12, 3),
         "step_tflops": round(acc["step_flop"] / (ms_max * 1e-3) / 1e12, 1),
@@ -453,6 +481,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-parity", dest="parity", action="store_false")
+    ap.add_argument("--no-graph", dest="graph", action="store_false",
+                    help="time eager launches for the value instead of replays of the step's CUDA graph")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -66,6 +66,7 @@ typedef enum mla_kv_dtype {
 #define MLA_DEVERR_TIMEOUT 2u     /* a bounded wait ran out; the kernel stopped early */
 #define MLA_DEVERR_SMEM_ALIGN 4u  /* shared memory was not 1024-byte aligned; nothing computed */
 #define MLA_DEVERR_BAD_PLAN 8u    /* the device plan image failed its header check */
+#define MLA_DEVERR_BAD_SLOT 16u   /* mla_append_kv: a slot at or past num_pool_pages * 64; that token skipped */
 
 MLA_API const char* mla_status_string(mla_status status);
 
@@ -173,6 +174,31 @@ MLA_API mla_status mla_combine_splits(const mla_plan_info* info, const void* pla
  *   o_lat device bf16 [batch][128][512], w_uv device bf16 [128][128][512],
  *   out   device bf16 [batch][128][128].  Tensor cores (tcgen05), fp32 accumulation. */
 MLA_API mla_status mla_out_proj(const void* o_lat, const void* w_uv, void* out, int32_t batch, void* stream);
+
+/* ---------------------------------------------------------------- cache append (the write side)
+ *
+ * P1 section 1: each token stores, once, its 512-d latent c_KV and its 64-d RoPE key k_R (576
+ * elements); every later decode step reads that row.  P1 section 3 pages the cache in blocks of
+ * 64 tokens.  This call writes num_tokens new rows into the pool: token i goes to slot
+ * slots[i] = physical page * 64 + row within the page (the caller derives it from its block
+ * table: page block_table[b][t / 64], row t % 64 for position t of sequence b).
+ *   c_kv   device bf16 [num_tokens][512], k_r device bf16 [num_tokens][64] (already rotated)
+ *   slots  device int32 [num_tokens]; a negative slot skips the token (padding); a slot at or
+ *          past num_pool_pages * 64 skips it and sets MLA_DEVERR_BAD_SLOT in *dev_error
+ *   bf16 cache: kv_pool [pages][64][576] receives c_KV then k_R; kv_scale and kr_pool are
+ *          ignored.
+ *   FP8 cache (MLA_KV_FP8_E4M3): per token, over the 512 latent values only,
+ *          sigma = max_i |c_i| / 448 in fp32 (1 when the row is all zeros), and code_i = the
+ *          e4m3 value nearest c_i / sigma (fp32 quotient, ties to the even code); kv_pool
+ *          [pages][64][512] receives the codes, kv_scale [pages][64] sigma, kr_pool
+ *          [pages][64][64] k_R unchanged.  Rows must be finite.
+ * The result is exact: byte for byte what the stated rule gives.  Two tokens with the same slot
+ * race (one of them wins).  c_kv, k_r, kv_pool and kr_pool 16-byte aligned, slots, kv_scale
+ * and dev_error 4-byte aligned.  num_tokens == 0 enqueues nothing.  One warp per token, plain
+ * vector loads and stores (a few hundred bytes per token: launch-bound at decode batch sizes). */
+MLA_API mla_status mla_append_kv(int32_t num_tokens, const void* c_kv, const void* k_r, const int32_t* slots,
+                                 mla_kv_dtype kv_dtype, int32_t num_pool_pages, void* kv_pool, float* kv_scale,
+                                 void* kr_pool, uint32_t* dev_error, void* stream);
 
 /* ---------------------------------------------------------------- decode + merge, no allocation
  *

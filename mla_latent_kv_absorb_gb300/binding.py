@@ -49,7 +49,7 @@ class PlanInfo(ctypes.Structure):
 
 EXPORTS = ("mla_status_string", "mla_last_error_string", "mla_plan_bytes_max", "mla_plan_splits", "mla_absorb_q", "mla_decode_paged",
            "mla_combine_splits", "mla_out_proj", "mla_read_device_error", "mla_debug_wait_timeout",
-           "mla_decode_paged_static_ws", "mla_decode_step_host")
+           "mla_decode_paged_static_ws", "mla_decode_step_host", "mla_append_kv")
 
 # capacity of the library's fixed split-partial array (mla_decode_paged_static_ws)
 MLA_STATIC_WS_MAX_PARTIALS = 128
@@ -100,6 +100,8 @@ def lib() -> ctypes.CDLL:
     L.mla_decode_step_host.argtypes = [P, i32, i32, ctypes.POINTER(PlanOptions), P, P, P, i32, P, P, ctypes.c_int, P,
                                        P, P, i32, ctypes.c_float, ctypes.POINTER(StepBuffers), P,
                                        ctypes.POINTER(PlanInfo), P]
+    L.mla_append_kv.restype = ctypes.c_int
+    L.mla_append_kv.argtypes = [i32, P, P, P, ctypes.c_int, i32, P, P, P, u32p, P]
     L.mla_read_device_error.restype = ctypes.c_int
     L.mla_read_device_error.argtypes = [u32p, ctypes.POINTER(ctypes.c_uint32), P]
     L.mla_debug_wait_timeout.restype = ctypes.c_int
@@ -264,6 +266,26 @@ def mla_combine_splits(info: PlanInfo, plan_dev: torch.Tensor, workspace: Option
     _check("mla_combine_splits", st)
 
 
+def mla_append_kv(c_kv: torch.Tensor, k_r: torch.Tensor, slots: torch.Tensor, *, kv_pool: torch.Tensor,
+                  dev_error: torch.Tensor, kv_scale: Optional[torch.Tensor] = None,
+                  kr_pool: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Write new tokens into the paged cache: token i to slot slots[i] (page * 64 + row; negative
+    = skip).  bf16 cache: kv_pool [pages, 64, 576].  FP8 cache (kv_scale given): c_KV quantised
+    per token into kv_pool [pages, 64, 512] (e4m3 codes) and kv_scale [pages, 64], k_R into
+    kr_pool [pages, 64, 64]."""
+    n = int(slots.shape[0]) if slots.dim() == 1 else -1
+    if n < 0:
+        raise ValueError("slots must be 1-d")
+    _need(slots, "slots", torch.int32, (n,))
+    _need(c_kv, "c_kv", torch.bfloat16, (n, D_C))
+    _need(k_r, "k_r", torch.bfloat16, (n, D_R))
+    _need(dev_error, "dev_error", torch.int32, (1,))
+    dtype = _kv_dtype(kv_pool, kv_scale, kr_pool)
+    st = lib().mla_append_kv(n, _ptr(c_kv), _ptr(k_r), _ptr(slots), dtype, int(kv_pool.shape[0]), _ptr(kv_pool),
+                             _ptr(kv_scale), _ptr(kr_pool), _ptr(dev_error), _stream(stream))
+    _check("mla_append_kv", st)
+
+
 def mla_read_device_error(dev_error: torch.Tensor, stream=None) -> int:
     """Device error bits (0 = none); waits for the stream."""
     bits = ctypes.c_uint32(0)
@@ -383,6 +405,22 @@ class DecodeStep:
         _check("mla_decode_step_host", st)
         self.info = info
         return out
+
+    def capture(self, q_c: torch.Tensor, q_r: torch.Tensor) -> "torch.cuda.CUDAGraph":
+        """Capture one step into a CUDA graph and return it.
+
+        The graph holds the step's kernels with their programmatic dependencies, reading
+        ``q_c`` / ``q_r`` and writing ``self.out`` at their current addresses: copy the next
+        step's queries into those tensors and call ``replay()`` (it runs on the current stream).
+        The lengths, block table and cache are those of this object and stay fixed in the graph
+        (a new plan needs a new capture).  One step runs eagerly first so that one-time set-up
+        stays out of the capture."""
+        self.run(q_c, q_r)
+        torch.cuda.synchronize(self.device)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            self.run(q_c, q_r)
+        return graph
 
     def device_error(self, stream=None) -> int:
         return mla_read_device_error(self.dev_error, stream)

@@ -14,6 +14,10 @@ Parity status of each function (what pins it, see ``tests/test_oracle_pins.py``)
                          single-row closed forms.
   lse_combine         -- split-partition invariance against an unsplit latent_attention and
                          equal-weight closed form.
+  e4m3_encode, quantize_token, append_kv
+                      -- every finite code round-trips, midpoints go to the even code, a sweep
+                         against torch's float8_e4m3fn cast, the half-step error bound, the
+                         all-zero row; appending every token of a synthetic cache rebuilds it.
 """
 from __future__ import annotations
 
@@ -64,6 +68,13 @@ def _load(path: str):
     L.oracle_latent_attention.argtypes = [i32, P, P, P, P, i32, P, P, i32, i32, P, P, P, P, f64, i32, P, P, P]
     L.oracle_out_proj.argtypes = [i32, P, P, P]
     L.oracle_lse_combine.argtypes = [i32, i32, P, P, P, P]
+    L.oracle_e4m3_encode.restype = ctypes.c_uint8
+    L.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+    L.oracle_e4m3_encode_many.argtypes = [P, i64, P]
+    L.oracle_quantize_token.restype = ctypes.c_float
+    L.oracle_quantize_token.argtypes = [P, P]
+    L.oracle_append_kv.restype = i32
+    L.oracle_append_kv.argtypes = [i32, P, P, P, i32, i32, P, P, P, P]
     return L
 
 
@@ -217,3 +228,40 @@ def decode_absorbed(inp, *, softmax_scale: float):
     o_lat, lse = latent_attention(inp, q_abs, softmax_scale=softmax_scale)
     out = out_proj(o_lat, inp.w_uv)
     return q_abs, o_lat, lse, out
+
+
+def e4m3_encode(x: np.ndarray) -> np.ndarray:
+    """Nearest e4m3 codes (uint8) of float32 values, ties to even, clamped to +-448."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    lib().oracle_e4m3_encode_many(_p(x), x.size, _p(out))
+    return out
+
+
+def quantize_token(c) -> tuple:
+    """One token's 512 bf16 latent values -> (codes uint8 [512], sigma float32)."""
+    c = _u16(c).reshape(-1)
+    assert c.size == D_C
+    codes = np.empty(D_C, dtype=np.uint8)
+    sigma = lib().oracle_quantize_token(_p(c), _p(codes))
+    return codes, np.float32(sigma)
+
+
+def append_kv(c_kv, k_r, slots, cache: dict) -> int:
+    """Write tokens into a paged cache held as numpy arrays, in place.
+
+    c_kv bf16 [n, 512], k_r bf16 [n, 64], slots int32 [n] (page * 64 + row; negative = skip).
+    cache: {"pool": uint16 [N, 64, 576]} for a bf16 cache, or {"c8": uint8 [N, 64, 512],
+    "scale": float32 [N, 64], "kr": uint16 [N, 64, 64]} for FP8.  Returns 0, or -1 when a slot
+    was past the pool (that token skipped)."""
+    ck, kr = _u16(c_kv), _u16(k_r)
+    sl = np.ascontiguousarray(slots, dtype=np.int32)
+    n = sl.size
+    assert ck.shape == (n, D_C) and kr.shape == (n, D_R)
+    fp8 = "c8" in cache
+    arrays = [cache.get(k) for k in ("pool", "c8", "scale", "kr")]
+    for a in arrays:
+        assert a is None or (isinstance(a, np.ndarray) and a.flags.c_contiguous)
+    num_pages = (cache["c8"] if fp8 else cache["pool"]).shape[0]
+    return int(lib().oracle_append_kv(n, _p(ck), _p(kr), _p(sl), 1 if fp8 else 0, num_pages,
+                                      *[_p(a) for a in arrays]))

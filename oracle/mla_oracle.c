@@ -330,3 +330,87 @@ void oracle_lse_combine(int rows, int n, const double* lse, const double* o, dou
         }
     }
 }
+
+/* ------------------------------------------------------------------ cache append (write side) */
+
+/*
+ * The e4m3 code nearest a finite float, ties to the code with the even mantissa field, and a
+ * magnitude at or past 448 (the largest finite code) gives 448.  The sign is kept, zero
+ * results included.  Straight from the format's definition (oracle_e4m3_value above): the
+ * non-negative finite codes 0x00..0x7E have increasing values, so take the last one not above
+ * |x| and the one after it and keep the nearer.
+ */
+uint8_t oracle_e4m3_encode(float x)
+{
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    const double a = fabs((double)x);
+    if (a >= 448.0) return sign | 0x7E;
+    int lo = 0;
+    while (lo + 1 <= 0x7E && oracle_e4m3_value((uint8_t)(lo + 1)) <= a) ++lo;
+    const double below = oracle_e4m3_value((uint8_t)lo);
+    if (below == a) return sign | (uint8_t)lo;
+    const int hi = lo + 1;
+    const double d_lo = a - below, d_hi = oracle_e4m3_value((uint8_t)hi) - a;
+    int c;
+    if (d_lo < d_hi)
+        c = lo;
+    else if (d_hi < d_lo)
+        c = hi;
+    else
+        c = (lo & 1) ? hi : lo; /* a tie: the even mantissa field */
+    return sign | (uint8_t)c;
+}
+
+void oracle_e4m3_encode_many(const float* x, int64_t n, uint8_t* out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_encode(x[i]);
+}
+
+/*
+ * One token's latent for the FP8 cache: sigma = (largest |c_i|) / 448 in fp32, or 1 when the
+ * row is all zeros; code_i = the e4m3 code nearest c_i / sigma, the quotient taken in fp32.
+ * c is the token's 512 bf16 latent values.  Returns sigma.
+ */
+float oracle_quantize_token(const uint16_t* c, uint8_t* codes)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < DC; ++i) {
+        const float v = fabsf((float)bf16_value(c[i]));
+        if (v > amax) amax = v;
+    }
+    const float sigma = amax > 0.0f ? amax / 448.0f : 1.0f;
+    for (int i = 0; i < DC; ++i) codes[i] = oracle_e4m3_encode((float)bf16_value(c[i]) / sigma);
+    return sigma;
+}
+
+/*
+ * Write n tokens into the paged cache (page 1 section 1: one row of c_KV and k_R per token;
+ * section 3: 64-token pages).  Token i goes to slot slots[i] = page * 64 + row; a negative slot
+ * skips the token, and so does a slot at or past num_pages * 64 (then the call returns -1).
+ * bf16 cache: pool row = the token's c_KV then k_R.  FP8 cache: c8 row = the codes of
+ * oracle_quantize_token, scale = its sigma, kr row = k_R.
+ */
+int oracle_append_kv(int n, const uint16_t* c_kv, const uint16_t* k_r, const int32_t* slots, int kv_fp8,
+                     int num_pages, uint16_t* pool, uint8_t* c8, float* scale, uint16_t* kr)
+{
+    int status = 0;
+    for (int i = 0; i < n; ++i) {
+        const int64_t slot = slots[i];
+        if (slot < 0) continue;
+        if (slot >= (int64_t)num_pages * PG) {
+            status = -1;
+            continue;
+        }
+        const uint16_t* c = c_kv + (int64_t)i * DC;
+        const uint16_t* r = k_r + (int64_t)i * DR;
+        if (!kv_fp8) {
+            uint16_t* row = pool + slot * DROW;
+            for (int j = 0; j < DC; ++j) row[j] = c[j];
+            for (int j = 0; j < DR; ++j) row[DC + j] = r[j];
+        } else {
+            scale[slot] = oracle_quantize_token(c, c8 + slot * DC);
+            for (int j = 0; j < DR; ++j) kr[slot * DR + j] = r[j];
+        }
+    }
+    return status;
+}

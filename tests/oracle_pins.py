@@ -325,6 +325,154 @@ def check_cache_geometry_golden():
     assert abs(g["softmax_scale"]["value"] - 1 / math.sqrt(oracle.D_HC + oracle.D_R)) < 1e-16
 
 
+# ------------------------------------------------------------------ cache append (write side)
+
+def _e4m3_values(codes: np.ndarray) -> np.ndarray:
+    """Values of e4m3 codes through torch's float8_e4m3fn (independent of the oracle's decoder)."""
+    return torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).view(torch.float8_e4m3fn).to(
+        torch.float64).numpy()
+
+
+def _torch_quantize(c: torch.Tensor):
+    """Per-row FP8 cache quantisation through torch: sigma = absmax / 448 in float32 (1 for an
+    all-zero row), codes = float8_e4m3fn cast of c / sigma."""
+    c = c.to(torch.float32)
+    amax = c.abs().amax(dim=-1)
+    sigma = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    codes = (c / sigma.unsqueeze(-1)).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes.numpy(), sigma.numpy()
+
+
+def check_e4m3_encode_round_trip():
+    """Every finite e4m3 code (both signs, -0 included) encodes back to itself."""
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], dtype=np.uint8)
+    got = oracle.e4m3_encode(_e4m3_values(codes).astype(np.float32))
+    assert np.array_equal(got, codes), np.nonzero(got != codes)
+
+
+def check_e4m3_encode_ties_and_neighbours():
+    """A value halfway between two adjacent codes goes to the one with the even mantissa field;
+    one float step below or above the midpoint goes to the nearer code; magnitudes from 448 up
+    give 448; both signs."""
+    v = _e4m3_values(np.arange(0x7F))
+    lo = np.arange(0x7E)
+    hi = lo + 1
+    mid64 = (v[lo] + v[hi]) / 2
+    mid = mid64.astype(np.float32)
+    assert np.array_equal(mid.astype(np.float64), mid64)  # midpoints are exact in float32
+    even = np.where(lo % 2 == 0, lo, hi)
+    below = np.nextafter(mid, np.float32(0))
+    above = np.nextafter(mid, np.float32(np.inf))
+    for sgn, sbit in ((1.0, 0x00), (-1.0, 0x80)):
+        s32 = np.float32(sgn)
+        assert np.array_equal(oracle.e4m3_encode(s32 * mid), (even | sbit).astype(np.uint8))
+        assert np.array_equal(oracle.e4m3_encode(s32 * below), (lo | sbit).astype(np.uint8))
+        assert np.array_equal(oracle.e4m3_encode(s32 * above), (hi | sbit).astype(np.uint8))
+        big = s32 * np.array([448.0, 455.0, 463.99, 464.0, 1e4, 3e38], np.float32)
+        assert np.array_equal(oracle.e4m3_encode(big), np.full(big.size, 0x7E | sbit, np.uint8))
+
+
+def check_e4m3_encode_against_torch():
+    """Every finite bf16 value below 464 in magnitude and 200,000 random float32 values spread
+    log-uniformly over the e4m3 range (subnormals included) encode as torch's float8_e4m3fn
+    cast (round to nearest, ties to even) does."""
+    x = (np.arange(65536, dtype=np.uint32) << 16).view(np.float32)
+    x = x[np.isfinite(x) & (np.abs(x) < 464)]
+    g = np.random.default_rng(5)
+    mag = np.exp2(g.uniform(-12.0, np.log2(460.0), 200_000)).astype(np.float32)
+    sgn = np.where(g.random(mag.size) < 0.5, np.float32(-1), np.float32(1))
+    x = np.concatenate([x, mag * sgn])
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = oracle.e4m3_encode(x)
+    bad = np.nonzero(got != ref)[0]
+    assert bad.size == 0, (x[bad[:5]], got[bad[:5]], ref[bad[:5]])
+
+
+def _quant_rows() -> torch.Tensor:
+    """bf16 latent rows covering the quantiser's cases: N(0,1) at three scales, a negative
+    outlier, many values landing among the e4m3 subnormals, exact ties once scaled, and an
+    all-zero row holding negative zeros."""
+    g = torch.Generator().manual_seed(21)
+    rows = [torch.randn(512, generator=g) * s for s in (1.0, 1e-3, 37.0)]
+    r = torch.randn(512, generator=g)
+    r[17] = -5e3
+    rows.append(r)
+    r = torch.randn(512, generator=g) * 1e-3
+    r[3] = 1.0
+    rows.append(r)
+    ties = torch.tensor([1.0625, 1.1875, -2.0 ** -10, 3 * 2.0 ** -10, 0.5 + 1 / 32, -(0.75 + 1 / 32)])
+    r = ties.repeat(86)[:512].clone()
+    r[0] = 448.0  # sigma = 1, so c / sigma = c exactly
+    rows.append(r)
+    r = torch.zeros(512)
+    r[::3] = -0.0
+    rows.append(r)
+    return torch.stack(rows).to(torch.bfloat16)
+
+
+def check_quantize_token_rule():
+    """Each row's largest magnitude maps to +-448 (code 0x7E / 0xFE); every code is within half
+    an e4m3 step of c / sigma; an all-zero row gets sigma 1 and (signed) zero codes; and the
+    whole token equals torch's pipeline (absmax / 448 in float32, float8_e4m3fn cast)."""
+    rows = _quant_rows()
+    ref_codes, ref_sigma = _torch_quantize(rows)
+    for i in range(rows.shape[0]):
+        codes, sigma = oracle.quantize_token(rows[i])
+        assert np.array_equal(codes, ref_codes[i]), (i, np.nonzero(codes != ref_codes[i])[0][:5])
+        assert sigma.tobytes() == np.float32(ref_sigma[i]).tobytes(), (i, sigma, ref_sigma[i])
+        c = rows[i].to(torch.float32).numpy()
+        if not np.any(c != 0):
+            assert sigma == np.float32(1.0)
+            assert np.array_equal(codes, np.where(np.signbit(c), 0x80, 0x00).astype(np.uint8))
+            continue
+        k = int(np.argmax(np.abs(c)))
+        assert codes[k] == (0xFE if c[k] < 0 else 0x7E)
+        q = (c / sigma).astype(np.float64)
+        e = np.floor(np.log2(np.maximum(np.abs(q), 2.0 ** -6)))
+        assert np.all(np.abs(_e4m3_values(codes) - q) <= np.exp2(e - 4)), i
+
+
+def check_append_rebuilds_cache():
+    """Appending every token of a synthetic bf16 cache (read from its pages in logical order)
+    into an empty pool rebuilds the cache bit for bit and leaves unused slots alone; into an
+    empty FP8 cache it gives torch's quantisation of the same rows and k_R unchanged.  Negative
+    slots are skipped; a slot past the pool is skipped and reported."""
+    inp = tiny_inputs(seq_lens=(1, 65, 130), seed=9, poison=False)
+    pool = inp.pool.contiguous().view(torch.int16).numpy().view(np.uint16)
+    N = inp.num_pool_pages
+    slots, rows = [], []
+    for b in range(inp.batch):
+        for t in range(int(inp.seq_lens[b])):
+            page, row = int(inp.block_table[b, t // 64]), t % 64
+            slots.append(page * 64 + row)
+            rows.append(pool[page, row])
+    slots = np.array(slots, np.int32)
+    rows = np.stack(rows)
+    c_kv, k_r = np.ascontiguousarray(rows[:, :512]), np.ascontiguousarray(rows[:, 512:])
+    empty = np.full((N, 64, 576), 0xFFFF, np.uint16)
+    assert oracle.append_kv(c_kv, k_r, slots, {"pool": empty}) == 0
+    used = np.zeros(N * 64, bool)
+    used[slots] = True
+    flat_new, flat_old = empty.reshape(N * 64, 576), pool.reshape(N * 64, 576)
+    assert np.array_equal(flat_new[used], flat_old[used])
+    assert np.all(flat_new[~used] == 0xFFFF)
+
+    fp8 = {"c8": np.full((N, 64, 512), 0x7F, np.uint8), "scale": np.full((N, 64), np.nan, np.float32),
+           "kr": np.full((N, 64, 64), 0xFFFF, np.uint16)}
+    assert oracle.append_kv(c_kv, k_r, slots, fp8) == 0
+    ref_codes, ref_sigma = _torch_quantize(torch.from_numpy(c_kv.view(np.int16)).view(torch.bfloat16))
+    assert np.array_equal(fp8["c8"].reshape(N * 64, 512)[slots], ref_codes)
+    assert np.array_equal(fp8["scale"].reshape(N * 64)[slots].view(np.uint32), ref_sigma.view(np.uint32))
+    assert np.array_equal(fp8["kr"].reshape(N * 64, 64)[slots], k_r)
+    assert np.all(fp8["c8"].reshape(N * 64, 512)[~used] == 0x7F)
+
+    cache = {"pool": np.full((N, 64, 576), 0xFFFF, np.uint16)}
+    assert oracle.append_kv(c_kv[:3], k_r[:3], np.array([-1, N * 64, 5], np.int32), cache) == -1
+    flat = cache["pool"].reshape(N * 64, 576)
+    assert np.array_equal(flat[5], rows[2])
+    assert np.all(np.delete(flat, 5, axis=0) == 0xFFFF)
+
+
 ALL_CHECKS = [
     check_e4m3_all_codes,
     check_single_token_is_projected_value,
@@ -343,4 +491,9 @@ ALL_CHECKS = [
     check_lse_combine_closed_forms,
     check_latent_attention_rows,
     check_cache_geometry_golden,
+    check_e4m3_encode_round_trip,
+    check_e4m3_encode_ties_and_neighbours,
+    check_e4m3_encode_against_torch,
+    check_quantize_token_rule,
+    check_append_rebuilds_cache,
 ]

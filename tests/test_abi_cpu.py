@@ -166,3 +166,29 @@ def test_step_host_rejects_bad_args(L):
                                     0x17000, 0x18000, 0x19000, plan_host.ctypes.data, 16)
     st, _ = _step_host(L, small_cap)
     assert st != binding.MLA_OK  # the plan does not fit its staging buffer
+
+
+def test_append_rejects_bad_args(L):
+    A = L.mla_append_kv
+    bf16, fp8 = binding.MLA_KV_BF16, binding.MLA_KV_FP8_E4M3
+    ok = dict(c=_p(0x10000), r=_p(0x20000), s=_p(0x30000), pool=_p(0x40000), scale=_p(0x50000),
+              kr=_p(0x60000), err=_p(0x70000))
+
+    def call(n=4, dtype=bf16, pages=8, **kw):
+        a = {**ok, **kw}
+        return A(n, a["c"], a["r"], a["s"], dtype, pages, a["pool"], a["scale"], a["kr"], a["err"], None)
+
+    assert call(n=0) == binding.MLA_OK                       # nothing to write: no launch
+    assert call(n=-1) == binding.MLA_ERR_INVALID_ARG
+    assert call(pages=0) == binding.MLA_ERR_INVALID_ARG
+    assert call(dtype=7) == binding.MLA_ERR_INVALID_ARG
+    assert call(c=None) == binding.MLA_ERR_INVALID_ARG
+    assert call(s=None) == binding.MLA_ERR_INVALID_ARG
+    assert call(err=None) == binding.MLA_ERR_INVALID_ARG
+    assert call(dtype=fp8, scale=None) == binding.MLA_ERR_INVALID_ARG
+    assert call(dtype=fp8, kr=None) == binding.MLA_ERR_INVALID_ARG
+    assert call(c=_p(0x10008)) == binding.MLA_ERR_ALIGNMENT
+    assert call(pool=_p(0x40004)) == binding.MLA_ERR_ALIGNMENT
+    assert call(s=_p(0x30002)) == binding.MLA_ERR_ALIGNMENT
+    assert call(dtype=fp8, kr=_p(0x60008)) == binding.MLA_ERR_ALIGNMENT
+    assert call(dtype=fp8, scale=_p(0x50002)) == binding.MLA_ERR_ALIGNMENT

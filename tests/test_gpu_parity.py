@@ -226,3 +226,26 @@ def test_run_host_new_lengths_and_fp8():
         out = step.run_host(inp.q_c.pin_memory(), inp.q_r.pin_memory(), seq_lens=short)
         assert step.device_error() == 0
         assert torch.equal(out, ref.cpu()), kv_dtype
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8_e4m3"])
+def test_graph_replay_matches_eager(kv_dtype):
+    """DecodeStep.capture: replaying the step's CUDA graph gives the bits of an eager step on
+    the same queries, also for queries copied into the captured tensors afterwards."""
+    inp = synth.make_inputs([3000, 700, 64 * 9 + 1], seed=13, poison_tail=True, kv_dtype=kv_dtype)
+    q_c, q_r, w_uk, w_uv, kv, bt = binding.inputs_to_device(inp, DEV)
+    step = binding.DecodeStep(inp.seq_lens, w_uk=w_uk, w_uv=w_uv, block_table=bt, min_pages_per_split=2, **kv)
+    assert step.info.num_combine > 0
+    graph = step.capture(q_c, q_r)
+    g = torch.Generator().manual_seed(5)
+    for _ in range(2):
+        new_c = torch.randn(tuple(q_c.shape), generator=g).to(torch.bfloat16).to(DEV)
+        new_r = torch.randn(tuple(q_r.shape), generator=g).to(torch.bfloat16).to(DEV)
+        q_c.copy_(new_c)
+        q_r.copy_(new_r)
+        graph.replay()
+        got = step.out.clone()
+        ref = step.run(new_c, new_r).clone()
+        torch.cuda.synchronize()
+        assert step.device_error() == 0
+        assert torch.equal(got, ref)

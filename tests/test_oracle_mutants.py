@@ -42,6 +42,19 @@ MUTANTS = {
     "out_proj_wrong_head": ("bf16_value(w_uv[((int64_t)h * DHC + d) * DC + c])",
                             "bf16_value(w_uv[((int64_t)(h ^ 1) * DHC + d) * DC + c])"),
     "combine_unnormalised_weight": ("const double w = exp(lj - L);", "const double w = exp(lj - mx);"),
+    "e4m3_encode_ties_away": ("c = (lo & 1) ? hi : lo; /* a tie: the even mantissa field */", "c = hi;"),
+    "e4m3_encode_zero_sign_lost": ("const uint8_t sign = signbit(x) ? 0x80 : 0x00;",
+                                   "const uint8_t sign = x < 0.0f ? 0x80 : 0x00;"),
+    "e4m3_encode_overflow_to_nan": ("if (a >= 448.0) return sign | 0x7E;", "if (a > 448.0) return sign | 0x7F;"),
+    "e4m3_encode_truncates": ("if (d_lo < d_hi)\n        c = lo;", "if (d_lo <= d_hi + 1e300)\n        c = lo;"),
+    "quantize_scale_447": ("const float sigma = amax > 0.0f ? amax / 448.0f : 1.0f;",
+                           "const float sigma = amax > 0.0f ? amax / 447.0f : 1.0f;"),
+    "quantize_zero_row_scale": ("const float sigma = amax > 0.0f ? amax / 448.0f : 1.0f;",
+                                "const float sigma = amax > 0.0f ? amax / 448.0f : 0.0f;"),
+    "append_rope_from_latent": ("for (int j = 0; j < DR; ++j) row[DC + j] = r[j];",
+                                "for (int j = 0; j < DR; ++j) row[DC + j] = c[j];"),
+    "append_fp8_kr_shifted": ("kr[slot * DR + j] = r[j];", "kr[slot * DR + j] = r[(j + 1) % DR];"),
+    "append_bad_slot_unreported": ("status = -1;\n            continue;", "status = 0;\n            continue;"),
     "bf16_widening_wrong": ("uint32_t u = (uint32_t)bits << 16;", "uint32_t u = ((uint32_t)bits << 16) | 0x8000u;"),
 }
 
