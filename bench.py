@@ -52,7 +52,8 @@ TRAFFIC_PATH = os.path.join(ROOT, "profiles", "decode_traffic.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 KERNEL_SOURCES = {
     "decode_bf16_kernel": ["mla_latent_kv_absorb_gb300/csrc/decode.cuh", "mla_latent_kv_absorb_gb300/csrc/ptx.cuh"],
-    "decode_fp8_kernel": ["mla_latent_kv_absorb_gb300/csrc/decode_fp8.cuh", "mla_latent_kv_absorb_gb300/csrc/ptx.cuh"],
+    "decode_fp8_kernel": ["mla_latent_kv_absorb_gb300/csrc/decode_fp8.cuh", "mla_latent_kv_absorb_gb300/csrc/decode.cuh",
+                          "mla_latent_kv_absorb_gb300/csrc/ptx.cuh"],
 }
 
 

@@ -95,7 +95,14 @@ constexpr int kOffXchg = kOffStatsStaging + kStagingSlots * kStatsBytes;
 constexpr int kOffP = kValueStages * kValueStageBytes;
 constexpr int kOffStats = kOffP + kMsgSlots * kPBytes;
 constexpr int kScoreEnd = kOffXchg + 4 * 2 * 128 * 4;
-constexpr int kValueEnd = kOffStats + kMsgSlots * kStatsBytes;
+constexpr int kValueEnd0 = kOffStats + kMsgSlots * kStatsBytes;
+// value CTA: one 32 x 32 fp32 transpose tile per correction warp for the output write-out
+// (rows padded to 144 bytes, so that both the row-wise writes and the column-wise reads of
+// 16-byte vectors fall in distinct bank groups)
+constexpr int kOutTileRowBytes = 144;
+constexpr int kOutTileBytes = 32 * kOutTileRowBytes;
+constexpr int kOffOutTile = (kValueEnd0 + 15) / 16 * 16;
+constexpr int kValueEnd = kOffOutTile + 4 * kOutTileBytes;
 constexpr int kOffBars = ((kScoreEnd > kValueEnd ? kScoreEnd : kValueEnd) + 7) / 8 * 8;
 
 enum Bar : int {
@@ -122,6 +129,7 @@ static_assert(kOffP % 1024 == 0, "P buffers are MMA operands (1024-byte aligned)
 static_assert(kChunkStages <= kMaxStages && kValueStages <= kMaxStages, "barrier slots per ring");
 static_assert(kOffBars % 8 == 0, "barriers need 8-byte alignment");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kOffOutTile % 16 == 0 && kOutTileRowBytes % 16 == 0, "the output tile is read and written in 16-byte vectors");
 static_assert(kStatsWarpBytes % 16 == 0 && kPWarpBytes % 16 == 0, "bulk copies move multiples of 16 bytes");
 
 // TMEM columns
@@ -742,34 +750,54 @@ out:
 }
 
 // Normalised output of an item: O / l to o_lat (bf16, sole item of its sequence) or to the
-// item's split partial (fp32).  Thread `row` owns TMEM lane `row`.
-__device__ __forceinline__ void write_output(const Params& p, const Item& it, float inv_l, uint32_t tmem,
-                                             uint32_t lane_off, int row)
+// item's split partial (fp32).  Lane `lane` of correction warp q4 owns TMEM lane (head)
+// 32 q4 + lane.  Each 32-column slice goes through the warp's tile in shared memory: written
+// one head row per lane, read back so that consecutive lanes cover consecutive columns of one
+// head, and every store instruction writes whole 128-byte lines (four heads at a time in fp32,
+// eight in bf16) instead of 16 bytes in each of 32 lines.
+template <class KernelParams>  // this kernel's Params, or the FP8 kernel's (same output fields)
+__device__ __forceinline__ void write_output(const KernelParams& p, const Item& it, float inv_l, uint32_t tmem,
+                                             uint32_t lane_off, uint8_t* tile, int q4, int lane)
 {
     using namespace dev;
+    float* mine = reinterpret_cast<float*>(tile + lane * kOutTileRowBytes);
 #pragma unroll 1
     for (int j = 0; j < 16; ++j) {
         uint32_t r[32];
         tmem_ld32(tmem + lane_off + 32 * j, r);
         tmem_wait_ld();
-        if (it.slot < 0) {
-            uint4* d4 = reinterpret_cast<uint4*>(p.o_lat + ((int64_t)it.seq * 128 + row) * 512 + 32 * j);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
+        for (int v = 0; v < 8; ++v)
+            reinterpret_cast<float4*>(mine)[v] =
+                make_float4(__uint_as_float(r[4 * v + 0]) * inv_l, __uint_as_float(r[4 * v + 1]) * inv_l,
+                            __uint_as_float(r[4 * v + 2]) * inv_l, __uint_as_float(r[4 * v + 3]) * inv_l);
+        __syncwarp();
+        if (it.slot < 0) {
+            // bf16: four lanes per head row (8 columns each), eight rows per instruction
+            const int c8 = lane & 3;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int rr = 8 * k + (lane >> 2);
+                const float4* src = reinterpret_cast<const float4*>(tile + rr * kOutTileRowBytes) + 2 * c8;
+                const float4 a = src[0], b = src[1];
                 uint4 o;
-                o.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv_l, __uint_as_float(r[8 * v + 1]) * inv_l);
-                o.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv_l, __uint_as_float(r[8 * v + 3]) * inv_l);
-                o.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv_l, __uint_as_float(r[8 * v + 5]) * inv_l);
-                o.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv_l, __uint_as_float(r[8 * v + 7]) * inv_l);
-                d4[v] = o;
+                o.x = pack_bf16x2(a.x, a.y);
+                o.y = pack_bf16x2(a.z, a.w);
+                o.z = pack_bf16x2(b.x, b.y);
+                o.w = pack_bf16x2(b.z, b.w);
+                *reinterpret_cast<uint4*>(p.o_lat + ((int64_t)it.seq * 128 + 32 * q4 + rr) * 512 + 32 * j + 8 * c8) = o;
             }
         } else {
-            float4* d4 = reinterpret_cast<float4*>(p.ws_o + ((int64_t)it.slot * 128 + row) * 512 + 32 * j);
+            // fp32: eight lanes per head row (4 columns each), four rows per instruction
+            const int c4 = lane & 7;
 #pragma unroll
-            for (int v = 0; v < 8; ++v)
-                d4[v] = make_float4(__uint_as_float(r[4 * v + 0]) * inv_l, __uint_as_float(r[4 * v + 1]) * inv_l,
-                                    __uint_as_float(r[4 * v + 2]) * inv_l, __uint_as_float(r[4 * v + 3]) * inv_l);
+            for (int k = 0; k < 8; ++k) {
+                const int rr = 4 * k + (lane >> 3);
+                const float4 a = reinterpret_cast<const float4*>(tile + rr * kOutTileRowBytes)[c4];
+                *reinterpret_cast<float4*>(p.ws_o + ((int64_t)it.slot * 128 + 32 * q4 + rr) * 512 + 32 * j + 4 * c4) = a;
+            }
         }
+        __syncwarp();  // the tile is rewritten by the next slice
     }
 }
 
@@ -778,8 +806,9 @@ __device__ __forceinline__ void value_correction(const Params& p, int item_begin
                                                  int warp, int lane, int tid128)
 {
     using namespace dev;
-    const int q4 = warp & 3, row = 32 * q4 + lane;
+    const int q4 = warp & 3;
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
+    uint8_t* out_tile = smem + kOffOutTile + q4 * kOutTileBytes;
     const uint32_t r_msg_free = dev::map_to_cta(dev::smem_u32(smem) + kOffBars + 8 * kMsgFree0, 0);
     MLA_TRACE_DECL;
     int g = 0, n_flagged = 0;
@@ -810,7 +839,7 @@ __device__ __forceinline__ void value_correction(const Params& p, int item_begin
             tc_fence_after();
             if (boundary) {  // the previous item's output leaves TMEM before this PV overwrites it
                 [[maybe_unused]] const long long te0 = MLA_TRACE_NOW();
-                write_output(p, prev, prev_inv_l, tmem, lane_off, row);
+                write_output(p, prev, prev_inv_l, tmem, lane_off, out_tile, q4, lane);
                 have_prev = false;
                 MLA_TRACE_ADD(9, MLA_TRACE_NOW() - te0);
             }
@@ -854,7 +883,7 @@ __device__ __forceinline__ void value_correction(const Params& p, int item_begin
         if (!MLA_TIMED(10, wait_warp(bars + 8 * kDrain, 0, w))) goto done;
         tc_fence_after();
         [[maybe_unused]] const long long te0 = MLA_TRACE_NOW();
-        write_output(p, prev, prev_inv_l, tmem, lane_off, row);
+        write_output(p, prev, prev_inv_l, tmem, lane_off, out_tile, q4, lane);
         MLA_TRACE_ADD(9, MLA_TRACE_NOW() - te0);
     }
 done:

@@ -53,6 +53,8 @@ using decode::Item;
 using decode::kTraceSlots;
 using decode::load_item;
 using decode::wait_freed;
+using decode::write_output;
+using decode::kOutTileBytes;
 #ifdef MLA_DECODE_TRACE
 using decode::kEvBase;
 using decode::kEvSlots;
@@ -96,7 +98,9 @@ constexpr int kScoreEnd = kOffSig + kSigSlots * kSigGroupBytes;
 // value CTA
 constexpr int kOffP = kValueStages * kValueStageBytes;
 constexpr int kOffStats = kOffP + kMsgSlots * kPBytes;
-constexpr int kValueEnd = kOffStats + kMsgSlots * kStatsBytes;
+// one 32 x 32 fp32 transpose tile per correction warp for the output write-out (as decode.cuh)
+constexpr int kOffOutTile = (kOffStats + kMsgSlots * kStatsBytes + 15) / 16 * 16;
+constexpr int kValueEnd = kOffOutTile + 4 * kOutTileBytes;
 constexpr int kOffBars = ((kScoreEnd > kValueEnd ? kScoreEnd : kValueEnd) + 7) / 8 * 8;
 
 enum Bar : int {
@@ -950,44 +954,16 @@ __device__ __forceinline__ void value_pconvert(const Params& p, int item_begin, 
     }
 }
 
-// Normalised output of an item: O / (g l) to o_lat (bf16, sole item of its sequence) or to the
-// item's split partial (fp32).  Thread `row` owns TMEM lane `row`.
-__device__ __forceinline__ void write_output(const Params& p, const Item& it, float inv_l, uint32_t tmem,
-                                             uint32_t lane_off, int row)
-{
-    using namespace dev;
-#pragma unroll 1
-    for (int j = 0; j < 16; ++j) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_off + 32 * j, r);
-        tmem_wait_ld();
-        if (it.slot < 0) {
-            uint4* d4 = reinterpret_cast<uint4*>(p.o_lat + ((int64_t)it.seq * 128 + row) * 512 + 32 * j);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                uint4 o;
-                o.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv_l, __uint_as_float(r[8 * v + 1]) * inv_l);
-                o.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv_l, __uint_as_float(r[8 * v + 3]) * inv_l);
-                o.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv_l, __uint_as_float(r[8 * v + 5]) * inv_l);
-                o.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv_l, __uint_as_float(r[8 * v + 7]) * inv_l);
-                d4[v] = o;
-            }
-        } else {
-            float4* d4 = reinterpret_cast<float4*>(p.ws_o + ((int64_t)it.slot * 128 + row) * 512 + 32 * j);
-#pragma unroll
-            for (int v = 0; v < 8; ++v)
-                d4[v] = make_float4(__uint_as_float(r[4 * v + 0]) * inv_l, __uint_as_float(r[4 * v + 1]) * inv_l,
-                                    __uint_as_float(r[4 * v + 2]) * inv_l, __uint_as_float(r[4 * v + 3]) * inv_l);
-        }
-    }
-}
+// The normalised output of an item, O / (g l), leaves through decode.cuh's write_output (its
+// inv_l here carries the item's token-factor normaliser g as well).
 
 __device__ __forceinline__ void value_correction(const Params& p, int item_begin, int item_end, int items_off,
                                                  uint8_t* smem, uint32_t bars, uint32_t tmem, const dev::WaitCtx& w,
                                                  int warp, int lane, int tid128)
 {
     using namespace dev;
-    const int q4 = warp & 3, row = 32 * q4 + lane;
+    const int q4 = warp & 3;
+    uint8_t* out_tile = smem + kOffOutTile + q4 * kOutTileBytes;
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
     const uint32_t r_msg_free = dev::map_to_cta(dev::smem_u32(smem) + kOffBars + 8 * kMsgFree0, 0);
     int g = 0, n_flagged = 0;
@@ -1016,7 +992,7 @@ __device__ __forceinline__ void value_correction(const Params& p, int item_begin
             if (!wait_warp_ool(bars + 8 * (kODrain0 + e), n_flagged >> 1, w)) goto done;
             tc_fence_after();
             if (boundary) {  // the previous item's output leaves TMEM before this PV overwrites it
-                write_output(p, prev, prev_inv_l, tmem, lane_off, row);
+                write_output(p, prev, prev_inv_l, tmem, lane_off, out_tile, q4, lane);
                 have_prev = false;
             }
             if (flags & 2u) {
@@ -1057,7 +1033,7 @@ __device__ __forceinline__ void value_correction(const Params& p, int item_begin
         // last item: every PV is done when the MMA thread's final commit lands
         if (!wait_warp_ool(bars + 8 * kDrain, 0, w)) goto done;
         tc_fence_after();
-        write_output(p, prev, prev_inv_l, tmem, lane_off, row);
+        write_output(p, prev, prev_inv_l, tmem, lane_off, out_tile, q4, lane);
     }
 done:
     tc_fence_before();
