@@ -78,3 +78,41 @@ def test_warmup_floor():
 
     with pytest.raises(SystemExit):
         bench.main(["--warmup", "2"])
+
+
+def test_kernel_hash_covers_included_sources():
+    """A decode kernel's recorded traffic is keyed by a hash of its sources: every header its
+    main file includes (transitively, within csrc/) must be part of that hash."""
+    import re
+
+    import bench
+
+    for kernel, files in bench.KERNEL_SOURCES.items():
+        todo, seen = [files[0]], set()
+        while todo:
+            rel = todo.pop()
+            if rel in seen:
+                continue
+            seen.add(rel)
+            text = open(os.path.join(ROOT, rel)).read()
+            for inc in re.findall(r'#include\s+"([^"]+\.cuh)"', text):
+                todo.append(os.path.join(os.path.dirname(rel), inc))
+        assert seen <= set(files), (kernel, sorted(seen - set(files)))
+
+
+def test_recorded_traffic_only_for_the_current_source(tmp_path, monkeypatch):
+    import json
+
+    import bench
+
+    path = tmp_path / "traffic.json"
+    rec = {"kernel": "decode_bf16_kernel", "workload": "b16_s65536", "tokens": 1000,
+           "dram_bytes_per_launch": 2_000_000, "kernel_hash": bench.kernel_hash("decode_bf16_kernel")}
+    path.write_text(json.dumps([rec]))
+    monkeypatch.setattr(bench, "TRAFFIC_PATH", str(path))
+    assert bench.recorded_traffic("decode_bf16_kernel", "b16_s65536", 1000) == 2_000_000
+    assert bench.recorded_traffic("decode_bf16_kernel", "b16_s65536", 500) == 1_000_000  # scaled by tokens
+    assert bench.recorded_traffic("decode_fp8_kernel", "b16_s65536", 1000) is None
+    rec["kernel_hash"] = "0" * 16  # taken on another version of the kernel
+    path.write_text(json.dumps([rec]))
+    assert bench.recorded_traffic("decode_bf16_kernel", "b16_s65536", 1000) is None
