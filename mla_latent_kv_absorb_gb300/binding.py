@@ -273,9 +273,9 @@ def mla_append_kv(c_kv: torch.Tensor, k_r: torch.Tensor, slots: torch.Tensor, *,
     = skip).  bf16 cache: kv_pool [pages, 64, 576].  FP8 cache (kv_scale given): c_KV quantised
     per token into kv_pool [pages, 64, 512] (e4m3 codes) and kv_scale [pages, 64], k_R into
     kr_pool [pages, 64, 64]."""
-    n = int(slots.shape[0]) if slots.dim() == 1 else -1
-    if n < 0:
-        raise ValueError("slots must be 1-d")
+    if not isinstance(slots, torch.Tensor) or slots.dim() != 1:
+        raise ValueError("slots must be a 1-d tensor")
+    n = int(slots.shape[0])
     _need(slots, "slots", torch.int32, (n,))
     _need(c_kv, "c_kv", torch.bfloat16, (n, D_C))
     _need(k_r, "k_r", torch.bfloat16, (n, D_R))

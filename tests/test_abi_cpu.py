@@ -192,3 +192,20 @@ def test_append_rejects_bad_args(L):
     assert call(s=_p(0x30002)) == binding.MLA_ERR_ALIGNMENT
     assert call(dtype=fp8, kr=_p(0x60008)) == binding.MLA_ERR_ALIGNMENT
     assert call(dtype=fp8, scale=_p(0x50002)) == binding.MLA_ERR_ALIGNMENT
+
+
+def test_append_binding_checks_tensors():
+    """The Python binding refuses host tensors, wrong dtypes and shapes before any call."""
+    import torch
+
+    c = torch.zeros(4, 512, dtype=torch.bfloat16)
+    r = torch.zeros(4, 64, dtype=torch.bfloat16)
+    s = torch.zeros(4, dtype=torch.int32)
+    pool = torch.zeros(2, 64, 576, dtype=torch.bfloat16)
+    err = torch.zeros(1, dtype=torch.int32)
+    with pytest.raises(ValueError, match="1-d"):
+        binding.mla_append_kv(c, r, s.view(2, 2), kv_pool=pool, dev_error=err)
+    with pytest.raises(ValueError, match="CUDA"):
+        binding.mla_append_kv(c, r, s, kv_pool=pool, dev_error=err)
+    with pytest.raises(TypeError):
+        binding.mla_append_kv(c, r, s.long(), kv_pool=pool, dev_error=err)
