@@ -213,7 +213,8 @@ def run_ours(args, rank, world, local):
     binding.lib()
     inp = synth.make_workload(args.workload, seed=synth.DEFAULT_SEED + rank, poison_tail=False)
     q_c, q_r, w_uk, w_uv, kv, bt = binding.inputs_to_device(inp, device)
-    step = binding.DecodeStep(inp.seq_lens, w_uk=w_uk, w_uv=w_uv, block_table=bt, **kv)
+    step = binding.DecodeStep(inp.seq_lens, w_uk=w_uk, w_uv=w_uv, block_table=bt,
+                              item_cost_pages=args.item_cost_pages, **kv)
     acc = workload_accounting(inp)
     peaks = load_peaks()
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=device)
@@ -359,7 +360,8 @@ def run_ours(args, rank, world, local):
                              "third pass of K steps with an event between kernels",
                    "graph": graph_note,
                    "plan": {"clusters": step.info.num_clusters, "items": step.info.num_items,
-                            "combine_seqs": step.info.num_combine, "max_splits": step.info.max_splits}},
+                            "combine_seqs": step.info.num_combine, "max_splits": step.info.max_splits,
+                            "item_cost_pages": args.item_cost_pages}},
         "step_us_eager": round(eager_ms * 1e3, 2),
         "kernels_us": {k: round(statistics.mean(v) * 1e3, 2) for k, v in k_ms.items()},
         "kv_tbps": round(acc["kv_bytes"] / (ms_max * 1e-3) / 1e12, 3),
@@ -482,6 +484,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-parity", dest="parity", action="store_false")
+    ap.add_argument("--item-cost-pages", type=int, default=0,
+                    help="planner: balance pages plus this charge per extra item of a CTA pair (0: equal pages)")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="time eager launches for the value instead of replays of the step's CUDA graph")
     args = ap.parse_args(argv)

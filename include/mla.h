@@ -84,6 +84,10 @@ typedef struct mla_plan_options {
     int32_t min_pages_per_split; /* 0 = default 8: no item boundary closer than this to a sequence edge */
     int32_t max_clusters;        /* 0 = num_sms / 2; otherwise at most this many CTA pairs */
     int64_t wait_timeout_ns;     /* 0 = default 2e9: bound on every device-side wait */
+    int32_t item_cost_pages;     /* 0 = cut into equal page runs; > 0: balance pages plus this many
+                                    pages' worth of cost for each item of a CTA pair after its
+                                    first (a second item reloads the query and writes an output) */
+    int32_t reserved;            /* must be 0 */
 } mla_plan_options;
 
 typedef struct mla_plan_info {

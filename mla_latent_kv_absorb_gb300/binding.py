@@ -37,7 +37,8 @@ class MlaError(RuntimeError):
 
 class PlanOptions(ctypes.Structure):
     _fields_ = [("min_pages_per_split", ctypes.c_int32), ("max_clusters", ctypes.c_int32),
-                ("wait_timeout_ns", ctypes.c_int64)]
+                ("wait_timeout_ns", ctypes.c_int64), ("item_cost_pages", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -152,7 +153,7 @@ def _need(t: torch.Tensor, name: str, dtype, shape=None, device=True):
 # --------------------------------------------------------------------------- C ABI, same names
 
 def mla_plan_splits(seq_lens, num_sms: int, *, min_pages_per_split: int = 0, max_clusters: int = 0,
-                    wait_timeout_ns: int = 0):
+                    wait_timeout_ns: int = 0, item_cost_pages: int = 0):
     """Host planning. Returns (plan image as an int32 numpy array, PlanInfo)."""
     lens = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
     B = int(lens.size)
@@ -160,7 +161,7 @@ def mla_plan_splits(seq_lens, num_sms: int, *, min_pages_per_split: int = 0, max
     if cap == 0:
         raise MlaError("mla_plan_splits", MLA_ERR_INVALID_ARG, "bad batch or SM count")
     buf = np.zeros(cap // 4, dtype=np.int32)
-    opts = PlanOptions(int(min_pages_per_split), int(max_clusters), int(wait_timeout_ns))
+    opts = PlanOptions(int(min_pages_per_split), int(max_clusters), int(wait_timeout_ns), int(item_cost_pages), 0)
     info = PlanInfo()
     st = lib().mla_plan_splits(lens.ctypes.data_as(ctypes.c_void_p), B, int(num_sms), ctypes.byref(opts),
                                buf.ctypes.data_as(ctypes.c_void_p), cap, ctypes.byref(info))
@@ -315,12 +316,13 @@ class DecodeStep:
     def __init__(self, seq_lens, *, w_uk: torch.Tensor, w_uv: torch.Tensor, kv_pool: torch.Tensor,
                  block_table: torch.Tensor, kv_scale: Optional[torch.Tensor] = None,
                  kr_pool: Optional[torch.Tensor] = None, device=None, min_pages_per_split: int = 0,
-                 max_clusters: int = 0, wait_timeout_ns: int = 0, softmax_scale: float = SOFTMAX_SCALE):
+                 max_clusters: int = 0, wait_timeout_ns: int = 0, item_cost_pages: int = 0,
+                 softmax_scale: float = SOFTMAX_SCALE):
         self.device = torch.device(device if device is not None else "cuda")
         self.seq_lens = np.asarray(seq_lens, dtype=np.int32)
         self.batch = int(self.seq_lens.size)
         self._plan_opts = dict(min_pages_per_split=min_pages_per_split, max_clusters=max_clusters,
-                               wait_timeout_ns=wait_timeout_ns)
+                               wait_timeout_ns=wait_timeout_ns, item_cost_pages=item_cost_pages)
         self._num_sms = num_sms(self.device)
         self.plan_host, self.info = mla_plan_splits(self.seq_lens, self._num_sms, **self._plan_opts)
         self.plan_dev = torch.from_numpy(self.plan_host).to(self.device)
@@ -394,7 +396,7 @@ class DecodeStep:
                            _addr(self.lse), _addr(self.out), _addr(self.dev_error), _addr(self._h_stage),
                            self._h_stage.numel() * 4)
         opts = PlanOptions(int(self._plan_opts["min_pages_per_split"]), int(self._plan_opts["max_clusters"]),
-                           int(self._plan_opts["wait_timeout_ns"]))
+                           int(self._plan_opts["wait_timeout_ns"]), int(self._plan_opts["item_cost_pages"]), 0)
         info = PlanInfo()
         st = lib().mla_decode_step_host(lens.ctypes.data_as(ctypes.c_void_p), B, self._num_sms, ctypes.byref(opts),
                                         _ptr(q_c), _ptr(q_r), _ptr(block_table), int(bt_dev.shape[1]),

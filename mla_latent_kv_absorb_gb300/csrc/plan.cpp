@@ -6,6 +6,13 @@
 // an equal, contiguous run of pages of the concatenated sequences, and moves a run's edge to
 // the nearest sequence edge when it would otherwise leave a sliver of fewer than
 // `min_pages_per_split` pages.  A sequence that ends up in one item needs no merge.
+//
+// With `item_cost_pages` > 0 the runs are balanced on cost instead of pages: a pair pays that
+// many pages' worth for each item after its first (the next item reloads the query into the
+// score CTA and the value CTA writes the previous output out).  Greedy packing under a cost cap
+// is optimal for contiguous runs (extending a run never lowers its cost), so the planner
+// bisects for the smallest cap whose packing fits the pairs and snaps those cuts like equal
+// ones.
 #include <algorithm>
 #include <climits>
 #include <cstring>
@@ -35,6 +42,35 @@ static int64_t plan_words(int64_t batch, int64_t clusters, int64_t items, int64_
     return kPlanHeaderWords + plan_round8(clusters + 1) + items * kItemWords + plan_round8(combine * kCombineWords);
 }
 
+// Greedy contiguous packing of the concatenated page list under cost cap T (T >= 1): each run
+// takes pages while its cost (pages + item_cost per item after the first) stays within T.
+// Returns the number of runs; writes their end points (cuts[0] = 0) when `cuts` is given.
+static int64_t pack_runs(const std::vector<int64_t>& start, int batch, int64_t T, int64_t item_cost,
+                         std::vector<int64_t>* cuts)
+{
+    const int64_t total = start[batch];
+    if (cuts) cuts->assign(1, 0);
+    int64_t g = 0, n = 0;
+    int s = 0;
+    while (g < total) {
+        ++n;
+        int64_t cost = 0;
+        bool first = true;
+        while (g < total) {
+            while (start[s + 1] <= g) ++s;
+            const int64_t room = T - cost - (first ? 0 : item_cost);
+            if (room <= 0) break;
+            const int64_t take = std::min(room, start[s + 1] - g);
+            cost += (first ? 0 : item_cost) + take;
+            g += take;
+            first = false;
+            if (g < start[s + 1]) break;  // the run ends inside this sequence
+        }
+        if (cuts) cuts->push_back(g);
+    }
+    return n;
+}
+
 extern "C" size_t mla_plan_bytes_max(int32_t batch, int32_t num_sms)
 {
     if (batch <= 0 || num_sms < 2) return 0;
@@ -49,11 +85,13 @@ extern "C" mla_status mla_plan_splits(const int32_t* seq_lens, int32_t batch, in
                                       mla_plan_info* info)
 {
     if (!seq_lens || !plan_host || !info || batch <= 0 || num_sms < 2) return MLA_ERR_INVALID_ARG;
-    int32_t min_pages = 8, max_clusters = num_sms / 2;
+    int32_t min_pages = 8, max_clusters = num_sms / 2, item_cost = 0;
     int64_t timeout_ns = 2000000000LL;
     if (opts) {
-        if (opts->min_pages_per_split < 0 || opts->max_clusters < 0 || opts->wait_timeout_ns < 0)
+        if (opts->min_pages_per_split < 0 || opts->max_clusters < 0 || opts->wait_timeout_ns < 0 ||
+            opts->item_cost_pages < 0 || opts->reserved != 0)
             return MLA_ERR_INVALID_ARG;
+        item_cost = opts->item_cost_pages;
         if (opts->min_pages_per_split > 0) min_pages = opts->min_pages_per_split;
         if (opts->max_clusters > 0) max_clusters = std::min(max_clusters, opts->max_clusters);
         if (opts->wait_timeout_ns > 0) timeout_ns = opts->wait_timeout_ns;
@@ -73,7 +111,23 @@ extern "C" mla_status mla_plan_splits(const int32_t* seq_lens, int32_t batch, in
 
     // how many CTA pairs: no fewer than min_pages pages each, no more than the GPU holds
     const int64_t want = std::max<int64_t>(1, total / std::max(1, min_pages));
-    const int64_t C = std::min<int64_t>(max_clusters, want);
+    int64_t C = std::min<int64_t>(max_clusters, want);
+
+    // target cut points: equal page shares, or the cost-balanced packing (which may use fewer pairs)
+    std::vector<int64_t> target;
+    if (item_cost > 0 && C > 1) {
+        int64_t lo = (total + C - 1) / C, hi = total + (int64_t)item_cost * batch;  // one run fits under hi
+        while (lo < hi) {
+            const int64_t mid = lo + (hi - lo) / 2;
+            if (pack_runs(start, batch, mid, item_cost, nullptr) <= C) hi = mid;
+            else lo = mid + 1;
+        }
+        pack_runs(start, batch, lo, item_cost, &target);
+        C = (int64_t)target.size() - 1;
+    } else {
+        target.resize(C + 1);
+        for (int64_t k = 0; k <= C; ++k) target[k] = (k * total + C / 2) / C;
+    }
 
     // cut points in the concatenated page list, snapped to sequence edges when a cut would
     // leave fewer than min_pages pages on either side within a sequence
@@ -82,7 +136,7 @@ extern "C" mla_status mla_plan_splits(const int32_t* seq_lens, int32_t batch, in
     cut[C] = total;
     int seq = 0;
     for (int64_t k = 1; k < C; ++k) {
-        int64_t g = (k * total + C / 2) / C;
+        int64_t g = target[k];
         while (seq < batch && start[seq + 1] <= g) ++seq;   // g lies in sequence `seq`
         if (seq < batch) {
             const int64_t lo = start[seq], hi = start[seq + 1];

@@ -111,3 +111,51 @@ def test_timeout_option_recorded():
     plan, info = binding.mla_plan_splits([100], 152, wait_timeout_ns=123456789)
     assert info.wait_timeout_ns == 123456789
     assert int(plan[12]) + (int(plan[13]) << 32) == 123456789
+
+
+def _pair_costs(lens, c, **kw):
+    plan, info = binding.mla_plan_splits(np.asarray(lens, np.int32), 152, item_cost_pages=c, **kw)
+    h, cl, items, _ = decode_plan(plan)
+    return np.array([int((items[cl[k]:cl[k + 1], 2] - items[cl[k]:cl[k + 1], 1]).sum())
+                     + c * max(0, int(cl[k + 1] - cl[k]) - 1) for k in range(h["clusters"])]), info
+
+
+@pytest.mark.parametrize("cost", [1, 7, 50])
+def test_item_cost_plans_are_valid(cost):
+    g = torch.Generator().manual_seed(42)
+    for lens in ([65536] * 16, synth.ragged_lengths(64, 128, 32768, g), [1] * 300, [5000, 1, 70000, 3], [65536],
+                 [4096] * 16, [2048]):
+        check_plan(lens, item_cost_pages=cost)
+    rng = np.random.default_rng(cost)
+    for _ in range(100):
+        lens = rng.integers(1, 70000, size=int(rng.integers(1, 200)))
+        check_plan(lens, num_sms=int(rng.choice([2, 16, 152])), min_pages_per_split=int(rng.integers(0, 20)),
+                   item_cost_pages=cost)
+
+
+def test_item_cost_balances_pairs():
+    """With a per-item charge the pairs that hold two items get fewer pages: the largest pair
+    cost (pages + charge per extra item) drops below that of equal page runs and comes within
+    one charge and one sequence-edge snap of the mean."""
+    c = 7
+    for lens in ([65536] * 16, [4096] * 16):
+        base_plan, base_info = binding.mla_plan_splits(np.asarray(lens, np.int32), 152)
+        h, cl, items, _ = decode_plan(base_plan)
+        base = np.array([int((items[cl[k]:cl[k + 1], 2] - items[cl[k]:cl[k + 1], 1]).sum())
+                         + c * max(0, int(cl[k + 1] - cl[k]) - 1) for k in range(h["clusters"])])
+        costs, info = _pair_costs(lens, c)
+        assert costs.max() < base.max(), (lens[0], costs.max(), base.max())
+        assert costs.max() <= costs.sum() / costs.size + c + 8
+
+
+def test_item_cost_rejects_bad_values():
+    with pytest.raises(binding.MlaError):
+        binding.mla_plan_splits([100], 152, item_cost_pages=-1)
+    opts = binding.PlanOptions(0, 0, 0, 0, 5)  # reserved must be 0
+    buf = np.zeros(4096, np.int32)
+    info = binding.PlanInfo()
+    lens = np.array([100], np.int32)
+    import ctypes
+    st = binding.lib().mla_plan_splits(lens.ctypes.data_as(ctypes.c_void_p), 1, 152, ctypes.byref(opts),
+                                       buf.ctypes.data_as(ctypes.c_void_p), buf.nbytes, ctypes.byref(info))
+    assert st == binding.MLA_ERR_INVALID_ARG
