@@ -55,12 +55,12 @@ def test_out_proj(batch):
 
 # ------------------------------------------------------------------------------------ decode kernel alone
 
-def _decode_only(inp, *, min_pages=0, max_clusters=0):
+def _decode_only(inp, *, min_pages=0, max_clusters=0, item_cost=0):
     """Run mla_decode_paged (+ merge) on bf16-rounded oracle q_abs; return (o_lat, lse, info, q_abs_bf16)."""
     q_abs_bf16 = bf16_round(oracle.absorb_q(inp.q_c, inp.w_uk))
     _, q_r, _, _, kv, bt = binding.inputs_to_device(inp, DEV)
     plan, info = binding.mla_plan_splits(inp.seq_lens, binding.num_sms(), min_pages_per_split=min_pages,
-                                         max_clusters=max_clusters)
+                                         max_clusters=max_clusters, item_cost_pages=item_cost)
     plan_dev = torch.from_numpy(plan).to(DEV)
     B = inp.batch
     o_lat = torch.full((B, 128, 512), float("nan"), dtype=torch.bfloat16, device=DEV)
@@ -106,6 +106,17 @@ def test_decode_few_clusters_many_items():
     inp = synth.make_inputs(lens, seed=501, poison_tail=True)
     o_lat, lse, info, q = _decode_only(inp, min_pages=1, max_clusters=2)
     assert info.num_clusters == 2 and info.num_items >= len(lens)
+    _check_latent(inp, o_lat, lse, q)
+
+
+@pytest.mark.parametrize("item_cost", [7, 50])
+def test_decode_cost_balanced_plan(item_cost):
+    """Plans cut with a per-item charge (pairs holding several items get fewer pages, and the
+    packing may leave pairs unused) decode to the oracle's result as equal-run plans do."""
+    lens = [64 * 40 + 5, 1, 9000, 300, 64 * 20, 4000]
+    inp = synth.make_inputs(lens, seed=503 + item_cost, poison_tail=True)
+    o_lat, lse, info, q = _decode_only(inp, min_pages=2, item_cost=item_cost)
+    assert info.num_combine > 0
     _check_latent(inp, o_lat, lse, q)
 
 
