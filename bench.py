@@ -486,7 +486,7 @@ def main(argv=None):
     ap.add_argument("--no-parity", dest="parity", action="store_false")
     ap.add_argument("--item-cost-pages", type=int, default=7,
                     help="planner: balance pages plus this charge per extra item of a CTA pair (0: equal page "
-                         "runs, the library's default); 7 measured best at B=16, S=65536")
+                         "runs, the library's default); 7 timed faster than 0 at B=16, S=65536")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="time eager launches for the value instead of replays of the step's CUDA graph")
     args = ap.parse_args(argv)
