@@ -14,7 +14,9 @@
  *   - Pointers marked "device" are CUDA device pointers; "host" pointers are ordinary memory.
  *   - bf16 tensors are passed as void* and are contiguous, row-major, in the shapes stated.
  *   - The caller allocates and owns every buffer, workspaces included.  The library calls no
- *     allocator and keeps no global mutable state; calls are safe from several host threads.
+ *     allocator.  Its only global mutable state is the fixed device array behind
+ *     mla_decode_paged_static_ws (and that call's per-device address cache); every other call
+ *     is safe from several host threads.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only enqueue work and
  *     return; results are ready when the stream reaches them.
  *   - Arguments, shapes, alignment and workspace sizes are checked on the host before any
@@ -146,7 +148,10 @@ MLA_API mla_status mla_absorb_q(const void* q_c, const void* w_uk, void* q_abs, 
  *                   per token, and k_R / scale is formed in bf16 for the RoPE MMA.
  *   block_table     device int32 [batch][max_pages_per_seq]; entry p of row b is the physical
  *                   page of tokens 64p..64p+63 of sequence b.  Only the first ceil(S_b/64)
- *                   entries of a row are read.
+ *                   entries of a row are read, and never an entry at or past
+ *                   max_pages_per_seq: a sequence whose pages do not fit in its row (this call
+ *                   has no host copy of the lengths to check) reads its missing pages as zeros
+ *                   and sets MLA_DEVERR_BAD_PAGE, like an entry outside the pool.
  *   softmax_scale   1/sqrt(d_hc + d_R) for the pages' model
  *   workspace       device buffer of info->workspace_bytes (split partials), 16-byte aligned;
  *                   may be NULL when info->workspace_bytes == 0
@@ -223,7 +228,12 @@ MLA_API mla_status mla_append_kv(int32_t num_tokens, const void* c_kv, const voi
  * that its merge launch reads.
  * Set-up: the first call on each device (with that device current) looks up the array's device
  * address and, through it, loads the library module that holds the array; make that first call
- * before any stream capture.
+ * before any stream capture.  The address is cached per device for the life of the process, so
+ * the cache must not outlive the device's primary context: after cudaDeviceReset (or any
+ * teardown of the primary context) do not call this entry point again in that process.
+ * Memory: the array costs device memory only on devices where the module is loaded.  Under the
+ * CUDA runtime's default lazy module loading that happens on the first call; with
+ * CUDA_MODULE_LOADING=EAGER every device that creates a context holds the array from then on.
  * One array per device: calls whose kernels may overlap (different streams, or several host
  * threads on one device) race on it and corrupt each other's results.  Calls in order on one
  * stream are safe. */
@@ -255,6 +265,8 @@ MLA_API mla_status mla_decode_paged_static_ws(const mla_plan_info* info, const v
  *   q_c_host, q_r_host  host bf16 [batch][128][128] / [batch][128][64]
  *   out_host          host bf16 [batch][128][128], receives out
  *   info_out          may be NULL; receives the plan header
+ * A sequence whose ceil(S_b/64) pages exceed max_pages_per_seq is rejected with
+ * MLA_ERR_INVALID_ARG before anything is copied or launched.
  * Device-side errors land in bufs->dev_error as for mla_decode_paged (read it afterwards). */
 typedef struct mla_step_buffers {
     void* q_c;

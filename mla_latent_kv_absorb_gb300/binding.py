@@ -302,6 +302,16 @@ def mla_debug_wait_timeout(dev_error: torch.Tensor, timeout_ns: int, stream=None
 
 # --------------------------------------------------------------------------- one decode step
 
+def _check_table_rows(seq_lens, block_table) -> None:
+    """Every page of every sequence needs an entry in its block-table row."""
+    if block_table is None or block_table.dim() != 2:
+        return
+    pages = (np.asarray(seq_lens, dtype=np.int64) + PAGE - 1) // PAGE
+    if pages.size and int(pages.max()) > int(block_table.shape[1]):
+        raise ValueError(f"block_table rows hold {int(block_table.shape[1])} pages, a sequence needs "
+                         f"{int(pages.max())}")
+
+
 def num_sms(device=None) -> int:
     return torch.cuda.get_device_properties(device if device is not None else torch.cuda.current_device()).multi_processor_count
 
@@ -329,6 +339,7 @@ class DecodeStep:
         self.w_uk, self.w_uv = w_uk, w_uv
         self.kv_pool, self.kv_scale, self.kr_pool = kv_pool, kv_scale, kr_pool
         self.block_table = block_table
+        _check_table_rows(self.seq_lens, block_table)
         self.softmax_scale = softmax_scale
         B = self.batch
         ws = int(self.info.workspace_bytes)
@@ -386,6 +397,7 @@ class DecodeStep:
                                         tuple(self._bt_dev.shape) != tuple(block_table.shape)):
             self._bt_dev = torch.empty(tuple(block_table.shape), dtype=torch.int32, device=self.device)
         bt_dev = self._bt_dev if block_table is not None else self.block_table
+        _check_table_rows(lens, bt_dev)
         if out is None:
             out = torch.empty(B, NUM_HEADS, D_HC, dtype=torch.bfloat16).pin_memory()
         _need(out, "out", torch.bfloat16, (B, NUM_HEADS, D_HC), device=False)

@@ -369,6 +369,8 @@ extern "C" mla_status mla_decode_step_host(const int32_t* seq_lens, int32_t batc
     if (!seq_lens || batch <= 0 || !q_c_host || !q_r_host || !bufs || !out_host || !bufs->plan_host ||
         !bufs->plan || !bufs->block_table || max_pages_per_seq <= 0)
         return MLA_ERR_INVALID_ARG;
+    for (int32_t b = 0; b < batch; ++b)  // every page of every sequence has a block-table entry
+        if (seq_lens[b] > 0 && (seq_lens[b] + 63) / 64 > max_pages_per_seq) return MLA_ERR_INVALID_ARG;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     mla_plan_info info;
     mla_status st = mla_plan_splits(seq_lens, batch, num_sms, opts, bufs->plan_host, bufs->plan_capacity, &info);

@@ -225,7 +225,7 @@ __device__ __forceinline__ void run_producer(const CUtensorMap* tm, const Params
             const int n = min(32, it.page_end - pg0);
             int page = 0;
             if (lane < n) {
-                page = __ldg(bt + pg0 + lane);
+                page = pg0 + lane < p.max_pages ? __ldg(bt + pg0 + lane) : -1;  // past the row: bad page
                 if (page < 0 || page >= p.num_pool_pages) raise_error(p.dev_error, MLA_DEVERR_BAD_PAGE);
             }
             for (int j = 0; j < n; ++j) {
@@ -276,7 +276,7 @@ __device__ __forceinline__ void score_producer(const CUtensorMap* tm, const Para
             const int n = min(32, it.page_end - pg0);  // a multiple of 4 unless it ends the item
             int page = 0;
             if (lane < n) {
-                page = __ldg(bt + pg0 + lane);
+                page = pg0 + lane < p.max_pages ? __ldg(bt + pg0 + lane) : -1;  // past the row: bad page
                 if (page < 0 || page >= p.num_pool_pages) raise_error(p.dev_error, MLA_DEVERR_BAD_PAGE);
             }
             for (int j = 0; j < n && ok; j += kGroupPages) {

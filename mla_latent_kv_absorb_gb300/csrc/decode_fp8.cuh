@@ -256,7 +256,7 @@ __device__ __forceinline__ void value_producer(const CUtensorMap* tm_c8, const P
             const int n = min(32, it.page_end - pg0);
             int page = 0;
             if (lane < n) {
-                page = __ldg(bt + pg0 + lane);
+                page = pg0 + lane < p.max_pages ? __ldg(bt + pg0 + lane) : -1;  // past the row: bad page
                 if (page < 0 || page >= p.num_pool_pages) raise_error(p.dev_error, MLA_DEVERR_BAD_PAGE);
             }
             for (int j = 0; j < n; ++j) {
@@ -305,7 +305,7 @@ __device__ __forceinline__ void score_producer(const CUtensorMap* tm_c8, const P
             const int n = min(32, it.page_end - pg0);  // a multiple of 4 unless it ends the item
             int page = 0;
             if (lane < n) {
-                page = __ldg(bt + pg0 + lane);
+                page = pg0 + lane < p.max_pages ? __ldg(bt + pg0 + lane) : -1;  // past the row: bad page
                 if (page < 0 || page >= p.num_pool_pages) raise_error(p.dev_error, MLA_DEVERR_BAD_PAGE);
             }
             for (int j = 0; j < n && ok; j += kGroupPages) {
@@ -367,7 +367,7 @@ __device__ __forceinline__ void kr_convert(const CUtensorMap* tm_kr, const Param
         // largest scale over the item's tokens: lane k takes pages k, k + 32, ...
         float smax = 0.f;
         for (int pg = it.page_begin + lane; pg < it.page_end; pg += 32) {
-            const int page = __ldg(bt + pg);
+            const int page = pg < p.max_pages ? __ldg(bt + pg) : -1;
             if (page < 0 || page >= p.num_pool_pages) continue;  // reported by the producers
             const int valid = min(64, it.seq_len - 64 * pg);
             const float4* sc = reinterpret_cast<const float4*>(p.kv_scale + (int64_t)page * 64);
@@ -396,7 +396,7 @@ __device__ __forceinline__ void kr_convert(const CUtensorMap* tm_kr, const Param
             // is used, so the group costs two memory round trips.
             int page_mine = 0;
             if (lane < npg) {
-                page_mine = __ldg(bt + pg + lane);
+                page_mine = pg + lane < p.max_pages ? __ldg(bt + pg + lane) : -1;
                 if (page_mine < 0 || page_mine >= p.num_pool_pages) page_mine = -1;  // reported by the producers
             }
             int pages[kGroupPages];

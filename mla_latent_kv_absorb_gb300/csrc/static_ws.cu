@@ -8,8 +8,10 @@
 // regular entry points take the workspace from the caller; this one takes it from the array below.
 //
 // The array lives in its own translation unit, hence in its own module: its storage is reserved
-// when that module is loaded (on the first call on each device), and code that never calls this
-// entry point never pays for it.
+// when that module is loaded.  Under the CUDA runtime's default lazy module loading that is the
+// first call on each device, and code that never calls this entry point never pays for it; with
+// CUDA_MODULE_LOADING=EAGER every device that creates a context loads the module, and holds the
+// array, from the start.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -37,7 +39,10 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
 void* g_ws_ptr[kMaxDevices] = {};
 
-// Address of g_static_ws on the current device, looked up once per device.
+// Address of g_static_ws on the current device, looked up once per device and kept for the life
+// of the process: valid only while the device's primary context lives (a cudaDeviceReset would
+// reload the module, perhaps elsewhere; the header tells callers not to use this entry point
+// after one).
 mla_status static_ws_ptr(void** out)
 {
     int dev = -1;

@@ -166,6 +166,19 @@ def test_step_host_rejects_bad_args(L):
                                     0x17000, 0x18000, 0x19000, plan_host.ctypes.data, 16)
     st, _ = _step_host(L, small_cap)
     assert st != binding.MLA_OK  # the plan does not fit its staging buffer
+    st, _ = _step_host(L, bufs, lens=(100, 64 * 80 + 1))  # 81 pages, rows of 80 entries
+    assert st == binding.MLA_ERR_INVALID_ARG
+
+
+def test_decode_step_rejects_short_table_rows():
+    """The binding checks that each sequence's pages fit its block-table row (no GPU needed:
+    the check runs before anything is allocated on the device)."""
+    import torch
+
+    bt = torch.zeros(2, 4, dtype=torch.int32)
+    with pytest.raises(ValueError, match="block_table rows"):
+        binding._check_table_rows(np.array([200, 300], dtype=np.int32), bt)
+    binding._check_table_rows(np.array([200, 256], dtype=np.int32), bt)
 
 
 def test_append_rejects_bad_args(L):

@@ -36,8 +36,8 @@ def test_static_ws_rejects_oversized_plan():
     assert "static workspace holds at most 128" in L.mla_last_error_string().decode()
 
 
-def _case(lens, seed, min_pages):
-    inp = synth.make_inputs(lens, seed=seed, poison_tail=True)
+def _case(lens, seed, min_pages, kv_dtype="bf16"):
+    inp = synth.make_inputs(lens, seed=seed, poison_tail=True, kv_dtype=kv_dtype)
     q_abs = bf16_round(oracle.absorb_q(inp.q_c, inp.w_uk)).to(DEV)
     _, q_r, _, _, kv, bt = binding.inputs_to_device(inp, DEV)
     plan, info = binding.mla_plan_splits(inp.seq_lens, binding.num_sms(), min_pages_per_split=min_pages)
@@ -113,3 +113,20 @@ def test_static_ws_single_item_plan():
     torch.cuda.synchronize()
     assert binding.mla_read_device_error(err) == 0
     assert torch.equal(o, ref[0]) and torch.equal(l, ref[1])
+
+
+@pytest.mark.gpu
+def test_static_ws_matches_workspace_entry_point_fp8():
+    """The e4m3 cache through the fixed array: split partials, two calls in a row."""
+    Ba, a = _case([2000, 64 * 30 + 17, 300], seed=904, min_pages=2, kv_dtype="fp8_e4m3")
+    Bb, b = _case([5000, 64], seed=905, min_pages=1, kv_dtype="fp8_e4m3")
+    assert a["info"].num_combine > 0 and b["info"].num_combine > 0
+    ref_a, ref_b = _reference(Ba, a), _reference(Bb, b)
+    oa, la, ea = _outputs(Ba)
+    ob, lb, eb = _outputs(Bb)
+    _static(a, oa, la, ea)
+    _static(b, ob, lb, eb)
+    torch.cuda.synchronize()
+    assert binding.mla_read_device_error(ea) == 0 and binding.mla_read_device_error(eb) == 0
+    assert torch.equal(oa, ref_a[0]) and torch.equal(la, ref_a[1])
+    assert torch.equal(ob, ref_b[0]) and torch.equal(lb, ref_b[1])
