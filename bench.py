@@ -231,10 +231,9 @@ def run_ours(args, rank, world, local):
                                  dev_error=step.dev_error, workspace=step.workspace, kv_scale=step.kv_scale,
                                  kr_pool=step.kr_pool, softmax_scale=step.softmax_scale, stream=stream)
         evs[2].record(stream)
-        binding.mla_combine_splits(step.info, step.plan_dev, step.workspace, step.o_lat, step.lse, stream)
+        binding.mla_merge_out_proj(step.info, step.plan_dev, step.workspace, step.o_lat, step.lse, step.w_uv,
+                                   step.out, step.dev_error, stream)
         evs[3].record(stream)
-        binding.mla_out_proj(step.o_lat, step.w_uv, step.out, stream)
-        evs[4].record(stream)
 
     # the step as one CUDA graph (its kernels keep their programmatic dependencies)
     graph, graph_note = None, "not used (--no-graph)"
@@ -267,7 +266,7 @@ def run_ours(args, rank, world, local):
     K = args.steps
     step_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     eager_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     dist_barrier(world)
     torch.cuda.synchronize(device)
     with ClockSampler(local) as clocks:
@@ -304,7 +303,7 @@ def run_ours(args, rank, world, local):
     step_ms = [e[0].elapsed_time(e[1]) for e in step_ev]
     eager_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in eager_ev)
     k_ms = {name: [e[i].elapsed_time(e[i + 1]) for e in evs]
-            for i, name in enumerate(["absorb", "decode", "combine", "out_proj"])}
+            for i, name in enumerate(["absorb", "decode", "merge_out_proj"])}
     ms = statistics.mean(step_ms)
     ms_max = dist_max(ms, world, device)
     decode_ms = statistics.mean(k_ms["decode"])

@@ -184,6 +184,25 @@ MLA_API mla_status mla_combine_splits(const mla_plan_info* info, const void* pla
  *   out   device bf16 [batch][128][128].  Tensor cores (tcgen05), fp32 accumulation. */
 MLA_API mla_status mla_out_proj(const void* o_lat, const void* w_uv, void* out, int32_t batch, void* stream);
 
+/* ---------------------------------------------------------------- a9 + a10 in one kernel
+ *
+ * The step's tail fused (P3 "Inside the blocks": the KV-split reduction; P1 section 1: W_UV
+ * applied after the attention): for every sequence, the log-sum-exp merge of its split partials
+ * (as mla_combine_splits) and out = W_UV o_lat (as mla_out_proj), in one launch.  Per head, the
+ * merged rows go straight into the projection's operand in shared memory; W_UV streams in while
+ * the decode kernel before it finishes (programmatic dependent launch).
+ *   info, plan_dev, workspace   the plan and the split partials mla_decode_paged wrote
+ *                               (workspace may be NULL when info->num_combine == 0)
+ *   o_lat, lse                  read for single-item sequences; for split sequences the merged
+ *                               o_lat (bf16) and lse (fp32) are written, as mla_combine_splits does
+ *   w_uv, out                   as mla_out_proj, with batch = info->batch
+ *   dev_error                   device uint32 word for MLA_DEVERR_* bits (a bounded wait that ran
+ *                               out), 4-byte aligned, or NULL
+ * The merged rows, and so `out`, are bit-identical to mla_combine_splits + mla_out_proj. */
+MLA_API mla_status mla_merge_out_proj(const mla_plan_info* info, const void* plan_dev, const void* workspace,
+                                      size_t workspace_bytes, void* o_lat, float* lse, const void* w_uv, void* out,
+                                      uint32_t* dev_error, void* stream);
+
 /* ---------------------------------------------------------------- cache append (the write side)
  *
  * P1 section 1: each token stores, once, its 512-d latent c_KV and its 64-d RoPE key k_R (576
@@ -251,7 +270,8 @@ MLA_API mla_status mla_decode_paged_static_ws(const mla_plan_info* info, const v
  * For callers whose queries, block table and lengths live in host memory: plans the step for
  * `seq_lens` on the host (as mla_plan_splits), copies the plan, the block table (when
  * block_table_host is not NULL) and the queries to the device (one cudaMemcpyAsync each, from
- * pinned memory for asynchronous DMA), runs absorb, decode, merge and out-proj on `stream`,
+ * pinned memory for asynchronous DMA), runs absorb, decode and the fused merge + out-proj
+ * (mla_merge_out_proj) on `stream`,
  * copies `out` back to out_host and waits for the stream.  One library call instead of a dozen
  * binding-level operations; it computes exactly what the four calls above compute.
  *   bufs              the device buffers, owned by the caller and sized for `batch`:

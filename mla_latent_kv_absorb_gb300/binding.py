@@ -50,7 +50,7 @@ class PlanInfo(ctypes.Structure):
 
 EXPORTS = ("mla_status_string", "mla_last_error_string", "mla_plan_bytes_max", "mla_plan_splits", "mla_absorb_q", "mla_decode_paged",
            "mla_combine_splits", "mla_out_proj", "mla_read_device_error", "mla_debug_wait_timeout",
-           "mla_decode_paged_static_ws", "mla_decode_step_host", "mla_append_kv")
+           "mla_decode_paged_static_ws", "mla_decode_step_host", "mla_append_kv", "mla_merge_out_proj")
 
 # capacity of the library's fixed split-partial array (mla_decode_paged_static_ws)
 MLA_STATIC_WS_MAX_PARTIALS = 128
@@ -97,6 +97,8 @@ def lib() -> ctypes.CDLL:
     L.mla_combine_splits.argtypes = [ctypes.POINTER(PlanInfo), P, P, sz, P, P, P]
     L.mla_out_proj.restype = ctypes.c_int
     L.mla_out_proj.argtypes = [P, P, P, i32, P]
+    L.mla_merge_out_proj.restype = ctypes.c_int
+    L.mla_merge_out_proj.argtypes = [ctypes.POINTER(PlanInfo), P, P, sz, P, P, P, P, P, P]
     L.mla_decode_step_host.restype = ctypes.c_int
     L.mla_decode_step_host.argtypes = [P, i32, i32, ctypes.POINTER(PlanOptions), P, P, P, i32, P, P, ctypes.c_int, P,
                                        P, P, i32, ctypes.c_float, ctypes.POINTER(StepBuffers), P,
@@ -267,6 +269,24 @@ def mla_combine_splits(info: PlanInfo, plan_dev: torch.Tensor, workspace: Option
     _check("mla_combine_splits", st)
 
 
+def mla_merge_out_proj(info: PlanInfo, plan_dev: torch.Tensor, workspace: Optional[torch.Tensor],
+                       o_lat: torch.Tensor, lse: torch.Tensor, w_uv: torch.Tensor, out: torch.Tensor,
+                       dev_error: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Split merge and W_UV projection in one launch (merged rows as mla_combine_splits writes
+    them, out as mla_out_proj computes it)."""
+    B = int(info.batch)
+    _need(o_lat, "o_lat", torch.bfloat16, (B, NUM_HEADS, D_C))
+    _need(lse, "lse", torch.float32, (B, NUM_HEADS))
+    _need(w_uv, "w_uv", torch.bfloat16, (NUM_HEADS, D_HC, D_C))
+    _need(out, "out", torch.bfloat16, (B, NUM_HEADS, D_HC))
+    if dev_error is not None:
+        _need(dev_error, "dev_error", torch.int32, (1,))
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().mla_merge_out_proj(ctypes.byref(info), _ptr(plan_dev), _ptr(workspace), ws_bytes, _ptr(o_lat),
+                                  _ptr(lse), _ptr(w_uv), _ptr(out), _ptr(dev_error), _stream(stream))
+    _check("mla_merge_out_proj", st)
+
+
 def mla_append_kv(c_kv: torch.Tensor, k_r: torch.Tensor, slots: torch.Tensor, *, kv_pool: torch.Tensor,
                   dev_error: torch.Tensor, kv_scale: Optional[torch.Tensor] = None,
                   kr_pool: Optional[torch.Tensor] = None, stream=None) -> None:
@@ -317,10 +337,10 @@ def num_sms(device=None) -> int:
 
 
 class DecodeStep:
-    """Device buffers and plan for one batch shape; ``run`` enqueues the four kernels.
+    """Device buffers and plan for one batch shape; ``run`` enqueues the step's three kernels.
 
-    absorb (q_c -> q_abs) -> paged decode (-> o_lat, lse, split partials) -> split merge ->
-    W_UV projection (-> out).  All buffers are allocated here, by torch, once.
+    absorb (q_c -> q_abs) -> paged decode (-> o_lat, lse, split partials) -> split merge and
+    W_UV projection in one kernel (-> out).  All buffers are allocated here, by torch, once.
     """
 
     def __init__(self, seq_lens, *, w_uk: torch.Tensor, w_uv: torch.Tensor, kv_pool: torch.Tensor,
@@ -357,8 +377,8 @@ class DecodeStep:
                          block_table=self.block_table, o_lat=self.o_lat, lse=self.lse, dev_error=self.dev_error,
                          workspace=self.workspace, kv_scale=self.kv_scale, kr_pool=self.kr_pool,
                          softmax_scale=self.softmax_scale, stream=stream)
-        mla_combine_splits(self.info, self.plan_dev, self.workspace, self.o_lat, self.lse, stream)
-        mla_out_proj(self.o_lat, self.w_uv, self.out, stream)
+        mla_merge_out_proj(self.info, self.plan_dev, self.workspace, self.o_lat, self.lse, self.w_uv, self.out,
+                           self.dev_error, stream)
         return self.out
 
     def run_host(self, q_c: torch.Tensor, q_r: torch.Tensor, *, block_table: Optional[torch.Tensor] = None,
@@ -441,7 +461,7 @@ class DecodeStep:
 
     @property
     def launches_per_step(self) -> int:
-        return 3 + (1 if self.info.num_combine > 0 else 0)
+        return 3  # absorb, decode, merge + projection
 
 
 def inputs_to_device(inp, device="cuda"):

@@ -15,6 +15,7 @@
 #include "decode_fp8.cuh"
 #include "head_gemm.cuh"
 #include "plan.h"
+#include "tail.cuh"
 
 namespace {
 
@@ -280,11 +281,16 @@ extern "C" mla_status mla_decode_paged(const mla_plan_info* info, const void* pl
         return launch_decode_fp8(info, plan_dev, q_abs, q_r, kv_pool, kv_scale, kr_pool, num_pool_pages, block_table,
                                  max_pages_per_seq, softmax_scale, workspace, o_lat, lse, dev_error, stream);
 
-    CUtensorMap tm_pool;
+    CUtensorMap tm_pool, tm_q;
     const cuuint64_t dims[3] = {576, 64, (cuuint64_t)num_pool_pages};
     const cuuint64_t strides[2] = {576 * 2, 64 * 576 * 2};
     const cuuint32_t box[3] = {64, 64, 1};
-    if (!make_map_bf16(&tm_pool, kv_pool, 3, dims, strides, box)) return MLA_ERR_CUDA;
+    // q_abs as [batch * 128 rows][512], boxes of 128 rows (one sequence's heads) x 64 dims
+    const cuuint64_t q_dims[2] = {512, (cuuint64_t)info->batch * 128};
+    const cuuint64_t q_str[1] = {512 * 2};
+    const cuuint32_t q_box[2] = {64, 128};
+    if (!make_map_bf16(&tm_pool, kv_pool, 3, dims, strides, box) || !make_map_bf16(&tm_q, q_abs, 2, q_dims, q_str, q_box))
+        return MLA_ERR_CUDA;
 
     mla::decode::Params p;
     p.plan = static_cast<const int32_t*>(plan_dev);
@@ -310,7 +316,7 @@ extern "C" mla_status mla_decode_paged(const mla_plan_info* info, const void* pl
 
     if (!set_smem(mla::decode::decode_bf16_kernel, mla::decode::kSmemBytes)) return MLA_ERR_CUDA;
     return launch_pdl(mla::decode::decode_bf16_kernel, dim3(2 * info->num_clusters), dim3(mla::decode::kThreads),
-                      mla::decode::kSmemBytes, static_cast<cudaStream_t>(stream), tm_pool, p);
+                      mla::decode::kSmemBytes, static_cast<cudaStream_t>(stream), tm_pool, tm_q, p);
 }
 
 extern "C" mla_status mla_combine_splits(const mla_plan_info* info, const void* plan_dev, const void* workspace,
@@ -328,6 +334,39 @@ extern "C" mla_status mla_combine_splits(const mla_plan_info* info, const void* 
     return launch_pdl(mla::combine::combine_kernel, grid, dim3(32 * mla::combine::kHeadsPerCta), 0,
                       static_cast<cudaStream_t>(stream), static_cast<const int32_t*>(plan_dev), ws_o, ws_lse,
                       static_cast<__nv_bfloat16*>(o_lat), lse);
+}
+
+extern "C" mla_status mla_merge_out_proj(const mla_plan_info* info, const void* plan_dev, const void* workspace,
+                                         size_t workspace_bytes, void* o_lat, float* lse, const void* w_uv, void* out,
+                                         uint32_t* dev_error, void* stream)
+{
+    if (!plan_header_ok(info) || !plan_dev || !o_lat || !lse || !w_uv || !out) return MLA_ERR_INVALID_ARG;
+    if (info->num_combine > 0 && (!workspace || workspace_bytes < (size_t)info->workspace_bytes))
+        return MLA_ERR_WORKSPACE;
+    if (!aligned16(plan_dev) || !aligned16(o_lat) || !aligned16(w_uv) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u) || (workspace && !aligned16(workspace)) ||
+        (reinterpret_cast<uintptr_t>(dev_error) & 3u))
+        return MLA_ERR_ALIGNMENT;
+    CUtensorMap tm_w;
+    const cuuint64_t w_dims[2] = {512, 128 * 128};
+    const cuuint64_t w_str[1] = {512 * 2};
+    const cuuint32_t w_box[2] = {mla::tail::kKC, 128};
+    if (!make_map_bf16(&tm_w, w_uv, 2, w_dims, w_str, w_box)) return MLA_ERR_CUDA;
+    mla::tail::Args a;
+    a.plan = static_cast<const int32_t*>(plan_dev);
+    a.ws_o = static_cast<const float*>(workspace);
+    a.ws_lse = workspace ? reinterpret_cast<const float*>(static_cast<const char*>(workspace) +
+                                                          (size_t)info->num_partials * mla::kPartialOBytes)
+                         : nullptr;
+    a.o_lat = static_cast<__nv_bfloat16*>(o_lat);
+    a.lse = lse;
+    a.out = static_cast<__nv_bfloat16*>(out);
+    a.batch = info->batch;
+    a.dev_error = dev_error;
+    a.timeout_ns = (uint64_t)info->wait_timeout_ns;
+    if (!set_smem(mla::tail::merge_out_proj_kernel, mla::tail::kSmemBytes)) return MLA_ERR_CUDA;
+    return launch_pdl(mla::tail::merge_out_proj_kernel, dim3(128, (info->batch + 127) / 128), dim3(mla::tail::kThreads),
+                      mla::tail::kSmemBytes, static_cast<cudaStream_t>(stream), tm_w, a);
 }
 
 extern "C" const char* mla_last_error_string(void) { return t_last_error; }
@@ -356,8 +395,8 @@ extern "C" mla_status mla_debug_wait_timeout(uint32_t* dev_error, int64_t timeou
     return launch_status();
 }
 
-// The whole step from host memory: plan on the host, one asynchronous copy per input, the four
-// kernels, the output copy back, one stream synchronisation.
+// The whole step from host memory: plan on the host, one asynchronous copy per input, the three
+// kernels (absorb, decode, merge + projection), the output copy back, one stream synchronisation.
 extern "C" mla_status mla_decode_step_host(const int32_t* seq_lens, int32_t batch, int32_t num_sms,
                                            const mla_plan_options* opts, const void* q_c_host, const void* q_r_host,
                                            const int32_t* block_table_host, int32_t max_pages_per_seq,
@@ -398,10 +437,9 @@ extern "C" mla_status mla_decode_step_host(const int32_t* seq_lens, int32_t batc
                                num_pool_pages, bufs->block_table, max_pages_per_seq, softmax_scale, bufs->workspace,
                                bufs->workspace_bytes, bufs->o_lat, bufs->lse, bufs->dev_error, stream)) != MLA_OK)
         return st;
-    if ((st = mla_combine_splits(&info, bufs->plan, bufs->workspace, bufs->workspace_bytes, bufs->o_lat, bufs->lse,
-                                 stream)) != MLA_OK)
+    if ((st = mla_merge_out_proj(&info, bufs->plan, bufs->workspace, bufs->workspace_bytes, bufs->o_lat, bufs->lse,
+                                 w_uv, bufs->out, bufs->dev_error, stream)) != MLA_OK)
         return st;
-    if ((st = mla_out_proj(bufs->o_lat, w_uv, bufs->out, batch, stream)) != MLA_OK) return st;
     const size_t out_bytes = (size_t)batch * 128 * 128 * 2;
     if (record_cuda(cudaMemcpyAsync(out_host, bufs->out, out_bytes, cudaMemcpyDeviceToHost, s),
                     "cudaMemcpyAsync(out)") != MLA_OK ||

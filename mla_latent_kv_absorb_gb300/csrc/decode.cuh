@@ -10,8 +10,10 @@
 // Why two CTAs.  The fp32 accumulator O[128 x 512] takes all 512 columns of one SM's tensor
 // memory, and the scores need 64 more; the bf16 query [128 x 576] is 144 KB.  So a cluster of
 // two CTAs on two SMs splits the work by role instead of recomputing anything:
-//   rank 0, the score CTA: q_abs lives in TMEM (256 columns, the A operand of "TS" MMAs) and
-//     q_R in shared memory (16 KB); the scores of four pages at a time go to the other 256
+//   rank 0, the score CTA: q_abs lives in TMEM (256 columns, the A operand of "TS" MMAs; each
+//     item's rows arrive through the TMA ring as four entries ahead of its pages and the MMA
+//     thread copies them in with tcgen05.cp) and q_R in shared memory (16 KB); the scores of
+//     four pages at a time go to the other 256
 //     TMEM columns, one N=256 MMA per K step.  At N=256 each MMA carries 128 cycles of tensor
 //     work, which hides the issuing thread's own overhead (its warp shares an SM sub-partition
 //     with softmax warps); at N=64 the single issuing thread, not the tensor pipe, was the limit.
@@ -35,7 +37,7 @@
 //   kv_full/kv_empty[S]   TMA rings: 4 K-chunk stages in the score CTA, 2 page stages in the
 //                         value CTA
 //   s_full/s_free         the four-page score buffer (score CTA)
-//   q_ready               query loaded into TMEM for an item (score CTA)
+//   q_ready               q_R of an item written to shared memory (score CTA softmax warps)
 //   stg_ready[4]          a staged P message is complete (four softmax warps of one set)
 //   stg_freed             counter, not a barrier: messages whose staging slot may be reused
 //                         (published by the tracker thread, which alone waits on copied)
@@ -73,6 +75,7 @@ constexpr int kBoxBytes = 64 * 128;               // 64 tokens x 64 bf16 columns
 constexpr int kBoxesPerRow = 9;                   // c_KV: 8 boxes, k_R: 1 box
 constexpr int kGroupPages = 4;                    // pages per score MMA (N = 256)
 constexpr int kChunkBytes = kGroupPages * kBoxBytes;  // one box column of a four-page group
+constexpr int kQueryEntries = 4;                  // ring entries carrying an item's q_abs (two 16 KB boxes each)
 constexpr int kValueStageBytes = 8 * kBoxBytes;   // 65,536: c_KV only
 constexpr int kPBytes = 128 * 128;                // P: 128 heads x 64 tokens bf16
 // Per message statistics, one 272-byte block per softmax warp (32 heads): factor[32] (rescale
@@ -259,19 +262,41 @@ __device__ __forceinline__ void run_producer(const CUtensorMap* tm, const Params
 
 // Streams this cluster's pages as K-chunks: chunk j of a four-page group holds 64-column box j
 // (boxes 0-7: c_KV, box 8: k_R) of the group's pages in rows 0-63, 64-127, 128-191, 192-255.
-__device__ __forceinline__ void score_producer(const CUtensorMap* tm, const Params& p, int item_begin, int item_end,
-                                               int items_off, uint32_t sbase, uint32_t bars, const dev::WaitCtx& w,
-                                               int lane)
+__device__ __forceinline__ void score_producer(const CUtensorMap* tm, const CUtensorMap* tm_q, const Params& p,
+                                               int item_begin, int item_end, int items_off, uint32_t sbase,
+                                               uint32_t bars, const dev::WaitCtx& w, int lane)
 {
     using namespace dev;
     MLA_TRACE_DECL;
     const uint64_t policy = l2_policy_evict_last();  // the value CTA reads these pages next
-    if (lane == 0) tma_prefetch_desc(tm);
+    if (lane == 0) {
+        tma_prefetch_desc(tm);
+        tma_prefetch_desc(tm_q);
+    }
     int s = 0, phase = 0, c = 0;
     bool ok = true;
     for (int i = item_begin; i < item_end && ok; ++i) {
         const Item it = load_item(p.plan, items_off, i);
         const int32_t* bt = p.block_table + (int64_t)it.seq * p.max_pages;
+        if (lane == 0) {
+            // the item's q_abs rows (128 heads x 512 dims) as four ring entries of two 64-dim
+            // boxes each, ahead of its pages
+            if (i == item_begin) griddep_wait();  // q_abs comes from the kernel launched before this one
+            for (int j = 0; j < kQueryEntries && ok; ++j, ++c) {
+                if (c >= kChunkStages) ok = MLA_TIMED(1, wait_phase(bars + 8 * (kEmpty0 + s), phase - 1, w));
+                if (!ok) break;
+                const uint32_t full = bars + 8 * (kFull0 + s);
+                const uint32_t dst = sbase + kOffChunks + s * kChunkBytes;
+                mbar_arrive_expect_tx(full, kChunkBytes);
+                tma_load_2d(dst, tm_q, full, 128 * j, 128 * it.seq, policy);
+                tma_load_2d(dst + kChunkBytes / 2, tm_q, full, 128 * j + 64, 128 * it.seq, policy);
+                if (++s == kChunkStages) {
+                    s = 0;
+                    ++phase;
+                }
+            }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
         for (int pg0 = it.page_begin; pg0 < it.page_end && ok; pg0 += 32) {
             const int n = min(32, it.page_end - pg0);  // a multiple of 4 unless it ends the item
             int page = 0;
@@ -330,8 +355,27 @@ __device__ __forceinline__ void score_mma(const Params& p, int item_begin, int i
     int s = 0, phase = 0, G = 0, n_item = 0;
     for (int i = item_begin; i < item_end; ++i, ++n_item) {
         const Item it = load_item(p.plan, items_off, i);
-        if (!MLA_TIMED(5, wait_phase(bars + 8 * kQReady, n_item, w))) goto out;
-        tc_fence_after();
+        // q_abs into TMEM columns 0-255 (dims 64 k .. 64 k + 63 -> columns 32 k .. 32 k + 31), once
+        // the previous item's QK, which reads those columns, has finished
+        if (n_item > 0 && !MLA_TIMED(5, wait_phase(bars + 8 * kSFull0, G - 1, w))) goto out;
+#pragma unroll 1
+        for (int j = 0; j < kQueryEntries; ++j) {
+            if (!MLA_TIMED(3, wait_phase(full0 + 8 * s, phase, w))) goto out;
+            tc_fence_after();
+            const uint64_t src = smem_desc(sbase + kOffChunks + s * kChunkBytes, 16, 1024);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4)
+                    tmem_cp_128x256b(tmem + kQCol + 64 * j + 32 * h + 8 * k4,
+                                     src + (uint64_t)(h * ((kChunkBytes / 2) >> 4) + 2 * k4));
+            mma_commit(empty0 + 8 * s);
+            if (++s == kChunkStages) {
+                s = 0;
+                ++phase;
+            }
+        }
+        bool qr_ready = false;
         for (int pg = it.page_begin; pg < it.page_end; pg += kGroupPages, ++G) {
             const int npg = min(kGroupPages, it.page_end - pg);
             const uint32_t idesc = idesc_bf16(128, 64 * npg, false, false);
@@ -350,6 +394,11 @@ __device__ __forceinline__ void score_mma(const Params& p, int item_begin, int i
                     mma_ts(d, a0 + 16, b0 + 4, idesc, 1u);
                     mma_ts(d, a0 + 24, b0 + 6, idesc, 1u);
                 } else {
+                    if (!qr_ready) {  // q_R of this item is in shared memory
+                        if (!MLA_TIMED(5, wait_phase(bars + 8 * kQReady, n_item, w))) goto out;
+                        tc_fence_after();
+                        qr_ready = true;
+                    }
                     mma_ss(d, qr_desc, b0, idesc, 1u);
                     mma_ss(d, qr_desc + 2, b0 + 2, idesc, 1u);
                     mma_ss(d, qr_desc + 4, b0 + 4, idesc, 1u);
@@ -373,35 +422,19 @@ out:
     MLA_TRACE_FLUSH(12, 12, 2);
 }
 
-// The query of row `row`: softmax set 0 writes q_abs dims 0..255 to TMEM columns 0..127 of lane
-// `row` and q_R to row `row` of the K-major, 128-byte-swizzled q_R tile in shared memory; set 1
-// writes q_abs dims 256..511 to columns 128..255.
-__device__ __forceinline__ void load_query(const Params& p, int seq, int row, int set, uint32_t taddr,
-                                           uint8_t* qr_smem)
+// q_R of row `row` into row `row` of the K-major, 128-byte-swizzled q_R tile in shared memory
+// (softmax set 0; q_abs reaches TMEM through the TMA ring and tcgen05.cp).
+__device__ __forceinline__ void load_query_rope(const Params& p, int seq, int row, uint8_t* qr_smem)
 {
     using namespace dev;
-    const uint4* qa = reinterpret_cast<const uint4*>(p.q_abs + ((int64_t)seq * 128 + row) * 512) + 32 * set;
-#pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
+    const uint4* qr = reinterpret_cast<const uint4*>(p.q_r + ((int64_t)seq * 128 + row) * 64);
+    uint8_t* dst = qr_smem + (row >> 3) * 1024 + (row & 7) * 128;
+    uint4 v[8];
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
-            const uint4 x = __ldg(qa + 8 * c + v);
-            r[4 * v + 0] = x.x;
-            r[4 * v + 1] = x.y;
-            r[4 * v + 2] = x.z;
-            r[4 * v + 3] = x.w;
-        }
-        tmem_st32(taddr + kQCol + 128 * set + 32 * c, r);
-    }
-    if (set == 0) {
-        const uint4* qr = reinterpret_cast<const uint4*>(p.q_r + ((int64_t)seq * 128 + row) * 64);
-        uint8_t* dst = qr_smem + (row >> 3) * 1024 + (row & 7) * 128;
+    for (int k = 0; k < 8; ++k) v[k] = __ldg(qr + k);
 #pragma unroll
-        for (int v = 0; v < 8; ++v) *reinterpret_cast<uint4*>(dst + ((v ^ (row & 7)) << 4)) = __ldg(qr + v);
-        fence_proxy_async_cta();  // read by the MMA (async proxy)
-    }
-    tmem_wait_st();
+    for (int k = 0; k < 8; ++k) *reinterpret_cast<uint4*>(dst + ((k ^ (row & 7)) << 4)) = v[k];
+    fence_proxy_async_cta();  // read by the MMA (async proxy)
 }
 
 // Softmax of one page held in registers: masks slots past the sequence end, p = 2^(s * scale *
@@ -556,13 +589,11 @@ __device__ __forceinline__ void score_softmax(const Params& p, int item_begin, i
     const uint32_t* freed = reinterpret_cast<const uint32_t*>(smem + kOffStgFreed);
     float* xchg = reinterpret_cast<float*>(smem + kOffXchg);  // [slot 2][kind 2: max, l][set 2][128]
     MLA_TRACE_DECL;
-    griddep_wait();  // q_abs comes from the kernel launched before this one
     int g = 0, G = 0;  // pages (messages) and four-page groups
     for (int i = item_begin; i < item_end; ++i) {
         const Item it = load_item(p.plan, items_off, i);
         [[maybe_unused]] const long long tq0 = MLA_TRACE_NOW();
-        load_query(p, it.seq, row, set, tmem + lane_off, smem + kOffQR);
-        tc_fence_before();
+        if (set == 0) load_query_rope(p, it.seq, row, smem + kOffQR);
         __syncwarp();
         if (lane == 0) mbar_arrive(bars + 8 * kQReady);
         MLA_TRACE_ADD(9, MLA_TRACE_NOW() - tq0);
@@ -896,7 +927,7 @@ done:
 // 11 warps: three SM sub-partitions hold three of them, and a sub-partition's 16K registers then
 // allow at most 3 x 32 x 168.
 __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
-decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_pool, const Params p)
+decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_pool, const __grid_constant__ CUtensorMap tm_q, const Params p)
 {
     using namespace dev;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -956,7 +987,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_pool, const Params p)
         const int item_end = cluster < n_clusters ? p.plan[cl_off + cluster + 1] : 0;
         if (rank == 0) {
             if (warp == 0)
-                score_producer(&tm_pool, p, item_begin, item_end, items_off, sbase, bars, w, lane);
+                score_producer(&tm_pool, &tm_q, p, item_begin, item_end, items_off, sbase, bars, w, lane);
             else if (warp == 1) {
                 if (lane == 0) score_mma(p, item_begin, item_end, items_off, sbase, bars, tmem, w);
             } else if (warp == kShipperWarp) {

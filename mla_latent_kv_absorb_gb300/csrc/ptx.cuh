@@ -326,6 +326,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
           "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]));
 }
 
+// Copy a 128-row x 32-byte slice of a shared-memory matrix (descriptor `src`, the layouts of MMA
+// operands) into TMEM: row i to lane i, eight consecutive 32-bit columns from `taddr`.  Issued
+// by one thread; it runs in order before that thread's later MMAs, and a later commit covers it.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t src)
+{
+    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(src) : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 

@@ -111,6 +111,24 @@ def test_combine_rejects_bad_args(L):
                                 _p(0x80000), None) == binding.MLA_ERR_ALIGNMENT
 
 
+def test_merge_out_proj_rejects_bad_args(L):
+    """The fused merge + projection checks its plan, buffers, workspace and alignment on the host."""
+    plan, info = _info()
+    assert info.num_combine > 0
+    def call(plan_p=0x20000, ws=0x90000, ws_bytes=None, o=0x70000, l=0x80000, w=0xA0000, out=0xB0000, err=None):
+        wb = info.workspace_bytes if ws_bytes is None else ws_bytes
+        return L.mla_merge_out_proj(ctypes.byref(info), _p(plan_p), _p(ws), wb, _p(o), _p(l), _p(w), _p(out),
+                                    _p(err), None)
+    assert call(plan_p=0) == binding.MLA_ERR_INVALID_ARG
+    assert call(w=0) == binding.MLA_ERR_INVALID_ARG
+    assert call(out=0) == binding.MLA_ERR_INVALID_ARG
+    assert call(ws=0, ws_bytes=0) == binding.MLA_ERR_WORKSPACE
+    assert call(ws_bytes=info.workspace_bytes - 1) == binding.MLA_ERR_WORKSPACE
+    assert call(w=0xA0008) == binding.MLA_ERR_ALIGNMENT
+    assert call(l=0x80002) == binding.MLA_ERR_ALIGNMENT
+    assert call(err=0x50002) == binding.MLA_ERR_ALIGNMENT
+
+
 def test_debug_and_error_reader_reject_bad_args(L):
     assert L.mla_debug_wait_timeout(None, 10 ** 8, None) == binding.MLA_ERR_INVALID_ARG
     assert L.mla_debug_wait_timeout(_p(0x50000), 10, None) == binding.MLA_ERR_INVALID_ARG
