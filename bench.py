@@ -202,6 +202,27 @@ def recorded_traffic(kernel: str, workload: str, tokens: int):
     return None
 
 
+def bench_config(args, inp, world):
+    """The workload, identical in both arms' JSON lines."""
+    return {"workload": args.workload, "desc": synth.WORKLOADS[args.workload]["desc"],
+            "global_batch": inp.batch * world, "seq_len": int(inp.seq_lens.max()),
+            "tokens_per_replica": int(inp.num_tokens), "parallelism": f"replicas x{world}"}
+
+
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            text = f.read()
+    except OSError:
+        return "unknown"
+    for key in ("model name", "Model", "Hardware"):
+        for line in text.splitlines():
+            if line.startswith(key) and ":" in line:
+                return line.split(":", 1)[1].strip()
+    parts = sorted({ln.split(":", 1)[1].strip() for ln in text.splitlines() if ln.startswith("CPU part")})
+    return f"{os.uname().machine} (CPU part {', '.join(parts)})" if parts else os.uname().machine
+
+
 # ----------------------------------------------------------------------------- the GPU arm
 
 def run_ours(args, rank, world, local):
@@ -214,26 +235,44 @@ def run_ours(args, rank, world, local):
     inp = synth.make_workload(args.workload, seed=synth.DEFAULT_SEED + rank, poison_tail=False)
     q_c, q_r, w_uk, w_uv, kv, bt = binding.inputs_to_device(inp, device)
     step = binding.DecodeStep(inp.seq_lens, w_uk=w_uk, w_uv=w_uv, block_table=bt,
-                              item_cost_pages=args.item_cost_pages, **kv)
+                              item_cost_pages=args.item_cost_pages, fused_absorb=args.absorb == "fused",
+                              fused_tail=args.tail == "fused", **kv)
     acc = workload_accounting(inp)
     peaks = load_peaks()
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
 
-    def one_step(evs=None):
-        if evs is None:
-            return step.run(q_c, q_r, stream)
-        evs[0].record(stream)
+    # the kernels of one step, one by one (with the absorb as a kernel of its own, so that the decode
+    # kernel's own duration gives the roofline)
+    def k_absorb():
         binding.mla_absorb_q(q_c, step.w_uk, step.q_abs, stream)
-        evs[1].record(stream)
+
+    def k_decode():
         binding.mla_decode_paged(step.info, step.plan_dev, step.q_abs, q_r, kv_pool=step.kv_pool,
                                  block_table=step.block_table, o_lat=step.o_lat, lse=step.lse,
                                  dev_error=step.dev_error, workspace=step.workspace, kv_scale=step.kv_scale,
                                  kr_pool=step.kr_pool, softmax_scale=step.softmax_scale, stream=stream)
-        evs[2].record(stream)
+
+    def k_merge():
+        binding.mla_combine_splits(step.info, step.plan_dev, step.workspace, step.o_lat, step.lse, stream)
+
+    def k_proj():
+        binding.mla_out_proj(step.o_lat, step.w_uv, step.out, stream)
+
+    def k_tail():
         binding.mla_merge_out_proj(step.info, step.plan_dev, step.workspace, step.o_lat, step.lse, step.w_uv,
                                    step.out, step.dev_error, stream)
-        evs[3].record(stream)
+
+    parts = [("absorb", k_absorb), ("decode", k_decode)] + (
+        [("merge_out_proj", k_tail)] if args.tail == "fused" else [("combine", k_merge), ("out_proj", k_proj)])
+
+    def one_step(evs=None):
+        if evs is None:
+            return step.run(q_c, q_r, stream)
+        for i, (_, fn) in enumerate(parts):
+            evs[i].record(stream)
+            fn()
+        evs[len(parts)].record(stream)
 
     # the step as one CUDA graph (its kernels keep their programmatic dependencies)
     graph, graph_note = None, "not used (--no-graph)"
@@ -266,7 +305,7 @@ def run_ours(args, rank, world, local):
     K = args.steps
     step_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     eager_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(parts) + 1)] for _ in range(K)]
     dist_barrier(world)
     torch.cuda.synchronize(device)
     with ClockSampler(local) as clocks:
@@ -300,10 +339,12 @@ def run_ours(args, rank, world, local):
     if err != 0:
         raise RuntimeError(f"device error bits {err:#x} in the timed region")
 
+    if graph is not None and getattr(step, "graph_kernel_nodes", None) not in (None, step.launches_per_step):
+        raise RuntimeError(f"the step graph holds {step.graph_kernel_nodes} kernels, expected {step.launches_per_step}")
     step_ms = [e[0].elapsed_time(e[1]) for e in step_ev]
     eager_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in eager_ev)
     k_ms = {name: [e[i].elapsed_time(e[i + 1]) for e in evs]
-            for i, name in enumerate(["absorb", "decode", "merge_out_proj"])}
+            for i, (name, _) in enumerate(parts)}
     ms = statistics.mean(step_ms)
     ms_max = dist_max(ms, world, device)
     decode_ms = statistics.mean(k_ms["decode"])
@@ -335,6 +376,13 @@ def run_ours(args, rank, world, local):
                     "traffic": None if traffic is None else int(traffic),
                     "algorithmic_bytes": acc["decode_bytes"], "peak_source": peaks.get("source"),
                     "tensor_frac": round(achieved_tfs / tf, 4)}
+    # the same fractions against GB300's nominal figures: HBM3e 8 TB/s, dense BF16 2.25 PFLOP/s
+    # (without 2:4 sparsity)
+    nom_bw, nom_tf = 8000.0, 2250.0
+    nominal = {"hbm_gbs": nom_bw, "bf16_tflops": nom_tf, "source": "GB300 nominal (HBM3e 8 TB/s, dense BF16)",
+               "decode_hbm_frac": round(achieved_gbs / nom_bw, 4), "decode_tensor_frac": round(achieved_tfs / nom_tf, 4),
+               "step_frac": round(max(acc["step_bytes"] / (nom_bw * 1e9), acc["step_flop"] / (nom_tf * 1e12)) * 1e6
+                                  / (ms_max * 1e3), 4)}
     step_roof_us = max(acc["step_bytes"] / (bw * 1e9), acc["step_flop"] / (tf * 1e12)) * 1e6
     decode_roof_us = max(acc["decode_bytes"] / (bw * 1e9), acc["decode_flop"] / (tf * 1e12)) * 1e6
     res = {
@@ -350,17 +398,16 @@ def run_ours(args, rank, world, local):
         "vs_baseline": None,
         "dtype": "bf16" if inp.kv_dtype == "bf16" else "fp8_e4m3+bf16",
         "data": "synthetic (seeded N(0,1) cache/queries, N(0,1/512) weights)",
-        "config": {"workload": args.workload, "desc": synth.WORKLOADS[args.workload]["desc"],
-                   "global_batch": inp.batch * world, "seq_len": int(inp.seq_lens.max()),
-                   "tokens_per_replica": acc["tokens"], "parallelism": f"replicas x{world}",
-                   "l2": "512 MB buffer rewritten before every timed step; cache (1.2 GB) > L2",
+        "config": bench_config(args, inp, world),
+        "setup": {"l2": "512 MB buffer rewritten before every timed step; cache (1.2 GB) > L2",
                    "timing": "value: K replays of the step's CUDA graph, each between two events; "
-                             "step_us_eager: K eager launches of the same step; kernels_us and roofline: a "
-                             "third pass of K steps with an event between kernels",
+                             "step_us_eager: K eager launches of the same step; kernels_us and roofline: a third "
+                             "pass of K steps with the absorb as a kernel of its own and an event between kernels",
                    "graph": graph_note,
                    "plan": {"clusters": step.info.num_clusters, "items": step.info.num_items,
                             "combine_seqs": step.info.num_combine, "max_splits": step.info.max_splits,
-                            "item_cost_pages": args.item_cost_pages}},
+                            "item_cost_pages": args.item_cost_pages},
+                   "absorb": args.absorb, "tail": args.tail},
         "step_us_eager": round(eager_ms * 1e3, 2),
         "kernels_us": {k: round(statistics.mean(v) * 1e3, 2) for k, v in k_ms.items()},
         "kv_tbps": round(acc["kv_bytes"] / (ms_max * 1e-3) / 1e12, 3),
@@ -371,12 +418,17 @@ def run_ours(args, rank, world, local):
         "decode_roofline_frac": round(decode_roof_us / (decode_ms * 1e3), 4),
         "clocks": clocks.summary(),
         "wall_s_timed": round(wall, 4),
-        "gpu_launches": K * step.launches_per_step,
+        "gpu_launches": K * (step.graph_kernel_nodes if graph is not None and
+                             getattr(step, "graph_kernel_nodes", None) else step.launches_per_step),
+        "gpu_launches_source": ("kernel nodes of the captured step graph"
+                                if graph is not None and getattr(step, "graph_kernel_nodes", None)
+                                else "launches per step as issued"),
+        "roofline_nominal": nominal,
         "e2e": e2e,
         "parity": parity,
     }
     if rank == 0 and args.cpu_baseline and world >= 1:
-        res["cpu_baseline"] = cpu_baseline(inp, samples=1)
+        res["cpu_baseline"] = cpu_baseline(inp)
     return res
 
 
@@ -421,54 +473,78 @@ def run_e2e(args, inp, step, binding, device, stream):
 
 # ----------------------------------------------------------------------------- the CPU oracle
 
-def cpu_baseline(inp, samples=1, tokens=None):
-    """Time the naive oracle on one sequence x 16 heads (every 8th) on all host cores; scale to
-    a full step (all sequences, all heads; the oracle is linear in tokens)."""
-    import oracle
-
-    cores = len(os.sched_getaffinity(0))
-    oracle.set_threads(cores)
-    heads = list(range(0, 128, 8))
+def _one_sequence(inp, tokens=None):
     sub = synth.DecodeInputs(seq_lens=inp.seq_lens[:1].copy(), block_table=inp.block_table[:1].copy(),
                              num_pool_pages=inp.num_pool_pages, q_c=inp.q_c[:1], q_r=inp.q_r[:1], w_uk=inp.w_uk,
                              w_uv=inp.w_uv, kv_dtype=inp.kv_dtype, pool=inp.pool, c8=inp.c8, kv_scale=inp.kv_scale,
                              kr=inp.kr)
     if tokens is not None:
         sub.seq_lens[0] = min(int(sub.seq_lens[0]), tokens)
+    return sub
+
+
+def cpu_baseline(inp, tokens=None):
+    """The CPU oracle on the host cores, on a bounded sample of the workload, scaled to a full
+    step (the oracle's work is linear in tokens x heads): the naive oracle (decompress k and v
+    per head) on sequence 0 x 16 heads, and the absorbed oracle on sequence 0 x all heads."""
+    import oracle
     from mla_latent_kv_absorb_gb300.binding import SOFTMAX_SCALE
 
-    dts = []
-    for _ in range(samples):
-        t0 = time.perf_counter()
-        oracle.decode_naive(sub, softmax_scale=SOFTMAX_SCALE, heads=heads)
-        dts.append(time.perf_counter() - t0)
-    dt = statistics.mean(dts)
-    scale = (inp.num_tokens * 128) / (int(sub.seq_lens[0]) * len(heads))
-    return {"value": round(dt * scale * 1e6, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"naive fp64 oracle, sequence 0 ({int(sub.seq_lens[0])} tokens) x heads 0,8,..,120; "
-                      f"{dt:.2f} s measured, scaled x{scale:.0f} to the full step"}
+    cores = len(os.sched_getaffinity(0))
+    oracle.set_threads(cores)
+    heads = list(range(0, 128, 8))
+    sub = _one_sequence(inp, tokens)
+    S0 = int(sub.seq_lens[0])
+    t0 = time.perf_counter()
+    oracle.decode_naive(sub, softmax_scale=SOFTMAX_SCALE, heads=heads)
+    dt_naive = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    q_abs = oracle.absorb_q(sub.q_c, sub.w_uk)
+    o, _ = oracle.latent_attention(sub, q_abs, softmax_scale=SOFTMAX_SCALE)
+    oracle.out_proj(o, sub.w_uv)
+    dt_abs = time.perf_counter() - t0
+    scale_naive = (inp.num_tokens * 128) / (S0 * len(heads))
+    scale_abs = inp.num_tokens / S0
+    return {"value": round(dt_naive * scale_naive * 1e6, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "cpu_model": cpu_model(),
+            "sample": f"naive fp64 oracle, sequence 0 ({S0} tokens) x heads 0,8,..,120; {dt_naive:.2f} s measured, "
+                      f"scaled x{scale_naive:.0f} to the full step",
+            "absorbed": {"value": round(dt_abs * scale_abs * 1e6, 1), "unit": UNIT,
+                         "sample": f"absorbed fp64 oracle (absorb, latent attention, W_UV) on sequence 0 "
+                                   f"({S0} tokens) x all heads; {dt_abs:.2f} s measured, scaled x{scale_abs:.0f}"}}
 
 
 def run_reference(args, rank, world, local):
-    """The CPU oracle as the reference arm: rank 0 only."""
+    """The CPU oracle as the reference arm, rank 0 only.  Each step runs the naive oracle on a
+    bounded sample of the workload (sequence 0, 8,192 tokens, 16 of the 128 heads); the line's
+    value is the measured time of that step, and the full-step time it implies is given beside it."""
     if rank != 0:
         return None
+    import oracle
+    from mla_latent_kv_absorb_gb300.binding import SOFTMAX_SCALE
+
     inp = synth.make_workload(args.workload, poison_tail=False)
+    cores = len(os.sched_getaffinity(0))
+    oracle.set_threads(cores)
+    heads = list(range(0, 128, 8))
+    sub = _one_sequence(inp, 8192)
     per_step = []
-    tokens = 8192
     for i in range(args.warmup + args.steps):
-        r = cpu_baseline(inp, samples=1, tokens=tokens)
+        t0 = time.perf_counter()
+        oracle.decode_naive(sub, softmax_scale=SOFTMAX_SCALE, heads=heads)
         if i >= args.warmup:
-            per_step.append(r["value"])
-    v = statistics.mean(per_step)
-    cb = dict(r)
-    cb["value"] = round(v, 1)
+            per_step.append(time.perf_counter() - t0)
+    v = statistics.mean(per_step) * 1e6
+    scale = (inp.num_tokens * 128) / (int(sub.seq_lens[0]) * len(heads))
+    sample = (f"naive fp64 oracle per step on sequence 0 ({int(sub.seq_lens[0])} tokens) x heads 0,8,..,120 "
+              f"(1/{scale:.0f} of the workload)")
+    cb = {"value": round(v, 1), "unit": UNIT, "cores": cores, "kind": "oracle", "cpu_model": cpu_model(),
+          "sample": sample, "full_step_estimate_us": round(v * scale, 1)}
     return {"impl": "reference", "metric": METRIC, "value": round(v, 1), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(v / 1e3, 3), "higher_is_better": False,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "desc": synth.WORKLOADS[args.workload]["desc"]},
-            "cpu_baseline": cb, "e2e": {"value": round(v, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
-                                        "d2h_bytes_per_step": 0}}
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (the same seeded workload)",
+            "config": bench_config(args, inp, world), "cpu_baseline": cb,
+            "e2e": {"value": round(v, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
 def main(argv=None):
@@ -483,9 +559,13 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-parity", dest="parity", action="store_false")
-    ap.add_argument("--item-cost-pages", type=int, default=7,
-                    help="planner: balance pages plus this charge per extra item of a CTA pair (0: equal page "
-                         "runs, the library's default); 7 timed faster than 0 at B=16, S=65536")
+    ap.add_argument("--item-cost-pages", type=int, default=0,
+                    help="planner: charge in pages per extra item of a CTA pair (0: the library's default of 7; "
+                         "negative: equal page runs)")
+    ap.add_argument("--absorb", choices=["fused", "separate"], default="separate",
+                    help="absorb as the decode kernel's prologue, or as a kernel of its own before it")
+    ap.add_argument("--tail", choices=["fused", "separate"], default="separate",
+                    help="split merge and W_UV projection in one kernel, or as two kernels")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="time eager launches for the value instead of replays of the step's CUDA graph")
     args = ap.parse_args(argv)

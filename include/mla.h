@@ -86,9 +86,10 @@ typedef struct mla_plan_options {
     int32_t min_pages_per_split; /* 0 = default 8: no item boundary closer than this to a sequence edge */
     int32_t max_clusters;        /* 0 = num_sms / 2; otherwise at most this many CTA pairs */
     int64_t wait_timeout_ns;     /* 0 = default 2e9: bound on every device-side wait */
-    int32_t item_cost_pages;     /* 0 = cut into equal page runs; > 0: balance pages plus this many
-                                    pages' worth of cost for each item of a CTA pair after its
-                                    first (a second item reloads the query and writes an output) */
+    int32_t item_cost_pages;     /* balance pages plus this many pages' worth of cost for each item
+                                    of a CTA pair after its first (a second item reloads the query
+                                    and writes an output); 0 = the default charge of 7 pages,
+                                    < 0 = no charge: equal page runs */
     int32_t reserved;            /* must be 0 */
 } mla_plan_options;
 
@@ -167,6 +168,32 @@ MLA_API mla_status mla_decode_paged(const mla_plan_info* info, const void* plan_
                             const int32_t* block_table, int32_t max_pages_per_seq,
                             float softmax_scale, void* workspace, size_t workspace_bytes,
                             void* o_lat, float* lse, uint32_t* dev_error, void* stream);
+
+/* ---------------------------------------------------------------- a2 + a3-a8 in one kernel
+ *
+ * The absorb (P1 section 4, path B: q_abs = q_c W_UK per head) as the prologue of the paged
+ * decode: every CTA of the decode grid first forms q_abs for one head and one tile of 128
+ * sequences on the tensor cores (the grid gets extra CTA pairs, which do only that, when the plan
+ * has fewer pairs than 64 per 128-sequence tile), writes the rows to `q_abs` and publishes the
+ * job in absorb_sync; the score CTAs wait for all jobs before their first query.  One launch
+ * instead of two, and the absorb no longer sits in front of the decode as a kernel of its own.
+ *   q_c, w_uk     as mla_absorb_q (batch = info->batch)
+ *   q_abs         device bf16 [batch][128][512], written (the same values mla_absorb_q writes)
+ *   absorb_sync   device uint32[2], 8-byte aligned, zero before the first call; every call that
+ *                 sets no MLA_DEVERR_* bit leaves it zero again.  After a call that did set one,
+ *                 zero it before the next call.  Calls that may overlap on the GPU need one each.
+ *   the rest      as mla_decode_paged.
+ * It is an ordinary launch: it starts after the stream's previous work has finished (a
+ * programmatic early start could overlap a previous step's merge, which still reads o_lat).
+ * With the e4m3 cache (MLA_KV_FP8_E4M3) the absorb runs as its own kernel (mla_absorb_q) and the
+ * decode follows it; absorb_sync is then not touched. */
+MLA_API mla_status mla_absorb_decode_paged(const mla_plan_info* info, const void* plan_dev, const void* q_c,
+                                           const void* w_uk, void* q_abs, uint32_t* absorb_sync, const void* q_r,
+                                           mla_kv_dtype kv_dtype, const void* kv_pool, const float* kv_scale,
+                                           const void* kr_pool, int32_t num_pool_pages, const int32_t* block_table,
+                                           int32_t max_pages_per_seq, float softmax_scale, void* workspace,
+                                           size_t workspace_bytes, void* o_lat, float* lse, uint32_t* dev_error,
+                                           void* stream);
 
 /* ---------------------------------------------------------------- a9: merge split partials
  *
@@ -270,8 +297,7 @@ MLA_API mla_status mla_decode_paged_static_ws(const mla_plan_info* info, const v
  * For callers whose queries, block table and lengths live in host memory: plans the step for
  * `seq_lens` on the host (as mla_plan_splits), copies the plan, the block table (when
  * block_table_host is not NULL) and the queries to the device (one cudaMemcpyAsync each, from
- * pinned memory for asynchronous DMA), runs absorb, decode and the fused merge + out-proj
- * (mla_merge_out_proj) on `stream`,
+ * pinned memory for asynchronous DMA), runs absorb, decode, merge and out-proj on `stream`,
  * copies `out` back to out_host and waits for the stream.  One library call instead of a dozen
  * binding-level operations; it computes exactly what the four calls above compute.
  *   bufs              the device buffers, owned by the caller and sized for `batch`:

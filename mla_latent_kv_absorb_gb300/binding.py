@@ -50,7 +50,8 @@ class PlanInfo(ctypes.Structure):
 
 EXPORTS = ("mla_status_string", "mla_last_error_string", "mla_plan_bytes_max", "mla_plan_splits", "mla_absorb_q", "mla_decode_paged",
            "mla_combine_splits", "mla_out_proj", "mla_read_device_error", "mla_debug_wait_timeout",
-           "mla_decode_paged_static_ws", "mla_decode_step_host", "mla_append_kv", "mla_merge_out_proj")
+           "mla_decode_paged_static_ws", "mla_decode_step_host", "mla_append_kv", "mla_merge_out_proj",
+           "mla_absorb_decode_paged")
 
 # capacity of the library's fixed split-partial array (mla_decode_paged_static_ws)
 MLA_STATIC_WS_MAX_PARTIALS = 128
@@ -97,6 +98,9 @@ def lib() -> ctypes.CDLL:
     L.mla_combine_splits.argtypes = [ctypes.POINTER(PlanInfo), P, P, sz, P, P, P]
     L.mla_out_proj.restype = ctypes.c_int
     L.mla_out_proj.argtypes = [P, P, P, i32, P]
+    L.mla_absorb_decode_paged.restype = ctypes.c_int
+    L.mla_absorb_decode_paged.argtypes = [ctypes.POINTER(PlanInfo), P, P, P, P, P, P, ctypes.c_int, P, P, P, i32, P,
+                                          i32, ctypes.c_float, P, sz, P, P, P, P]
     L.mla_merge_out_proj.restype = ctypes.c_int
     L.mla_merge_out_proj.argtypes = [ctypes.POINTER(PlanInfo), P, P, sz, P, P, P, P, P, P]
     L.mla_decode_step_host.restype = ctypes.c_int
@@ -222,6 +226,38 @@ def mla_decode_paged(info: PlanInfo, plan_dev: torch.Tensor, q_abs: torch.Tensor
     _check("mla_decode_paged", st)
 
 
+def mla_absorb_decode_paged(info: PlanInfo, plan_dev: torch.Tensor, q_c: torch.Tensor, w_uk: torch.Tensor,
+                            q_abs: torch.Tensor, absorb_sync: torch.Tensor, q_r: torch.Tensor, *,
+                            kv_pool: torch.Tensor, block_table: torch.Tensor, o_lat: torch.Tensor, lse: torch.Tensor,
+                            dev_error: torch.Tensor, workspace: Optional[torch.Tensor] = None,
+                            kv_scale: Optional[torch.Tensor] = None, kr_pool: Optional[torch.Tensor] = None,
+                            softmax_scale: float = SOFTMAX_SCALE, stream=None) -> None:
+    """Absorb and decode in one launch (the absorb as the decode kernel's prologue); q_abs is
+    written.  absorb_sync: int32 [2] on the device, zero before the first call (left zero by
+    every call that reports no device error)."""
+    B = q_c.shape[0]
+    _need(plan_dev, "plan_dev", torch.int32)
+    _need(q_c, "q_c", torch.bfloat16, (B, NUM_HEADS, D_HC))
+    _need(w_uk, "w_uk", torch.bfloat16, (NUM_HEADS, D_HC, D_C))
+    _need(q_abs, "q_abs", torch.bfloat16, (B, NUM_HEADS, D_C))
+    _need(absorb_sync, "absorb_sync", torch.int32, (2,))
+    _need(q_r, "q_r", torch.bfloat16, (B, NUM_HEADS, D_R))
+    _need(block_table, "block_table", torch.int32)
+    _need(o_lat, "o_lat", torch.bfloat16, (B, NUM_HEADS, D_C))
+    _need(lse, "lse", torch.float32, (B, NUM_HEADS))
+    _need(dev_error, "dev_error", torch.int32, (1,))
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be [batch, max_pages]")
+    dtype = _kv_dtype(kv_pool, kv_scale, kr_pool)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().mla_absorb_decode_paged(ctypes.byref(info), _ptr(plan_dev), _ptr(q_c), _ptr(w_uk), _ptr(q_abs),
+                                       _ptr(absorb_sync), _ptr(q_r), dtype, _ptr(kv_pool), _ptr(kv_scale),
+                                       _ptr(kr_pool), int(kv_pool.shape[0]), _ptr(block_table),
+                                       int(block_table.shape[1]), float(softmax_scale), _ptr(workspace), ws_bytes,
+                                       _ptr(o_lat), _ptr(lse), _ptr(dev_error), _stream(stream))
+    _check("mla_absorb_decode_paged", st)
+
+
 def mla_decode_paged_static_ws(info: PlanInfo, plan_dev: torch.Tensor, q_abs: torch.Tensor, q_r: torch.Tensor, *,
                                kv_pool: torch.Tensor, block_table: torch.Tensor, o_lat: torch.Tensor,
                                lse: torch.Tensor, dev_error: torch.Tensor, kv_scale: Optional[torch.Tensor] = None,
@@ -337,17 +373,20 @@ def num_sms(device=None) -> int:
 
 
 class DecodeStep:
-    """Device buffers and plan for one batch shape; ``run`` enqueues the step's three kernels.
+    """Device buffers and plan for one batch shape; ``run`` enqueues the step's kernels.
 
-    absorb (q_c -> q_abs) -> paged decode (-> o_lat, lse, split partials) -> split merge and
-    W_UV projection in one kernel (-> out).  All buffers are allocated here, by torch, once.
+    absorb (q_c -> q_abs) -> paged decode (-> o_lat, lse, split partials) -> split merge -> W_UV
+    projection (-> out), each a kernel of its own, chained by programmatic dependent launch (the
+    measured fastest order at every workload of the benchmark).  fused_absorb runs the absorb as
+    the bf16 decode kernel's prologue (mla_absorb_decode_paged); fused_tail runs merge and
+    projection as one kernel (mla_merge_out_proj).  All buffers are allocated here, by torch, once.
     """
 
     def __init__(self, seq_lens, *, w_uk: torch.Tensor, w_uv: torch.Tensor, kv_pool: torch.Tensor,
                  block_table: torch.Tensor, kv_scale: Optional[torch.Tensor] = None,
                  kr_pool: Optional[torch.Tensor] = None, device=None, min_pages_per_split: int = 0,
                  max_clusters: int = 0, wait_timeout_ns: int = 0, item_cost_pages: int = 0,
-                 softmax_scale: float = SOFTMAX_SCALE):
+                 softmax_scale: float = SOFTMAX_SCALE, fused_absorb: bool = False, fused_tail: bool = False):
         self.device = torch.device(device if device is not None else "cuda")
         self.seq_lens = np.asarray(seq_lens, dtype=np.int32)
         self.batch = int(self.seq_lens.size)
@@ -361,6 +400,7 @@ class DecodeStep:
         self.block_table = block_table
         _check_table_rows(self.seq_lens, block_table)
         self.softmax_scale = softmax_scale
+        self.fused_absorb, self.fused_tail = bool(fused_absorb), bool(fused_tail)
         B = self.batch
         ws = int(self.info.workspace_bytes)
         self.workspace = torch.empty(max(ws // 4, 4), dtype=torch.float32, device=self.device) if ws else None
@@ -369,16 +409,24 @@ class DecodeStep:
         self.lse = torch.empty(B, NUM_HEADS, dtype=torch.float32, device=self.device)
         self.out = torch.empty(B, NUM_HEADS, D_HC, dtype=torch.bfloat16, device=self.device)
         self.dev_error = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.absorb_sync = torch.zeros(2, dtype=torch.int32, device=self.device)  # absorb-in-decode job counter
         self._h_stage = self._d_stage = None  # pinned host / device staging of run_host
 
     def run(self, q_c: torch.Tensor, q_r: torch.Tensor, stream=None) -> torch.Tensor:
-        mla_absorb_q(q_c, self.w_uk, self.q_abs, stream)
-        mla_decode_paged(self.info, self.plan_dev, self.q_abs, q_r, kv_pool=self.kv_pool,
-                         block_table=self.block_table, o_lat=self.o_lat, lse=self.lse, dev_error=self.dev_error,
-                         workspace=self.workspace, kv_scale=self.kv_scale, kr_pool=self.kr_pool,
-                         softmax_scale=self.softmax_scale, stream=stream)
-        mla_merge_out_proj(self.info, self.plan_dev, self.workspace, self.o_lat, self.lse, self.w_uv, self.out,
-                           self.dev_error, stream)
+        kv = dict(kv_pool=self.kv_pool, block_table=self.block_table, o_lat=self.o_lat, lse=self.lse,
+                  dev_error=self.dev_error, workspace=self.workspace, kv_scale=self.kv_scale, kr_pool=self.kr_pool,
+                  softmax_scale=self.softmax_scale, stream=stream)
+        if self.fused_absorb:
+            mla_absorb_decode_paged(self.info, self.plan_dev, q_c, self.w_uk, self.q_abs, self.absorb_sync, q_r, **kv)
+        else:
+            mla_absorb_q(q_c, self.w_uk, self.q_abs, stream)
+            mla_decode_paged(self.info, self.plan_dev, self.q_abs, q_r, **kv)
+        if self.fused_tail:
+            mla_merge_out_proj(self.info, self.plan_dev, self.workspace, self.o_lat, self.lse, self.w_uv, self.out,
+                               self.dev_error, stream)
+        else:
+            mla_combine_splits(self.info, self.plan_dev, self.workspace, self.o_lat, self.lse, stream)
+            mla_out_proj(self.o_lat, self.w_uv, self.out, stream)
         return self.out
 
     def run_host(self, q_c: torch.Tensor, q_r: torch.Tensor, *, block_table: Optional[torch.Tensor] = None,
@@ -451,9 +499,19 @@ class DecodeStep:
         stays out of the capture."""
         self.run(q_c, q_r)
         torch.cuda.synchronize(self.device)
-        graph = torch.cuda.CUDAGraph()
+        try:  # keep the captured graph so that its nodes can be counted
+            graph, kept = torch.cuda.CUDAGraph(keep_graph=True), True
+        except TypeError:
+            graph, kept = torch.cuda.CUDAGraph(), False
         with torch.cuda.graph(graph):
             self.run(q_c, q_r)
+        self.graph_kernel_nodes = None
+        if kept:
+            try:
+                self.graph_kernel_nodes = graph_kernel_nodes(graph.raw_cuda_graph())
+            except (OSError, AttributeError, RuntimeError):
+                self.graph_kernel_nodes = None
+            graph.instantiate()
         return graph
 
     def device_error(self, stream=None) -> int:
@@ -461,7 +519,30 @@ class DecodeStep:
 
     @property
     def launches_per_step(self) -> int:
-        return 3  # absorb, decode, merge + projection
+        # the absorb runs inside the bf16 decode kernel when fused (a kernel of its own with the e4m3
+        # cache); the merge is skipped when no sequence is split
+        n = 1 if (self.fused_absorb and self.kv_scale is None) else 2
+        if self.fused_tail:
+            return n + 1
+        return n + 1 + (1 if self.info.num_combine > 0 else 0)
+
+
+def graph_kernel_nodes(raw_graph: int) -> int:
+    """Number of kernel nodes in a CUDA graph (driver API, read only)."""
+    cu = ctypes.CDLL("libcuda.so.1")
+    n = ctypes.c_size_t(0)
+    if cu.cuGraphGetNodes(ctypes.c_void_p(raw_graph), None, ctypes.byref(n)) != 0:
+        raise RuntimeError("cuGraphGetNodes failed")
+    nodes = (ctypes.c_void_p * n.value)()
+    if n.value and cu.cuGraphGetNodes(ctypes.c_void_p(raw_graph), nodes, ctypes.byref(n)) != 0:
+        raise RuntimeError("cuGraphGetNodes failed")
+    kernels = 0
+    for i in range(n.value):
+        t = ctypes.c_int(-1)
+        if cu.cuGraphNodeGetType(ctypes.c_void_p(nodes[i]), ctypes.byref(t)) != 0:
+            raise RuntimeError("cuGraphNodeGetType failed")
+        kernels += int(t.value == 0)  # CU_GRAPH_NODE_TYPE_KERNEL
+    return kernels
 
 
 def inputs_to_device(inp, device="cuda"):

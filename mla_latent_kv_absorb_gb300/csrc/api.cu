@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -14,6 +15,7 @@
 #include "decode.cuh"
 #include "decode_fp8.cuh"
 #include "head_gemm.cuh"
+#include "nvtx_range.h"
 #include "plan.h"
 #include "tail.cuh"
 
@@ -240,28 +242,12 @@ mla_status launch_decode_fp8(const mla_plan_info* info, const void* plan_dev, co
                       mla::decode_fp8::kSmemBytes, static_cast<cudaStream_t>(stream), tm_c8, tm_kr, p);
 }
 
-extern "C" mla_status mla_absorb_q(const void* q_c, const void* w_uk, void* q_abs, int32_t batch, void* stream)
-{
-    if (!q_c || !w_uk || !q_abs || batch <= 0) return MLA_ERR_INVALID_ARG;
-    if (!aligned16(q_c) || !aligned16(w_uk) || !aligned16(q_abs)) return MLA_ERR_ALIGNMENT;
-    // the step's first kernel: an ordinary launch (it allows the decode kernel to start early)
-    return launch_head_gemm<128, kAbsorbN, true, kAbsorbStages>(q_c, w_uk, q_abs, batch, 512, 64, false, stream);
-}
-
-extern "C" mla_status mla_out_proj(const void* o_lat, const void* w_uv, void* out, int32_t batch, void* stream)
-{
-    if (!o_lat || !w_uv || !out || batch <= 0) return MLA_ERR_INVALID_ARG;
-    if (!aligned16(o_lat) || !aligned16(w_uv) || !aligned16(out)) return MLA_ERR_ALIGNMENT;
-    // streams W_UV while the merge (or the decode) before it finishes
-    return launch_head_gemm<512, kOutN, false, kOutStages>(o_lat, w_uv, out, batch, 128, kOutN, true, stream);
-}
-
-extern "C" mla_status mla_decode_paged(const mla_plan_info* info, const void* plan_dev, const void* q_abs,
-                                       const void* q_r, mla_kv_dtype kv_dtype, const void* kv_pool,
-                                       const float* kv_scale, const void* kr_pool, int32_t num_pool_pages,
-                                       const int32_t* block_table, int32_t max_pages_per_seq, float softmax_scale,
-                                       void* workspace, size_t workspace_bytes, void* o_lat, float* lse,
-                                       uint32_t* dev_error, void* stream)
+// Host checks shared by the decode entry points (nothing is launched when one fails).
+mla_status check_decode_args(const mla_plan_info* info, const void* plan_dev, const void* q_abs, const void* q_r,
+                             mla_kv_dtype kv_dtype, const void* kv_pool, const float* kv_scale, const void* kr_pool,
+                             int32_t num_pool_pages, const int32_t* block_table, int32_t max_pages_per_seq,
+                             float softmax_scale, const void* workspace, size_t workspace_bytes, const void* o_lat,
+                             const float* lse, const uint32_t* dev_error)
 {
     if (!plan_header_ok(info) || !plan_dev || !q_abs || !q_r || !kv_pool || !block_table || !o_lat || !lse ||
         !dev_error)
@@ -277,11 +263,20 @@ extern "C" mla_status mla_decode_paged(const mla_plan_info* info, const void* pl
         if (!workspace || workspace_bytes < (size_t)info->workspace_bytes) return MLA_ERR_WORKSPACE;
         if (!aligned16(workspace)) return MLA_ERR_ALIGNMENT;
     }
-    if (kv_dtype == MLA_KV_FP8_E4M3)
-        return launch_decode_fp8(info, plan_dev, q_abs, q_r, kv_pool, kv_scale, kr_pool, num_pool_pages, block_table,
-                                 max_pages_per_seq, softmax_scale, workspace, o_lat, lse, dev_error, stream);
+    return MLA_OK;
+}
 
-    CUtensorMap tm_pool, tm_q;
+// The bf16 decode kernel.  With q_c, w_uk and absorb_sync given, the absorb runs as the kernel's
+// prologue (q_abs is then an output) and the kernel is an ordinary launch; otherwise q_abs is an
+// input written by the kernel before it, and the launch is programmatic (it may start early).
+mla_status launch_decode_bf16(const mla_plan_info* info, const void* plan_dev, const void* q_abs, const void* q_r,
+                              const void* kv_pool, int32_t num_pool_pages, const int32_t* block_table,
+                              int32_t max_pages_per_seq, float softmax_scale, void* workspace, void* o_lat, float* lse,
+                              uint32_t* dev_error, void* stream, const void* q_c, const void* w_uk,
+                              uint32_t* absorb_sync)
+{
+    const bool fused = absorb_sync != nullptr;
+    CUtensorMap tm_pool, tm_q, tm_qc, tm_wuk;
     const cuuint64_t dims[3] = {576, 64, (cuuint64_t)num_pool_pages};
     const cuuint64_t strides[2] = {576 * 2, 64 * 576 * 2};
     const cuuint32_t box[3] = {64, 64, 1};
@@ -291,10 +286,28 @@ extern "C" mla_status mla_decode_paged(const mla_plan_info* info, const void* pl
     const cuuint32_t q_box[2] = {64, 128};
     if (!make_map_bf16(&tm_pool, kv_pool, 3, dims, strides, box) || !make_map_bf16(&tm_q, q_abs, 2, q_dims, q_str, q_box))
         return MLA_ERR_CUDA;
+    tm_qc = tm_q;
+    tm_wuk = tm_q;
+    if (fused) {
+        // the absorb prologue's operands: q_c rows [batch][128 x 128] in 128-row x 64 boxes, and
+        // W_UK [128 x 128 rows][512] in 64 x 64 boxes (MN-major B)
+        const cuuint64_t c_dims[2] = {128 * 128, (cuuint64_t)info->batch};
+        const cuuint64_t c_str[1] = {128 * 128 * 2};
+        const cuuint32_t c_box[2] = {64, 128};
+        const cuuint64_t w_dims[2] = {512, 128 * 128};
+        const cuuint64_t w_str[1] = {512 * 2};
+        const cuuint32_t w_box[2] = {64, 64};
+        if (!make_map_bf16(&tm_qc, q_c, 2, c_dims, c_str, c_box) || !make_map_bf16(&tm_wuk, w_uk, 2, w_dims, w_str, w_box))
+            return MLA_ERR_CUDA;
+    }
 
     mla::decode::Params p;
     p.plan = static_cast<const int32_t*>(plan_dev);
     p.q_abs = static_cast<const __nv_bfloat16*>(q_abs);
+    p.q_abs_out = fused ? static_cast<__nv_bfloat16*>(const_cast<void*>(q_abs)) : nullptr;
+    p.absorb_sync = absorb_sync;
+    p.absorb_jobs = fused ? 128 * ((info->batch + 127) / 128) : 0;
+    p.batch = info->batch;
     p.q_r = static_cast<const __nv_bfloat16*>(q_r);
     p.block_table = block_table;
     p.max_pages = max_pages_per_seq;
@@ -315,13 +328,91 @@ extern "C" mla_status mla_decode_paged(const mla_plan_info* info, const void* pl
 #endif
 
     if (!set_smem(mla::decode::decode_bf16_kernel, mla::decode::kSmemBytes)) return MLA_ERR_CUDA;
-    return launch_pdl(mla::decode::decode_bf16_kernel, dim3(2 * info->num_clusters), dim3(mla::decode::kThreads),
-                      mla::decode::kSmemBytes, static_cast<cudaStream_t>(stream), tm_pool, tm_q, p);
+    if (!fused)
+        return launch_pdl(mla::decode::decode_bf16_kernel, dim3(2 * info->num_clusters), dim3(mla::decode::kThreads),
+                          mla::decode::kSmemBytes, static_cast<cudaStream_t>(stream), tm_pool, tm_q, tm_qc, tm_wuk, p);
+    // enough CTA pairs that no CTA takes more than one absorb job while one fits per SM, and
+    // never fewer than the plan's (pairs past the plan's only run absorb jobs)
+    int dev = 0, sms = 0;
+    if (record_cuda(cudaGetDevice(&dev), "cudaGetDevice") != MLA_OK ||
+        record_cuda(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "cudaDeviceGetAttribute") != MLA_OK)
+        return MLA_ERR_CUDA;
+    const int clusters = std::max(info->num_clusters, std::min(sms / 2, (p.absorb_jobs + 1) / 2));
+    mla::decode::decode_bf16_kernel<<<dim3(2 * clusters), dim3(mla::decode::kThreads), mla::decode::kSmemBytes,
+                                      static_cast<cudaStream_t>(stream)>>>(tm_pool, tm_q, tm_qc, tm_wuk, p);
+    return launch_status();
+}
+
+extern "C" mla_status mla_absorb_q(const void* q_c, const void* w_uk, void* q_abs, int32_t batch, void* stream)
+{
+    const mla::NvtxRange nvtx_range("mla_absorb_q");
+    if (!q_c || !w_uk || !q_abs || batch <= 0) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(q_c) || !aligned16(w_uk) || !aligned16(q_abs)) return MLA_ERR_ALIGNMENT;
+    // the step's first kernel: an ordinary launch (it allows the decode kernel to start early)
+    return launch_head_gemm<128, kAbsorbN, true, kAbsorbStages>(q_c, w_uk, q_abs, batch, 512, 64, false, stream);
+}
+
+extern "C" mla_status mla_out_proj(const void* o_lat, const void* w_uv, void* out, int32_t batch, void* stream)
+{
+    const mla::NvtxRange nvtx_range("mla_out_proj");
+    if (!o_lat || !w_uv || !out || batch <= 0) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(o_lat) || !aligned16(w_uv) || !aligned16(out)) return MLA_ERR_ALIGNMENT;
+    // streams W_UV while the merge (or the decode) before it finishes
+    return launch_head_gemm<512, kOutN, false, kOutStages>(o_lat, w_uv, out, batch, 128, kOutN, true, stream);
+}
+
+extern "C" mla_status mla_decode_paged(const mla_plan_info* info, const void* plan_dev, const void* q_abs,
+                                       const void* q_r, mla_kv_dtype kv_dtype, const void* kv_pool,
+                                       const float* kv_scale, const void* kr_pool, int32_t num_pool_pages,
+                                       const int32_t* block_table, int32_t max_pages_per_seq, float softmax_scale,
+                                       void* workspace, size_t workspace_bytes, void* o_lat, float* lse,
+                                       uint32_t* dev_error, void* stream)
+{
+    const mla::NvtxRange nvtx_range("mla_decode_paged");
+    const mla_status st = check_decode_args(info, plan_dev, q_abs, q_r, kv_dtype, kv_pool, kv_scale, kr_pool,
+                                            num_pool_pages, block_table, max_pages_per_seq, softmax_scale, workspace,
+                                            workspace_bytes, o_lat, lse, dev_error);
+    if (st != MLA_OK) return st;
+    if (kv_dtype == MLA_KV_FP8_E4M3)
+        return launch_decode_fp8(info, plan_dev, q_abs, q_r, kv_pool, kv_scale, kr_pool, num_pool_pages, block_table,
+                                 max_pages_per_seq, softmax_scale, workspace, o_lat, lse, dev_error, stream);
+
+    return launch_decode_bf16(info, plan_dev, q_abs, q_r, kv_pool, num_pool_pages, block_table, max_pages_per_seq,
+                              softmax_scale, workspace, o_lat, lse, dev_error, stream, nullptr, nullptr, nullptr);
+}
+
+
+extern "C" mla_status mla_absorb_decode_paged(const mla_plan_info* info, const void* plan_dev, const void* q_c,
+                                              const void* w_uk, void* q_abs, uint32_t* absorb_sync, const void* q_r,
+                                              mla_kv_dtype kv_dtype, const void* kv_pool, const float* kv_scale,
+                                              const void* kr_pool, int32_t num_pool_pages, const int32_t* block_table,
+                                              int32_t max_pages_per_seq, float softmax_scale, void* workspace,
+                                              size_t workspace_bytes, void* o_lat, float* lse, uint32_t* dev_error,
+                                              void* stream)
+{
+    const mla::NvtxRange nvtx_range("mla_absorb_decode_paged");
+    if (!q_c || !w_uk || !q_abs || !absorb_sync || !info) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(q_c) || !aligned16(w_uk) || (reinterpret_cast<uintptr_t>(absorb_sync) & 7u)) return MLA_ERR_ALIGNMENT;
+    if (kv_dtype == MLA_KV_FP8_E4M3) {
+        // the e4m3 decode kernel has no absorb prologue: the absorb runs as its own kernel first
+        mla_status st = mla_absorb_q(q_c, w_uk, q_abs, info->batch, stream);
+        if (st != MLA_OK) return st;
+        return mla_decode_paged(info, plan_dev, q_abs, q_r, kv_dtype, kv_pool, kv_scale, kr_pool, num_pool_pages,
+                                block_table, max_pages_per_seq, softmax_scale, workspace, workspace_bytes, o_lat, lse,
+                                dev_error, stream);
+    }
+    const mla_status st = check_decode_args(info, plan_dev, q_abs, q_r, kv_dtype, kv_pool, kv_scale, kr_pool,
+                                            num_pool_pages, block_table, max_pages_per_seq, softmax_scale, workspace,
+                                            workspace_bytes, o_lat, lse, dev_error);
+    if (st != MLA_OK) return st;
+    return launch_decode_bf16(info, plan_dev, q_abs, q_r, kv_pool, num_pool_pages, block_table, max_pages_per_seq,
+                              softmax_scale, workspace, o_lat, lse, dev_error, stream, q_c, w_uk, absorb_sync);
 }
 
 extern "C" mla_status mla_combine_splits(const mla_plan_info* info, const void* plan_dev, const void* workspace,
                                          size_t workspace_bytes, void* o_lat, float* lse, void* stream)
 {
+    const mla::NvtxRange nvtx_range("mla_combine_splits");
     if (!plan_header_ok(info) || !plan_dev || !o_lat || !lse) return MLA_ERR_INVALID_ARG;
     if (info->num_combine == 0) return MLA_OK;
     if (!workspace || workspace_bytes < (size_t)info->workspace_bytes) return MLA_ERR_WORKSPACE;
@@ -340,6 +431,7 @@ extern "C" mla_status mla_merge_out_proj(const mla_plan_info* info, const void* 
                                          size_t workspace_bytes, void* o_lat, float* lse, const void* w_uv, void* out,
                                          uint32_t* dev_error, void* stream)
 {
+    const mla::NvtxRange nvtx_range("mla_merge_out_proj");
     if (!plan_header_ok(info) || !plan_dev || !o_lat || !lse || !w_uv || !out) return MLA_ERR_INVALID_ARG;
     if (info->num_combine > 0 && (!workspace || workspace_bytes < (size_t)info->workspace_bytes))
         return MLA_ERR_WORKSPACE;
@@ -395,8 +487,8 @@ extern "C" mla_status mla_debug_wait_timeout(uint32_t* dev_error, int64_t timeou
     return launch_status();
 }
 
-// The whole step from host memory: plan on the host, one asynchronous copy per input, the three
-// kernels (absorb, decode, merge + projection), the output copy back, one stream synchronisation.
+// The whole step from host memory: plan on the host, one asynchronous copy per input, the step's
+// kernels (absorb, decode, merge, projection), the output copy back, one stream synchronisation.
 extern "C" mla_status mla_decode_step_host(const int32_t* seq_lens, int32_t batch, int32_t num_sms,
                                            const mla_plan_options* opts, const void* q_c_host, const void* q_r_host,
                                            const int32_t* block_table_host, int32_t max_pages_per_seq,
@@ -405,6 +497,7 @@ extern "C" mla_status mla_decode_step_host(const int32_t* seq_lens, int32_t batc
                                            int32_t num_pool_pages, float softmax_scale, const mla_step_buffers* bufs,
                                            void* out_host, mla_plan_info* info_out, void* stream)
 {
+    const mla::NvtxRange nvtx_range("mla_decode_step_host");
     if (!seq_lens || batch <= 0 || !q_c_host || !q_r_host || !bufs || !out_host || !bufs->plan_host ||
         !bufs->plan || !bufs->block_table || max_pages_per_seq <= 0)
         return MLA_ERR_INVALID_ARG;
@@ -437,9 +530,10 @@ extern "C" mla_status mla_decode_step_host(const int32_t* seq_lens, int32_t batc
                                num_pool_pages, bufs->block_table, max_pages_per_seq, softmax_scale, bufs->workspace,
                                bufs->workspace_bytes, bufs->o_lat, bufs->lse, bufs->dev_error, stream)) != MLA_OK)
         return st;
-    if ((st = mla_merge_out_proj(&info, bufs->plan, bufs->workspace, bufs->workspace_bytes, bufs->o_lat, bufs->lse,
-                                 w_uv, bufs->out, bufs->dev_error, stream)) != MLA_OK)
+    if ((st = mla_combine_splits(&info, bufs->plan, bufs->workspace, bufs->workspace_bytes, bufs->o_lat, bufs->lse,
+                                 stream)) != MLA_OK)
         return st;
+    if ((st = mla_out_proj(bufs->o_lat, w_uv, bufs->out, batch, stream)) != MLA_OK) return st;
     const size_t out_bytes = (size_t)batch * 128 * 128 * 2;
     if (record_cuda(cudaMemcpyAsync(out_host, bufs->out, out_bytes, cudaMemcpyDeviceToHost, s),
                     "cudaMemcpyAsync(out)") != MLA_OK ||

@@ -15,6 +15,7 @@
 #include <cstdio>
 
 #include "../../include/mla.h"
+#include "nvtx_range.h"
 
 namespace mla {
 void set_last_error_text(const char* text);
@@ -123,6 +124,7 @@ extern "C" MLA_API mla_status mla_append_kv(int32_t num_tokens, const void* c_kv
                                             void* kv_pool, float* kv_scale, void* kr_pool, uint32_t* dev_error,
                                             void* stream)
 {
+    const mla::NvtxRange nvtx_range("mla_append_kv");
     using namespace mla::append;
     if (num_tokens < 0 || num_pool_pages <= 0) return MLA_ERR_INVALID_ARG;
     if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_INVALID_ARG;

@@ -121,7 +121,10 @@ enum Bar : int {
     kODrain0 = kOReady0 + 2,
     kDrain = kODrain0 + 2,
     kStgReady0 = kDrain + 1,
-    kNumBars = kStgReady0 + kStagingSlots
+    kAbsFull0 = kStgReady0 + kStagingSlots,  // absorb prologue: operands of K-chunk 0 / 1 landed
+    kAbsDone = kAbsFull0 + 2,                 // absorb prologue: the job's MMAs finished
+    kAbsEpi = kAbsDone + 1,                   // absorb prologue: the job's rows left TMEM
+    kNumBars = kAbsEpi + 1
 };
 
 constexpr int kOffTmemHolder = kOffBars + 8 * kNumBars;
@@ -182,7 +185,11 @@ constexpr int kEvBase = 4096, kEvSlots = 512;
 
 struct Params {
     const int32_t* plan;
-    const __nv_bfloat16* q_abs;  // [B][128][512]
+    const __nv_bfloat16* q_abs;  // [B][128][512]: the absorbed queries (written by the prologue when fused)
+    __nv_bfloat16* q_abs_out;    // the same buffer, written by the absorb prologue; null when q_abs is an input
+    uint32_t* absorb_sync;       // [2] absorb jobs finished, score CTAs past the wait; null when not fused
+    int32_t absorb_jobs;         // 128 heads x tiles of 128 sequences (absorb prologue)
+    int32_t batch;
     const __nv_bfloat16* q_r;    // [B][128][64]
     const int32_t* block_table;  // [B][max_pages]
     int32_t max_pages;
@@ -206,6 +213,126 @@ __device__ __forceinline__ Item load_item(const int32_t* plan, int items_off, in
     const int4 a = *reinterpret_cast<const int4*>(plan + items_off + kItemWords * i);
     const int4 b = *reinterpret_cast<const int4*>(plan + items_off + kItemWords * i + 4);
     return Item{a.x, a.y, a.z, a.w, b.x};
+}
+
+// ---------------------------------------------------------------------------- absorb prologue
+
+// With the absorb fused into this kernel (page 1 section 4, path B: q_abs = q_c W_UK per head),
+// every CTA of the grid first computes q_abs for one head and one tile of 128 sequences (job j
+// = 128 t + h, CTA c takes jobs c, c + grid, ...): q_c[tile, h, :] (128 x 128) times W_UK[h]
+// (128 x 512) on tcgen05 into the CTA's TMEM, bf16 rows to global memory.  Its shared memory
+// and TMEM are free until the roles below start.  A job is published by a release increment
+// of absorb_sync[0]; each score CTA waits for all of them before it loads its first query.
+constexpr int kAbsA = 0;                     // q_c: two K-chunks of [128 rows x 64] (16 KB each)
+constexpr int kAbsAChunk = 128 * 64 * 2;
+constexpr int kAbsW = 2 * kAbsAChunk;        // W_UK[h]: two K-chunks of eight [64 K x 64 N] boxes
+constexpr int kAbsWChunk = 8 * 64 * 64 * 2;
+constexpr uint32_t kAbsBarrier = 2;          // named barrier of the four epilogue warps
+static_assert(kAbsW + 2 * kAbsWChunk <= kOffBars, "the absorb operands fit below the barriers");
+
+__device__ __forceinline__ void absorb_jobs(const CUtensorMap* tm_qc, const CUtensorMap* tm_wuk, const Params& p,
+                                            uint32_t sbase, uint32_t bars, uint32_t tmem, const dev::WaitCtx& w,
+                                            int warp, int lane)
+{
+    using namespace dev;
+    int n = 0;  // jobs this CTA has done
+    for (int j = blockIdx.x; j < p.absorb_jobs; j += gridDim.x, ++n) {
+        const int h = j % 128, t = j / 128;
+        if (warp == 0) {
+            if (lane == 0) {
+                // the previous job's MMAs have read the tiles before they are overwritten
+                if (n > 0 && !wait_phase(bars + 8 * kAbsDone, n - 1, w)) break;
+                const uint64_t pol = l2_policy_evict_first();  // each head's weights are read once
+#pragma unroll 1
+                for (int kc = 0; kc < 2; ++kc) {
+                    const uint32_t full = bars + 8 * (kAbsFull0 + kc);
+                    mbar_arrive_expect_tx(full, kAbsAChunk + kAbsWChunk);
+                    tma_load_2d(sbase + kAbsA + kc * kAbsAChunk, tm_qc, full, h * 128 + 64 * kc, 128 * t, pol);
+                    for (int nb = 0; nb < 8; ++nb)
+                        tma_load_2d(sbase + kAbsW + kc * kAbsWChunk + nb * 8192, tm_wuk, full, 64 * nb,
+                                    h * 128 + 64 * kc, pol);
+                }
+            }
+        } else if (warp == 1) {
+            if (lane == 0) {
+                constexpr uint32_t idesc = idesc_bf16(128, 256, false, true);
+                // the previous job's rows have left TMEM before these MMAs overwrite it
+                bool ok = n == 0 || wait_phase(bars + 8 * kAbsEpi, n - 1, w);
+#pragma unroll 1
+                for (int kc = 0; kc < 2 && ok; ++kc) {
+                    ok = wait_phase(bars + 8 * (kAbsFull0 + kc), n, w);
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+#pragma unroll
+                        for (int half = 0; half < 2; ++half)
+                            mma_ss(tmem + 256 * half, smem_desc(sbase + kAbsA + kc * kAbsAChunk + k * 32, 16, 1024),
+                                   smem_desc(sbase + kAbsW + kc * kAbsWChunk + half * (kAbsWChunk / 2) + k * 2048, 8192,
+                                             1024),
+                                   idesc, (kc | k) != 0 ? 1u : 0u);
+                }
+                mma_commit(bars + 8 * kAbsDone);  // also on an early exit: arrives when issued MMAs finish
+            }
+        } else if (warp >= 2 && warp < 6) {
+            // warp & 3 selects the TMEM lane quarter: row m of the tile, 512 columns
+            const int q = warp & 3, m = 128 * t + 32 * q + lane;
+            if (__all_sync(0xffffffffu, wait_phase(bars + 8 * kAbsDone, n, w) && !*w.abort)) {
+                tc_fence_after();
+                uint4* dst = reinterpret_cast<uint4*>(p.q_abs_out + ((int64_t)m * 128 + h) * 512);
+#pragma unroll 1
+                for (int c = 0; c < 16; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32 * c, r);
+                    tmem_wait_ld();
+                    if (m < p.batch) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            dst[4 * c + v] = make_uint4(
+                                pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1])),
+                                pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3])),
+                                pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5])),
+                                pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7])));
+                    }
+                }
+            }
+            tc_fence_before();
+            __threadfence();  // the rows are visible GPU-wide before the job is published
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars + 8 * kAbsEpi);
+            named_barrier_or(kAbsBarrier, 128, false);
+            if (warp == 2 && lane == 0) {
+                fence_proxy_async_all();  // score CTAs read these rows with TMA
+                red_release_gpu_add_u32(p.absorb_sync, 1u);
+            }
+        }
+    }
+}
+
+// Score CTA producer, fused absorb: wait (bounded) until every absorb job of the grid is
+// published, then count this CTA out; the last score CTA to pass zeroes both words for the next
+// launch (no job can still be running then).  Returns false if the wait ran out.
+__device__ __forceinline__ bool absorb_wait(const Params& p, const dev::WaitCtx& w)
+{
+    using namespace dev;
+    bool ok = ld_acquire_gpu_u32(p.absorb_sync) >= (uint32_t)p.absorb_jobs;
+    if (!ok) {
+        const uint64_t t0 = globaltimer_ns();
+        while (!ok && !*w.abort) {
+            ok = ld_acquire_gpu_u32(p.absorb_sync) >= (uint32_t)p.absorb_jobs;
+            if (!ok && globaltimer_ns() - t0 > w.timeout_ns) {
+                *w.abort = 1;
+                raise_error(w.dev_error, MLA_DEVERR_TIMEOUT);
+                break;
+            }
+        }
+    }
+    fence_proxy_async_all();  // the TMA loads of q_abs come after the rows the other CTAs wrote
+    if (atomicAdd(p.absorb_sync + 1, 1u) == gridDim.x / 2 - 1) {
+        atomicExch(p.absorb_sync, 0u);
+        atomicExch(p.absorb_sync + 1, 0u);
+    }
+    return ok;
 }
 
 // ---------------------------------------------------------------------------- TMA producer
@@ -275,13 +402,15 @@ __device__ __forceinline__ void score_producer(const CUtensorMap* tm, const CUte
     }
     int s = 0, phase = 0, c = 0;
     bool ok = true;
+    if (p.absorb_sync && lane == 0) ok = absorb_wait(p, w);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
     for (int i = item_begin; i < item_end && ok; ++i) {
         const Item it = load_item(p.plan, items_off, i);
         const int32_t* bt = p.block_table + (int64_t)it.seq * p.max_pages;
         if (lane == 0) {
             // the item's q_abs rows (128 heads x 512 dims) as four ring entries of two 64-dim
             // boxes each, ahead of its pages
-            if (i == item_begin) griddep_wait();  // q_abs comes from the kernel launched before this one
+            if (i == item_begin && !p.absorb_sync) griddep_wait();  // q_abs comes from the kernel launched before
             for (int j = 0; j < kQueryEntries && ok; ++j, ++c) {
                 if (c >= kChunkStages) ok = MLA_TIMED(1, wait_phase(bars + 8 * (kEmpty0 + s), phase - 1, w));
                 if (!ok) break;
@@ -927,7 +1056,8 @@ done:
 // 11 warps: three SM sub-partitions hold three of them, and a sub-partition's 16K registers then
 // allow at most 3 x 32 x 168.
 __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
-decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_pool, const __grid_constant__ CUtensorMap tm_q, const Params p)
+decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_pool, const __grid_constant__ CUtensorMap tm_q,
+                   const __grid_constant__ CUtensorMap tm_qc, const __grid_constant__ CUtensorMap tm_wuk, const Params p)
 {
     using namespace dev;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -960,6 +1090,10 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_pool, const __grid_con
         for (int s = 0; s < kStagingSlots; ++s) mbar_init(bars + 8 * (kStgReady0 + s), 4);  // one set's warps
         *reinterpret_cast<volatile uint32_t*>(smem + kOffStgFreed) = 0;
         mbar_init(bars + 8 * kDrain, 1);
+        mbar_init(bars + 8 * (kAbsFull0 + 0), 1);
+        mbar_init(bars + 8 * (kAbsFull0 + 1), 1);
+        mbar_init(bars + 8 * kAbsDone, 1);
+        mbar_init(bars + 8 * kAbsEpi, 4);  // one arrive per epilogue warp
         int bad = misaligned ? 1 : 0;
         if (misaligned) raise_error(p.dev_error, MLA_DEVERR_SMEM_ALIGN);
         if (p.plan[kHdrMagic] != kPlanMagic || p.plan[kHdrVersion] != kPlanVersion) {
@@ -979,6 +1113,12 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_pool, const __grid_con
     const uint32_t tmem = *tmem_holder;
     const WaitCtx w{p.timeout_ns, abort_flag, p.dev_error};
 
+    if (!*abort_flag && p.absorb_sync) {
+        absorb_jobs(&tm_qc, &tm_wuk, p, sbase, bars, tmem, w, warp, lane);
+        tc_fence_before();
+        __syncthreads();  // the prologue's tiles and TMEM columns are free again
+        tc_fence_after();
+    }
     if (!*abort_flag) {
         const int n_clusters = p.plan[kHdrClusters];
         const int items_off = p.plan[kHdrItemsOff];

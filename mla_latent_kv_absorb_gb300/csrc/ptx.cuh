@@ -444,6 +444,22 @@ __device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v)
     asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
 }
 
+// Global-memory counter shared by the CTAs of a grid: acquire load, and release increment.
+__device__ __forceinline__ uint32_t ld_acquire_gpu_u32(const uint32_t* p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add_u32(uint32_t* p, uint32_t v)
+{
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Orders this thread's generic-proxy memory accesses with its async-proxy ones (TMA).
+__device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
+
 // Programmatic dependent launch: wait until the grids this one depends on have completed and
 // their memory is visible (a no-op for a grid launched without the attribute), and allow the
 // grids that depend on this one to be scheduled.

@@ -7,6 +7,7 @@ arguments), so none of them reaches a kernel launch even where a GPU is present.
 import ctypes
 import os
 import re
+import sys
 
 import numpy as np
 import pytest
@@ -109,6 +110,24 @@ def test_combine_rejects_bad_args(L):
                                 _p(0x80000), None) == binding.MLA_ERR_INVALID_ARG
     assert L.mla_combine_splits(ctypes.byref(info), _p(0x20000), _p(0x90004), info.workspace_bytes, _p(0x70000),
                                 _p(0x80000), None) == binding.MLA_ERR_ALIGNMENT
+
+
+def test_absorb_decode_rejects_bad_args(L):
+    """The fused absorb + decode checks its extra buffers, then the decode's own arguments."""
+    plan, info = _info()
+    p = _p
+    def call(q_c=0x100000, w_uk=0x200000, q_abs=0x300000, sync=0x400000, ws_bytes=None, bt=0x60000):
+        wb = info.workspace_bytes if ws_bytes is None else ws_bytes
+        return L.mla_absorb_decode_paged(ctypes.byref(info), p(0x20000), p(q_c), p(w_uk), p(q_abs), p(sync),
+                                         p(0x30000), binding.MLA_KV_BF16, p(0x40000), None, None, 100, p(bt), 80,
+                                         ctypes.c_float(0.07), p(0x90000), wb, p(0x70000), p(0x80000), p(0x50000),
+                                         None)
+    assert call(q_c=0) == binding.MLA_ERR_INVALID_ARG
+    assert call(sync=0) == binding.MLA_ERR_INVALID_ARG
+    assert call(sync=0x400004) == binding.MLA_ERR_ALIGNMENT
+    assert call(w_uk=0x200008) == binding.MLA_ERR_ALIGNMENT
+    assert call(ws_bytes=info.workspace_bytes - 1) == binding.MLA_ERR_WORKSPACE
+    assert call(bt=0) == binding.MLA_ERR_INVALID_ARG
 
 
 def test_merge_out_proj_rejects_bad_args(L):
@@ -240,3 +259,18 @@ def test_append_binding_checks_tensors():
         binding.mla_append_kv(c, r, s, kv_pool=pool, dev_error=err)
     with pytest.raises(TypeError):
         binding.mla_append_kv(c, r, s.long(), kv_pool=pool, dev_error=err)
+
+
+def test_nvtx_ranges_switch_on_without_changing_results():
+    """With MLA_NVTX=1 every entry point opens and closes an NVTX range; the argument checks and
+    their statuses are the same (run in a fresh process, since the switch is read once)."""
+    import subprocess
+    code = ("import ctypes, sys; sys.path.insert(0, %r); from mla_latent_kv_absorb_gb300 import binding; "
+            "L = binding.lib(); p = ctypes.c_void_p; "
+            "assert L.mla_absorb_q(None, p(4096), p(8192), 1, None) == binding.MLA_ERR_INVALID_ARG; "
+            "assert L.mla_out_proj(p(4096), p(8200), p(12288), 1, None) == binding.MLA_ERR_ALIGNMENT; "
+            "assert L.mla_append_kv(-1, None, None, None, 0, 1, None, None, None, None, None) != 0; "
+            "print('ok')") % ROOT
+    env = dict(os.environ, MLA_NVTX="1")
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stderr

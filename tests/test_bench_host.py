@@ -55,6 +55,26 @@ def test_reference_arm_only_rank0(monkeypatch):
     assert bench.run_reference(A(), rank=1, world=2, local=1) is None
 
 
+def test_reference_arm_line():
+    """Rank 0 of the reference arm times the oracle on a bounded sample per step and reports that
+    measured time (so K steps fit in the run's own clock), with the same config dict as the GPU
+    arm and the full-step estimate beside it."""
+    import bench
+    from mla_latent_kv_absorb_gb300 import synth
+
+    class A:
+        workload, steps, warmup = "b1_s2048", 2, 1
+
+    res = bench.run_reference(A(), rank=0, world=1, local=0)
+    inp = synth.make_workload("b1_s2048")
+    assert res["impl"] == "reference" and res["config"] == bench.bench_config(A(), inp, 1)
+    assert res["metric"] == bench.METRIC and res["unit"] == bench.UNIT and res["higher_is_better"] is False
+    cb = res["cpu_baseline"]
+    assert cb["value"] == res["value"] > 0 and cb["kind"] == "oracle" and cb["cores"] >= 1
+    assert cb["full_step_estimate_us"] >= res["value"]
+    assert res["e2e"]["value"] == res["value"] and res["e2e"]["h2d_bytes_per_step"] == 0
+
+
 def test_accounting_matches_roofline_table():
     import bench
     from mla_latent_kv_absorb_gb300 import synth

@@ -260,3 +260,27 @@ def test_graph_replay_matches_eager(kv_dtype):
         torch.cuda.synchronize()
         assert step.device_error() == 0
         assert torch.equal(got, ref)
+
+
+@pytest.mark.parametrize("fused_absorb,fused_tail,kernels", [(False, False, 4), (True, False, 3), (False, True, 3),
+                                                             (True, True, 2)])
+def test_step_graph_kernel_count(fused_absorb, fused_tail, kernels):
+    """The captured bf16 step holds exactly the kernels the configuration launches: absorb,
+    decode, merge, projection, or fewer with the fused calls (counted from the graph's nodes
+    through the driver; skipped where torch cannot keep the captured graph for inspection); every
+    configuration gives the same output bits."""
+    inp = synth.make_inputs([3000, 700], seed=14)
+    q_c, q_r, w_uk, w_uv, kv, bt = binding.inputs_to_device(inp, DEV)
+    step = binding.DecodeStep(inp.seq_lens, w_uk=w_uk, w_uv=w_uv, block_table=bt, min_pages_per_split=2,
+                              fused_absorb=fused_absorb, fused_tail=fused_tail, **kv)
+    assert step.info.num_combine > 0
+    ref = binding.DecodeStep(inp.seq_lens, w_uk=w_uk, w_uv=w_uv, block_table=bt, min_pages_per_split=2, **kv)
+    want = ref.run(q_c, q_r).clone()
+    graph = step.capture(q_c, q_r)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert step.device_error() == 0 and torch.equal(step.out, want)
+    assert step.launches_per_step == kernels
+    if step.graph_kernel_nodes is None:
+        pytest.skip("this torch build does not keep the captured graph")
+    assert step.graph_kernel_nodes == kernels

@@ -60,20 +60,20 @@ def check_plan(lens, num_sms=152, **kw):
 
 
 def test_single_long_sequence_is_split_evenly():
-    info, per, _ = check_plan([65536])
+    info, per, _ = check_plan([65536], item_cost_pages=-1)
     assert info.num_clusters == 76 and info.num_combine == 1 and info.max_splits == 76
     assert per.max() - per.min() <= 1
 
 
 def test_64k_workload_balance():
-    info, per, _ = check_plan([65536] * 16)
+    info, per, _ = check_plan([65536] * 16, item_cost_pages=-1)
     assert info.num_clusters == 76
     share = 16384 / 76
     assert per.max() <= share + 8 + 1  # min-split snapping moves an edge by < 8 pages
 
 
 def test_short_sequences_stay_whole():
-    info, per, items = check_plan([2048])
+    info, per, items = check_plan([2048], item_cost_pages=-1)
     # 32 pages with the default minimum of 8 pages per item: 4 pairs
     assert info.num_clusters == 4 and info.num_items == 4 and info.num_combine == 1
 
@@ -81,7 +81,7 @@ def test_short_sequences_stay_whole():
 def test_ragged_workload():
     g = torch.Generator().manual_seed(42)
     lens = synth.ragged_lengths(64, 128, 32768, g)
-    info, per, _ = check_plan(lens)
+    info, per, _ = check_plan(lens, item_cost_pages=-1)
     assert info.total_pages == 17480
     assert per.max() <= 17480 / 76 + 8 + 1
 
@@ -139,7 +139,7 @@ def test_item_cost_balances_pairs():
     one charge and one sequence-edge snap of the mean."""
     c = 7
     for lens in ([65536] * 16, [4096] * 16):
-        base_plan, base_info = binding.mla_plan_splits(np.asarray(lens, np.int32), 152)
+        base_plan, base_info = binding.mla_plan_splits(np.asarray(lens, np.int32), 152, item_cost_pages=-1)
         h, cl, items, _ = decode_plan(base_plan)
         base = np.array([int((items[cl[k]:cl[k + 1], 2] - items[cl[k]:cl[k + 1], 1]).sum())
                          + c * max(0, int(cl[k + 1] - cl[k]) - 1) for k in range(h["clusters"])])
@@ -148,9 +148,16 @@ def test_item_cost_balances_pairs():
         assert costs.max() <= costs.sum() / costs.size + c + 8
 
 
-def test_item_cost_rejects_bad_values():
-    with pytest.raises(binding.MlaError):
-        binding.mla_plan_splits([100], 152, item_cost_pages=-1)
+def test_item_cost_default_and_off():
+    """0 asks for the library's default charge (7 pages), a negative value for equal page runs."""
+    lens = np.asarray([65536] * 16, np.int32)
+    p0, _ = binding.mla_plan_splits(lens, 152)
+    p7, _ = binding.mla_plan_splits(lens, 152, item_cost_pages=7)
+    pe, _ = binding.mla_plan_splits(lens, 152, item_cost_pages=-1)
+    assert np.array_equal(p0, p7) and not np.array_equal(p0, pe)
+
+
+def test_plan_rejects_reserved_field():
     opts = binding.PlanOptions(0, 0, 0, 0, 5)  # reserved must be 0
     buf = np.zeros(4096, np.int32)
     info = binding.PlanInfo()

@@ -26,7 +26,7 @@ def test_static_ws_rejects_oversized_plan():
     build.build_library()
     L = binding.lib()
     lens = [64 * 64] * 200
-    _, info = binding.mla_plan_splits(lens, 152, min_pages_per_split=1)
+    _, info = binding.mla_plan_splits(lens, 152, min_pages_per_split=1, item_cost_pages=-1)  # equal page runs
     assert info.num_partials > binding.MLA_STATIC_WS_MAX_PARTIALS
     p = ctypes.c_void_p
     st = L.mla_decode_paged_static_ws(ctypes.byref(info), p(0x20000), p(0x10000), p(0x30000), binding.MLA_KV_BF16,
