@@ -55,7 +55,7 @@ class DecodeInputs:
     q_r: torch.Tensor             # bf16 [B, 128, 64]
     w_uk: torch.Tensor            # bf16 [128, 128, 512]
     w_uv: torch.Tensor            # bf16 [128, 128, 512]
-    kv_dtype: str                 # "bf16" or "fp8_e4m3"
+    kv_dtype: str                 # "bf16", "fp8_e4m3" or "nvfp4" (c8 then holds [N_pg, 64, 288] NVFP4 rows)
     pool: Optional[torch.Tensor] = None      # bf16 [N_pg, 64, 576]   (bf16 cache)
     c8: Optional[torch.Tensor] = None        # uint8 [N_pg, 64, 512]  (fp8 cache: e4m3 codes)
     kv_scale: Optional[torch.Tensor] = None  # fp32 [N_pg, 64]        (fp8 cache)

@@ -18,6 +18,12 @@ Parity status of each function (what pins it, see ``tests/test_oracle_pins.py``)
                       -- every finite code round-trips, midpoints go to the even code, a sweep
                          against torch's float8_e4m3fn cast, the half-step error bound, the
                          all-zero row; appending every token of a synthetic cache rebuilds it.
+  e2m1_value, e2m1_encode, quantize_token_nvfp4 (and the NVFP4 cache in every decode function)
+                      -- the sixteen e2m1 values of the format; round trips, midpoints to the
+                         even code, saturation; the token's largest value maps to code 6 under
+                         block scale 448; every code nearest to its scaled value; zero rows and
+                         zero blocks; S = 1 and q = 0 closed forms and absorbed = naive on an
+                         NVFP4 cache built by append_kv.
 """
 from __future__ import annotations
 
@@ -33,6 +39,7 @@ _SRC = os.path.join(_HERE, "mla_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "_build", "libmla_oracle.so")
 
 NUM_HEADS, D_HC, D_C, D_R, D_ROW, PAGE = 128, 128, 512, 64, 576, 64
+NV_ROW = D_C // 2 + D_C // 16  # NVFP4 row of one token: packed e2m1 codes, then e4m3 block scales
 
 _lib = None
 
@@ -73,6 +80,13 @@ def _load(path: str):
     L.oracle_e4m3_encode_many.argtypes = [P, i64, P]
     L.oracle_quantize_token.restype = ctypes.c_float
     L.oracle_quantize_token.argtypes = [P, P]
+    L.oracle_e2m1_value.restype = f64
+    L.oracle_e2m1_value.argtypes = [ctypes.c_uint8]
+    L.oracle_e2m1_encode.restype = ctypes.c_uint8
+    L.oracle_e2m1_encode.argtypes = [ctypes.c_float]
+    L.oracle_e2m1_encode_many.argtypes = [P, i64, P]
+    L.oracle_quantize_token_nvfp4.restype = ctypes.c_float
+    L.oracle_quantize_token_nvfp4.argtypes = [P, P]
     L.oracle_append_kv.restype = i32
     L.oracle_append_kv.argtypes = [i32, P, P, P, i32, i32, P, P, P, P]
     return L
@@ -117,7 +131,7 @@ class _Cache:
     """The paged cache of a ``synth.DecodeInputs`` as C arrays."""
 
     def __init__(self, inp):
-        self.kv_fp8 = 1 if inp.kv_dtype == "fp8_e4m3" else 0
+        self.kv_fp8 = {"bf16": 0, "fp8_e4m3": 1, "nvfp4": 2}[inp.kv_dtype]
         self.num_pages = int(inp.num_pool_pages)
         self.pool = _u16(inp.pool) if inp.pool is not None else None
         self.c8 = _arr(inp.c8, np.uint8) if inp.c8 is not None else None
@@ -238,6 +252,30 @@ def e4m3_encode(x: np.ndarray) -> np.ndarray:
     return out
 
 
+def e2m1_value(codes) -> np.ndarray:
+    """Values of e2m1 codes (the low 4 bits of each uint8)."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    return np.array([lib().oracle_e2m1_value(int(c)) for c in codes.reshape(-1)], dtype=np.float64).reshape(codes.shape)
+
+
+def e2m1_encode(x: np.ndarray) -> np.ndarray:
+    """Nearest e2m1 codes (uint8, low 4 bits) of float32 values, ties to even, clamped to +-6."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    lib().oracle_e2m1_encode_many(_p(x), x.size, _p(out))
+    return out
+
+
+def quantize_token_nvfp4(c) -> tuple:
+    """One token's 512 bf16 latent values -> (NVFP4 row uint8 [288]: 256 bytes of packed e2m1
+    codes then 32 e4m3 block scales, sigma float32)."""
+    c = _u16(c).reshape(-1)
+    assert c.size == D_C
+    row = np.zeros(NV_ROW, dtype=np.uint8)
+    sigma = lib().oracle_quantize_token_nvfp4(_p(c), _p(row))
+    return row, np.float32(sigma)
+
+
 def quantize_token(c) -> tuple:
     """One token's 512 bf16 latent values -> (codes uint8 [512], sigma float32)."""
     c = _u16(c).reshape(-1)
@@ -251,17 +289,18 @@ def append_kv(c_kv, k_r, slots, cache: dict) -> int:
     """Write tokens into a paged cache held as numpy arrays, in place.
 
     c_kv bf16 [n, 512], k_r bf16 [n, 64], slots int32 [n] (page * 64 + row; negative = skip).
-    cache: {"pool": uint16 [N, 64, 576]} for a bf16 cache, or {"c8": uint8 [N, 64, 512],
-    "scale": float32 [N, 64], "kr": uint16 [N, 64, 64]} for FP8.  Returns 0, or -1 when a slot
-    was past the pool (that token skipped)."""
+    cache: {"pool": uint16 [N, 64, 576]} for a bf16 cache, {"c8": uint8 [N, 64, 512],
+    "scale": float32 [N, 64], "kr": uint16 [N, 64, 64]} for FP8, or {"c4": uint8 [N, 64, 288],
+    "scale", "kr"} for NVFP4.  Returns 0, or -1 when a slot was past the pool (that token
+    skipped)."""
     ck, kr = _u16(c_kv), _u16(k_r)
     sl = np.ascontiguousarray(slots, dtype=np.int32)
     n = sl.size
     assert ck.shape == (n, D_C) and kr.shape == (n, D_R)
-    fp8 = "c8" in cache
-    arrays = [cache.get(k) for k in ("pool", "c8", "scale", "kr")]
+    mode = 2 if "c4" in cache else (1 if "c8" in cache else 0)
+    codes = cache.get("c4") if mode == 2 else cache.get("c8")
+    arrays = [cache.get("pool"), codes, cache.get("scale"), cache.get("kr")]
     for a in arrays:
         assert a is None or (isinstance(a, np.ndarray) and a.flags.c_contiguous)
-    num_pages = (cache["c8"] if fp8 else cache["pool"]).shape[0]
-    return int(lib().oracle_append_kv(n, _p(ck), _p(kr), _p(sl), 1 if fp8 else 0, num_pages,
-                                      *[_p(a) for a in arrays]))
+    num_pages = (codes if mode else cache["pool"]).shape[0]
+    return int(lib().oracle_append_kv(n, _p(ck), _p(kr), _p(sl), mode, num_pages, *[_p(a) for a in arrays]))

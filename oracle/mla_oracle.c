@@ -36,6 +36,8 @@
 #endif
 
 enum { NH = 128, DHC = 128, DC = 512, DR = 64, DROW = 576, PG = 64 };
+/* NVFP4 row of one token: 256 bytes of packed e2m1 codes, then 32 e4m3 block scales */
+enum { NV_CODES = DC / 2, NV_BLOCKS = DC / 16, NV_ROW = NV_CODES + NV_BLOCKS };
 
 /* ------------------------------------------------------------------ element decoding */
 
@@ -68,6 +70,16 @@ void oracle_e4m3_decode(const uint8_t* codes, int64_t n, double* out)
     for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_value(codes[i]);
 }
 
+/* e2m1 (the element type of NVFP4): 1 sign bit, 2 exponent bits with bias 1, 1 mantissa bit, no
+ * infinities or NaN.  Exponent field 0 is subnormal (0 or 0.5); field e > 0 is (1 + m/2) 2^(e-1):
+ * magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6.  Codes are the low 4 bits. */
+double oracle_e2m1_value(uint8_t code)
+{
+    const int s = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
+    const double mag = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return s ? -mag : mag;
+}
+
 void oracle_set_threads(int n)
 {
 #ifdef _OPENMP
@@ -89,10 +101,14 @@ int oracle_max_threads(void)
 /* ------------------------------------------------------------------ the paged cache */
 
 typedef struct {
-    int kv_fp8;               /* 0: bf16 rows [N][64][576]; 1: e4m3 c_KV + fp32 scale + bf16 k_R */
+    int kv_fp8;               /* 0: bf16 rows [N][64][576]; 1: e4m3 c_KV + fp32 scale + bf16 k_R;
+                                 2: NVFP4 c_KV (e2m1 codes, e4m3 scale per 16 values, fp32 scale per
+                                 token) + bf16 k_R */
     int num_pages;
     const uint16_t* pool;     /* bf16 [N][64][576] */
-    const uint8_t* c8;        /* e4m3 [N][64][512] */
+    const uint8_t* c8;        /* e4m3 [N][64][512]; NVFP4: rows [N][64][288], 256 bytes of packed e2m1
+                                 codes (value 2j in the low nibble of byte j, 2j + 1 in the high
+                                 nibble) then 32 e4m3 scales, one per 16 latent values */
     const float* scale;       /* fp32 [N][64] */
     const uint16_t* kr;       /* bf16 [N][64][64] */
 } cache_view;
@@ -108,11 +124,22 @@ static int gather_row(const cache_view* cv, const int32_t* bt_row, int64_t t, do
         const uint16_t* row = cv->pool + tok * DROW;
         for (int i = 0; i < DC; ++i) ckv[i] = bf16_value(row[i]);
         for (int i = 0; i < DR; ++i) kr[i] = bf16_value(row[DC + i]);
-    } else {
+    } else if (cv->kv_fp8 == 1) {
         /* dequantised latent: the stored code times the token's scale */
         const uint8_t* row = cv->c8 + tok * DC;
         double sigma = (double)cv->scale[tok];
         for (int i = 0; i < DC; ++i) ckv[i] = oracle_e4m3_value(row[i]) * sigma;
+        const uint16_t* r = cv->kr + tok * DR;
+        for (int i = 0; i < DR; ++i) kr[i] = bf16_value(r[i]);
+    } else {
+        /* NVFP4: e2m1 code times its block's e4m3 scale times the token's fp32 scale (exact in double) */
+        const uint8_t* row = cv->c8 + tok * NV_ROW;
+        const uint8_t* bs = row + NV_CODES;
+        double sigma = (double)cv->scale[tok];
+        for (int i = 0; i < DC; ++i) {
+            const uint8_t code = (i & 1) ? (uint8_t)(row[i / 2] >> 4) : (uint8_t)(row[i / 2] & 0x0F);
+            ckv[i] = oracle_e2m1_value(code) * oracle_e4m3_value(bs[i / 16]) * sigma;
+        }
         const uint16_t* r = cv->kr + tok * DR;
         for (int i = 0; i < DR; ++i) kr[i] = bf16_value(r[i]);
     }
@@ -384,11 +411,82 @@ float oracle_quantize_token(const uint16_t* c, uint8_t* codes)
 }
 
 /*
+ * The e2m1 code nearest a finite value, ties to the code with the even mantissa field (m = 0),
+ * magnitudes at or past 6 (the largest) give 6; the sign is kept, zero results included.  The
+ * non-negative codes 0..7 have increasing values: take the last one not above |x| and the next.
+ */
+uint8_t oracle_e2m1_encode(float x)
+{
+    const uint8_t sign = signbit(x) ? 0x8 : 0x0;
+    const double a = fabs((double)x);
+    if (a >= 6.0) return sign | 0x7;
+    int k = 0;  /* the largest magnitude code not above a */
+    while (k + 1 <= 7 && oracle_e2m1_value((uint8_t)(k + 1)) <= a) ++k;
+    const double v_below = oracle_e2m1_value((uint8_t)k);
+    if (v_below == a) return sign | (uint8_t)k;
+    const double gap_below = a - v_below, gap_above = oracle_e2m1_value((uint8_t)(k + 1)) - a;
+    int code = k;
+    if (gap_above < gap_below || (gap_above == gap_below && (k & 1)))
+        code = k + 1; /* nearer above, or a tie whose even mantissa field (m = 0) is above */
+    return sign | (uint8_t)code;
+}
+
+void oracle_e2m1_encode_many(const float* x, int64_t n, uint8_t* out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e2m1_encode(x[i]);
+}
+
+/*
+ * One token's latent for the NVFP4 cache (two-level scaling: an fp32 scale per token and an e4m3
+ * scale per 16 consecutive latent values, e2m1 codes).  All in fp32, in this order:
+ *   sigma  = (largest |c_i| of the token) / 2688   (2688 = 6 * 448), or 1 for an all-zero row;
+ *   t_b    = ((largest |c_i| of block b) / sigma) / 6,   S_b = the e4m3 code nearest t_b;
+ *   code_i = the e2m1 code nearest c_i / (sigma * S_b), or a zero of c_i's sign when S_b is 0.
+ * c is the token's 512 bf16 latent values; row receives the 288-byte NVFP4 row: 256 bytes of
+ * codes (value 2j in the low nibble of byte j), then the 32 block scales.  Returns sigma.
+ */
+float oracle_quantize_token_nvfp4(const uint16_t* c, uint8_t* row)
+{
+    uint8_t* codes = row;
+    uint8_t* bscale = row + NV_CODES;
+    float amax = 0.0f;
+    for (int i = 0; i < DC; ++i) {
+        const float v = fabsf((float)bf16_value(c[i]));
+        if (v > amax) amax = v;
+    }
+    const float sigma = amax > 0.0f ? amax / 2688.0f : 1.0f;
+    for (int b = 0; b < DC / 16; ++b) {
+        float bmax = 0.0f;
+        for (int i = 16 * b; i < 16 * b + 16; ++i) {
+            const float v = fabsf((float)bf16_value(c[i]));
+            if (v > bmax) bmax = v;
+        }
+        const uint8_t s8 = oracle_e4m3_encode((bmax / sigma) / 6.0f);
+        bscale[b] = s8;
+        const float den = sigma * (float)oracle_e4m3_value(s8);
+        for (int i = 16 * b; i < 16 * b + 16; ++i) {
+            const float x = (float)bf16_value(c[i]);
+            uint8_t q;
+            if (den == 0.0f)
+                q = signbit(x) ? 0x8 : 0x0;
+            else
+                q = oracle_e2m1_encode(x / den);
+            if (i & 1)
+                codes[i / 2] = (uint8_t)((codes[i / 2] & 0x0F) | (q << 4));
+            else
+                codes[i / 2] = q;
+        }
+    }
+    return sigma;
+}
+
+/*
  * Write n tokens into the paged cache (page 1 section 1: one row of c_KV and k_R per token;
  * section 3: 64-token pages).  Token i goes to slot slots[i] = page * 64 + row; a negative slot
  * skips the token, and so does a slot at or past num_pages * 64 (then the call returns -1).
- * bf16 cache: pool row = the token's c_KV then k_R.  FP8 cache: c8 row = the codes of
- * oracle_quantize_token, scale = its sigma, kr row = k_R.
+ * bf16 cache: pool row = the token's c_KV then k_R.  FP8 cache (kv_fp8 = 1): c8 row = the
+ * codes of oracle_quantize_token, scale = its sigma, kr row = k_R.  NVFP4 cache (kv_fp8 = 2): c8
+ * row = the 288-byte row of oracle_quantize_token_nvfp4, scale = its sigma, kr row = k_R.
  */
 int oracle_append_kv(int n, const uint16_t* c_kv, const uint16_t* k_r, const int32_t* slots, int kv_fp8,
                      int num_pages, uint16_t* pool, uint8_t* c8, float* scale, uint16_t* kr)
@@ -407,9 +505,12 @@ int oracle_append_kv(int n, const uint16_t* c_kv, const uint16_t* k_r, const int
             uint16_t* row = pool + slot * DROW;
             for (int j = 0; j < DC; ++j) row[j] = c[j];
             for (int j = 0; j < DR; ++j) row[DC + j] = r[j];
-        } else {
+        } else if (kv_fp8 == 1) {
             scale[slot] = oracle_quantize_token(c, c8 + slot * DC);
             for (int j = 0; j < DR; ++j) kr[slot * DR + j] = r[j];
+        } else {
+            scale[slot] = oracle_quantize_token_nvfp4(c, c8 + slot * NV_ROW);
+            memcpy(kr + slot * DR, r, DR * sizeof(uint16_t)); /* k_R unchanged */
         }
     }
     return status;

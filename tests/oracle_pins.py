@@ -497,3 +497,177 @@ ALL_CHECKS = [
     check_quantize_token_rule,
     check_append_rebuilds_cache,
 ]
+
+
+# ----------------------------------------------------------------------------- NVFP4 cache (e2m1 + e4m3 block scales)
+
+# e2m1 values straight from the format (sign, 2 exponent bits with bias 1, 1 mantissa bit;
+# exponent field 0 subnormal): codes 0..7 and their negatives 8..15.
+E2M1_TABLE = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0])
+
+
+def check_e2m1_values():
+    """The sixteen e2m1 codes decode to the format's values, -0 included."""
+    got = oracle.e2m1_value(np.arange(16, dtype=np.uint8))
+    assert np.array_equal(got, E2M1_TABLE)
+    assert np.signbit(got[8]) and not np.signbit(got[0])
+
+
+def _nearest_ok(codes: np.ndarray, x: np.ndarray) -> np.ndarray:
+    """For each x, is the code's value at least as near as every e2m1 value (after clamping the
+    magnitude to 6)?"""
+    vals = E2M1_TABLE[codes & 0xF]
+    xc = np.clip(x.astype(np.float64), -6.0, 6.0)
+    best = np.min(np.abs(xc[:, None] - E2M1_TABLE[None, :8] * np.where(xc < 0, -1.0, 1.0)[:, None]), axis=1)
+    return np.abs(vals - xc) <= best + 0.0
+
+
+def check_e2m1_encode_rule():
+    """Every code round-trips (both signs, -0 -> 0x8); midpoints go to the even mantissa field;
+    one float32 step either side goes to the nearer value; magnitudes >= 6 give 6; and 100,000
+    random values get a nearest code."""
+    for c in range(16):
+        assert int(oracle.e2m1_encode(np.array([E2M1_TABLE[c]], np.float32))[0]) == c, c
+    mids = {0.25: 0x0, 0.75: 0x2, 1.25: 0x2, 1.75: 0x4, 2.5: 0x4, 3.5: 0x6, 5.0: 0x6}
+    for m, code in mids.items():
+        assert int(oracle.e2m1_encode(np.array([m], np.float32))[0]) == code, m
+        assert int(oracle.e2m1_encode(np.array([-m], np.float32))[0]) == (code | 0x8), -m
+        up, down = np.nextafter(np.float32(m), np.float32(10)), np.nextafter(np.float32(m), np.float32(-10))
+        hi_code = int(np.searchsorted(E2M1_TABLE[:8], m))
+        assert int(oracle.e2m1_encode(np.array([up], np.float32))[0]) == hi_code, m
+        assert int(oracle.e2m1_encode(np.array([down], np.float32))[0]) == hi_code - 1, m
+    big = np.array([6.0, 6.5, 7.0, 1e30, -6.0, -1e30], np.float32)
+    assert np.array_equal(oracle.e2m1_encode(big), np.array([7, 7, 7, 7, 15, 15], np.uint8))
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal(100000) * 3).astype(np.float32)
+    codes = oracle.e2m1_encode(x)
+    assert _nearest_ok(codes, x).all()
+    assert np.array_equal(codes >= 8, np.signbit(x))
+
+
+def _bf16_rows(rows: np.ndarray) -> np.ndarray:
+    """float32 rows rounded to bf16, as uint16 bit patterns."""
+    return torch.from_numpy(np.ascontiguousarray(rows, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(
+        np.uint16)
+
+
+def _nvfp4_deq(row: np.ndarray, sigma: float) -> np.ndarray:
+    """Values of one NVFP4 row through the format table and torch's e4m3 (library), not the oracle."""
+    codes = np.empty(512, np.uint8)
+    codes[0::2] = row[:256] & 0xF
+    codes[1::2] = row[:256] >> 4
+    scales = _e4m3_values(row[256:288])
+    return E2M1_TABLE[codes] * np.repeat(scales, 16) * float(sigma)
+
+
+def check_nvfp4_quantize_rule():
+    """sigma = absmax / 2688 (float32; 1 for a zero row); block scale = e4m3 nearest to
+    ((block absmax / sigma) / 6) (torch's e4m3 cast); the token's largest value maps to code 6 in a
+    block of scale 448; every code is the nearest e2m1 to x / (sigma S_b) (float32); value 2j sits
+    in the low nibble of byte j; zero rows and zero blocks give zero codes and scales."""
+    rng = np.random.default_rng(11)
+    rows = [rng.standard_normal(512) * s for s in (1.0, 0.01, 300.0)]
+    r = rng.standard_normal(512)
+    r[64:96] = 0.0  # two zero blocks
+    rows.append(r)
+    rows.append(np.zeros(512))
+    one = np.zeros(512)
+    one[0] = 2.0
+    rows.append(one)
+    two = np.zeros(512)
+    two[1] = -3.0
+    rows.append(two)
+    bits = _bf16_rows(np.stack(rows))
+    vals = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float32).numpy()
+    for i in range(bits.shape[0]):
+        row, sigma = oracle.quantize_token_nvfp4(bits[i])
+        c = vals[i]
+        amax = np.float32(np.abs(c).max())
+        want_sigma = np.float32(amax / np.float32(2688.0)) if amax > 0 else np.float32(1.0)
+        assert sigma == want_sigma, i
+        bmax = np.abs(c).reshape(32, 16).max(axis=1).astype(np.float32)
+        t = ((bmax / sigma).astype(np.float32) / np.float32(6.0)).astype(np.float32)
+        want_scales = torch.from_numpy(t).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert np.array_equal(row[256:288], want_scales), i
+        S = _e4m3_values(row[256:288])
+        codes = np.empty(512, np.uint8)
+        codes[0::2] = row[:256] & 0xF
+        codes[1::2] = row[:256] >> 4
+        den = (sigma * np.repeat(S, 16).astype(np.float32)).astype(np.float32)
+        live = den > 0
+        q = np.where(live, c / np.where(live, den, 1), 0).astype(np.float32)
+        assert _nearest_ok(codes[live], q[live]).all(), i
+        assert np.all(E2M1_TABLE[codes[~live]] == 0), i
+        if amax > 0:
+            k = int(np.argmax(np.abs(c)))
+            assert S[k // 16] == 448.0 and abs(E2M1_TABLE[codes[k]]) == 6.0, i
+    row, sigma = oracle.quantize_token_nvfp4(bits[4])
+    assert sigma == 1.0 and not row.any()
+    row, _ = oracle.quantize_token_nvfp4(bits[5])
+    assert row[0] == 0x07 and not row[1:256].any()        # value 0 in the low nibble
+    row, _ = oracle.quantize_token_nvfp4(bits[6])
+    assert row[0] == 0xF0 and not row[1:256].any()        # value 1 (negative) in the high nibble
+
+
+def nvfp4_inputs(seq_lens=(1, 65, 130), seed=7, poison=True):
+    """A synthetic decode batch whose cache is NVFP4: the bf16 cache's rows appended, through the
+    oracle's quantiser, into the same page layout (k_R kept in bf16)."""
+    inp = tiny_inputs(seq_lens, seed=seed, poison=poison)
+    pool = inp.pool.contiguous().view(torch.int16).numpy().view(np.uint16)
+    N = inp.num_pool_pages
+    flat = pool.reshape(N * 64, 576)
+    slots = np.arange(N * 64, dtype=np.int32)
+    c_kv = np.ascontiguousarray(np.nan_to_num(flat[:, :512].view(np.int16)).view(np.uint16))
+    finite = np.isfinite(torch.from_numpy(flat[:, :512].view(np.int16)).view(torch.bfloat16).float().numpy()).all(1)
+    slots = np.where(finite, slots, -1).astype(np.int32)
+    cache = {"c4": np.zeros((N, 64, 288), np.uint8), "scale": np.ones((N, 64), np.float32),
+             "kr": np.ascontiguousarray(pool[:, :, 512:])}
+    assert oracle.append_kv(c_kv, np.ascontiguousarray(flat[:, 512:]), slots, cache) == 0
+    if poison:  # slots that were poisoned stay poisoned: NaN scales and k_R
+        cache["scale"].reshape(-1)[~finite] = np.nan
+    inp.kv_dtype = "nvfp4"
+    inp.c8 = torch.from_numpy(cache["c4"])
+    inp.kv_scale = torch.from_numpy(cache["scale"])
+    inp.kr = torch.from_numpy(cache["kr"].view(np.int16)).view(torch.bfloat16)
+    inp.pool = None
+    return inp
+
+
+def _nvfp4_rows_f64(inp, b: int) -> tuple:
+    S = int(inp.seq_lens[b])
+    cs, rs = [], []
+    for t in range(S):
+        page, slot = int(inp.block_table[b, t // 64]), t % 64
+        cs.append(_nvfp4_deq(inp.c8[page, slot].numpy(), float(inp.kv_scale[page, slot])))
+        rs.append(inp.kr[page, slot].to(torch.float64).numpy())
+    return np.stack(cs), np.stack(rs)
+
+
+def check_nvfp4_cache_closed_forms():
+    """With an NVFP4 cache (values through the format table and torch's e4m3): S = 1 gives
+    W_UV[h] c_0, zero queries give W_UV[h] mean(c), and the absorbed path equals the naive one."""
+    inp = nvfp4_inputs((1, 1), seed=21)
+    heads = [0, 7, 127]
+    out = oracle.decode_naive(inp, softmax_scale=SCALE, heads=heads)
+    wv = _f64(inp.w_uv)
+    for b in range(2):
+        c, _ = _nvfp4_rows_f64(inp, b)
+        for i, h in enumerate(heads):
+            assert np.allclose(out[b, i], wv[h] @ c[0], rtol=1e-12, atol=1e-13), (b, h)
+    inp = nvfp4_inputs((70, 3), seed=22)
+    inp.q_c = torch.zeros_like(inp.q_c)
+    inp.q_r = torch.zeros_like(inp.q_r)
+    out = oracle.decode_naive(inp, softmax_scale=SCALE, heads=heads)
+    wv = _f64(inp.w_uv)
+    for b in range(2):
+        c, _ = _nvfp4_rows_f64(inp, b)
+        for i, h in enumerate(heads):
+            assert np.allclose(out[b, i], wv[h] @ c.mean(axis=0), rtol=1e-11, atol=1e-13), (b, h)
+    inp = nvfp4_inputs((1, 65, 130), seed=23)
+    hs = list(range(0, 128, 9))
+    naive = oracle.decode_naive(inp, softmax_scale=SCALE, heads=hs)
+    _, _, _, absorbed = oracle.decode_absorbed(inp, softmax_scale=SCALE)
+    assert _rel(absorbed[:, hs, :], naive) < 1e-12
+
+
+ALL_CHECKS += [check_e2m1_values, check_e2m1_encode_rule, check_nvfp4_quantize_rule, check_nvfp4_cache_closed_forms]

@@ -56,6 +56,24 @@ MUTANTS = {
     "append_fp8_kr_shifted": ("kr[slot * DR + j] = r[j];", "kr[slot * DR + j] = r[(j + 1) % DR];"),
     "append_bad_slot_unreported": ("status = -1;\n            continue;", "status = 0;\n            continue;"),
     "bf16_widening_wrong": ("uint32_t u = (uint32_t)bits << 16;", "uint32_t u = ((uint32_t)bits << 16) | 0x8000u;"),
+    # NVFP4 (e2m1 codes with e4m3 block scales)
+    "e2m1_subnormal_quarter": ("const double mag = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);",
+                               "const double mag = e == 0 ? 0.25 * m : ldexp(1.0 + 0.5 * m, e - 1);"),
+    "e2m1_bias_off_by_one": ("const double mag = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);",
+                             "const double mag = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 2);"),
+    "e2m1_ties_away": ("if (gap_above < gap_below || (gap_above == gap_below && (k & 1)))",
+                       "if (gap_above <= gap_below)"),
+    "e2m1_no_saturation": ("if (a >= 6.0) return sign | 0x7;", "if (a >= 7.0) return sign | 0x7;"),
+    "nvfp4_sigma_without_six": ("const float sigma = amax > 0.0f ? amax / 2688.0f : 1.0f;",
+                                "const float sigma = amax > 0.0f ? amax / 448.0f : 1.0f;"),
+    "nvfp4_nibbles_swapped": ("const uint8_t code = (i & 1) ? (uint8_t)(row[i / 2] >> 4) : (uint8_t)(row[i / 2] & 0x0F);",
+                              "const uint8_t code = (i & 1) ? (uint8_t)(row[i / 2] & 0x0F) : (uint8_t)(row[i / 2] >> 4);"),
+    "nvfp4_block_of_32": ("ckv[i] = oracle_e2m1_value(code) * oracle_e4m3_value(bs[i / 16]) * sigma;",
+                          "ckv[i] = oracle_e2m1_value(code) * oracle_e4m3_value(bs[i / 32]) * sigma;"),
+    "nvfp4_block_scale_ignored": ("ckv[i] = oracle_e2m1_value(code) * oracle_e4m3_value(bs[i / 16]) * sigma;",
+                                  "ckv[i] = oracle_e2m1_value(code) * sigma;"),
+    "nvfp4_block_scale_not_divided_by_six": ("const uint8_t s8 = oracle_e4m3_encode((bmax / sigma) / 6.0f);",
+                                             "const uint8_t s8 = oracle_e4m3_encode(bmax / sigma);"),
 }
 
 
