@@ -60,7 +60,11 @@ typedef enum mla_status {
 
 typedef enum mla_kv_dtype {
     MLA_KV_BF16 = 0,     /* one bf16 pool [pages][64][576]: c_KV (512) then k_R (64) per row */
-    MLA_KV_FP8_E4M3 = 1  /* c_KV as e4m3 codes [pages][64][512], fp32 scale [pages][64], k_R bf16 [pages][64][64] */
+    MLA_KV_FP8_E4M3 = 1, /* c_KV as e4m3 codes [pages][64][512], fp32 scale [pages][64], k_R bf16 [pages][64][64] */
+    MLA_KV_NVFP4 = 2     /* c_KV as NVFP4 rows [pages][64][288] (256 bytes of e2m1 codes, two per byte with
+                            value 2j in the low nibble of byte j, then 32 e4m3 scales, one per 16 values),
+                            fp32 scale [pages][64], k_R bf16 [pages][64][64].  Written by mla_append_kv;
+                            the decode calls return MLA_ERR_UNSUPPORTED for it */
 } mla_kv_dtype;
 
 /* Bits of the device error word. */

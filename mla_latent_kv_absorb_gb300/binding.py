@@ -22,7 +22,8 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmla_gb30
 MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_ALIGNMENT, MLA_ERR_UNSUPPORTED = 0, 1, 2, 3
 MLA_ERR_WORKSPACE, MLA_ERR_CUDA, MLA_ERR_DEVICE_FAULT = 4, 5, 6
 # mla_kv_dtype
-MLA_KV_BF16, MLA_KV_FP8_E4M3 = 0, 1
+MLA_KV_BF16, MLA_KV_FP8_E4M3, MLA_KV_NVFP4 = 0, 1, 2
+NVFP4_ROW = D_C // 2 + D_C // 16  # bytes of one token's NVFP4 row: packed e2m1 codes, then e4m3 block scales
 # device error bits
 MLA_DEVERR_BAD_PAGE, MLA_DEVERR_TIMEOUT, MLA_DEVERR_SMEM_ALIGN, MLA_DEVERR_BAD_PLAN = 1, 2, 4, 8
 
@@ -206,18 +207,7 @@ def mla_decode_paged(info: PlanInfo, plan_dev: torch.Tensor, q_abs: torch.Tensor
     _need(dev_error, "dev_error", torch.int32, (1,))
     if block_table.dim() != 2 or block_table.shape[0] != B:
         raise ValueError("block_table must be [batch, max_pages]")
-    if kv_scale is None:
-        _need(kv_pool, "kv_pool", torch.bfloat16)
-        if kv_pool.dim() != 3 or tuple(kv_pool.shape[1:]) != (PAGE, D_ROW):
-            raise ValueError("bf16 kv_pool must be [pages, 64, 576]")
-        dtype = MLA_KV_BF16
-    else:
-        _need(kv_pool, "kv_pool (e4m3 codes)", torch.uint8)
-        if kv_pool.dim() != 3 or tuple(kv_pool.shape[1:]) != (PAGE, D_C):
-            raise ValueError("fp8 kv_pool must be [pages, 64, 512]")
-        _need(kv_scale, "kv_scale", torch.float32, (kv_pool.shape[0], PAGE))
-        _need(kr_pool, "kr_pool", torch.bfloat16, (kv_pool.shape[0], PAGE, D_R))
-        dtype = MLA_KV_FP8_E4M3
+    dtype = _kv_dtype(kv_pool, kv_scale, kr_pool)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = lib().mla_decode_paged(ctypes.byref(info), _ptr(plan_dev), _ptr(q_abs), _ptr(q_r), dtype, _ptr(kv_pool),
                                 _ptr(kv_scale), _ptr(kr_pool), int(kv_pool.shape[0]), _ptr(block_table),
@@ -289,9 +279,13 @@ def _kv_dtype(kv_pool, kv_scale, kr_pool) -> int:
         if kv_pool.dim() != 3 or tuple(kv_pool.shape[1:]) != (PAGE, D_ROW):
             raise ValueError("bf16 kv_pool must be [pages, 64, 576]")
         return MLA_KV_BF16
-    _need(kv_pool, "kv_pool (e4m3 codes)", torch.uint8)
+    _need(kv_pool, "kv_pool (e4m3 codes or NVFP4 rows)", torch.uint8)
+    if kv_pool.dim() == 3 and tuple(kv_pool.shape[1:]) == (PAGE, NVFP4_ROW):
+        _need(kv_scale, "kv_scale", torch.float32, (kv_pool.shape[0], PAGE))
+        _need(kr_pool, "kr_pool", torch.bfloat16, (kv_pool.shape[0], PAGE, D_R))
+        return MLA_KV_NVFP4
     if kv_pool.dim() != 3 or tuple(kv_pool.shape[1:]) != (PAGE, D_C):
-        raise ValueError("fp8 kv_pool must be [pages, 64, 512]")
+        raise ValueError("fp8 kv_pool must be [pages, 64, 512] (NVFP4: [pages, 64, 288])")
     _need(kv_scale, "kv_scale", torch.float32, (kv_pool.shape[0], PAGE))
     _need(kr_pool, "kr_pool", torch.bfloat16, (kv_pool.shape[0], PAGE, D_R))
     return MLA_KV_FP8_E4M3

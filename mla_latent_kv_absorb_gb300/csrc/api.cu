@@ -254,6 +254,7 @@ mla_status check_decode_args(const mla_plan_info* info, const void* plan_dev, co
         return MLA_ERR_INVALID_ARG;
     if (num_pool_pages <= 0 || max_pages_per_seq <= 0 || !(softmax_scale > 0.f) || !std::isfinite(softmax_scale))
         return MLA_ERR_INVALID_ARG;
+    if (kv_dtype == MLA_KV_NVFP4) return MLA_ERR_UNSUPPORTED;  // written by mla_append_kv; no decode kernel reads it
     if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_INVALID_ARG;
     if (kv_dtype == MLA_KV_FP8_E4M3 && (!kv_scale || !kr_pool)) return MLA_ERR_INVALID_ARG;
     if (!aligned16(plan_dev) || !aligned16(q_abs) || !aligned16(q_r) || !aligned16(kv_pool) || !aligned16(o_lat) ||

@@ -242,6 +242,21 @@ def test_append_rejects_bad_args(L):
     assert call(s=_p(0x30002)) == binding.MLA_ERR_ALIGNMENT
     assert call(dtype=fp8, kr=_p(0x60008)) == binding.MLA_ERR_ALIGNMENT
     assert call(dtype=fp8, scale=_p(0x50002)) == binding.MLA_ERR_ALIGNMENT
+    nv = binding.MLA_KV_NVFP4
+    assert call(dtype=nv, scale=None) == binding.MLA_ERR_INVALID_ARG
+    assert call(dtype=nv, kr=None) == binding.MLA_ERR_INVALID_ARG
+    assert call(dtype=nv, pool=_p(0x40008)) == binding.MLA_ERR_ALIGNMENT
+    assert call(dtype=nv, kr=_p(0x60008)) == binding.MLA_ERR_ALIGNMENT
+
+
+def test_decode_rejects_nvfp4_cache(L):
+    """The NVFP4 cache is written by mla_append_kv; the decode entry points report it unsupported."""
+    plan, info = _info()
+    p = _p
+    st = L.mla_decode_paged(ctypes.byref(info), p(0x20000), p(0x10000), p(0x30000), binding.MLA_KV_NVFP4,
+                            p(0x40000), p(0x50000), p(0x60000), 100, p(0x60000), 80, ctypes.c_float(0.07),
+                            p(0x90000), info.workspace_bytes, p(0x70000), p(0x80000), p(0x50000), None)
+    assert st == binding.MLA_ERR_UNSUPPORTED
 
 
 def test_append_binding_checks_tensors():

@@ -130,3 +130,54 @@ def test_append_then_decode_step():
     torch.cuda.synchronize()
     assert step.device_error() == 0
     assert torch.equal(out, ref)
+
+
+def _nvfp4_tokens(n: int, seed: int):
+    """Like _tokens, plus NVFP4 cases: rows with zero blocks, a block far below the token's
+    maximum (its scale rounds to a subnormal e4m3 or to zero), and a lone outlier."""
+    c, r = _tokens(n, seed)
+    if n >= 8:
+        g = torch.Generator().manual_seed(seed + 1)
+        x = torch.randn(4, 512, generator=g)
+        x[0, 32:64] = 0.0                          # two zero blocks
+        x[1, 0] = 1e4                              # one outlier: the other blocks' scales shrink
+        x[2, 16:32] *= 1e-9                        # a block whose scale rounds to zero
+        x[3, :16] = -0.0
+        c[-4:] = x.to(torch.bfloat16)
+    return c, r
+
+
+@pytest.mark.parametrize("n", [1, 13, 300])
+def test_append_nvfp4_matches_oracle(n):
+    c, r = _nvfp4_tokens(n, seed=200 + n)
+    slots = _slots(n, seed=200 + n)
+    g = torch.Generator().manual_seed(97)
+    rows0 = torch.randint(0, 256, (PAGES, 64, binding.NVFP4_ROW), generator=g, dtype=torch.uint8)
+    sc0 = torch.rand(PAGES, 64, generator=g)
+    kr0 = torch.randn(PAGES, 64, 64, generator=g).to(torch.bfloat16)
+    ref = {"c4": rows0.numpy().copy(), "scale": sc0.numpy().copy(), "kr": _u16(kr0).copy()}
+    assert oracle.append_kv(c, r, slots, ref) == 0
+    rows, sc, kr = rows0.to(DEV), sc0.to(DEV), kr0.to(DEV)
+    assert _append(c, r, slots, kv_pool=rows, kv_scale=sc, kr_pool=kr) == 0
+    got = rows.cpu().numpy()
+    bad = np.argwhere(got != ref["c4"])
+    assert bad.size == 0, f"{len(bad)} bytes differ, first at {bad[:3].tolist()}"
+    assert np.array_equal(sc.cpu().numpy().view(np.uint32), ref["scale"].view(np.uint32))
+    assert np.array_equal(_u16(kr.cpu()), ref["kr"])
+
+
+def test_nvfp4_cache_is_rejected_by_the_decode():
+    """No decode kernel reads the NVFP4 cache yet: the decode call says so on the host."""
+    inp = synth.make_inputs([100], seed=5)
+    q_abs = torch.zeros(1, 128, 512, dtype=torch.bfloat16, device=DEV)
+    plan, info = binding.mla_plan_splits(inp.seq_lens, binding.num_sms())
+    rows = torch.zeros(inp.num_pool_pages, 64, binding.NVFP4_ROW, dtype=torch.uint8, device=DEV)
+    with pytest.raises(binding.MlaError) as e:
+        binding.mla_decode_paged(info, torch.from_numpy(plan).to(DEV), q_abs, inp.q_r.to(DEV), kv_pool=rows,
+                                 kv_scale=torch.ones(inp.num_pool_pages, 64, device=DEV),
+                                 kr_pool=torch.zeros(inp.num_pool_pages, 64, 64, dtype=torch.bfloat16, device=DEV),
+                                 block_table=torch.from_numpy(inp.block_table).to(DEV),
+                                 o_lat=torch.empty(1, 128, 512, dtype=torch.bfloat16, device=DEV),
+                                 lse=torch.empty(1, 128, device=DEV), dev_error=torch.zeros(1, dtype=torch.int32,
+                                                                                            device=DEV))
+    assert e.value.status == binding.MLA_ERR_UNSUPPORTED
