@@ -63,8 +63,8 @@ typedef enum mla_kv_dtype {
     MLA_KV_FP8_E4M3 = 1, /* c_KV as e4m3 codes [pages][64][512], fp32 scale [pages][64], k_R bf16 [pages][64][64] */
     MLA_KV_NVFP4 = 2     /* c_KV as NVFP4 rows [pages][64][288] (256 bytes of e2m1 codes, two per byte with
                             value 2j in the low nibble of byte j, then 32 e4m3 scales, one per 16 values),
-                            fp32 scale [pages][64], k_R bf16 [pages][64][64].  Written by mla_append_kv;
-                            the decode calls return MLA_ERR_UNSUPPORTED for it */
+                            fp32 scale [pages][64], k_R bf16 [pages][64][64].  Written by mla_append_kv,
+                            read by mla_gather_kv; the decode calls return MLA_ERR_UNSUPPORTED for it */
 } mla_kv_dtype;
 
 /* Bits of the device error word. */
@@ -258,6 +258,28 @@ MLA_API mla_status mla_merge_out_proj(const mla_plan_info* info, const void* pla
 MLA_API mla_status mla_append_kv(int32_t num_tokens, const void* c_kv, const void* k_r, const int32_t* slots,
                                  mla_kv_dtype kv_dtype, int32_t num_pool_pages, void* kv_pool, float* kv_scale,
                                  void* kr_pool, uint32_t* dev_error, void* stream);
+
+/* ---------------------------------------------------------------- gather: paged cache -> contiguous rows
+ *
+ * P1's "NVFP4 quantized gather" (table of contents; section 5 on reading packed fp4 pages with
+ * 16-byte vector loads): every sequence's cache rows, in logical order, out of the paged pool into
+ * one contiguous bf16 array, dequantised on the way, for consumers that want whole rows.
+ *   kv_dtype, kv_pool, kv_scale, kr_pool, num_pool_pages   the cache, as for mla_decode_paged
+ *                     (kv_pool 16-byte aligned), or MLA_KV_NVFP4 as for mla_append_kv
+ *   block_table       device int32 [batch][max_pages_per_seq]
+ *   seq_lens          device int32 [batch], each <= max_pages_per_seq * 64
+ *   cu_seqlens        device int32 [batch + 1]: row offsets, cu_seqlens[b + 1] = cu_seqlens[b] + seq_lens[b]
+ *   out               device bf16 [cu_seqlens[batch]][576], 16-byte aligned: c_KV then k_R per row
+ *   dev_error         device uint32 word: MLA_DEVERR_BAD_PAGE for an entry outside the pool
+ *                     (that row is not written)
+ * bf16 cache: the stored bits.  FP8 cache: each latent value is float(code) * sigma in fp32 (one
+ * rounding), then rounded to bf16 (nearest, ties to even).  NVFP4 cache: float(e2m1 code) *
+ * float(e4m3 block scale) (exact) * sigma in fp32 (one rounding), then to bf16.  k_R is copied.
+ * One warp per token; a streaming copy (at most 1152 bytes written per token). */
+MLA_API mla_status mla_gather_kv(mla_kv_dtype kv_dtype, const void* kv_pool, const float* kv_scale,
+                                 const void* kr_pool, int32_t num_pool_pages, const int32_t* block_table,
+                                 int32_t max_pages_per_seq, const int32_t* seq_lens, const int32_t* cu_seqlens,
+                                 int32_t batch, void* out, uint32_t* dev_error, void* stream);
 
 /* ---------------------------------------------------------------- decode + merge, no allocation
  *

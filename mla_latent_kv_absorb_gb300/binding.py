@@ -52,7 +52,7 @@ class PlanInfo(ctypes.Structure):
 EXPORTS = ("mla_status_string", "mla_last_error_string", "mla_plan_bytes_max", "mla_plan_splits", "mla_absorb_q", "mla_decode_paged",
            "mla_combine_splits", "mla_out_proj", "mla_read_device_error", "mla_debug_wait_timeout",
            "mla_decode_paged_static_ws", "mla_decode_step_host", "mla_append_kv", "mla_merge_out_proj",
-           "mla_absorb_decode_paged")
+           "mla_absorb_decode_paged", "mla_gather_kv")
 
 # capacity of the library's fixed split-partial array (mla_decode_paged_static_ws)
 MLA_STATIC_WS_MAX_PARTIALS = 128
@@ -102,6 +102,8 @@ def lib() -> ctypes.CDLL:
     L.mla_absorb_decode_paged.restype = ctypes.c_int
     L.mla_absorb_decode_paged.argtypes = [ctypes.POINTER(PlanInfo), P, P, P, P, P, P, ctypes.c_int, P, P, P, i32, P,
                                           i32, ctypes.c_float, P, sz, P, P, P, P]
+    L.mla_gather_kv.restype = ctypes.c_int
+    L.mla_gather_kv.argtypes = [ctypes.c_int, P, P, P, i32, P, i32, P, P, i32, P, P, P]
     L.mla_merge_out_proj.restype = ctypes.c_int
     L.mla_merge_out_proj.argtypes = [ctypes.POINTER(PlanInfo), P, P, sz, P, P, P, P, P, P]
     L.mla_decode_step_host.restype = ctypes.c_int
@@ -335,6 +337,29 @@ def mla_append_kv(c_kv: torch.Tensor, k_r: torch.Tensor, slots: torch.Tensor, *,
     st = lib().mla_append_kv(n, _ptr(c_kv), _ptr(k_r), _ptr(slots), dtype, int(kv_pool.shape[0]), _ptr(kv_pool),
                              _ptr(kv_scale), _ptr(kr_pool), _ptr(dev_error), _stream(stream))
     _check("mla_append_kv", st)
+
+
+def mla_gather_kv(*, kv_pool: torch.Tensor, block_table: torch.Tensor, seq_lens: torch.Tensor,
+                  cu_seqlens: torch.Tensor, out: torch.Tensor, dev_error: torch.Tensor,
+                  kv_scale: Optional[torch.Tensor] = None, kr_pool: Optional[torch.Tensor] = None,
+                  stream=None) -> None:
+    """Every sequence's cache rows in logical order into out [total, 576] (bf16), dequantised
+    from an FP8 or NVFP4 cache; cu_seqlens [B + 1] gives each sequence's first row."""
+    dtype = _kv_dtype(kv_pool, kv_scale, kr_pool)
+    _need(block_table, "block_table", torch.int32)
+    B = int(seq_lens.shape[0])
+    _need(seq_lens, "seq_lens", torch.int32, (B,))
+    _need(cu_seqlens, "cu_seqlens", torch.int32, (B + 1,))
+    _need(out, "out", torch.bfloat16)
+    _need(dev_error, "dev_error", torch.int32, (1,))
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be [batch, max_pages]")
+    if out.dim() != 2 or out.shape[1] != D_ROW:
+        raise ValueError("out must be [total tokens, 576]")
+    st = lib().mla_gather_kv(dtype, _ptr(kv_pool), _ptr(kv_scale), _ptr(kr_pool), int(kv_pool.shape[0]),
+                             _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens), _ptr(cu_seqlens), B,
+                             _ptr(out), _ptr(dev_error), _stream(stream))
+    _check("mla_gather_kv", st)
 
 
 def mla_read_device_error(dev_error: torch.Tensor, stream=None) -> int:

@@ -30,7 +30,7 @@ def _nvcc() -> str:
 
 
 def _sources():
-    return [os.path.join(CSRC, f) for f in ("api.cu", "static_ws.cu", "append.cu", "plan.cpp")]
+    return [os.path.join(CSRC, f) for f in ("api.cu", "static_ws.cu", "append.cu", "gather.cu", "plan.cpp")]
 
 
 def _deps():

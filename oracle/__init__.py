@@ -87,6 +87,8 @@ def _load(path: str):
     L.oracle_e2m1_encode_many.argtypes = [P, i64, P]
     L.oracle_quantize_token_nvfp4.restype = ctypes.c_float
     L.oracle_quantize_token_nvfp4.argtypes = [P, P]
+    L.oracle_gather_kv.restype = i32
+    L.oracle_gather_kv.argtypes = [i32, P, P, i32, P, i32, i32, P, P, P, P, P]
     L.oracle_append_kv.restype = i32
     L.oracle_append_kv.argtypes = [i32, P, P, P, i32, i32, P, P, P, P]
     return L
@@ -283,6 +285,22 @@ def quantize_token(c) -> tuple:
     codes = np.empty(D_C, dtype=np.uint8)
     sigma = lib().oracle_quantize_token(_p(c), _p(codes))
     return codes, np.float32(sigma)
+
+
+def gather_kv(inp) -> tuple:
+    """Every sequence's cache rows, in logical order, as one contiguous bf16 array (uint16 bits)
+    [total tokens, 576], with the row offsets cu_seqlens [B + 1]: the stored bits of a bf16 cache;
+    for FP8 and NVFP4 caches each latent value formed in fp32 (code times scales, one rounding)
+    and rounded to bf16."""
+    sl = _arr(inp.seq_lens, np.int32)
+    cu = np.zeros(inp.batch + 1, np.int32)
+    cu[1:] = np.cumsum(sl)
+    out = np.zeros((int(cu[-1]), D_ROW), np.uint16)
+    bt = _arr(inp.block_table, np.int32)
+    rc = lib().oracle_gather_kv(inp.batch, _p(sl), _p(bt), inp.max_pages, _p(cu), *_Cache(inp).args(), _p(out))
+    if rc != 0:
+        raise ValueError("block table entry out of range")
+    return out, cu
 
 
 def append_kv(c_kv, k_r, slots, cache: dict) -> int:

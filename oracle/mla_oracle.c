@@ -480,6 +480,62 @@ float oracle_quantize_token_nvfp4(const uint16_t* c, uint8_t* row)
     return sigma;
 }
 
+/* The bf16 nearest a float, ties to even (NaN stays a quiet NaN): keep the top 16 bits after
+ * adding half of the dropped part's range, plus one when the kept part is odd. */
+static uint16_t bf16_rne(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) return (uint16_t)((u >> 16) | 0x0040u);
+    return (uint16_t)((u + 0x7FFFu + ((u >> 16) & 1u)) >> 16);
+}
+
+/*
+ * Gather (page 1, the "NVFP4 quantized gather" of the table of contents and section 5): the
+ * rows of each sequence, in logical order, out of the paged cache into one contiguous bf16
+ * array out[cu_seqlens[b] + t][576] (c_KV then k_R).  bf16 cache: the stored bits.  FP8 cache:
+ * each latent value is float(e4m3 code) * sigma in fp32 (one rounding), then rounded to bf16.
+ * NVFP4 cache: float(e2m1 code) * float(e4m3 block scale) (exact) * sigma in fp32 (one rounding),
+ * then to bf16.  k_R is copied.  Returns -1 if a block-table entry is out of range (that row
+ * is left untouched), else 0.
+ */
+int oracle_gather_kv(int B, const int32_t* seq_lens, const int32_t* block_table, int max_pages,
+                     const int32_t* cu_seqlens, int kv_fp8, int num_pages, const uint16_t* pool,
+                     const uint8_t* c8, const float* scale, const uint16_t* kr, uint16_t* out)
+{
+    int status = 0;
+    for (int b = 0; b < B; ++b) {
+        for (int64_t t = 0; t < seq_lens[b]; ++t) {
+            const int64_t page = block_table[(int64_t)b * max_pages + t / PG];
+            if (page < 0 || page >= num_pages) {
+                status = -1;
+                continue;
+            }
+            const int64_t tok = page * PG + (t % PG);
+            uint16_t* dst = out + ((int64_t)cu_seqlens[b] + t) * DROW;
+            if (kv_fp8 == 0) {
+                memcpy(dst, pool + tok * DROW, DROW * sizeof(uint16_t));
+                continue;
+            }
+            const float sigma = scale[tok];
+            if (kv_fp8 == 1) {
+                const uint8_t* row = c8 + tok * DC;
+                for (int i = 0; i < DC; ++i) dst[i] = bf16_rne((float)oracle_e4m3_value(row[i]) * sigma);
+            } else {
+                const uint8_t* row = c8 + tok * NV_ROW;
+                for (int i = 0; i < DC; ++i) {
+                    const uint8_t byte = row[i >> 1];
+                    const uint8_t e2 = (i & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xF);
+                    const float v = (float)oracle_e2m1_value(e2) * (float)oracle_e4m3_value(row[NV_CODES + i / 16]);
+                    dst[i] = bf16_rne(v * sigma);
+                }
+            }
+            memcpy(dst + DC, kr + tok * DR, DR * sizeof(uint16_t));
+        }
+    }
+    return status;
+}
+
 /*
  * Write n tokens into the paged cache (page 1 section 1: one row of c_KV and k_R per token;
  * section 3: 64-token pages).  Token i goes to slot slots[i] = page * 64 + row; a negative slot

@@ -671,3 +671,46 @@ def check_nvfp4_cache_closed_forms():
 
 
 ALL_CHECKS += [check_e2m1_values, check_e2m1_encode_rule, check_nvfp4_quantize_rule, check_nvfp4_cache_closed_forms]
+
+
+def _bf16_bits_of_f32(x: np.ndarray) -> np.ndarray:
+    """bf16 nearest to float32 values (torch's conversion: ties to even), as uint16 bits."""
+    return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(
+        np.uint16)
+
+
+def check_gather_kv():
+    """The gathered rows, in logical order: the stored bits of a bf16 cache; for FP8,
+    bf16(float32(e4m3 value) * sigma); for NVFP4, bf16(float32(e2m1 value * e4m3 block scale) *
+    sigma), each value formed with torch's e4m3 decoding and conversions (library routines) and
+    numpy float32 products; k_R copied; row offsets the cumulative lengths."""
+    for kind in ("bf16", "fp8_e4m3", "nvfp4"):
+        inp = nvfp4_inputs((3, 64, 130), seed=31) if kind == "nvfp4" else tiny_inputs((3, 64, 130), seed=31,
+                                                                                       kv_dtype=kind)
+        out, cu = oracle.gather_kv(inp)
+        assert list(cu) == [0, 3, 67, 197]
+        for b in range(inp.batch):
+            for t in range(int(inp.seq_lens[b])):
+                page, slot = int(inp.block_table[b, t // 64]), t % 64
+                got = out[cu[b] + t]
+                if kind == "bf16":
+                    want = inp.pool[page, slot].contiguous().view(torch.int16).numpy().view(np.uint16)
+                    assert np.array_equal(got, want), (kind, b, t)
+                    continue
+                sigma = np.float32(inp.kv_scale[page, slot])
+                if kind == "fp8_e4m3":
+                    vals = _e4m3_values(inp.c8[page, slot].numpy()).astype(np.float32)
+                else:
+                    row = inp.c8[page, slot].numpy()
+                    codes = np.empty(512, np.uint8)
+                    codes[0::2] = row[:256] & 0xF
+                    codes[1::2] = row[:256] >> 4
+                    vals = (E2M1_TABLE[codes].astype(np.float32) *
+                            np.repeat(_e4m3_values(row[256:288]).astype(np.float32), 16)).astype(np.float32)
+                want = _bf16_bits_of_f32((vals * sigma).astype(np.float32))
+                assert np.array_equal(got[:512], want), (kind, b, t)
+                assert np.array_equal(got[512:], inp.kr[page, slot].contiguous().view(torch.int16).numpy().view(
+                    np.uint16)), (kind, b, t)
+
+
+ALL_CHECKS += [check_gather_kv]

@@ -249,6 +249,28 @@ def test_append_rejects_bad_args(L):
     assert call(dtype=nv, kr=_p(0x60008)) == binding.MLA_ERR_ALIGNMENT
 
 
+def test_gather_rejects_bad_args(L):
+    G = L.mla_gather_kv
+    ok = dict(pool=_p(0x40000), scale=_p(0x50000), kr=_p(0x60000), bt=_p(0x10000), sl=_p(0x20000),
+              cu=_p(0x30000), out=_p(0x70000), err=_p(0x80000))
+
+    def call(dtype=binding.MLA_KV_BF16, pages=8, maxp=4, batch=2, **kw):
+        a = {**ok, **kw}
+        return G(dtype, a["pool"], a["scale"], a["kr"], pages, a["bt"], maxp, a["sl"], a["cu"], batch, a["out"],
+                 a["err"], None)
+
+    assert call(dtype=9) == binding.MLA_ERR_INVALID_ARG
+    assert call(batch=0) == binding.MLA_ERR_INVALID_ARG
+    assert call(pages=0) == binding.MLA_ERR_INVALID_ARG
+    assert call(out=None) == binding.MLA_ERR_INVALID_ARG
+    assert call(dtype=binding.MLA_KV_NVFP4, scale=None) == binding.MLA_ERR_INVALID_ARG
+    assert call(dtype=binding.MLA_KV_FP8_E4M3, kr=None) == binding.MLA_ERR_INVALID_ARG
+    assert call(pool=_p(0x40008)) == binding.MLA_ERR_ALIGNMENT
+    assert call(out=_p(0x70008)) == binding.MLA_ERR_ALIGNMENT
+    assert call(cu=_p(0x30002)) == binding.MLA_ERR_ALIGNMENT
+    assert call(batch=70000) == binding.MLA_ERR_UNSUPPORTED
+
+
 def test_decode_rejects_nvfp4_cache(L):
     """The NVFP4 cache is written by mla_append_kv; the decode entry points report it unsupported."""
     plan, info = _info()

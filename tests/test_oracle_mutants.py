@@ -72,6 +72,14 @@ MUTANTS = {
                           "ckv[i] = oracle_e2m1_value(code) * oracle_e4m3_value(bs[i / 32]) * sigma;"),
     "nvfp4_block_scale_ignored": ("ckv[i] = oracle_e2m1_value(code) * oracle_e4m3_value(bs[i / 16]) * sigma;",
                                   "ckv[i] = oracle_e2m1_value(code) * sigma;"),
+    "gather_fp8_scale_ignored": ("dst[i] = bf16_rne((float)oracle_e4m3_value(row[i]) * sigma);",
+                                 "dst[i] = bf16_rne((float)oracle_e4m3_value(row[i]));"),
+    "gather_nvfp4_nibbles_swapped": ("const uint8_t e2 = (i & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xF);",
+                                     "const uint8_t e2 = (i & 1) ? (uint8_t)(byte & 0xF) : (uint8_t)(byte >> 4);"),
+    "gather_bf16_truncates": ("return (uint16_t)((u + 0x7FFFu + ((u >> 16) & 1u)) >> 16);",
+                              "return (uint16_t)(u >> 16);"),
+    "gather_rows_shifted": ("uint16_t* dst = out + ((int64_t)cu_seqlens[b] + t) * DROW;",
+                            "uint16_t* dst = out + ((int64_t)cu_seqlens[b] + (t + 1) % seq_lens[b]) * DROW;"),
     "nvfp4_block_scale_not_divided_by_six": ("const uint8_t s8 = oracle_e4m3_encode((bmax / sigma) / 6.0f);",
                                              "const uint8_t s8 = oracle_e4m3_encode(bmax / sigma);"),
 }
