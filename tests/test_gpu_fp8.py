@@ -117,8 +117,9 @@ def test_fp8_zero_and_wide_scales():
 def test_fp8_sharp_softmax_rescales():
     """Queries scaled by 8: scores with a spread of about 8 nats, so the running max moves past the
     rescale threshold often and P~ spans the whole e4m3 range.  (The error grows with the spread:
-    k_R / sigma is rounded to bf16 for the RoPE MMA, 2^-9 per value; at a spread of 16 nats the
-    largest output error reaches about 0.06.)"""
+    the kernel holds each query row as an e4m3 hi/lo pair, about 2^-8 relative per value, so the
+    score noise scales with the size of the dot products; at a spread of 16 nats it reaches about
+    0.025 nats and the largest output error about 0.06.  k_R / sigma in bf16 adds far less.)"""
     inp = synth.make_inputs([1500, 300], seed=813, kv_dtype="fp8_e4m3", poison_tail=True)
     inp.q_c = (inp.q_c.float() * 8).to(torch.bfloat16)
     inp.q_r = (inp.q_r.float() * 8).to(torch.bfloat16)
