@@ -13,12 +13,16 @@
  * Conventions shared by every entry point
  *   - Pointers marked "device" are CUDA device pointers; "host" pointers are ordinary memory.
  *   - bf16 tensors are passed as void* and are contiguous, row-major, in the shapes stated.
- *   - The caller allocates and owns every buffer, workspaces included.  The library calls no
- *     allocator.  Its only global mutable state is the fixed device array behind
+ *   - The caller allocates and owns every buffer, workspaces included.  The library allocates
+ *     no device memory for data; the one exception to "no allocation" is
+ *     mla_step_graph_create, whose handle holds a host object and a CUDA graph until
+ *     mla_step_graph_destroy.  Its only global mutable state is the fixed device array behind
  *     mla_decode_paged_static_ws (and that call's per-device address cache); every other call
  *     is safe from several host threads.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only enqueue work and
- *     return; results are ready when the stream reaches them.
+ *     return; results are ready when the stream reaches them.  The exceptions, which wait for
+ *     the stream: mla_decode_step_host, mla_step_graph_create and mla_step_graph_run with
+ *     `wait` set (and mla_read_device_error).
  *   - Arguments, shapes, alignment and workspace sizes are checked on the host before any
  *     launch; a failed check returns an error and enqueues nothing.  A failed launch returns
  *     MLA_ERR_CUDA.  Problems only the GPU can see (a block-table entry outside the pool, a
@@ -363,6 +367,37 @@ MLA_API mla_status mla_decode_step_host(const int32_t* seq_lens, int32_t batch, 
                                         const void* kv_pool, const float* kv_scale, const void* kr_pool,
                                         int32_t num_pool_pages, float softmax_scale, const mla_step_buffers* bufs,
                                         void* out_host, mla_plan_info* info_out, void* stream);
+
+/* ---- the step from host memory as a captured CUDA graph ------------------------------------
+ * For a run of steps with unchanged sequence lengths (and the same host and device buffers):
+ * mla_step_graph_create does what mla_decode_step_host does up to the launches -- the same
+ * arguments, checks and plan -- then copies the plan to the device once (on `stream`, waiting
+ * for it) and captures, on a stream of its own, the per-step work as one CUDA graph: the block
+ * table (when block_table_host is not NULL) and query copies to the device, absorb, decode,
+ * merge, out-proj and the copy of `out` back to out_host.  Each mla_step_graph_run launches that
+ * graph on `stream` (any stream of the device the graph was made on) and, when `wait` is
+ * non-zero, waits for it; every launch reads the host buffers as they are at that time, so the
+ * caller writes the next step's queries (and table) into the same buffers between runs.
+ * Lengths or buffers that change need a new graph: the plan, the grid sizes and every pointer
+ * are fixed in it.
+ *   q_c_host, q_r_host, out_host, block_table_host: page-locked host memory (cudaHostAlloc or
+ *     cudaHostRegister), else MLA_ERR_INVALID_ARG before anything is copied or captured.
+ *   graph_out: receives the handle (NULL on failure); the handle owns host memory and the
+ *     graph, released by mla_step_graph_destroy (NULL is accepted and ignored).
+ * Results are bit-identical to mla_decode_step_host with the same inputs.  Launches of one graph
+ * on different streams, or of two graphs sharing buffers, may overlap and race on the buffers:
+ * order them on one stream.  Device-side errors land in bufs->dev_error. */
+typedef struct mla_step_graph mla_step_graph;
+MLA_API mla_status mla_step_graph_create(const int32_t* seq_lens, int32_t batch, int32_t num_sms,
+                                         const mla_plan_options* opts, const void* q_c_host, const void* q_r_host,
+                                         const int32_t* block_table_host, int32_t max_pages_per_seq,
+                                         const void* w_uk, const void* w_uv, mla_kv_dtype kv_dtype,
+                                         const void* kv_pool, const float* kv_scale, const void* kr_pool,
+                                         int32_t num_pool_pages, float softmax_scale, const mla_step_buffers* bufs,
+                                         void* out_host, mla_plan_info* info_out, void* stream,
+                                         mla_step_graph** graph_out);
+MLA_API mla_status mla_step_graph_run(mla_step_graph* graph, int32_t wait, void* stream);
+MLA_API mla_status mla_step_graph_destroy(mla_step_graph* graph);
 
 /* ---------------------------------------------------------------- device error word
  *

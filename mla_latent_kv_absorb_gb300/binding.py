@@ -52,7 +52,8 @@ class PlanInfo(ctypes.Structure):
 EXPORTS = ("mla_status_string", "mla_last_error_string", "mla_plan_bytes_max", "mla_plan_splits", "mla_absorb_q", "mla_decode_paged",
            "mla_combine_splits", "mla_out_proj", "mla_read_device_error", "mla_debug_wait_timeout",
            "mla_decode_paged_static_ws", "mla_decode_step_host", "mla_append_kv", "mla_merge_out_proj",
-           "mla_absorb_decode_paged", "mla_gather_kv")
+           "mla_absorb_decode_paged", "mla_gather_kv", "mla_step_graph_create", "mla_step_graph_run",
+           "mla_step_graph_destroy")
 
 # capacity of the library's fixed split-partial array (mla_decode_paged_static_ws)
 MLA_STATIC_WS_MAX_PARTIALS = 128
@@ -110,6 +111,14 @@ def lib() -> ctypes.CDLL:
     L.mla_decode_step_host.argtypes = [P, i32, i32, ctypes.POINTER(PlanOptions), P, P, P, i32, P, P, ctypes.c_int, P,
                                        P, P, i32, ctypes.c_float, ctypes.POINTER(StepBuffers), P,
                                        ctypes.POINTER(PlanInfo), P]
+    step_args = [P, i32, i32, ctypes.POINTER(PlanOptions), P, P, P, i32, P, P, ctypes.c_int, P, P, P, i32,
+                 ctypes.c_float, ctypes.POINTER(StepBuffers), P, ctypes.POINTER(PlanInfo), P]
+    L.mla_step_graph_create.restype = ctypes.c_int
+    L.mla_step_graph_create.argtypes = step_args + [ctypes.POINTER(ctypes.c_void_p)]
+    L.mla_step_graph_run.restype = ctypes.c_int
+    L.mla_step_graph_run.argtypes = [P, i32, P]
+    L.mla_step_graph_destroy.restype = ctypes.c_int
+    L.mla_step_graph_destroy.argtypes = [P]
     L.mla_append_kv.restype = ctypes.c_int
     L.mla_append_kv.argtypes = [i32, P, P, P, ctypes.c_int, i32, P, P, P, u32p, P]
     L.mla_read_device_error.restype = ctypes.c_int
@@ -430,6 +439,7 @@ class DecodeStep:
         self.dev_error = torch.zeros(1, dtype=torch.int32, device=self.device)
         self.absorb_sync = torch.zeros(2, dtype=torch.int32, device=self.device)  # absorb-in-decode job counter
         self._h_stage = self._d_stage = None  # pinned host / device staging of run_host
+        self._host_graph = None  # (mla_step_graph handle, key of the buffers and lengths it was made for)
 
     def run(self, q_c: torch.Tensor, q_r: torch.Tensor, stream=None) -> torch.Tensor:
         kv = dict(kv_pool=self.kv_pool, block_table=self.block_table, o_lat=self.o_lat, lse=self.lse,
@@ -448,19 +458,45 @@ class DecodeStep:
             mla_out_proj(self.o_lat, self.w_uv, self.out, stream)
         return self.out
 
+    @staticmethod
+    def _host_key(q_c, q_r, block_table, lens, out):
+        bt = None if block_table is None else (block_table.data_ptr(), tuple(block_table.shape), block_table.dtype)
+        return (lens.tobytes(), q_c.data_ptr(), q_c.numel(), q_c.dtype, q_r.data_ptr(), q_r.numel(), q_r.dtype, bt,
+                out.data_ptr(), out.numel(), out.dtype)
+
+    def _drop_host_graph(self) -> None:
+        if self._host_graph is not None:
+            handle, self._host_graph = self._host_graph[0], None
+            lib().mla_step_graph_destroy(handle)
+
+    def __del__(self):
+        try:
+            self._drop_host_graph()
+        except Exception:
+            pass
+
     def run_host(self, q_c: torch.Tensor, q_r: torch.Tensor, *, block_table: Optional[torch.Tensor] = None,
                  seq_lens=None, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-        """One decode step from host (CPU) tensors, end to end, in one library call
-        (``mla_decode_step_host``): plan on the host for ``seq_lens`` (the lengths given at
-        construction when None; same batch size), copy the plan, the block table (a CPU int32
-        [batch, max_pages] tensor, when given; otherwise the device table given at construction
-        is used) and the queries to the device (asynchronous DMA when they are pinned), run the
-        four kernels, and copy the result into ``out`` (a CPU bf16 [batch, 128, 128] tensor,
-        pinned and allocated once if not given).  Returns ``out`` once the stream is done."""
+        """One decode step from host (CPU) tensors, end to end: plan on the host for ``seq_lens``
+        (the lengths given at construction when None; same batch size), copy the block table (a
+        CPU int32 [batch, max_pages] tensor, when given; otherwise the device table given at
+        construction is used) and the queries to the device, run the four kernels, and copy the
+        result into ``out`` (a CPU bf16 [batch, 128, 128] tensor, pinned and allocated once if not
+        given).  Returns ``out`` once the stream is done.
+
+        When ``out``, the queries and the table are all pinned, the step is captured once as a
+        CUDA graph (``mla_step_graph_create``: the plan is copied to the device at capture) and
+        later calls with the same tensors and lengths only launch it (``mla_step_graph_run``),
+        so a serving loop that writes each step's queries into the same pinned tensors pays for
+        the copies and kernels only.  Otherwise each call is one ``mla_decode_step_host``."""
+        lens = self.seq_lens if seq_lens is None else np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+        if self._host_graph is not None and out is not None:
+            if self._host_key(q_c, q_r, block_table, lens, out) == self._host_graph[1]:
+                _check("mla_step_graph_run", lib().mla_step_graph_run(self._host_graph[0], 1, _stream(stream)))
+                return out
         B = self.batch
         _need(q_c, "q_c", torch.bfloat16, (B, NUM_HEADS, D_HC), device=False)
         _need(q_r, "q_r", torch.bfloat16, (B, NUM_HEADS, D_R), device=False)
-        lens = self.seq_lens if seq_lens is None else np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
         if lens.size != B:
             raise ValueError("run_host: seq_lens must keep the batch size")
         if block_table is not None:
@@ -469,6 +505,7 @@ class DecodeStep:
                 raise ValueError("block_table must be [batch, max_pages]")
         if not np.array_equal(lens, self.seq_lens) or self._h_stage is None:
             # new lengths: size the workspace for their plan (the library plans again itself)
+            self._drop_host_graph()
             self.seq_lens = lens.copy()
             _, info = mla_plan_splits(lens, self._num_sms, **self._plan_opts)
             ws = int(info.workspace_bytes)
@@ -482,9 +519,12 @@ class DecodeStep:
                 self._q_r_dev = torch.empty(B, NUM_HEADS, D_R, dtype=torch.bfloat16, device=self.device)
         if block_table is not None and (getattr(self, "_bt_dev", None) is None or
                                         tuple(self._bt_dev.shape) != tuple(block_table.shape)):
+            self._drop_host_graph()
             self._bt_dev = torch.empty(tuple(block_table.shape), dtype=torch.int32, device=self.device)
         bt_dev = self._bt_dev if block_table is not None else self.block_table
         _check_table_rows(lens, bt_dev)
+        use_graph = out is not None and q_c.is_pinned() and q_r.is_pinned() and out.is_pinned() and \
+            (block_table is None or block_table.is_pinned())
         if out is None:
             out = torch.empty(B, NUM_HEADS, D_HC, dtype=torch.bfloat16).pin_memory()
         _need(out, "out", torch.bfloat16, (B, NUM_HEADS, D_HC), device=False)
@@ -497,13 +537,19 @@ class DecodeStep:
         opts = PlanOptions(int(self._plan_opts["min_pages_per_split"]), int(self._plan_opts["max_clusters"]),
                            int(self._plan_opts["wait_timeout_ns"]), int(self._plan_opts["item_cost_pages"]), 0)
         info = PlanInfo()
-        st = lib().mla_decode_step_host(lens.ctypes.data_as(ctypes.c_void_p), B, self._num_sms, ctypes.byref(opts),
-                                        _ptr(q_c), _ptr(q_r), _ptr(block_table), int(bt_dev.shape[1]),
-                                        _ptr(self.w_uk), _ptr(self.w_uv), dtype, _ptr(self.kv_pool),
-                                        _ptr(self.kv_scale), _ptr(self.kr_pool), int(self.kv_pool.shape[0]),
-                                        float(self.softmax_scale), ctypes.byref(bufs), _ptr(out), ctypes.byref(info),
-                                        _stream(stream))
-        _check("mla_decode_step_host", st)
+        args = (lens.ctypes.data_as(ctypes.c_void_p), B, self._num_sms, ctypes.byref(opts), _ptr(q_c), _ptr(q_r),
+                _ptr(block_table), int(bt_dev.shape[1]), _ptr(self.w_uk), _ptr(self.w_uv), dtype, _ptr(self.kv_pool),
+                _ptr(self.kv_scale), _ptr(self.kr_pool), int(self.kv_pool.shape[0]), float(self.softmax_scale),
+                ctypes.byref(bufs), _ptr(out), ctypes.byref(info), _stream(stream))
+        if use_graph:
+            self._drop_host_graph()
+            handle = ctypes.c_void_p()
+            _check("mla_step_graph_create", lib().mla_step_graph_create(*args, ctypes.byref(handle)))
+            self._host_graph = (handle, self._host_key(q_c, q_r, block_table, lens, out))
+            self.info = info
+            _check("mla_step_graph_run", lib().mla_step_graph_run(handle, 1, _stream(stream)))
+            return out
+        _check("mla_decode_step_host", lib().mla_decode_step_host(*args))
         self.info = info
         return out
 

@@ -488,32 +488,39 @@ extern "C" mla_status mla_debug_wait_timeout(uint32_t* dev_error, int64_t timeou
     return launch_status();
 }
 
-// The whole step from host memory: plan on the host, one asynchronous copy per input, the step's
-// kernels (absorb, decode, merge, projection), the output copy back, one stream synchronisation.
-extern "C" mla_status mla_decode_step_host(const int32_t* seq_lens, int32_t batch, int32_t num_sms,
-                                           const mla_plan_options* opts, const void* q_c_host, const void* q_r_host,
-                                           const int32_t* block_table_host, int32_t max_pages_per_seq,
-                                           const void* w_uk, const void* w_uv, mla_kv_dtype kv_dtype,
-                                           const void* kv_pool, const float* kv_scale, const void* kr_pool,
-                                           int32_t num_pool_pages, float softmax_scale, const mla_step_buffers* bufs,
-                                           void* out_host, mla_plan_info* info_out, void* stream)
+namespace {
+
+// Host checks of the step-from-host entry points, then the plan for seq_lens into
+// bufs->plan_host (nothing is copied or launched here).
+mla_status step_prepare(const int32_t* seq_lens, int32_t batch, int32_t num_sms, const mla_plan_options* opts,
+                        const void* q_c_host, const void* q_r_host, int32_t max_pages_per_seq,
+                        const mla_step_buffers* bufs, const void* out_host, mla_plan_info* info)
 {
-    const mla::NvtxRange nvtx_range("mla_decode_step_host");
     if (!seq_lens || batch <= 0 || !q_c_host || !q_r_host || !bufs || !out_host || !bufs->plan_host ||
         !bufs->plan || !bufs->block_table || max_pages_per_seq <= 0)
         return MLA_ERR_INVALID_ARG;
     for (int32_t b = 0; b < batch; ++b)  // every page of every sequence has a block-table entry
         if (seq_lens[b] > 0 && (seq_lens[b] + 63) / 64 > max_pages_per_seq) return MLA_ERR_INVALID_ARG;
-    const cudaStream_t s = static_cast<cudaStream_t>(stream);
-    mla_plan_info info;
-    mla_status st = mla_plan_splits(seq_lens, batch, num_sms, opts, bufs->plan_host, bufs->plan_capacity, &info);
+    const mla_status st = mla_plan_splits(seq_lens, batch, num_sms, opts, bufs->plan_host, bufs->plan_capacity, info);
     if (st != MLA_OK) return st;
-    if (info_out) *info_out = info;
-    if (info.workspace_bytes > 0 && (!bufs->workspace || bufs->workspace_bytes < (size_t)info.workspace_bytes))
+    if (info->workspace_bytes > 0 && (!bufs->workspace || bufs->workspace_bytes < (size_t)info->workspace_bytes))
         return MLA_ERR_WORKSPACE;
+    return MLA_OK;
+}
+
+// The step's stream work after planning: the plan copy (when copy_plan), the block table and
+// query copies, absorb, decode, merge, projection, and the output copy back.
+mla_status step_enqueue(const mla_plan_info& info, bool copy_plan, const void* q_c_host, const void* q_r_host,
+                        const int32_t* block_table_host, int32_t max_pages_per_seq, const void* w_uk, const void* w_uv,
+                        mla_kv_dtype kv_dtype, const void* kv_pool, const float* kv_scale, const void* kr_pool,
+                        int32_t num_pool_pages, float softmax_scale, const mla_step_buffers* bufs, void* out_host,
+                        cudaStream_t s)
+{
+    const int32_t batch = info.batch;
     const size_t q_c_bytes = (size_t)batch * 128 * 128 * 2, q_r_bytes = (size_t)batch * 128 * 64 * 2;
-    if (record_cuda(cudaMemcpyAsync(bufs->plan, bufs->plan_host, (size_t)info.plan_bytes, cudaMemcpyHostToDevice, s),
-                    "cudaMemcpyAsync(plan)") != MLA_OK)
+    if (copy_plan && record_cuda(cudaMemcpyAsync(bufs->plan, bufs->plan_host, (size_t)info.plan_bytes,
+                                                 cudaMemcpyHostToDevice, s),
+                                 "cudaMemcpyAsync(plan)") != MLA_OK)
         return MLA_ERR_CUDA;
     if (block_table_host &&
         record_cuda(cudaMemcpyAsync(bufs->block_table, block_table_host,
@@ -526,19 +533,160 @@ extern "C" mla_status mla_decode_step_host(const int32_t* seq_lens, int32_t batc
         record_cuda(cudaMemcpyAsync(bufs->q_r, q_r_host, q_r_bytes, cudaMemcpyHostToDevice, s),
                     "cudaMemcpyAsync(q_r)") != MLA_OK)
         return MLA_ERR_CUDA;
-    if ((st = mla_absorb_q(bufs->q_c, w_uk, bufs->q_abs, batch, stream)) != MLA_OK) return st;
+    mla_status st;
+    if ((st = mla_absorb_q(bufs->q_c, w_uk, bufs->q_abs, batch, s)) != MLA_OK) return st;
     if ((st = mla_decode_paged(&info, bufs->plan, bufs->q_abs, bufs->q_r, kv_dtype, kv_pool, kv_scale, kr_pool,
                                num_pool_pages, bufs->block_table, max_pages_per_seq, softmax_scale, bufs->workspace,
-                               bufs->workspace_bytes, bufs->o_lat, bufs->lse, bufs->dev_error, stream)) != MLA_OK)
+                               bufs->workspace_bytes, bufs->o_lat, bufs->lse, bufs->dev_error, s)) != MLA_OK)
         return st;
     if ((st = mla_combine_splits(&info, bufs->plan, bufs->workspace, bufs->workspace_bytes, bufs->o_lat, bufs->lse,
-                                 stream)) != MLA_OK)
+                                 s)) != MLA_OK)
         return st;
-    if ((st = mla_out_proj(bufs->o_lat, w_uv, bufs->out, batch, stream)) != MLA_OK) return st;
-    const size_t out_bytes = (size_t)batch * 128 * 128 * 2;
-    if (record_cuda(cudaMemcpyAsync(out_host, bufs->out, out_bytes, cudaMemcpyDeviceToHost, s),
-                    "cudaMemcpyAsync(out)") != MLA_OK ||
+    if ((st = mla_out_proj(bufs->o_lat, w_uv, bufs->out, batch, s)) != MLA_OK) return st;
+    return record_cuda(cudaMemcpyAsync(out_host, bufs->out, (size_t)batch * 128 * 128 * 2, cudaMemcpyDeviceToHost, s),
+                       "cudaMemcpyAsync(out)");
+}
+
+// True when p is host memory the CUDA runtime has page-locked (cudaHostAlloc / cudaHostRegister).
+bool pinned_host(const void* p)
+{
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        (void)cudaGetLastError();  // the failed query leaves its error behind: clear it
+        return false;
+    }
+    return a.type == cudaMemoryTypeHost;
+}
+
+// Loads the step's kernels (and sets their shared-memory limits) outside any stream capture, so
+// that module loading never happens while a graph is being captured.
+mla_status step_load_kernels(mla_kv_dtype kv_dtype)
+{
+    using AbsK = decltype(&mla::gemm::head_gemm_kernel<128, kAbsorbN, true, kAbsorbStages>);
+    const AbsK absorb = mla::gemm::head_gemm_kernel<128, kAbsorbN, true, kAbsorbStages>;
+    const AbsK outp = mla::gemm::head_gemm_kernel<512, kOutN, false, kOutStages>;
+    if (!set_smem(absorb, AbsorbCfg::kSmemBytes) || !set_smem(outp, OutCfg::kSmemBytes)) return MLA_ERR_CUDA;
+    const bool dec_ok = kv_dtype == MLA_KV_FP8_E4M3
+                            ? set_smem(mla::decode_fp8::decode_fp8_kernel, mla::decode_fp8::kSmemBytes)
+                            : set_smem(mla::decode::decode_bf16_kernel, mla::decode::kSmemBytes);
+    if (!dec_ok) return MLA_ERR_CUDA;
+    cudaFuncAttributes fa;
+    return record_cuda(cudaFuncGetAttributes(&fa, mla::combine::combine_kernel), "cudaFuncGetAttributes(combine)");
+}
+
+}  // namespace
+
+// The whole step from host memory: plan on the host, one asynchronous copy per input, the step's
+// kernels (absorb, decode, merge, projection), the output copy back, one stream synchronisation.
+extern "C" mla_status mla_decode_step_host(const int32_t* seq_lens, int32_t batch, int32_t num_sms,
+                                           const mla_plan_options* opts, const void* q_c_host, const void* q_r_host,
+                                           const int32_t* block_table_host, int32_t max_pages_per_seq,
+                                           const void* w_uk, const void* w_uv, mla_kv_dtype kv_dtype,
+                                           const void* kv_pool, const float* kv_scale, const void* kr_pool,
+                                           int32_t num_pool_pages, float softmax_scale, const mla_step_buffers* bufs,
+                                           void* out_host, mla_plan_info* info_out, void* stream)
+{
+    const mla::NvtxRange nvtx_range("mla_decode_step_host");
+    mla_plan_info info{};
+    mla_status st = step_prepare(seq_lens, batch, num_sms, opts, q_c_host, q_r_host, max_pages_per_seq, bufs,
+                                 out_host, &info);
+    if (st != MLA_OK && st != MLA_ERR_WORKSPACE) return st;
+    if (info_out) *info_out = info;
+    if (st != MLA_OK) return st;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((st = step_enqueue(info, true, q_c_host, q_r_host, block_table_host, max_pages_per_seq, w_uk, w_uv, kv_dtype,
+                           kv_pool, kv_scale, kr_pool, num_pool_pages, softmax_scale, bufs, out_host, s)) != MLA_OK)
+        return st;
+    return record_cuda(cudaStreamSynchronize(s), "cudaStreamSynchronize");
+}
+
+// A captured step for fixed sequence lengths: the per-step copies and kernels as one executable
+// CUDA graph (the plan was copied to the device once, when the graph was made).
+struct mla_step_graph {
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    int device = -1;
+};
+
+extern "C" mla_status mla_step_graph_create(const int32_t* seq_lens, int32_t batch, int32_t num_sms,
+                                            const mla_plan_options* opts, const void* q_c_host, const void* q_r_host,
+                                            const int32_t* block_table_host, int32_t max_pages_per_seq,
+                                            const void* w_uk, const void* w_uv, mla_kv_dtype kv_dtype,
+                                            const void* kv_pool, const float* kv_scale, const void* kr_pool,
+                                            int32_t num_pool_pages, float softmax_scale,
+                                            const mla_step_buffers* bufs, void* out_host, mla_plan_info* info_out,
+                                            void* stream, mla_step_graph** graph_out)
+{
+    const mla::NvtxRange nvtx_range("mla_step_graph_create");
+    if (!graph_out) return MLA_ERR_INVALID_ARG;
+    *graph_out = nullptr;
+    mla_plan_info info{};
+    mla_status st = step_prepare(seq_lens, batch, num_sms, opts, q_c_host, q_r_host, max_pages_per_seq, bufs,
+                                 out_host, &info);
+    if (st != MLA_OK && st != MLA_ERR_WORKSPACE) return st;
+    if (info_out) *info_out = info;
+    if (st != MLA_OK) return st;
+    // the graph's copies are DMA from page-locked host memory
+    if (!pinned_host(q_c_host) || !pinned_host(q_r_host) || !pinned_host(out_host) ||
+        (block_table_host && !pinned_host(block_table_host)))
+        return MLA_ERR_INVALID_ARG;
+    if ((st = step_load_kernels(kv_dtype)) != MLA_OK) return st;
+    int dev = 0;
+    if (record_cuda(cudaGetDevice(&dev), "cudaGetDevice") != MLA_OK) return MLA_ERR_CUDA;
+    // the plan goes to the device once, outside the graph
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (record_cuda(cudaMemcpyAsync(bufs->plan, bufs->plan_host, (size_t)info.plan_bytes, cudaMemcpyHostToDevice, s),
+                    "cudaMemcpyAsync(plan)") != MLA_OK ||
         record_cuda(cudaStreamSynchronize(s), "cudaStreamSynchronize") != MLA_OK)
         return MLA_ERR_CUDA;
+    // capture on a stream of our own (the caller's may be the legacy default stream, which
+    // cannot be captured)
+    cudaStream_t cs = nullptr;
+    if (record_cuda(cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking), "cudaStreamCreateWithFlags") != MLA_OK)
+        return MLA_ERR_CUDA;
+    cudaGraph_t graph = nullptr;
+    st = record_cuda(cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal), "cudaStreamBeginCapture");
+    if (st == MLA_OK) {
+        st = step_enqueue(info, false, q_c_host, q_r_host, block_table_host, max_pages_per_seq, w_uk, w_uv, kv_dtype,
+                          kv_pool, kv_scale, kr_pool, num_pool_pages, softmax_scale, bufs, out_host, cs);
+        const mla_status end = record_cuda(cudaStreamEndCapture(cs, &graph), "cudaStreamEndCapture");
+        if (st == MLA_OK) st = end;
+    }
+    cudaStreamDestroy(cs);
+    cudaGraphExec_t exec = nullptr;
+    if (st == MLA_OK)
+        st = record_cuda(cudaGraphInstantiate(&exec, graph, 0), "cudaGraphInstantiate");
+    if (st != MLA_OK) {
+        if (graph) cudaGraphDestroy(graph);
+        return st;
+    }
+    mla_step_graph* g = new mla_step_graph;
+    g->graph = graph;
+    g->exec = exec;
+    g->device = dev;
+    *graph_out = g;
     return MLA_OK;
+}
+
+extern "C" mla_status mla_step_graph_run(mla_step_graph* graph, int32_t wait, void* stream)
+{
+    const mla::NvtxRange nvtx_range("mla_step_graph_run");
+    if (!graph || !graph->exec) return MLA_ERR_INVALID_ARG;
+    int dev = -1;
+    if (record_cuda(cudaGetDevice(&dev), "cudaGetDevice") != MLA_OK) return MLA_ERR_CUDA;
+    if (dev != graph->device) return MLA_ERR_INVALID_ARG;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (record_cuda(cudaGraphLaunch(graph->exec, s), "cudaGraphLaunch") != MLA_OK) return MLA_ERR_CUDA;
+    if (!wait) return MLA_OK;
+    return record_cuda(cudaStreamSynchronize(s), "cudaStreamSynchronize");
+}
+
+extern "C" mla_status mla_step_graph_destroy(mla_step_graph* graph)
+{
+    if (!graph) return MLA_OK;
+    mla_status st = MLA_OK;
+    if (graph->exec && cudaGraphExecDestroy(graph->exec) != cudaSuccess) st = MLA_ERR_CUDA;
+    if (graph->graph && cudaGraphDestroy(graph->graph) != cudaSuccess) st = MLA_ERR_CUDA;
+    delete graph;
+    return st;
 }

@@ -207,6 +207,47 @@ def test_step_host_rejects_bad_args(L):
     assert st == binding.MLA_ERR_INVALID_ARG
 
 
+def test_step_graph_rejects_bad_args(L):
+    """The captured-step entry points check their arguments before any copy or capture: a missing
+    handle pointer or buffers are invalid arguments, the workspace rule is the one of
+    mla_decode_step_host, host buffers that are not page-locked are refused, and destroying NULL
+    is a no-op."""
+    cap = int(L.mla_plan_bytes_max(2, 152))
+    plan_host = np.zeros(cap // 4, dtype=np.int32)
+    lens = np.asarray((100, 5000), dtype=np.int32)
+    q_c = np.zeros(2 * 128 * 128, dtype=np.uint16)
+    q_r = np.zeros(2 * 128 * 64, dtype=np.uint16)
+    out = np.zeros(2 * 128 * 128, dtype=np.uint16)
+    opts = binding.PlanOptions(2, 0, 0)
+
+    def create(bufs, handle, *, out_ptr=out.ctypes.data):
+        info = binding.PlanInfo()
+        st = L.mla_step_graph_create(lens.ctypes.data_as(ctypes.c_void_p), 2, 152, ctypes.byref(opts),
+                                     _p(q_c.ctypes.data), _p(q_r.ctypes.data), None, 80, _p(0x3000), _p(0x4000),
+                                     binding.MLA_KV_BF16, _p(0x5000), None, None, 100, ctypes.c_float(0.07),
+                                     ctypes.byref(bufs) if bufs is not None else None, _p(out_ptr),
+                                     ctypes.byref(info), None, handle)
+        return st, info
+
+    bufs = binding.StepBuffers(0x10000, 0x11000, 0x12000, 0x13000, 0x14000, 0x15000, 1 << 30, 0x16000, 0x17000,
+                               0x18000, 0x19000, plan_host.ctypes.data, cap)
+    small_ws = binding.StepBuffers(0x10000, 0x11000, 0x12000, 0x13000, 0x14000, 0x15000, 64, 0x16000, 0x17000,
+                                   0x18000, 0x19000, plan_host.ctypes.data, cap)
+    h = ctypes.c_void_p(0xdead)
+    st, _ = create(bufs, None)
+    assert st == binding.MLA_ERR_INVALID_ARG
+    st, _ = create(None, ctypes.byref(h))
+    assert st == binding.MLA_ERR_INVALID_ARG and h.value is None  # the handle is cleared on failure
+    st, _ = create(bufs, ctypes.byref(h), out_ptr=0)
+    assert st == binding.MLA_ERR_INVALID_ARG
+    st, info = create(small_ws, ctypes.byref(h))
+    assert st == binding.MLA_ERR_WORKSPACE and info.workspace_bytes > 64
+    st, info = create(bufs, ctypes.byref(h))  # plain numpy memory is not page-locked
+    assert st == binding.MLA_ERR_INVALID_ARG and info.batch == 2 and h.value is None
+    assert L.mla_step_graph_run(None, 1, None) == binding.MLA_ERR_INVALID_ARG
+    assert L.mla_step_graph_destroy(None) == binding.MLA_OK
+
+
 def test_decode_step_rejects_short_table_rows():
     """The binding checks that each sequence's pages fit its block-table row (no GPU needed:
     the check runs before anything is allocated on the device)."""
