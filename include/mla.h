@@ -98,31 +98,43 @@ typedef struct mla_plan_options {
                                     of a CTA pair after its first (a second item reloads the query
                                     and writes an output); 0 = the default charge of 7 pages,
                                     < 0 = no charge: equal page runs */
-    int32_t reserved;            /* must be 0 */
+    int32_t queries_per_seq;     /* query tokens per sequence, q (0 or 1 = ordinary decode; at most
+                                    MLA_MAX_QUERIES_PER_SEQ).  With q > 1 (several new tokens per
+                                    sequence decoded at once: speculative drafts, a short chunk)
+                                    the plan covers batch * q query rows, row b * q + t being token
+                                    t of sequence b, which sees the first S_b - q + 1 + t cached
+                                    tokens (causal among the new tokens, which the cache already
+                                    holds; S_b >= q).  Every per-row tensor of the calls below
+                                    (q_c, q_R, q_abs, o_lat, lse, out) then has batch * q rows of
+                                    128 heads; the block table keeps one row per sequence.  Each
+                                    query row scans its pages on its own (no shared scan). */
 } mla_plan_options;
+#define MLA_MAX_QUERIES_PER_SEQ 4096
 
 typedef struct mla_plan_info {
-    int32_t batch;
+    int32_t batch;           /* query rows: sequences x queries_per_seq */
     int32_t num_clusters;    /* CTA pairs the decode launch uses (grid = 2 * num_clusters CTAs) */
     int32_t num_items;       /* work items (sequence, page range) */
     int32_t num_partials;    /* items that write a split partial into the workspace */
     int32_t num_combine;     /* sequences with more than one item */
     int32_t max_splits;      /* most items any one sequence has */
-    int32_t total_pages;     /* sum over sequences of ceil(S_b / 64) */
-    int32_t reserved;
+    int32_t total_pages;     /* sum over query rows of ceil(visible length / 64) */
+    int32_t queries_per_seq; /* q of the plan (1 for ordinary decode) */
     int64_t plan_bytes;      /* bytes of the plan image written to plan_host */
     int64_t workspace_bytes; /* bytes mla_decode_paged needs in `workspace` */
     int64_t wait_timeout_ns;
 } mla_plan_info;
 
-/* Upper bound on the plan image size for `batch` sequences on `num_sms` SMs. */
+/* Upper bound on the plan image size for `batch` query rows (sequences x queries_per_seq) on
+ * `num_sms` SMs. */
 MLA_API size_t mla_plan_bytes_max(int32_t batch, int32_t num_sms);
 
 /* Builds the plan image in host memory.
- *   seq_lens   host int32 [batch], each >= 1 (the context length S_b of sequence b)
+ *   seq_lens   host int32 [batch], each >= max(1, queries_per_seq) (the context length S_b of
+ *              sequence b, new tokens included)
  *   num_sms    SMs of the device the decode runs on (>= 2)
  *   opts       may be NULL (defaults)
- *   plan_host  host buffer of plan_capacity bytes (>= mla_plan_bytes_max); the caller copies
+ *   plan_host  host buffer of plan_capacity bytes (>= mla_plan_bytes_max(batch * q, num_sms)); the caller copies
  *              info->plan_bytes of it to device memory (16-byte aligned) for the calls below.
  * Pure host code: needs no GPU. */
 MLA_API mla_status mla_plan_splits(const int32_t* seq_lens, int32_t batch, int32_t num_sms,
@@ -155,7 +167,8 @@ MLA_API mla_status mla_absorb_q(const void* q_c, const void* w_uk, void* q_abs, 
  *                   tensor-core MMAs as loaded; q_abs and P enter them as e4m3 pairs (hi +
  *                   lo, about 2^-8 relative), the scales are applied to the scores and to P
  *                   per token, and k_R / scale is formed in bf16 for the RoPE MMA.
- *   block_table     device int32 [batch][max_pages_per_seq]; entry p of row b is the physical
+ *   block_table     device int32 [batch / q][max_pages_per_seq] (q = info->queries_per_seq: one
+ *                   row per sequence, shared by its q query rows); entry p of row b is the physical
  *                   page of tokens 64p..64p+63 of sequence b.  Only the first ceil(S_b/64)
  *                   entries of a row are read, and never an entry at or past
  *                   max_pages_per_seq: a sequence whose pages do not fit in its row (this call
@@ -270,7 +283,7 @@ MLA_API mla_status mla_append_kv(int32_t num_tokens, const void* c_kv, const voi
  * one contiguous bf16 array, dequantised on the way, for consumers that want whole rows.
  *   kv_dtype, kv_pool, kv_scale, kr_pool, num_pool_pages   the cache, as for mla_decode_paged
  *                     (kv_pool 16-byte aligned), or MLA_KV_NVFP4 as for mla_append_kv
- *   block_table       device int32 [batch][max_pages_per_seq]
+ *   block_table       device int32 [batch / info->queries_per_seq][max_pages_per_seq]
  *   seq_lens          device int32 [batch], each <= max_pages_per_seq * 64
  *   cu_seqlens        device int32 [batch + 1]: row offsets, cu_seqlens[b + 1] = cu_seqlens[b] + seq_lens[b]
  *   out               device bf16 [cu_seqlens[batch]][576], 16-byte aligned: c_KV then k_R per row
@@ -330,16 +343,18 @@ MLA_API mla_status mla_decode_paged_static_ws(const mla_plan_info* info, const v
  * pinned memory for asynchronous DMA), runs absorb, decode, merge and out-proj on `stream`,
  * copies `out` back to out_host and waits for the stream.  One library call instead of a dozen
  * binding-level operations; it computes exactly what the four calls above compute.
- *   bufs              the device buffers, owned by the caller and sized for `batch`:
+ *   `batch` counts sequences; with opts->queries_per_seq = q > 1 every per-row tensor has
+ *   R = batch * q query rows (R = batch otherwise).
+ *   bufs              the device buffers, owned by the caller and sized for R rows:
  *                       q_c, q_r, q_abs, o_lat, lse, out (as above), dev_error,
  *                       block_table  int32 [batch][max_pages_per_seq] (written when a host table
  *                                    is given, else read as it stands),
- *                       plan         >= mla_plan_bytes_max(batch, num_sms) bytes, 16-byte aligned,
+ *                       plan         >= mla_plan_bytes_max(R, num_sms) bytes, 16-byte aligned,
  *                       workspace    workspace_bytes >= the plan's workspace_bytes (else
  *                                    MLA_ERR_WORKSPACE before anything is copied or launched);
- *                     and plan_host: pinned host memory of plan_capacity >= mla_plan_bytes_max.
- *   q_c_host, q_r_host  host bf16 [batch][128][128] / [batch][128][64]
- *   out_host          host bf16 [batch][128][128], receives out
+ *                     and plan_host: pinned host memory of plan_capacity >= mla_plan_bytes_max(R, num_sms).
+ *   q_c_host, q_r_host  host bf16 [R][128][128] / [R][128][64]
+ *   out_host          host bf16 [R][128][128], receives out
  *   info_out          may be NULL; receives the plan header
  * A sequence whose ceil(S_b/64) pages exceed max_pages_per_seq is rejected with
  * MLA_ERR_INVALID_ARG before anything is copied or launched.

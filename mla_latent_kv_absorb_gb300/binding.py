@@ -39,13 +39,13 @@ class MlaError(RuntimeError):
 class PlanOptions(ctypes.Structure):
     _fields_ = [("min_pages_per_split", ctypes.c_int32), ("max_clusters", ctypes.c_int32),
                 ("wait_timeout_ns", ctypes.c_int64), ("item_cost_pages", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("queries_per_seq", ctypes.c_int32)]
 
 
 class PlanInfo(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("num_clusters", ctypes.c_int32), ("num_items", ctypes.c_int32),
                 ("num_partials", ctypes.c_int32), ("num_combine", ctypes.c_int32), ("max_splits", ctypes.c_int32),
-                ("total_pages", ctypes.c_int32), ("reserved", ctypes.c_int32), ("plan_bytes", ctypes.c_int64),
+                ("total_pages", ctypes.c_int32), ("queries_per_seq", ctypes.c_int32), ("plan_bytes", ctypes.c_int64),
                 ("workspace_bytes", ctypes.c_int64), ("wait_timeout_ns", ctypes.c_int64)]
 
 
@@ -171,15 +171,18 @@ def _need(t: torch.Tensor, name: str, dtype, shape=None, device=True):
 # --------------------------------------------------------------------------- C ABI, same names
 
 def mla_plan_splits(seq_lens, num_sms: int, *, min_pages_per_split: int = 0, max_clusters: int = 0,
-                    wait_timeout_ns: int = 0, item_cost_pages: int = 0):
-    """Host planning. Returns (plan image as an int32 numpy array, PlanInfo)."""
+                    wait_timeout_ns: int = 0, item_cost_pages: int = 0, queries_per_seq: int = 0):
+    """Host planning. Returns (plan image as an int32 numpy array, PlanInfo).  With
+    queries_per_seq = q > 1 the plan covers len(seq_lens) * q query rows (token t of sequence b
+    is row b * q + t and sees the first S_b - q + 1 + t cached tokens)."""
     lens = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
     B = int(lens.size)
-    cap = int(lib().mla_plan_bytes_max(B, int(num_sms)))
+    cap = int(lib().mla_plan_bytes_max(B * max(1, int(queries_per_seq)), int(num_sms)))
     if cap == 0:
         raise MlaError("mla_plan_splits", MLA_ERR_INVALID_ARG, "bad batch or SM count")
     buf = np.zeros(cap // 4, dtype=np.int32)
-    opts = PlanOptions(int(min_pages_per_split), int(max_clusters), int(wait_timeout_ns), int(item_cost_pages), 0)
+    opts = PlanOptions(int(min_pages_per_split), int(max_clusters), int(wait_timeout_ns), int(item_cost_pages),
+                       int(queries_per_seq))
     info = PlanInfo()
     st = lib().mla_plan_splits(lens.ctypes.data_as(ctypes.c_void_p), B, int(num_sms), ctypes.byref(opts),
                                buf.ctypes.data_as(ctypes.c_void_p), cap, ctypes.byref(info))
@@ -216,8 +219,8 @@ def mla_decode_paged(info: PlanInfo, plan_dev: torch.Tensor, q_abs: torch.Tensor
     _need(o_lat, "o_lat", torch.bfloat16, (B, NUM_HEADS, D_C))
     _need(lse, "lse", torch.float32, (B, NUM_HEADS))
     _need(dev_error, "dev_error", torch.int32, (1,))
-    if block_table.dim() != 2 or block_table.shape[0] != B:
-        raise ValueError("block_table must be [batch, max_pages]")
+    if block_table.dim() != 2 or block_table.shape[0] * max(1, int(info.queries_per_seq)) != B:
+        raise ValueError("block_table must be [sequences, max_pages] (query rows / queries_per_seq)")
     dtype = _kv_dtype(kv_pool, kv_scale, kr_pool)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = lib().mla_decode_paged(ctypes.byref(info), _ptr(plan_dev), _ptr(q_abs), _ptr(q_r), dtype, _ptr(kv_pool),
@@ -247,8 +250,8 @@ def mla_absorb_decode_paged(info: PlanInfo, plan_dev: torch.Tensor, q_c: torch.T
     _need(o_lat, "o_lat", torch.bfloat16, (B, NUM_HEADS, D_C))
     _need(lse, "lse", torch.float32, (B, NUM_HEADS))
     _need(dev_error, "dev_error", torch.int32, (1,))
-    if block_table.dim() != 2 or block_table.shape[0] != B:
-        raise ValueError("block_table must be [batch, max_pages]")
+    if block_table.dim() != 2 or block_table.shape[0] * max(1, int(info.queries_per_seq)) != B:
+        raise ValueError("block_table must be [sequences, max_pages] (query rows / queries_per_seq)")
     dtype = _kv_dtype(kv_pool, kv_scale, kr_pool)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = lib().mla_absorb_decode_paged(ctypes.byref(info), _ptr(plan_dev), _ptr(q_c), _ptr(w_uk), _ptr(q_abs),
@@ -274,8 +277,8 @@ def mla_decode_paged_static_ws(info: PlanInfo, plan_dev: torch.Tensor, q_abs: to
     _need(o_lat, "o_lat", torch.bfloat16, (B, NUM_HEADS, D_C))
     _need(lse, "lse", torch.float32, (B, NUM_HEADS))
     _need(dev_error, "dev_error", torch.int32, (1,))
-    if block_table.dim() != 2 or block_table.shape[0] != B:
-        raise ValueError("block_table must be [batch, max_pages]")
+    if block_table.dim() != 2 or block_table.shape[0] * max(1, int(info.queries_per_seq)) != B:
+        raise ValueError("block_table must be [sequences, max_pages] (query rows / queries_per_seq)")
     dtype = _kv_dtype(kv_pool, kv_scale, kr_pool)
     st = lib().mla_decode_paged_static_ws(ctypes.byref(info), _ptr(plan_dev), _ptr(q_abs), _ptr(q_r), dtype,
                                           _ptr(kv_pool), _ptr(kv_scale), _ptr(kr_pool), int(kv_pool.shape[0]),
@@ -414,12 +417,17 @@ class DecodeStep:
                  block_table: torch.Tensor, kv_scale: Optional[torch.Tensor] = None,
                  kr_pool: Optional[torch.Tensor] = None, device=None, min_pages_per_split: int = 0,
                  max_clusters: int = 0, wait_timeout_ns: int = 0, item_cost_pages: int = 0,
-                 softmax_scale: float = SOFTMAX_SCALE, fused_absorb: bool = False, fused_tail: bool = False):
+                 softmax_scale: float = SOFTMAX_SCALE, fused_absorb: bool = False, fused_tail: bool = False,
+                 queries_per_seq: int = 1):
         self.device = torch.device(device if device is not None else "cuda")
         self.seq_lens = np.asarray(seq_lens, dtype=np.int32)
-        self.batch = int(self.seq_lens.size)
+        self.num_seqs = int(self.seq_lens.size)
+        self.queries_per_seq = max(1, int(queries_per_seq))
+        # query rows: token t of sequence b is row b * q + t (q_c, q_r, q_abs, o_lat, lse, out)
+        self.batch = self.num_seqs * self.queries_per_seq
         self._plan_opts = dict(min_pages_per_split=min_pages_per_split, max_clusters=max_clusters,
-                               wait_timeout_ns=wait_timeout_ns, item_cost_pages=item_cost_pages)
+                               wait_timeout_ns=wait_timeout_ns, item_cost_pages=item_cost_pages,
+                               queries_per_seq=self.queries_per_seq)
         self._num_sms = num_sms(self.device)
         self.plan_host, self.info = mla_plan_splits(self.seq_lens, self._num_sms, **self._plan_opts)
         self.plan_dev = torch.from_numpy(self.plan_host).to(self.device)
@@ -497,12 +505,12 @@ class DecodeStep:
         B = self.batch
         _need(q_c, "q_c", torch.bfloat16, (B, NUM_HEADS, D_HC), device=False)
         _need(q_r, "q_r", torch.bfloat16, (B, NUM_HEADS, D_R), device=False)
-        if lens.size != B:
-            raise ValueError("run_host: seq_lens must keep the batch size")
+        if lens.size != self.num_seqs:
+            raise ValueError("run_host: seq_lens must keep the number of sequences")
         if block_table is not None:
             _need(block_table, "block_table", torch.int32, device=False)
-            if block_table.dim() != 2 or block_table.shape[0] != B:
-                raise ValueError("block_table must be [batch, max_pages]")
+            if block_table.dim() != 2 or block_table.shape[0] != self.num_seqs:
+                raise ValueError("block_table must be [sequences, max_pages]")
         if not np.array_equal(lens, self.seq_lens) or self._h_stage is None:
             # new lengths: size the workspace for their plan (the library plans again itself)
             self._drop_host_graph()
@@ -535,9 +543,10 @@ class DecodeStep:
                            _addr(self.lse), _addr(self.out), _addr(self.dev_error), _addr(self._h_stage),
                            self._h_stage.numel() * 4)
         opts = PlanOptions(int(self._plan_opts["min_pages_per_split"]), int(self._plan_opts["max_clusters"]),
-                           int(self._plan_opts["wait_timeout_ns"]), int(self._plan_opts["item_cost_pages"]), 0)
+                           int(self._plan_opts["wait_timeout_ns"]), int(self._plan_opts["item_cost_pages"]),
+                           self.queries_per_seq)
         info = PlanInfo()
-        args = (lens.ctypes.data_as(ctypes.c_void_p), B, self._num_sms, ctypes.byref(opts), _ptr(q_c), _ptr(q_r),
+        args = (lens.ctypes.data_as(ctypes.c_void_p), self.num_seqs, self._num_sms, ctypes.byref(opts), _ptr(q_c), _ptr(q_r),
                 _ptr(block_table), int(bt_dev.shape[1]), _ptr(self.w_uk), _ptr(self.w_uv), dtype, _ptr(self.kv_pool),
                 _ptr(self.kv_scale), _ptr(self.kr_pool), int(self.kv_pool.shape[0]), float(self.softmax_scale),
                 ctypes.byref(bufs), _ptr(out), ctypes.byref(info), _stream(stream))

@@ -516,7 +516,8 @@ mla_status step_enqueue(const mla_plan_info& info, bool copy_plan, const void* q
                         int32_t num_pool_pages, float softmax_scale, const mla_step_buffers* bufs, void* out_host,
                         cudaStream_t s)
 {
-    const int32_t batch = info.batch;
+    const int32_t batch = info.batch;  // query rows
+    const int32_t table_rows = info.batch / std::max(1, info.queries_per_seq);
     const size_t q_c_bytes = (size_t)batch * 128 * 128 * 2, q_r_bytes = (size_t)batch * 128 * 64 * 2;
     if (copy_plan && record_cuda(cudaMemcpyAsync(bufs->plan, bufs->plan_host, (size_t)info.plan_bytes,
                                                  cudaMemcpyHostToDevice, s),
@@ -524,7 +525,7 @@ mla_status step_enqueue(const mla_plan_info& info, bool copy_plan, const void* q
         return MLA_ERR_CUDA;
     if (block_table_host &&
         record_cuda(cudaMemcpyAsync(bufs->block_table, block_table_host,
-                                    (size_t)batch * (size_t)max_pages_per_seq * sizeof(int32_t),
+                                    (size_t)table_rows * (size_t)max_pages_per_seq * sizeof(int32_t),
                                     cudaMemcpyHostToDevice, s),
                     "cudaMemcpyAsync(block table)") != MLA_OK)
         return MLA_ERR_CUDA;

@@ -191,7 +191,7 @@ struct Params {
     int32_t absorb_jobs;         // 128 heads x tiles of 128 sequences (absorb prologue)
     int32_t batch;
     const __nv_bfloat16* q_r;    // [B][128][64]
-    const int32_t* block_table;  // [B][max_pages]
+    const int32_t* block_table;  // [sequences][max_pages]; an item reads row item.table_row
     int32_t max_pages;
     int32_t num_pool_pages;
     float scale_log2;            // softmax_scale * log2(e)
@@ -205,14 +205,14 @@ struct Params {
 };
 
 struct Item {
-    int seq, page_begin, page_end, seq_len, slot;
+    int seq, page_begin, page_end, seq_len, slot, table_row;
 };
 
 __device__ __forceinline__ Item load_item(const int32_t* plan, int items_off, int i)
 {
     const int4 a = *reinterpret_cast<const int4*>(plan + items_off + kItemWords * i);
     const int4 b = *reinterpret_cast<const int4*>(plan + items_off + kItemWords * i + 4);
-    return Item{a.x, a.y, a.z, a.w, b.x};
+    return Item{a.x, a.y, a.z, a.w, b.x, b.y};
 }
 
 // ---------------------------------------------------------------------------- absorb prologue
@@ -350,7 +350,7 @@ __device__ __forceinline__ void run_producer(const CUtensorMap* tm, const Params
     bool ok = true;
     for (int i = item_begin; i < item_end && ok; ++i) {
         const Item it = load_item(p.plan, items_off, i);
-        const int32_t* bt = p.block_table + (int64_t)it.seq * p.max_pages;
+        const int32_t* bt = p.block_table + (int64_t)it.table_row * p.max_pages;
         for (int pg0 = it.page_begin; pg0 < it.page_end && ok; pg0 += 32) {
             const int n = min(32, it.page_end - pg0);
             int page = 0;
@@ -406,7 +406,7 @@ __device__ __forceinline__ void score_producer(const CUtensorMap* tm, const CUte
     ok = __shfl_sync(0xffffffffu, ok, 0);
     for (int i = item_begin; i < item_end && ok; ++i) {
         const Item it = load_item(p.plan, items_off, i);
-        const int32_t* bt = p.block_table + (int64_t)it.seq * p.max_pages;
+        const int32_t* bt = p.block_table + (int64_t)it.table_row * p.max_pages;
         if (lane == 0) {
             // the item's q_abs rows (128 heads x 512 dims) as four ring entries of two 64-dim
             // boxes each, ahead of its pages

@@ -149,7 +149,7 @@ struct Params {
     const int32_t* plan;
     const __nv_bfloat16* q_abs;  // [B][128][512]
     const __nv_bfloat16* q_r;    // [B][128][64]
-    const int32_t* block_table;  // [B][max_pages]
+    const int32_t* block_table;  // [sequences][max_pages]; an item reads row item.table_row
     int32_t max_pages;
     int32_t num_pool_pages;
     float scale_log2;            // softmax_scale * log2(e)
@@ -251,7 +251,7 @@ __device__ __forceinline__ void value_producer(const CUtensorMap* tm_c8, const P
     bool ok = true;
     for (int i = item_begin; i < item_end && ok; ++i) {
         const Item it = load_item(p.plan, items_off, i);
-        const int32_t* bt = p.block_table + (int64_t)it.seq * p.max_pages;
+        const int32_t* bt = p.block_table + (int64_t)it.table_row * p.max_pages;
         for (int pg0 = it.page_begin; pg0 < it.page_end && ok; pg0 += 32) {
             const int n = min(32, it.page_end - pg0);
             int page = 0;
@@ -300,7 +300,7 @@ __device__ __forceinline__ void score_producer(const CUtensorMap* tm_c8, const P
     bool ok = true;
     for (int i = item_begin; i < item_end && ok; ++i) {
         const Item it = load_item(p.plan, items_off, i);
-        const int32_t* bt = p.block_table + (int64_t)it.seq * p.max_pages;
+        const int32_t* bt = p.block_table + (int64_t)it.table_row * p.max_pages;
         for (int pg0 = it.page_begin; pg0 < it.page_end && ok; pg0 += 32) {
             const int n = min(32, it.page_end - pg0);  // a multiple of 4 unless it ends the item
             int page = 0;
@@ -363,7 +363,7 @@ __device__ __forceinline__ void kr_convert(const CUtensorMap* tm_kr, const Param
     int G = 0;
     for (int i = item_begin; i < item_end; ++i) {
         const Item it = load_item(p.plan, items_off, i);
-        const int32_t* bt = p.block_table + (int64_t)it.seq * p.max_pages;
+        const int32_t* bt = p.block_table + (int64_t)it.table_row * p.max_pages;
         // largest scale over the item's tokens: lane k takes pages k, k + 32, ...
         float smax = 0.f;
         for (int pg = it.page_begin + lane; pg < it.page_end; pg += 32) {

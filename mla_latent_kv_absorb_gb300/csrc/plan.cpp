@@ -90,24 +90,36 @@ extern "C" mla_status mla_plan_splits(const int32_t* seq_lens, int32_t batch, in
                                       mla_plan_info* info)
 {
     if (!seq_lens || !plan_host || !info || batch <= 0 || num_sms < 2) return MLA_ERR_INVALID_ARG;
-    int32_t min_pages = 8, max_clusters = num_sms / 2, item_cost = kDefaultItemCostPages;
+    int32_t min_pages = 8, max_clusters = num_sms / 2, item_cost = kDefaultItemCostPages, qps = 1;
     int64_t timeout_ns = 2000000000LL;
     if (opts) {
         if (opts->min_pages_per_split < 0 || opts->max_clusters < 0 || opts->wait_timeout_ns < 0 ||
-            opts->reserved != 0)
+            opts->queries_per_seq < 0 || opts->queries_per_seq > MLA_MAX_QUERIES_PER_SEQ)
             return MLA_ERR_INVALID_ARG;
         if (opts->item_cost_pages != 0) item_cost = std::max(0, opts->item_cost_pages);  // < 0: equal page runs
         if (opts->min_pages_per_split > 0) min_pages = opts->min_pages_per_split;
         if (opts->max_clusters > 0) max_clusters = std::min(max_clusters, opts->max_clusters);
         if (opts->wait_timeout_ns > 0) timeout_ns = opts->wait_timeout_ns;
+        if (opts->queries_per_seq > 0) qps = opts->queries_per_seq;
     }
-    if (plan_capacity < mla_plan_bytes_max(batch, num_sms)) return MLA_ERR_WORKSPACE;
+    // query rows: token t of sequence b (row b * qps + t) sees the first S_b - qps + 1 + t
+    // cached tokens (the cache already holds all of the sequence's query tokens)
+    const int64_t rows64 = (int64_t)batch * qps;
+    if (rows64 > INT32_MAX / 2) return MLA_ERR_UNSUPPORTED;
+    const int32_t rows = (int32_t)rows64;
+    if (plan_capacity < mla_plan_bytes_max(rows, num_sms)) return MLA_ERR_WORKSPACE;
+    std::vector<int32_t> row_len(rows);
+    for (int b = 0; b < batch; ++b) {
+        if (seq_lens[b] < qps) return MLA_ERR_INVALID_ARG;  // also rejects S_b < 1
+        for (int t = 0; t < qps; ++t) row_len[(int64_t)b * qps + t] = seq_lens[b] - qps + 1 + t;
+    }
+    batch = rows;
+    seq_lens = row_len.data();
 
-    // pages of each sequence and where each starts in the concatenated page list
+    // pages of each query row and where each starts in the concatenated page list
     std::vector<int64_t> pages(batch), start(batch + 1);
     start[0] = 0;
     for (int b = 0; b < batch; ++b) {
-        if (seq_lens[b] < 1) return MLA_ERR_INVALID_ARG;
         pages[b] = (seq_lens[b] + 63) / 64;
         start[b + 1] = start[b] + pages[b];
     }
@@ -170,6 +182,7 @@ extern "C" mla_status mla_plan_splits(const int32_t* seq_lens, int32_t batch, in
             it.page_end = (int32_t)(e - start[ss]);
             it.seq_len = seq_lens[ss];
             it.partial_slot = -1;
+            it.table_row = ss / qps;
             items.push_back(it);
             ++items_per_seq[ss];
             g = e;
@@ -216,6 +229,7 @@ extern "C" mla_status mla_plan_splits(const int32_t* seq_lens, int32_t batch, in
     w[kHdrMaxSplits] = max_splits;
     w[kHdrTimeoutLo] = (int32_t)(uint32_t)(timeout_ns & 0xffffffffu);
     w[kHdrTimeoutHi] = (int32_t)(uint32_t)((uint64_t)timeout_ns >> 32);
+    w[kHdrQueriesPerSeq] = qps;
     for (int64_t k = 0; k <= C; ++k) w[cl_off + k] = cluster_begin[k];
     std::memcpy(w + it_off, items.data(), (size_t)n_items * sizeof(PlanItem));
     if (n_comb) std::memcpy(w + cb_off, combine.data(), (size_t)n_comb * sizeof(PlanCombine));
@@ -227,7 +241,7 @@ extern "C" mla_status mla_plan_splits(const int32_t* seq_lens, int32_t batch, in
     info->num_combine = (int32_t)n_comb;
     info->max_splits = max_splits;
     info->total_pages = (int32_t)total;
-    info->reserved = 0;
+    info->queries_per_seq = qps;
     info->plan_bytes = words * 4;
     info->workspace_bytes = (int64_t)next_slot * (kPartialOBytes + kPartialLseBytes);
     info->wait_timeout_ns = timeout_ns;

@@ -9,7 +9,7 @@
 namespace mla {
 
 constexpr int32_t kPlanMagic = 0x504C4D41;  // "AMLP" little-endian
-constexpr int32_t kPlanVersion = 1;
+constexpr int32_t kPlanVersion = 2;
 constexpr int kPlanHeaderWords = 16;
 constexpr int kItemWords = 8;
 constexpr int kCombineWords = 4;
@@ -29,13 +29,17 @@ enum PlanHeader : int {
     kHdrMaxSplits = 11,
     kHdrTimeoutLo = 12,
     kHdrTimeoutHi = 13,
+    kHdrQueriesPerSeq = 14,  // query tokens per sequence (1: ordinary decode)
 };
 
-// One work item: pages [page_begin, page_end) of sequence `seq` (context length seq_len).
-// partial_slot < 0: the item covers the whole sequence and writes o_lat / lse directly;
-// otherwise it writes split partial number partial_slot of the workspace.
+// One work item: pages [page_begin, page_end) of query row `seq` (its visible context length
+// is seq_len), whose pages are listed in block-table row `table_row`.  With one query token
+// per sequence the two indices are equal; with q tokens per sequence, query row b * q + t is
+// token t of sequence b (table row b).  partial_slot < 0: the item covers the whole row and
+// writes o_lat / lse directly; otherwise it writes split partial number partial_slot of the
+// workspace.
 struct PlanItem {
-    int32_t seq, page_begin, page_end, seq_len, partial_slot, pad0, pad1, pad2;
+    int32_t seq, page_begin, page_end, seq_len, partial_slot, table_row, pad1, pad2;
 };
 
 // A sequence cut into n_parts items whose partials are the consecutive slots

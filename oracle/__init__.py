@@ -28,6 +28,7 @@ Parity status of each function (what pins it, see ``tests/test_oracle_pins.py``)
 from __future__ import annotations
 
 import ctypes
+import dataclasses
 import os
 import subprocess
 from typing import Optional, Sequence
@@ -91,6 +92,8 @@ def _load(path: str):
     L.oracle_gather_kv.argtypes = [i32, P, P, i32, P, i32, i32, P, P, P, P, P]
     L.oracle_append_kv.restype = i32
     L.oracle_append_kv.argtypes = [i32, P, P, P, i32, i32, P, P, P, P]
+    L.oracle_query_rows.restype = ctypes.c_int
+    L.oracle_query_rows.argtypes = [i32, i32, P, P, P]
     return L
 
 
@@ -322,3 +325,26 @@ def append_kv(c_kv, k_r, slots, cache: dict) -> int:
         assert a is None or (isinstance(a, np.ndarray) and a.flags.c_contiguous)
     num_pages = (codes if mode else cache["pool"]).shape[0]
     return int(lib().oracle_append_kv(n, _p(ck), _p(kr), _p(sl), mode, num_pages, *[_p(a) for a in arrays]))
+
+
+def query_rows(seq_lens, q: int):
+    """Several new tokens per sequence (oracle_query_rows): (row_len, row_table) for the
+    B * q query rows, row b*q + t being new token t of sequence b."""
+    sl = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+    B = int(sl.size)
+    row_len = np.empty(B * q, dtype=np.int32)
+    row_table = np.empty(B * q, dtype=np.int32)
+    if lib().oracle_query_rows(B, int(q), _p(sl), _p(row_len), _p(row_table)) != 0:
+        raise ValueError("every sequence needs at least q tokens (and q >= 1)")
+    return row_len, row_table
+
+
+def query_row_inputs(inp, q: int):
+    """The inputs of a q-tokens-per-sequence step as B * q ordinary decode queries: inp.q_c and
+    inp.q_r already hold B * q rows; each query row gets its visible length and its sequence's
+    block-table row.  Every oracle function then applies unchanged."""
+    row_len, row_table = query_rows(inp.seq_lens, q)
+    if int(inp.q_c.shape[0]) != row_len.size or int(inp.q_r.shape[0]) != row_len.size:
+        raise ValueError("q_c and q_r need B * q rows")
+    return dataclasses.replace(inp, seq_lens=row_len,
+                               block_table=np.ascontiguousarray(np.asarray(inp.block_table)[row_table]))

@@ -571,3 +571,29 @@ int oracle_append_kv(int n, const uint16_t* c_kv, const uint16_t* k_r, const int
     }
     return status;
 }
+
+/*
+ * Several new tokens of a sequence decoded in one step.  Page 1 section 6 (with the
+ * kPrefillThresh = 256 of section 3's mla_config.h) runs chunks of fewer than 256 new tokens
+ * through the absorbed decode path; speculative drafts are the same shape.  Reading taken:
+ * the cache already holds the q new tokens of sequence b (S_b counts them), new token t
+ * (0 <= t < q) is the token at position S_b - q + t, and it attends causally to positions
+ * 0 .. S_b - q + t of its sequence.  Each new token is then an ordinary decode query over a
+ * prefix of the sequence.  Query row b*q + t of the per-row tensors is token t of sequence b.
+ * Fills row_len[b*q + t] = S_b - q + 1 + t (tokens visible to that query) and
+ * row_table[b*q + t] = b (the block-table row holding its pages).  Returns -1 (nothing
+ * written) if q < 1 or some S_b < q, else 0.
+ */
+int oracle_query_rows(int B, int q, const int32_t* seq_lens, int32_t* row_len, int32_t* row_table)
+{
+    if (q < 1) return -1;
+    for (int b = 0; b < B; ++b)
+        if (seq_lens[b] < q) return -1;
+    for (int b = 0; b < B; ++b)
+        for (int t = 0; t < q; ++t) {
+            const int64_t row = (int64_t)b * q + t;
+            row_len[row] = seq_lens[b] - q + 1 + t;
+            row_table[row] = b;
+        }
+    return 0;
+}

@@ -6,6 +6,7 @@ so that ``test_oracle_pins.py`` can run them against the real oracle and
 """
 from __future__ import annotations
 
+import dataclasses
 import json
 import math
 import os
@@ -714,3 +715,69 @@ def check_gather_kv():
 
 
 ALL_CHECKS += [check_gather_kv]
+
+
+# ----------------------------------------------------------------------------- several new tokens per sequence
+
+def mq_inputs(seq_lens=(5, 70, 131), q=3, seed=41):
+    """A tiny bf16 cache with q query rows per sequence (row b*q + t: new token t of sequence b)."""
+    inp = tiny_inputs(seq_lens, seed=seed, poison=True)
+    g = torch.Generator().manual_seed(seed + 1)
+    rows = inp.batch * q
+    inp.q_c = torch.randn(rows, synth.NUM_HEADS, synth.D_HC, generator=g).to(torch.bfloat16)
+    inp.q_r = torch.randn(rows, synth.NUM_HEADS, synth.D_R, generator=g).to(torch.bfloat16)
+    return inp
+
+
+def check_multi_query_single_token_is_decode():
+    """q = 1: the query rows are the sequences themselves, and the step is the ordinary decode."""
+    inp = tiny_inputs((5, 70, 131), seed=42)
+    rows = oracle.query_row_inputs(inp, 1)
+    assert np.array_equal(rows.seq_lens, inp.seq_lens) and np.array_equal(rows.block_table, inp.block_table)
+    heads = np.array([0, 77])
+    assert np.array_equal(oracle.decode_naive(rows, softmax_scale=SCALE, heads=heads),
+                          oracle.decode_naive(inp, softmax_scale=SCALE, heads=heads))
+
+
+def check_multi_query_rows_are_prefix_decodes():
+    """Query row b*q + t is an ordinary decode of sequence b cut to its first S_b - q + 1 + t
+    tokens, with that row's query: built here by slicing the inputs by hand, one sequence at a
+    time.  Pins the row order, the causal lengths and the block-table row of each query."""
+    q = 3
+    inp = mq_inputs(q=q)
+    heads = np.array([0, 77])
+    got = oracle.decode_naive(oracle.query_row_inputs(inp, q), softmax_scale=SCALE, heads=heads)
+    for b in range(inp.batch):
+        for t in range(q):
+            r = b * q + t
+            one = dataclasses.replace(inp, seq_lens=np.array([int(inp.seq_lens[b]) - q + 1 + t], np.int32),
+                                      block_table=np.ascontiguousarray(inp.block_table[b:b + 1]),
+                                      q_c=inp.q_c[r:r + 1], q_r=inp.q_r[r:r + 1])
+            want = oracle.decode_naive(one, softmax_scale=SCALE, heads=heads)
+            assert np.array_equal(got[r], want[0]), (b, t)
+
+
+def check_multi_query_is_causal():
+    """A new token does not see the new tokens after it: changing the cache row of new token
+    t' leaves the outputs of tokens t < t' bit for bit and changes those of t >= t'."""
+    q = 3
+    inp = mq_inputs(q=q)
+    heads = np.array([5])
+    base = oracle.decode_naive(oracle.query_row_inputs(inp, q), softmax_scale=SCALE, heads=heads)
+    g = torch.Generator().manual_seed(3)
+    for b in range(inp.batch):
+        for tp in range(q):
+            pos = int(inp.seq_lens[b]) - q + tp  # the cache position of new token tp
+            page, slot = int(inp.block_table[b, pos // 64]), pos % 64
+            mod = dataclasses.replace(inp, pool=inp.pool.clone())
+            mod.pool[page, slot] = (4 * torch.randn(576, generator=g)).to(torch.bfloat16)
+            out = oracle.decode_naive(oracle.query_row_inputs(mod, q), softmax_scale=SCALE, heads=heads)
+            for t in range(q):
+                same = np.array_equal(out[b * q + t], base[b * q + t])
+                assert same == (t < tp), (b, tp, t)
+            others = [r for r in range(inp.batch * q) if r // q != b]
+            assert np.array_equal(out[others], base[others])
+
+
+ALL_CHECKS += [check_multi_query_single_token_is_decode, check_multi_query_rows_are_prefix_decodes,
+               check_multi_query_is_causal]

@@ -76,6 +76,10 @@ MUTANTS = {
                                  "dst[i] = bf16_rne((float)oracle_e4m3_value(row[i]));"),
     "gather_nvfp4_nibbles_swapped": ("const uint8_t e2 = (i & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xF);",
                                      "const uint8_t e2 = (i & 1) ? (uint8_t)(byte & 0xF) : (uint8_t)(byte >> 4);"),
+    # several new tokens per sequence
+    "query_rows_causal_off_by_one": ("row_len[row] = seq_lens[b] - q + 1 + t;", "row_len[row] = seq_lens[b] - q + t;"),
+    "query_rows_token_major": ("const int64_t row = (int64_t)b * q + t;", "const int64_t row = (int64_t)t * B + b;"),
+    "query_rows_first_table_row": ("row_table[row] = b;", "row_table[row] = 0;"),
     "gather_bf16_truncates": ("return (uint16_t)((u + 0x7FFFu + ((u >> 16) & 1u)) >> 16);",
                               "return (uint16_t)(u >> 16);"),
     "gather_rows_shifted": ("uint16_t* dst = out + ((int64_t)cu_seqlens[b] + t) * DROW;",

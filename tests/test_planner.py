@@ -24,7 +24,7 @@ def check_plan(lens, num_sms=152, **kw):
     h, cl, items, comb = decode_plan(plan)
     B = lens.size
     pages = (lens.astype(np.int64) + 63) // 64
-    assert h["magic"] == 0x504C4D41 and h["version"] == 1 and h["batch"] == B
+    assert h["magic"] == 0x504C4D41 and h["version"] == 2 and h["batch"] == B
     assert h["total"] == pages.sum() == info.total_pages
     assert 1 <= h["clusters"] <= num_sms // 2 and h["clusters"] == info.num_clusters
     assert cl[0] == 0 and cl[-1] == h["items"] and np.all(np.diff(cl) >= 0)
@@ -157,12 +157,48 @@ def test_item_cost_default_and_off():
     assert np.array_equal(p0, p7) and not np.array_equal(p0, pe)
 
 
-def test_plan_rejects_reserved_field():
-    opts = binding.PlanOptions(0, 0, 0, 0, 5)  # reserved must be 0
-    buf = np.zeros(4096, np.int32)
-    info = binding.PlanInfo()
-    lens = np.array([100], np.int32)
+def test_plan_rejects_bad_queries_per_seq():
+    """queries_per_seq must lie in [0, MLA_MAX_QUERIES_PER_SEQ] and no sequence may be shorter
+    than its query tokens."""
     import ctypes
-    st = binding.lib().mla_plan_splits(lens.ctypes.data_as(ctypes.c_void_p), 1, 152, ctypes.byref(opts),
-                                       buf.ctypes.data_as(ctypes.c_void_p), buf.nbytes, ctypes.byref(info))
-    assert st == binding.MLA_ERR_INVALID_ARG
+    buf = np.zeros(1 << 16, np.int32)
+    info = binding.PlanInfo()
+    lens = np.array([100, 3], np.int32)
+    for q, want in ((-1, binding.MLA_ERR_INVALID_ARG), (4097, binding.MLA_ERR_INVALID_ARG),
+                    (4, binding.MLA_ERR_INVALID_ARG), (3, binding.MLA_OK)):
+        opts = binding.PlanOptions(0, 0, 0, 0, q)
+        st = binding.lib().mla_plan_splits(lens.ctypes.data_as(ctypes.c_void_p), 2, 152, ctypes.byref(opts),
+                                           buf.ctypes.data_as(ctypes.c_void_p), buf.nbytes, ctypes.byref(info))
+        assert st == want, q
+
+
+def _items(plan):
+    off, n = int(plan[8]), int(plan[4])
+    return plan[off: off + 8 * n].reshape(n, 8)
+
+
+@pytest.mark.parametrize("q", [2, 5])
+def test_multi_query_rows(q):
+    """With q query tokens per sequence the plan covers B * q rows: row b * q + t has visible
+    length S_b - q + 1 + t, every page of it once, and reads block-table row b."""
+    lens = np.array([700, 64 * 9 + q - 1, 5000, q], np.int32)
+    plan, info = binding.mla_plan_splits(lens, 152, min_pages_per_split=2, queries_per_seq=q)
+    assert info.batch == lens.size * q and info.queries_per_seq == q and int(plan[14]) == q
+    items = _items(plan)
+    for b in range(lens.size):
+        for t in range(q):
+            row = b * q + t
+            mine = items[items[:, 0] == row]
+            L = int(lens[b]) - q + 1 + t
+            assert (mine[:, 3] == L).all() and (mine[:, 5] == b).all()
+            covered = sorted(p for it in mine for p in range(it[1], it[2]))
+            assert covered == list(range((L + 63) // 64))
+    assert info.total_pages == sum((int(lens[b]) - q + 1 + t + 63) // 64 for b in range(lens.size) for t in range(q))
+
+
+def test_single_query_rows_read_their_own_table_row():
+    lens = np.array([3000, 700, 64 * 9 + 1], np.int32)
+    for q in (0, 1):
+        plan, info = binding.mla_plan_splits(lens, 152, min_pages_per_split=2, queries_per_seq=q)
+        items = _items(plan)
+        assert (items[:, 0] == items[:, 5]).all() and info.queries_per_seq == 1 and info.batch == 3
