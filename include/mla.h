@@ -336,6 +336,36 @@ MLA_API mla_status mla_decode_paged_static_ws(const mla_plan_info* info, const v
                             float softmax_scale, void* o_lat, float* lse, uint32_t* dev_error,
                             void* stream);
 
+/* ---- prefill chunk, decompressed form -------------------------------------------------------
+ * P1 section 4 gives two forms of the same attention: path A decompresses per-head keys and
+ * values (k_h = W_UK[h] c, v_h = W_UV[h] c) and attends with head dim 128 + 64; path B absorbs
+ * W_UK into the query (the decode calls above).  Section 3's mla_config.h sets
+ * kPrefillThresh = 256 and section 6 measures the switch: chunks of at least 256 new tokens
+ * run path A, shorter ones path B (the decode with opts->queries_per_seq = chunk length).
+ * This call runs path A for the last chunk_len tokens of one sequence of seq_len tokens whose
+ * cache rows (the chunk's included) are already in the pool: query t (position
+ * seq_len - chunk_len + t) attends causally to positions 0 .. seq_len - chunk_len + t, and
+ *   out[t,h,:] = sum_j softmax_j((q_c[t,h] . k_h[j] + q_R[t,h] . k_R[j]) * softmax_scale) v_h[j].
+ * Steps, all on `stream`: the sequence's rows gathered into bf16 (dequantised for FP8 and
+ * NVFP4 caches, as mla_gather_kv), k_h and v_h for all heads (tcgen05 GEMMs), then a causal
+ * attention kernel (128 queries x 1 head per CTA, 64-key tiles, online softmax).
+ *   kv_dtype, kv_pool, kv_scale, kr_pool, num_pool_pages   the cache, as mla_gather_kv
+ *   block_table_row  device int32 [max_pages]: the sequence's pages (ceil(seq_len/64) <= max_pages)
+ *   q_c, q_r         device bf16 [chunk_len][128][128] / [chunk_len][128][64]
+ *   w_uk, w_uv       device bf16 [128][128][512]
+ *   workspace        device, >= mla_prefill_workspace_bytes(seq_len), 16-byte aligned: the
+ *                    gathered rows [seq_len][576], k [seq_len][128][128], v [seq_len][128][128]
+ *   out              device bf16 [chunk_len][128][128]
+ * 1 <= chunk_len <= seq_len <= 65535 * 128.  Device-side problems (a page outside the pool, a
+ * wait that ran out) set bits in dev_error. */
+MLA_API size_t mla_prefill_workspace_bytes(int32_t seq_len);
+MLA_API mla_status mla_prefill_decompressed(mla_kv_dtype kv_dtype, const void* kv_pool, const float* kv_scale,
+                                            const void* kr_pool, int32_t num_pool_pages,
+                                            const int32_t* block_table_row, int32_t max_pages, int32_t seq_len,
+                                            int32_t chunk_len, const void* q_c, const void* q_r, const void* w_uk,
+                                            const void* w_uv, float softmax_scale, void* workspace,
+                                            size_t workspace_bytes, void* out, uint32_t* dev_error, void* stream);
+
 /* ---- the whole step from host memory in one call ------------------------------------------
  * For callers whose queries, block table and lengths live in host memory: plans the step for
  * `seq_lens` on the host (as mla_plan_splits), copies the plan, the block table (when

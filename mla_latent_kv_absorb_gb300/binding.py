@@ -53,7 +53,7 @@ EXPORTS = ("mla_status_string", "mla_last_error_string", "mla_plan_bytes_max", "
            "mla_combine_splits", "mla_out_proj", "mla_read_device_error", "mla_debug_wait_timeout",
            "mla_decode_paged_static_ws", "mla_decode_step_host", "mla_append_kv", "mla_merge_out_proj",
            "mla_absorb_decode_paged", "mla_gather_kv", "mla_step_graph_create", "mla_step_graph_run",
-           "mla_step_graph_destroy")
+           "mla_step_graph_destroy", "mla_prefill_workspace_bytes", "mla_prefill_decompressed")
 
 # capacity of the library's fixed split-partial array (mla_decode_paged_static_ws)
 MLA_STATIC_WS_MAX_PARTIALS = 128
@@ -119,6 +119,11 @@ def lib() -> ctypes.CDLL:
     L.mla_step_graph_run.argtypes = [P, i32, P]
     L.mla_step_graph_destroy.restype = ctypes.c_int
     L.mla_step_graph_destroy.argtypes = [P]
+    L.mla_prefill_workspace_bytes.restype = sz
+    L.mla_prefill_workspace_bytes.argtypes = [i32]
+    L.mla_prefill_decompressed.restype = ctypes.c_int
+    L.mla_prefill_decompressed.argtypes = [ctypes.c_int, P, P, P, i32, P, i32, i32, i32, P, P, P, P, ctypes.c_float,
+                                           P, sz, P, u32p, P]
     L.mla_append_kv.restype = ctypes.c_int
     L.mla_append_kv.argtypes = [i32, P, P, P, ctypes.c_int, i32, P, P, P, u32p, P]
     L.mla_read_device_error.restype = ctypes.c_int
@@ -372,6 +377,60 @@ def mla_gather_kv(*, kv_pool: torch.Tensor, block_table: torch.Tensor, seq_lens:
                              _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens), _ptr(cu_seqlens), B,
                              _ptr(out), _ptr(dev_error), _stream(stream))
     _check("mla_gather_kv", st)
+
+
+# Chunks of at least this many new tokens take the decompressed form, shorter ones the absorbed
+# decode (page 1 section 3, kPrefillThresh in mla_config.h; section 6 measures the switch).
+PREFILL_THRESHOLD = 256
+
+
+def mla_prefill_decompressed(*, kv_pool: torch.Tensor, block_table_row: torch.Tensor, seq_len: int,
+                             q_c: torch.Tensor, q_r: torch.Tensor, w_uk: torch.Tensor, w_uv: torch.Tensor,
+                             out: torch.Tensor, dev_error: torch.Tensor, workspace: Optional[torch.Tensor] = None,
+                             kv_scale: Optional[torch.Tensor] = None, kr_pool: Optional[torch.Tensor] = None,
+                             softmax_scale: float = SOFTMAX_SCALE, stream=None) -> None:
+    """The last T = q_c.shape[0] tokens of one sequence of seq_len cached tokens, attended
+    causally in the decompressed form: out [T, 128, 128].  workspace: at least
+    mla_prefill_workspace_bytes(seq_len) bytes (allocated here when None)."""
+    T = int(q_c.shape[0])
+    _need(q_c, "q_c", torch.bfloat16, (T, NUM_HEADS, D_HC))
+    _need(q_r, "q_r", torch.bfloat16, (T, NUM_HEADS, D_R))
+    _need(out, "out", torch.bfloat16, (T, NUM_HEADS, D_HC))
+    _need(block_table_row, "block_table_row", torch.int32)
+    _need(dev_error, "dev_error", torch.int32, (1,))
+    need = int(lib().mla_prefill_workspace_bytes(int(seq_len)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q_c.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    dtype = _kv_dtype(kv_pool, kv_scale, kr_pool)
+    st = lib().mla_prefill_decompressed(dtype, _ptr(kv_pool), _ptr(kv_scale), _ptr(kr_pool), int(kv_pool.shape[0]),
+                                        _ptr(block_table_row), int(block_table_row.numel()), int(seq_len), T,
+                                        _ptr(q_c), _ptr(q_r), _ptr(w_uk), _ptr(w_uv), float(softmax_scale),
+                                        _ptr(workspace), ws_bytes, _ptr(out), _ptr(dev_error), _stream(stream))
+    _check("mla_prefill_decompressed", st)
+
+
+def prefill_chunk(seq_len: int, q_c: torch.Tensor, q_r: torch.Tensor, *, w_uk: torch.Tensor, w_uv: torch.Tensor,
+                  kv_pool: torch.Tensor, block_table_row: torch.Tensor, kv_scale: Optional[torch.Tensor] = None,
+                  kr_pool: Optional[torch.Tensor] = None, threshold: int = PREFILL_THRESHOLD,
+                  softmax_scale: float = SOFTMAX_SCALE, stream=None):
+    """A chunk of T = q_c.shape[0] new tokens at the end of one sequence of seq_len cached
+    tokens (the chunk's cache rows included): chunks shorter than `threshold` run the absorbed
+    decode with T query rows (DecodeStep, queries_per_seq = T), longer ones the decompressed
+    form (mla_prefill_decompressed).  Returns (out [T, 128, 128], device error word)."""
+    T = int(q_c.shape[0])
+    bt = block_table_row.reshape(1, -1)
+    if T < threshold:
+        step = DecodeStep(np.array([seq_len], np.int32), w_uk=w_uk, w_uv=w_uv, kv_pool=kv_pool, block_table=bt,
+                          kv_scale=kv_scale, kr_pool=kr_pool, device=q_c.device, queries_per_seq=T,
+                          softmax_scale=softmax_scale)
+        return step.run(q_c, q_r, stream), step.dev_error
+    out = torch.empty(T, NUM_HEADS, D_HC, dtype=torch.bfloat16, device=q_c.device)
+    err = torch.zeros(1, dtype=torch.int32, device=q_c.device)
+    mla_prefill_decompressed(kv_pool=kv_pool, block_table_row=bt[0], seq_len=seq_len, q_c=q_c, q_r=q_r, w_uk=w_uk,
+                             w_uv=w_uv, out=out, dev_error=err, kv_scale=kv_scale, kr_pool=kr_pool,
+                             softmax_scale=softmax_scale, stream=stream)
+    return out, err
 
 
 def mla_read_device_error(dev_error: torch.Tensor, stream=None) -> int:

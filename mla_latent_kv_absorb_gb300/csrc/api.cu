@@ -17,6 +17,7 @@
 #include "head_gemm.cuh"
 #include "nvtx_range.h"
 #include "plan.h"
+#include "prefill.cuh"
 #include "tail.cuh"
 
 namespace {
@@ -124,14 +125,17 @@ mla_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sm
 
 // Shared by absorb and out-proj: activations [batch][128][K] (K-major rows of 128*K), weights
 // [128][128][512].
+// shared_act_row > 0: one activation row of that many elements per batch row, shared by all
+// heads (the first K_TOTAL elements are the operand).
 template <int K_TOTAL, int N_TILE, bool W_MN, int STAGES>
 mla_status launch_head_gemm(const void* act, const void* weight, void* out, int32_t batch, int n_total,
-                            cuuint32_t w_box_rows, bool pdl, void* stream)
+                            cuuint32_t w_box_rows, bool pdl, void* stream, int shared_act_row = 0)
 {
     using C = Cfg<K_TOTAL, N_TILE, W_MN, STAGES>;
     CUtensorMap tm_a, tm_w;
-    const cuuint64_t a_dims[2] = {(cuuint64_t)128 * K_TOTAL, (cuuint64_t)batch};
-    const cuuint64_t a_str[1] = {(cuuint64_t)128 * K_TOTAL * 2};
+    const cuuint64_t a_row = shared_act_row > 0 ? (cuuint64_t)shared_act_row : (cuuint64_t)128 * K_TOTAL;
+    const cuuint64_t a_dims[2] = {a_row, (cuuint64_t)batch};
+    const cuuint64_t a_str[1] = {a_row * 2};
     const cuuint32_t a_box[2] = {64, 128};
     const cuuint64_t w_dims[2] = {512, 128 * 128};
     const cuuint64_t w_str[1] = {512 * 2};
@@ -142,6 +146,7 @@ mla_status launch_head_gemm(const void* act, const void* weight, void* out, int3
     if (!set_smem(kernel, C::kSmemBytes)) return MLA_ERR_CUDA;
     mla::gemm::Args args;
     args.out = static_cast<__nv_bfloat16*>(out);
+    args.a_x_per_head = shared_act_row > 0 ? 0 : K_TOTAL;
     args.batch = batch;
     args.out_row_stride = (int64_t)128 * n_total;
     args.n_total = n_total;
@@ -460,6 +465,102 @@ extern "C" mla_status mla_merge_out_proj(const mla_plan_info* info, const void* 
     if (!set_smem(mla::tail::merge_out_proj_kernel, mla::tail::kSmemBytes)) return MLA_ERR_CUDA;
     return launch_pdl(mla::tail::merge_out_proj_kernel, dim3(128, (info->batch + 127) / 128), dim3(mla::tail::kThreads),
                       mla::tail::kSmemBytes, static_cast<cudaStream_t>(stream), tm_w, a);
+}
+
+namespace mla {
+// gather.cu: one sequence's cache rows into contiguous bf16 rows [seq_len][576]
+mla_status gather_one_sequence(mla_kv_dtype kv_dtype, const void* kv_pool, const float* kv_scale, const void* kr_pool,
+                               int32_t num_pool_pages, const int32_t* block_table_row, int32_t max_pages,
+                               int32_t seq_len, void* out, uint32_t* dev_error, void* stream);
+}  // namespace mla
+
+namespace {
+
+// Workspace of the decompressed prefill: gathered rows [S][576], k [S][128][128], v [S][128][128]
+// (bf16), each section 1024-byte aligned.
+struct PrefillLayout {
+    size_t rows, k, v, total;
+};
+
+PrefillLayout prefill_layout(int64_t seq_len)
+{
+    const auto up = [](size_t x) { return (x + 1023) & ~(size_t)1023; };
+    const size_t rows = up((size_t)seq_len * 576 * 2), kv = up((size_t)seq_len * 128 * 128 * 2);
+    return PrefillLayout{0, rows, rows + kv, rows + 2 * kv};
+}
+
+}  // namespace
+
+extern "C" size_t mla_prefill_workspace_bytes(int32_t seq_len)
+{
+    return seq_len > 0 ? prefill_layout(seq_len).total : 0;
+}
+
+extern "C" mla_status mla_prefill_decompressed(mla_kv_dtype kv_dtype, const void* kv_pool, const float* kv_scale,
+                                               const void* kr_pool, int32_t num_pool_pages,
+                                               const int32_t* block_table_row, int32_t max_pages, int32_t seq_len,
+                                               int32_t chunk_len, const void* q_c, const void* q_r, const void* w_uk,
+                                               const void* w_uv, float softmax_scale, void* workspace,
+                                               size_t workspace_bytes, void* out, uint32_t* dev_error, void* stream)
+{
+    const mla::NvtxRange nvtx_range("mla_prefill_decompressed");
+    if (!kv_pool || !block_table_row || !q_c || !q_r || !w_uk || !w_uv || !workspace || !out || !dev_error)
+        return MLA_ERR_INVALID_ARG;
+    if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3 && kv_dtype != MLA_KV_NVFP4) return MLA_ERR_INVALID_ARG;
+    if (kv_dtype != MLA_KV_BF16 && (!kv_scale || !kr_pool)) return MLA_ERR_INVALID_ARG;
+    if (seq_len < 1 || chunk_len < 1 || chunk_len > seq_len || num_pool_pages < 1 || max_pages < 1 ||
+        (seq_len + 63) / 64 > max_pages || !(softmax_scale > 0.f) || !std::isfinite(softmax_scale))
+        return MLA_ERR_INVALID_ARG;
+    if (!aligned16(kv_pool) || !aligned16(q_c) || !aligned16(q_r) || !aligned16(w_uk) || !aligned16(w_uv) ||
+        !aligned16(workspace) || !aligned16(out) || (reinterpret_cast<uintptr_t>(block_table_row) & 3u) ||
+        (reinterpret_cast<uintptr_t>(dev_error) & 3u) ||
+        (kv_dtype != MLA_KV_BF16 && (!aligned16(kr_pool) || (reinterpret_cast<uintptr_t>(kv_scale) & 3u))))
+        return MLA_ERR_ALIGNMENT;
+    if ((int64_t)seq_len > (int64_t)65535 * 128) return MLA_ERR_UNSUPPORTED;  // grid z of the decompression
+    const PrefillLayout lay = prefill_layout(seq_len);
+    if (workspace_bytes < lay.total) return MLA_ERR_WORKSPACE;
+    char* ws = static_cast<char*>(workspace);
+    void *rows = ws + lay.rows, *k = ws + lay.k, *v = ws + lay.v;
+
+    // 1. the sequence's cache rows, dequantised to bf16
+    mla_status st = mla::gather_one_sequence(kv_dtype, kv_pool, kv_scale, kr_pool, num_pool_pages, block_table_row,
+                                             max_pages, seq_len, rows, dev_error, stream);
+    if (st != MLA_OK) return st;
+    // 2. per-head keys and values (the out-proj GEMM shape, activations shared by the heads)
+    if ((st = launch_head_gemm<512, kOutN, false, kOutStages>(rows, w_uk, k, seq_len, 128, kOutN, false, stream, 576)) !=
+            MLA_OK ||
+        (st = launch_head_gemm<512, kOutN, false, kOutStages>(rows, w_uv, v, seq_len, 128, kOutN, false, stream, 576)) !=
+            MLA_OK)
+        return st;
+    // 3. causal attention of the chunk's queries
+    CUtensorMap tm_qc, tm_qr, tm_k, tm_kr, tm_v;
+    const cuuint64_t qc_dims[3] = {128, 128, (cuuint64_t)chunk_len};
+    const cuuint64_t qc_str[2] = {128 * 2, 128 * 128 * 2};
+    const cuuint64_t qr_dims[3] = {64, 128, (cuuint64_t)chunk_len};
+    const cuuint64_t qr_str[2] = {64 * 2, 128 * 64 * 2};
+    const cuuint32_t q_box[3] = {64, 1, 128};
+    const cuuint64_t k_dims[3] = {128, 128, (cuuint64_t)seq_len};
+    const cuuint64_t k_str[2] = {128 * 2, 128 * 128 * 2};
+    const cuuint32_t k_box[3] = {64, 1, 64};
+    const cuuint64_t r_dims[2] = {576, (cuuint64_t)seq_len};
+    const cuuint64_t r_str[1] = {576 * 2};
+    const cuuint32_t r_box[2] = {64, 64};
+    if (!make_map_bf16(&tm_qc, q_c, 3, qc_dims, qc_str, q_box) || !make_map_bf16(&tm_qr, q_r, 3, qr_dims, qr_str, q_box) ||
+        !make_map_bf16(&tm_k, k, 3, k_dims, k_str, k_box) || !make_map_bf16(&tm_kr, rows, 2, r_dims, r_str, r_box) ||
+        !make_map_bf16(&tm_v, v, 3, k_dims, k_str, k_box))
+        return MLA_ERR_CUDA;
+    mla::prefill::Params p;
+    p.seq_len = seq_len;
+    p.chunk_len = chunk_len;
+    p.scale_log2 = softmax_scale * 1.4426950408889634f;
+    p.out = static_cast<__nv_bfloat16*>(out);
+    p.dev_error = dev_error;
+    p.timeout_ns = kDefaultTimeoutNs;
+    if (!set_smem(mla::prefill::prefill_attn_kernel, mla::prefill::kSmemBytes)) return MLA_ERR_CUDA;
+    const dim3 grid((unsigned)((chunk_len + mla::prefill::kQ - 1) / mla::prefill::kQ), 128);
+    mla::prefill::prefill_attn_kernel<<<grid, mla::prefill::kThreads, mla::prefill::kSmemBytes,
+                                        static_cast<cudaStream_t>(stream)>>>(tm_qc, tm_qr, tm_k, tm_kr, tm_v, p);
+    return launch_status();
 }
 
 extern "C" const char* mla_last_error_string(void) { return t_last_error; }

@@ -63,8 +63,9 @@ struct Args {
     int64_t num_pool_pages;
     const int32_t* block_table;   // [B][max_pages]
     int max_pages;
-    const int32_t* seq_lens;      // [B]
+    const int32_t* seq_lens;      // [B], or NULL: one sequence of one_len tokens (cu_seqlens unused)
     const int32_t* cu_seqlens;    // [B + 1]
+    int32_t one_len;
     uint4* out;                   // bf16 [total][576]
     uint32_t* dev_error;
 };
@@ -74,7 +75,7 @@ __global__ void __launch_bounds__(kWarps * 32) gather_kv_kernel(const Args a)
 {
     const int lane = threadIdx.x & 31, b = blockIdx.y;
     const int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
-    if (t >= __ldg(a.seq_lens + b)) return;
+    if (t >= (a.seq_lens ? __ldg(a.seq_lens + b) : a.one_len)) return;
     const int64_t pg = t / 64;
     const int32_t page = pg < a.max_pages ? __ldg(a.block_table + (int64_t)b * a.max_pages + pg) : -1;
     if (page < 0 || page >= a.num_pool_pages) {
@@ -82,7 +83,7 @@ __global__ void __launch_bounds__(kWarps * 32) gather_kv_kernel(const Args a)
         return;
     }
     const int64_t tok = (int64_t)page * 64 + t % 64;
-    uint4* dst = a.out + ((int64_t)__ldg(a.cu_seqlens + b) + t) * 72;  // 72 x 16 bytes per row
+    uint4* dst = a.out + ((a.seq_lens ? (int64_t)__ldg(a.cu_seqlens + b) : 0) + t) * 72;  // 72 x 16 bytes per row
     if (a.kv_dtype == MLA_KV_BF16) {
         const uint4* src = reinterpret_cast<const uint4*>(a.pool) + tok * 72;
         dst[lane] = __ldg(src + lane);
@@ -128,6 +129,23 @@ namespace {
 
 inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// grid over the tokens of max_pages pages of `batch` sequences
+mla_status launch(const mla::gather::Args& a, int32_t max_pages, int32_t batch, void* stream)
+{
+    using namespace mla::gather;
+    const int64_t tokens = (int64_t)max_pages * 64;
+    const dim3 grid((unsigned)((tokens + kWarps - 1) / kWarps), (unsigned)batch), block(kWarps * 32);
+    gather_kv_kernel<<<grid, block, 0, static_cast<cudaStream_t>(stream)>>>(a);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        char msg[200];
+        snprintf(msg, sizeof msg, "gather kernel launch: %s (%s)", cudaGetErrorString(e), cudaGetErrorName(e));
+        mla::set_last_error_text(msg);
+        return MLA_ERR_CUDA;
+    }
+    return MLA_OK;
+}
+
 }  // namespace
 
 extern "C" MLA_API mla_status mla_gather_kv(mla_kv_dtype kv_dtype, const void* kv_pool, const float* kv_scale,
@@ -157,17 +175,33 @@ extern "C" MLA_API mla_status mla_gather_kv(mla_kv_dtype kv_dtype, const void* k
     a.max_pages = max_pages_per_seq;
     a.seq_lens = seq_lens;
     a.cu_seqlens = cu_seqlens;
+    a.one_len = 0;
     a.out = static_cast<uint4*>(out);
     a.dev_error = dev_error;
-    const int64_t tokens = (int64_t)max_pages_per_seq * 64;
-    const dim3 grid((unsigned)((tokens + kWarps - 1) / kWarps), (unsigned)batch), block(kWarps * 32);
-    gather_kv_kernel<<<grid, block, 0, static_cast<cudaStream_t>(stream)>>>(a);
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) {
-        char msg[200];
-        snprintf(msg, sizeof msg, "gather kernel launch: %s (%s)", cudaGetErrorString(e), cudaGetErrorName(e));
-        mla::set_last_error_text(msg);
-        return MLA_ERR_CUDA;
-    }
-    return MLA_OK;
+    return launch(a, max_pages_per_seq, batch, stream);
 }
+
+namespace mla {
+// One sequence of seq_len tokens (its block-table row given), rows to out [seq_len][576]; the
+// caller has checked the arguments as mla_gather_kv does.
+mla_status gather_one_sequence(mla_kv_dtype kv_dtype, const void* kv_pool, const float* kv_scale, const void* kr_pool,
+                               int32_t num_pool_pages, const int32_t* block_table_row, int32_t max_pages,
+                               int32_t seq_len, void* out, uint32_t* dev_error, void* stream)
+{
+    using namespace mla::gather;
+    Args a;
+    a.kv_dtype = (int)kv_dtype;
+    a.pool = static_cast<const uint8_t*>(kv_pool);
+    a.scale = kv_scale;
+    a.kr = static_cast<const uint4*>(kr_pool);
+    a.num_pool_pages = num_pool_pages;
+    a.block_table = block_table_row;
+    a.max_pages = max_pages;
+    a.seq_lens = nullptr;
+    a.cu_seqlens = nullptr;
+    a.one_len = seq_len;
+    a.out = static_cast<uint4*>(out);
+    a.dev_error = dev_error;
+    return launch(a, (seq_len + 63) / 64, 1, stream);
+}
+}  // namespace mla

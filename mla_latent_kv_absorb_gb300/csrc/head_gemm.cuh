@@ -3,6 +3,10 @@
 //   absorb   (page 1 section 4, path B):  q_abs[b,h,c] = sum_d q_c[b,h,d] * W_UK[h,d,c]
 //   out-proj (value side of absorption):  out[b,h,d]   = sum_c o_lat[b,h,c] * W_UV[h,d,c]
 //
+//   decompression (page 1 section 4, path A): k[s,h,d] = sum_c c_KV[s,c] * W_UK[h,d,c] and
+//            v[s,h,d] = sum_c c_KV[s,c] * W_UV[h,d,c], the out-proj shape with one activation
+//            row per token shared by all heads.
+//
 // One CTA computes a 128 (batch rows) x N_TILE tile of one head.  The batch rows are the MMA's
 // M dimension, so small batches leave rows empty (TMA fills rows past the batch with zeros,
 // which costs no HBM traffic) and the kernel is a stream over the head's weight slice: both
@@ -43,6 +47,7 @@ struct Cfg {
 
 struct Args {
     __nv_bfloat16* out;
+    int a_x_per_head;        // K_TOTAL when each head has its own activation row, 0 when shared
     int batch;
     int64_t out_row_stride;  // elements between consecutive batch rows of `out`
     int n_total;             // N of one head (512 absorb, 128 out-proj)
@@ -124,7 +129,8 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
                     mbar_arrive_expect_tx(bar_full + 8 * s, C::kStageBytes);
                     load_w(kc, s);
                 }
-                tma_load_2d(sbase + s * C::kStageBytes, &tm_a, bar_full + 8 * s, h * K_TOTAL + kc * C::kKC, m0, pol_a);
+                tma_load_2d(sbase + s * C::kStageBytes, &tm_a, bar_full + 8 * s, h * args.a_x_per_head + kc * C::kKC,
+                            m0, pol_a);
                 ++issued;
             }
             if (*abort_flag) {  // let loads already in flight land before the CTA can exit

@@ -248,6 +248,26 @@ def test_step_graph_rejects_bad_args(L):
     assert L.mla_step_graph_destroy(None) == binding.MLA_OK
 
 
+def test_prefill_rejects_bad_args(L):
+    """The decompressed prefill checks its arguments before any launch."""
+    F = L.mla_prefill_decompressed
+    ws = int(L.mla_prefill_workspace_bytes(1000))
+    assert ws >= 1000 * (1152 + 2 * 32768) and L.mla_prefill_workspace_bytes(0) == 0
+
+    def call(*, seq=1000, chunk=300, q=0x10000, ws_bytes=ws, bt=0x4000, dtype=binding.MLA_KV_BF16, pages=16):
+        return F(dtype, _p(0x1000), None, None, 100, _p(bt), pages, seq, chunk, _p(q), _p(0x20000), _p(0x30000),
+                 _p(0x40000), ctypes.c_float(0.07), _p(0x50000), ws_bytes, _p(0x60000), _p(0x70000), None)
+
+    assert call(q=0) == binding.MLA_ERR_INVALID_ARG
+    assert call(chunk=1001) == binding.MLA_ERR_INVALID_ARG          # more new tokens than the sequence
+    assert call(chunk=0) == binding.MLA_ERR_INVALID_ARG
+    assert call(pages=15) == binding.MLA_ERR_INVALID_ARG            # 1000 tokens need 16 pages
+    assert call(dtype=binding.MLA_KV_FP8_E4M3) == binding.MLA_ERR_INVALID_ARG  # no scales / k_R pool
+    assert call(q=0x10008) == binding.MLA_ERR_ALIGNMENT
+    assert call(bt=0x4002) == binding.MLA_ERR_ALIGNMENT
+    assert call(ws_bytes=ws - 1) == binding.MLA_ERR_WORKSPACE
+
+
 def test_decode_step_rejects_short_table_rows():
     """The binding checks that each sequence's pages fit its block-table row (no GPU needed:
     the check runs before anything is allocated on the device)."""
