@@ -154,18 +154,28 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- accounting
 
+def visible_tokens(seq_lens, q: int) -> int:
+    """Cached tokens the step's queries attend to, summed over query rows: with q new tokens per
+    sequence, token t of sequence b sees the first S_b - q + 1 + t."""
+    lens = np.asarray(seq_lens, dtype=np.int64)
+    return int((q * lens - q * (q - 1) // 2).sum())
+
+
 def workload_accounting(inp):
-    """Algorithmic bytes and FLOPs of one step (no partial-output traffic, no decompression)."""
-    B, T = inp.batch, inp.num_tokens
+    """Algorithmic bytes and FLOPs of one step (no partial-output traffic, no decompression).
+    Every cached token is read once (the minimum, also when several query rows of a sequence
+    attend to it); every (query row, visible token) pair costs the absorbed QK and PV FLOPs."""
+    R, T = inp.rows, inp.num_tokens
+    scanned = visible_tokens(inp.seq_lens, inp.queries_per_seq)
     row_bytes = 1152 if inp.kv_dtype == "bf16" else 512 + 4 + 128
     kv_bytes = T * row_bytes
     w_bytes = 2 * 128 * 128 * 512 * 2
-    q_bytes = B * 128 * (128 + 64) * 2
-    out_bytes = B * 128 * 128 * 2
-    decode_bytes = kv_bytes + B * 128 * (512 + 64) * 2 + B * 128 * (512 * 2 + 4)
-    attn_flop = T * 128 * 2 * (576 + 512)
-    proj_flop = 2 * B * 128 * (2 * 128 * 512)
-    return dict(tokens=T, kv_bytes=kv_bytes, step_bytes=kv_bytes + w_bytes + q_bytes + out_bytes,
+    q_bytes = R * 128 * (128 + 64) * 2
+    out_bytes = R * 128 * 128 * 2
+    decode_bytes = kv_bytes + R * 128 * (512 + 64) * 2 + R * 128 * (512 * 2 + 4)
+    attn_flop = scanned * 128 * 2 * (576 + 512)
+    proj_flop = 2 * R * 128 * (2 * 128 * 512)
+    return dict(tokens=T, scanned=scanned, kv_bytes=kv_bytes, step_bytes=kv_bytes + w_bytes + q_bytes + out_bytes,
                 decode_bytes=decode_bytes, step_flop=attn_flop + proj_flop, decode_flop=attn_flop)
 
 
@@ -206,9 +216,12 @@ def recorded_traffic(kernel: str, workload: str, tokens: int):
 
 def bench_config(args, inp, world):
     """The workload, identical in both arms' JSON lines."""
-    return {"workload": args.workload, "desc": synth.WORKLOADS[args.workload]["desc"],
-            "global_batch": inp.batch * world, "seq_len": int(inp.seq_lens.max()),
-            "tokens_per_replica": int(inp.num_tokens), "parallelism": f"replicas x{world}"}
+    cfg = {"workload": args.workload, "desc": synth.WORKLOADS[args.workload]["desc"],
+           "global_batch": inp.batch * world, "seq_len": int(inp.seq_lens.max()),
+           "tokens_per_replica": int(inp.num_tokens), "parallelism": f"replicas x{world}"}
+    if inp.queries_per_seq > 1:
+        cfg["queries_per_seq"] = inp.queries_per_seq
+    return cfg
 
 
 def cpu_model() -> str:
@@ -238,7 +251,7 @@ def run_ours(args, rank, world, local):
     q_c, q_r, w_uk, w_uv, kv, bt = binding.inputs_to_device(inp, device)
     step = binding.DecodeStep(inp.seq_lens, w_uk=w_uk, w_uv=w_uv, block_table=bt,
                               item_cost_pages=args.item_cost_pages, fused_absorb=args.absorb == "fused",
-                              fused_tail=args.tail == "fused", **kv)
+                              fused_tail=args.tail == "fused", queries_per_seq=inp.queries_per_seq, **kv)
     acc = workload_accounting(inp)
     peaks = load_peaks()
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=device)
@@ -439,6 +452,8 @@ def sampled_parity(inp, out_dev):
     from mla_latent_kv_absorb_gb300 import binding
 
     heads = [0, 77, 127]
+    if inp.queries_per_seq > 1:
+        inp = oracle.query_row_inputs(inp, inp.queries_per_seq)  # one decode query per row
     q_abs = oracle.absorb_q(inp.q_c, inp.w_uk)
     o, _ = oracle.latent_attention(inp, q_abs, softmax_scale=binding.SOFTMAX_SCALE, heads=heads)
     full = np.zeros((inp.batch, 128, 512))
@@ -479,13 +494,26 @@ def run_e2e(args, inp, step, binding, device, stream):
 # ----------------------------------------------------------------------------- the CPU oracle
 
 def _one_sequence(inp, tokens=None):
+    q = inp.queries_per_seq
+    keep = min(q, 16)  # a long chunk is sampled by its last 16 query rows (same visible lengths)
     sub = synth.DecodeInputs(seq_lens=inp.seq_lens[:1].copy(), block_table=inp.block_table[:1].copy(),
-                             num_pool_pages=inp.num_pool_pages, q_c=inp.q_c[:1], q_r=inp.q_r[:1], w_uk=inp.w_uk,
-                             w_uv=inp.w_uv, kv_dtype=inp.kv_dtype, pool=inp.pool, c8=inp.c8, kv_scale=inp.kv_scale,
-                             kr=inp.kr)
+                             num_pool_pages=inp.num_pool_pages, q_c=inp.q_c[q - keep:q], q_r=inp.q_r[q - keep:q],
+                             w_uk=inp.w_uk, w_uv=inp.w_uv, kv_dtype=inp.kv_dtype, pool=inp.pool, c8=inp.c8,
+                             kv_scale=inp.kv_scale, kr=inp.kr, queries_per_seq=keep)
+    q = keep
     if tokens is not None:
-        sub.seq_lens[0] = min(int(sub.seq_lens[0]), tokens)
+        sub.seq_lens[0] = max(q, min(int(sub.seq_lens[0]), tokens))
     return sub
+
+
+def _rows_note(sub) -> str:
+    return f", {sub.queries_per_seq} query rows" if sub.queries_per_seq > 1 else ""
+
+
+def _query_rows(sub):
+    """The sample as ordinary decode queries (one per query row) for the oracle."""
+    import oracle
+    return oracle.query_row_inputs(sub, sub.queries_per_seq) if sub.queries_per_seq > 1 else sub
 
 
 def cpu_baseline(inp, tokens=None):
@@ -500,23 +528,28 @@ def cpu_baseline(inp, tokens=None):
     heads = list(range(0, 128, 8))
     sub = _one_sequence(inp, tokens)
     S0 = int(sub.seq_lens[0])
+    rows = _query_rows(sub)
+    seen = visible_tokens(sub.seq_lens, sub.queries_per_seq)
     t0 = time.perf_counter()
-    oracle.decode_naive(sub, softmax_scale=SOFTMAX_SCALE, heads=heads)
+    oracle.decode_naive(rows, softmax_scale=SOFTMAX_SCALE, heads=heads)
     dt_naive = time.perf_counter() - t0
     t0 = time.perf_counter()
-    q_abs = oracle.absorb_q(sub.q_c, sub.w_uk)
-    o, _ = oracle.latent_attention(sub, q_abs, softmax_scale=SOFTMAX_SCALE)
-    oracle.out_proj(o, sub.w_uv)
+    q_abs = oracle.absorb_q(rows.q_c, rows.w_uk)
+    o, _ = oracle.latent_attention(rows, q_abs, softmax_scale=SOFTMAX_SCALE)
+    oracle.out_proj(o, rows.w_uv)
     dt_abs = time.perf_counter() - t0
-    scale_naive = (inp.num_tokens * 128) / (S0 * len(heads))
-    scale_abs = inp.num_tokens / S0
+    total_seen = visible_tokens(inp.seq_lens, inp.queries_per_seq)
+    scale_naive = (total_seen * 128) / (seen * len(heads))
+    scale_abs = total_seen / seen
     return {"value": round(dt_naive * scale_naive * 1e6, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
             "cpu_model": cpu_model(),
-            "sample": f"naive fp64 oracle, sequence 0 ({S0} tokens) x heads 0,8,..,120; {dt_naive:.2f} s measured, "
+            "sample": f"naive fp64 oracle, sequence 0 ({S0} tokens{_rows_note(sub)}) x heads 0,8,..,120; "
+                      f"{dt_naive:.2f} s measured, "
                       f"scaled x{scale_naive:.0f} to the full step",
             "absorbed": {"value": round(dt_abs * scale_abs * 1e6, 1), "unit": UNIT,
                          "sample": f"absorbed fp64 oracle (absorb, latent attention, W_UV) on sequence 0 "
-                                   f"({S0} tokens) x all heads; {dt_abs:.2f} s measured, scaled x{scale_abs:.0f}"}}
+                                   f"({S0} tokens{_rows_note(sub)}) x all heads; {dt_abs:.2f} s measured, "
+                                   f"scaled x{scale_abs:.0f}"}}
 
 
 def run_reference(args, rank, world, local):
@@ -533,15 +566,18 @@ def run_reference(args, rank, world, local):
     oracle.set_threads(cores)
     heads = list(range(0, 128, 8))
     sub = _one_sequence(inp, 8192)
+    rows = _query_rows(sub)
     per_step = []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        oracle.decode_naive(sub, softmax_scale=SOFTMAX_SCALE, heads=heads)
+        oracle.decode_naive(rows, softmax_scale=SOFTMAX_SCALE, heads=heads)
         if i >= args.warmup:
             per_step.append(time.perf_counter() - t0)
     v = statistics.mean(per_step) * 1e6
-    scale = (inp.num_tokens * 128) / (int(sub.seq_lens[0]) * len(heads))
-    sample = (f"naive fp64 oracle per step on sequence 0 ({int(sub.seq_lens[0])} tokens) x heads 0,8,..,120 "
+    scale = (visible_tokens(inp.seq_lens, inp.queries_per_seq) * 128) / (
+        visible_tokens(sub.seq_lens, sub.queries_per_seq) * len(heads))
+    sample = (f"naive fp64 oracle per step on sequence 0 ({int(sub.seq_lens[0])} tokens{_rows_note(sub)}) "
+              f"x heads 0,8,..,120 "
               f"(1/{scale:.0f} of the workload)")
     cb = {"value": round(v, 1), "unit": UNIT, "cores": cores, "kind": "oracle", "cpu_model": cpu_model(),
           "sample": sample, "full_step_estimate_us": round(v * scale, 1)}
@@ -550,6 +586,144 @@ def run_reference(args, rank, world, local):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (the same seeded workload)",
             "config": bench_config(args, inp, world), "cpu_baseline": cb,
             "e2e": {"value": round(v, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ----------------------------------------------------------------------------- prefill chunk
+
+def prefill_accounting(S: int, T: int, row_bytes: int):
+    """Algorithmic FLOPs and bytes of one decompressed prefill chunk: key and value
+    decompression of all S tokens for 128 heads, causal attention of the T new tokens (head
+    dim 192 for scores, 128 for values); bytes = the cache rows, both weights, queries, output."""
+    seen = visible_tokens([S], T)
+    flop = 2 * (2 * S * 512 * 128 * 128) + seen * 128 * 2 * (192 + 128)
+    nbytes = S * row_bytes + 2 * (128 * 128 * 512 * 2) + T * 128 * 192 * 2 + T * 128 * 128 * 2
+    return dict(flop=flop, bytes=nbytes, seen=seen)
+
+
+def run_prefill(args, rank, world, local):
+    """A chunk of new tokens at the end of one sequence through the decompressed form
+    (mla_prefill_decompressed: gather, key and value decompression, causal attention)."""
+    from mla_latent_kv_absorb_gb300 import binding
+
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    dist_init(world, "nccl")
+    binding.lib()
+    inp = synth.make_workload(args.workload, seed=synth.DEFAULT_SEED + rank, poison_tail=False)
+    S, T = int(inp.seq_lens[0]), inp.queries_per_seq
+    q_c, q_r, w_uk, w_uv, kv, bt = binding.inputs_to_device(inp, device)
+    pool = kv.pop("kv_pool")
+    ws = torch.empty(int(binding.lib().mla_prefill_workspace_bytes(S)), dtype=torch.uint8, device=device)
+    out = torch.empty(T, 128, 128, dtype=torch.bfloat16, device=device)
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=device)
+
+    def step(qc=q_c, qr=q_r):
+        binding.mla_prefill_decompressed(kv_pool=pool, block_table_row=bt[0], seq_len=S, q_c=qc, q_r=qr, w_uk=w_uk,
+                                         w_uv=w_uv, out=out, dev_error=err, workspace=ws, stream=stream, **kv)
+
+    t0, n = time.perf_counter(), 0
+    while n < args.warmup or time.perf_counter() - t0 < args.min_warmup_s:
+        flush.fill_(n & 0xFF)
+        step()
+        n += 1
+    torch.cuda.synchronize(device)
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    dist_barrier(world)
+    torch.cuda.synchronize(device)
+    with ClockSampler(local) as clocks:
+        for i in range(K):
+            flush.fill_(i & 0xFF)
+            evs[i][0].record(stream)
+            step()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize(device)
+    dist_barrier(world)
+    if binding.mla_read_device_error(err) != 0:
+        raise RuntimeError("device error in the timed region")
+    ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    ms_max = dist_max(ms, world, device)
+    row_bytes = 1152 if inp.kv_dtype == "bf16" else (644 if inp.kv_dtype == "fp8_e4m3" else 420)
+    acc = prefill_accounting(S, T, row_bytes)
+    peaks = load_peaks()
+    tf, bw = peaks.get("bf16_tflops"), peaks.get("hbm_gbs")
+    achieved_tf = acc["flop"] / (ms_max * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "kernel": "whole chunk (gather, 2 decompression GEMMs, attention)",
+                "achieved": round(achieved_tf, 1), "peak": tf, "unit": "TFLOP/s", "frac": round(achieved_tf / tf, 4),
+                "traffic": None, "algorithmic_flop": acc["flop"], "algorithmic_bytes": acc["bytes"],
+                "peak_source": peaks.get("source"),
+                "hbm_frac": round(acc["bytes"] / (ms_max * 1e-3) / 1e9 / bw, 4)}
+    if acc["bytes"] / (bw * 1e9) > acc["flop"] / (tf * 1e12):
+        roofline["bound"] = "hbm"
+
+    # sampled parity: query rows first, middle, last x three heads against the oracle
+    parity = None
+    if args.parity and rank == 0:
+        import dataclasses
+
+        import oracle
+        rows = oracle.query_row_inputs(inp, T)
+        idx = np.array([0, T // 2, T - 1])
+        sub = dataclasses.replace(rows, seq_lens=rows.seq_lens[idx].copy(),
+                                  block_table=np.ascontiguousarray(rows.block_table[idx]),
+                                  q_c=rows.q_c[idx], q_r=rows.q_r[idx], queries_per_seq=1)
+        heads = [0, 77, 127]
+        ref = oracle.decode_naive(sub, softmax_scale=binding.SOFTMAX_SCALE, heads=heads)
+        got = out[torch.from_numpy(idx).to(device)][:, heads, :].double().cpu().numpy()
+        d = got - ref
+        tol = {"max_abs": 2e-2, "rel_l2": 1e-2}
+        max_abs, rel = float(np.abs(d).max()), float(np.linalg.norm(d) / np.linalg.norm(ref))
+        parity = {"rows": idx.tolist(), "heads": heads, "max_abs": max_abs, "rel_l2": rel, "tol": tol,
+                  "ok": bool(np.isfinite(got).all() and max_abs <= tol["max_abs"] and rel <= tol["rel_l2"])}
+
+    # e2e: queries from pinned host memory, the chunk, the output back, wall clock
+    e2e = None
+    if args.e2e:
+        q_c_h, q_r_h = inp.q_c.pin_memory(), inp.q_r.pin_memory()
+        out_h = torch.empty(T, 128, 128, dtype=torch.bfloat16).pin_memory()
+        times = []
+        for i in range(args.warmup + K):
+            torch.cuda.synchronize(device)
+            t0 = time.perf_counter()
+            q_c.copy_(q_c_h, non_blocking=True)
+            q_r.copy_(q_r_h, non_blocking=True)
+            step()
+            out_h.copy_(out, non_blocking=True)
+            torch.cuda.synchronize(device)
+            if i >= args.warmup:
+                times.append(time.perf_counter() - t0)
+        e2e = {"value": round(statistics.mean(times) * 1e6, 2), "unit": UNIT,
+               "h2d_bytes_per_step": int(q_c_h.numel() * 2 + q_r_h.numel() * 2),
+               "d2h_bytes_per_step": int(out_h.numel() * 2)}
+
+    cb = None
+    if args.cpu_baseline and rank == 0:
+        import oracle
+        cores = len(os.sched_getaffinity(0))
+        oracle.set_threads(cores)
+        sub = _one_sequence(inp)
+        heads = list(range(0, 128, 8))
+        t0 = time.perf_counter()
+        oracle.decode_naive(_query_rows(sub), softmax_scale=binding.SOFTMAX_SCALE, heads=heads)
+        dt = time.perf_counter() - t0
+        scale = (acc["seen"] * 128) / (visible_tokens(sub.seq_lens, sub.queries_per_seq) * len(heads))
+        cb = {"value": round(dt * scale * 1e6, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+              "cpu_model": cpu_model(),
+              "sample": f"naive fp64 oracle on the chunk's last {sub.queries_per_seq} query rows x heads 0,8,..,120; "
+                        f"{dt:.2f} s measured, scaled x{scale:.0f} to the chunk"}
+
+    return {"metric": "MLA prefill chunk us/chunk (decompressed form), TFLOP/s as fraction of GB300 roofline",
+            "value": round(ms_max * 1e3, 2), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": round(ms_max, 5), "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic (seeded N(0,1) cache/queries, N(0,1/512) weights)",
+            "config": bench_config(args, inp, world),
+            "setup": {"l2": "512 MB buffer rewritten before every timed chunk",
+                      "timing": "CUDA events around each mla_prefill_decompressed call"},
+            "chunk_tflops": round(achieved_tf, 1), "roofline": roofline, "clocks": clocks.summary(),
+            "gpu_launches": 4 * K, "gpu_launches_source": "gather, two decompression GEMMs, attention per chunk",
+            "e2e": e2e, "parity": parity, "cpu_baseline": cb}
 
 
 def main(argv=None):
@@ -579,6 +753,8 @@ def main(argv=None):
     rank, world, local = dist_env()
     if args.impl == "reference":
         res = run_reference(args, rank, world, local)
+    elif synth.WORKLOADS[args.workload].get("prefill"):
+        res = run_prefill(args, rank, world, local)
     else:
         res = run_ours(args, rank, world, local)
     if rank == 0 and res is not None:

@@ -61,10 +61,15 @@ class DecodeInputs:
     kv_scale: Optional[torch.Tensor] = None  # fp32 [N_pg, 64]        (fp8 cache)
     kr: Optional[torch.Tensor] = None        # bf16 [N_pg, 64, 64]    (fp8 cache)
     seed: int = DEFAULT_SEED
+    queries_per_seq: int = 1      # q_c / q_r hold batch * queries_per_seq rows (row b*q + t: token t of b)
 
     @property
     def batch(self) -> int:
         return int(self.seq_lens.shape[0])
+
+    @property
+    def rows(self) -> int:
+        return self.batch * self.queries_per_seq
 
     @property
     def max_pages(self) -> int:
@@ -93,11 +98,13 @@ def make_inputs(
     poison_tail: bool = False,
     ragged: Optional[tuple] = None,
     batch: Optional[int] = None,
+    queries_per_seq: int = 1,
 ) -> DecodeInputs:
     """Draw one decode batch.
 
     ``seq_lens``: list of context lengths, or ``None`` with ``ragged=(lo, hi)`` and
-    ``batch`` to draw them (first, from the same generator).
+    ``batch`` to draw them (first, from the same generator).  ``queries_per_seq`` = q > 1 draws
+    q query rows per sequence (several new tokens decoded at once; the lengths count them).
     """
     gen = torch.Generator(device="cpu")
     gen.manual_seed(seed)
@@ -113,8 +120,11 @@ def make_inputs(
     n_pages = int(pages_per_seq.sum())
     max_pages = int(pages_per_seq.max())
 
-    q_c = _bf16(torch.randn(B, NUM_HEADS, D_HC, generator=gen))
-    q_r = _bf16(torch.randn(B, NUM_HEADS, D_R, generator=gen))
+    if queries_per_seq < 1 or (lens < queries_per_seq).any():
+        raise ValueError("queries_per_seq must be >= 1 and at most every length")
+    rows = B * queries_per_seq
+    q_c = _bf16(torch.randn(rows, NUM_HEADS, D_HC, generator=gen))
+    q_r = _bf16(torch.randn(rows, NUM_HEADS, D_R, generator=gen))
     wstd = 1.0 / math.sqrt(D_C)
     w_uk = _bf16(torch.randn(NUM_HEADS, D_HC, D_C, generator=gen) * wstd)
     w_uv = _bf16(torch.randn(NUM_HEADS, D_HC, D_C, generator=gen) * wstd)
@@ -153,7 +163,7 @@ def make_inputs(
 
     inp = DecodeInputs(
         seq_lens=lens, block_table=block_table, num_pool_pages=n_pages,
-        q_c=q_c, q_r=q_r, w_uk=w_uk, w_uv=w_uv, kv_dtype=kv_dtype, seed=seed,
+        q_c=q_c, q_r=q_r, w_uk=w_uk, w_uv=w_uv, kv_dtype=kv_dtype, seed=seed, queries_per_seq=queries_per_seq,
     )
     if kv_dtype == "bf16":
         pool = torch.empty(n_pages, PAGE, D_ROW, dtype=torch.bfloat16)
@@ -190,12 +200,19 @@ WORKLOADS = {
                        desc="B=64, S uniform on [128, 32768] from the seed, shuffled pages, bf16 cache"),
     "b128_s8192_fp8": dict(seq_lens=[8192] * 128, shuffle_pages=True, kv_dtype="fp8_e4m3",
                            desc="B=128, S=8192 each, c_KV e4m3 + fp32 per-token absmax scale, k_R bf16"),
+    "b16_s8192_q4": dict(seq_lens=[8192] * 16, shuffle_pages=True, queries_per_seq=4,
+                         desc="B=16, S=8192 each, 4 new tokens per sequence decoded at once (causal among them), "
+                              "bf16 cache"),
+    "prefill_s16384_t4096": dict(seq_lens=[16384], shuffle_pages=True, queries_per_seq=4096, prefill=True,
+                                 desc="prefill chunk: the last 4,096 tokens of one 16,384-token sequence, causal, "
+                                      "decompressed form, bf16 cache"),
 }
 
 
 def make_workload(name: str, *, seed: int = DEFAULT_SEED, poison_tail: bool = False) -> DecodeInputs:
     kw = dict(WORKLOADS[name])
     kw.pop("desc")
+    kw.pop("prefill", None)
     return make_inputs(kw.pop("seq_lens"), seed=seed, poison_tail=poison_tail, **kw)
 
 

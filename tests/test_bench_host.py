@@ -5,6 +5,7 @@ import os
 import socket
 import sys
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -80,17 +81,21 @@ def test_accounting_matches_roofline_table():
     from mla_latent_kv_absorb_gb300 import synth
 
     class Fake:
-        kv_dtype = "bf16"
-        batch = 16
-        num_tokens = 16 * 65536
+        def __init__(self, kv_dtype, lens, q=1):
+            self.kv_dtype, self.seq_lens, self.queries_per_seq = kv_dtype, np.asarray(lens, np.int32), q
+            self.batch, self.num_tokens, self.rows = len(lens), int(sum(lens)), len(lens) * q
 
-    acc = bench.workload_accounting(Fake())
+    acc = bench.workload_accounting(Fake("bf16", [65536] * 16))
     assert acc["kv_bytes"] == 1_207_959_552          # 16 x 1024 pages x 73,728 B
     assert abs(acc["step_flop"] / 1e9 - 292.6) < 0.5   # QK + PV + absorb + out-proj
     assert abs(acc["step_bytes"] / 1e6 - 1242.8) < 1.0
-    Fake.kv_dtype, Fake.batch, Fake.num_tokens = "fp8_e4m3", 128, 128 * 8192
-    acc = bench.workload_accounting(Fake())
+    acc = bench.workload_accounting(Fake("fp8_e4m3", [8192] * 128))
     assert acc["kv_bytes"] == 128 * 8192 * 644         # e4m3 latent + fp32 scale + bf16 k_R
+    # four new tokens per sequence: the cache is read once, the attention FLOPs follow the rows
+    acc = bench.workload_accounting(Fake("bf16", [8192] * 16, q=4))
+    assert acc["kv_bytes"] == 16 * 8192 * 1152
+    assert acc["scanned"] == 16 * (8189 + 8190 + 8191 + 8192)
+    assert acc["decode_flop"] == acc["scanned"] * 128 * 2 * (576 + 512)
 
 
 def test_warmup_floor():
