@@ -203,6 +203,9 @@ WORKLOADS = {
     "b16_s8192_q4": dict(seq_lens=[8192] * 16, shuffle_pages=True, queries_per_seq=4,
                          desc="B=16, S=8192 each, 4 new tokens per sequence decoded at once (causal among them), "
                               "bf16 cache"),
+    "prefill_s4096_t1024": dict(seq_lens=[4096], shuffle_pages=True, queries_per_seq=1024, prefill=True,
+                                desc="prefill chunk: the last 1,024 tokens of one 4,096-token sequence, causal, "
+                                     "decompressed form, bf16 cache"),
     "prefill_s16384_t4096": dict(seq_lens=[16384], shuffle_pages=True, queries_per_seq=4096, prefill=True,
                                  desc="prefill chunk: the last 4,096 tokens of one 16,384-token sequence, causal, "
                                       "decompressed form, bf16 cache"),
