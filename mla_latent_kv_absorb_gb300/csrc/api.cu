@@ -127,9 +127,11 @@ mla_status launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sm
 // [128][128][512].
 // shared_act_row > 0: one activation row of that many elements per batch row, shared by all
 // heads (the first K_TOTAL elements are the operand).
+// head_major: out is [128 heads][batch][n_total] instead of [batch][128 heads][n_total].
 template <int K_TOTAL, int N_TILE, bool W_MN, int STAGES>
 mla_status launch_head_gemm(const void* act, const void* weight, void* out, int32_t batch, int n_total,
-                            cuuint32_t w_box_rows, bool pdl, void* stream, int shared_act_row = 0)
+                            cuuint32_t w_box_rows, bool pdl, void* stream, int shared_act_row = 0,
+                            bool head_major = false)
 {
     using C = Cfg<K_TOTAL, N_TILE, W_MN, STAGES>;
     CUtensorMap tm_a, tm_w;
@@ -148,7 +150,8 @@ mla_status launch_head_gemm(const void* act, const void* weight, void* out, int3
     args.out = static_cast<__nv_bfloat16*>(out);
     args.a_x_per_head = shared_act_row > 0 ? 0 : K_TOTAL;
     args.batch = batch;
-    args.out_row_stride = (int64_t)128 * n_total;
+    args.out_row_stride = head_major ? (int64_t)n_total : (int64_t)128 * n_total;
+    args.out_head_stride = head_major ? (int64_t)batch * n_total : (int64_t)n_total;
     args.n_total = n_total;
     args.dev_error = nullptr;
     args.timeout_ns = kDefaultTimeoutNs;
@@ -476,8 +479,8 @@ mla_status gather_one_sequence(mla_kv_dtype kv_dtype, const void* kv_pool, const
 
 namespace {
 
-// Workspace of the decompressed prefill: gathered rows [S][576], k [S][128][128], v [S][128][128]
-// (bf16), each section 1024-byte aligned.
+// Workspace of the decompressed prefill: gathered rows [S][576], k [128][S][128], v [128][S][128]
+// (bf16, head-major), each section 1024-byte aligned.
 struct PrefillLayout {
     size_t rows, k, v, total;
 };
@@ -527,10 +530,10 @@ extern "C" mla_status mla_prefill_decompressed(mla_kv_dtype kv_dtype, const void
                                              max_pages, seq_len, rows, dev_error, stream);
     if (st != MLA_OK) return st;
     // 2. per-head keys and values (the out-proj GEMM shape, activations shared by the heads)
-    if ((st = launch_head_gemm<512, kOutN, false, kOutStages>(rows, w_uk, k, seq_len, 128, kOutN, false, stream, 576)) !=
-            MLA_OK ||
-        (st = launch_head_gemm<512, kOutN, false, kOutStages>(rows, w_uv, v, seq_len, 128, kOutN, false, stream, 576)) !=
-            MLA_OK)
+    if ((st = launch_head_gemm<512, kOutN, false, kOutStages>(rows, w_uk, k, seq_len, 128, kOutN, false, stream, 576,
+                                                              true)) != MLA_OK ||
+        (st = launch_head_gemm<512, kOutN, false, kOutStages>(rows, w_uv, v, seq_len, 128, kOutN, false, stream, 576,
+                                                              true)) != MLA_OK)
         return st;
     // 3. causal attention of the chunk's queries
     CUtensorMap tm_qc, tm_qr, tm_k, tm_kr, tm_v;
@@ -539,9 +542,10 @@ extern "C" mla_status mla_prefill_decompressed(mla_kv_dtype kv_dtype, const void
     const cuuint64_t qr_dims[3] = {64, 128, (cuuint64_t)chunk_len};
     const cuuint64_t qr_str[2] = {64 * 2, 128 * 64 * 2};
     const cuuint32_t q_box[3] = {64, 1, 128};
-    const cuuint64_t k_dims[3] = {128, 128, (cuuint64_t)seq_len};
-    const cuuint64_t k_str[2] = {128 * 2, 128 * 128 * 2};
-    const cuuint32_t k_box[3] = {64, 1, 64};
+    // k and v head-major [128 heads][S][128]: boxes of 64 dims x 64 keys of one head
+    const cuuint64_t k_dims[3] = {128, (cuuint64_t)seq_len, 128};
+    const cuuint64_t k_str[2] = {128 * 2, (cuuint64_t)seq_len * 128 * 2};
+    const cuuint32_t k_box[3] = {64, 64, 1};
     const cuuint64_t r_dims[2] = {576, (cuuint64_t)seq_len};
     const cuuint64_t r_str[1] = {576 * 2};
     const cuuint32_t r_box[2] = {64, 64};
@@ -557,7 +561,8 @@ extern "C" mla_status mla_prefill_decompressed(mla_kv_dtype kv_dtype, const void
     p.dev_error = dev_error;
     p.timeout_ns = kDefaultTimeoutNs;
     if (!set_smem(mla::prefill::prefill_attn_kernel, mla::prefill::kSmemBytes)) return MLA_ERR_CUDA;
-    const dim3 grid((unsigned)((chunk_len + mla::prefill::kQ - 1) / mla::prefill::kQ), 128);
+    constexpr int kQueriesPerCta = mla::prefill::kQ * mla::prefill::kQT;
+    const dim3 grid((unsigned)((chunk_len + kQueriesPerCta - 1) / kQueriesPerCta), 128);
     mla::prefill::prefill_attn_kernel<<<grid, mla::prefill::kThreads, mla::prefill::kSmemBytes,
                                         static_cast<cudaStream_t>(stream)>>>(tm_qc, tm_qr, tm_k, tm_kr, tm_v, p);
     return launch_status();

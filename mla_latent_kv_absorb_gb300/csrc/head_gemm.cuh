@@ -3,9 +3,9 @@
 //   absorb   (page 1 section 4, path B):  q_abs[b,h,c] = sum_d q_c[b,h,d] * W_UK[h,d,c]
 //   out-proj (value side of absorption):  out[b,h,d]   = sum_c o_lat[b,h,c] * W_UV[h,d,c]
 //
-//   decompression (page 1 section 4, path A): k[s,h,d] = sum_c c_KV[s,c] * W_UK[h,d,c] and
-//            v[s,h,d] = sum_c c_KV[s,c] * W_UV[h,d,c], the out-proj shape with one activation
-//            row per token shared by all heads.
+//   decompression (page 1 section 4, path A): k[h,s,d] = sum_c c_KV[s,c] * W_UK[h,d,c] and
+//            v[h,s,d] = sum_c c_KV[s,c] * W_UV[h,d,c], the out-proj shape with one activation
+//            row per token shared by all heads, written head-major.
 //
 // One CTA computes a 128 (batch rows) x N_TILE tile of one head.  The batch rows are the MMA's
 // M dimension, so small batches leave rows empty (TMA fills rows past the batch with zeros,
@@ -50,6 +50,7 @@ struct Args {
     int a_x_per_head;        // K_TOTAL when each head has its own activation row, 0 when shared
     int batch;
     int64_t out_row_stride;  // elements between consecutive batch rows of `out`
+    int64_t out_head_stride; // elements between the outputs of consecutive heads
     int n_total;             // N of one head (512 absorb, 128 out-proj)
     uint32_t* dev_error;
     uint64_t timeout_ns;
@@ -162,7 +163,7 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
         const int q = warp & 3, row = 32 * q + lane, m = m0 + row;
         if (__all_sync(0xffffffffu, wait_phase(bar_done, 0, w) && !*abort_flag)) {
             tc_fence_after();
-            __nv_bfloat16* dst = args.out + (int64_t)m * args.out_row_stride + (int64_t)h * args.n_total + n0;
+            __nv_bfloat16* dst = args.out + (int64_t)m * args.out_row_stride + (int64_t)h * args.out_head_stride + n0;
 #pragma unroll 1
             for (int j = 0; j < N_TILE / 32; ++j) {
                 uint32_t r[32];

@@ -198,6 +198,22 @@ def test_end_to_end_b16_s65536_sampled():
     assert_close(out[:, heads, :], ref, TOL_BF16, "out (3 heads)")
 
 
+def test_end_to_end_one_sequence_of_a_million_tokens():
+    """The longest case: one sequence of 1,048,575 tokens (16,384 pages, the last one short by a
+    token, NaN-poisoned past its end), so every CTA pair scans a piece of it and the merge
+    combines more partials than one warp has lanes; the oracle computes three heads."""
+    inp = synth.make_inputs([1048575], seed=77, poison_tail=True)
+    out, step = _run_step(inp)
+    assert step.info.num_combine == 1 and step.info.max_splits == binding.num_sms() // 2 > 32
+    heads = [0, 64, 127]
+    q_abs = oracle.absorb_q(inp.q_c, inp.w_uk)
+    o, _ = oracle.latent_attention(inp, q_abs, softmax_scale=SCALE, heads=heads)
+    full = np.zeros((inp.batch, 128, 512))
+    full[:, heads, :] = o
+    ref = oracle.out_proj(full, inp.w_uv)[:, heads, :]
+    assert_close(out[:, heads, :], ref, TOL_BF16, "out (3 heads, 1M tokens)")
+
+
 def test_step_is_deterministic():
     inp = synth.make_inputs([5000, 300, 64], seed=7, poison_tail=True)
     q_c, q_r, w_uk, w_uv, kv, bt = binding.inputs_to_device(inp, DEV)
