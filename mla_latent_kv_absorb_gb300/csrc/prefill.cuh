@@ -14,23 +14,39 @@
 // One CTA = two tiles of 128 queries (A and B) of one head, sharing every 64-key tile, so 40 KB
 // of keys and values feed twice the MMA work (the per-SM TMA ingress, not the tensor core, set
 // the pace with one query tile).  Keys (k and k_R, 24 KB a tile) and values (16 KB) have rings
-// of their own, two stages each: a key stage is refilled as soon as its QK products are done,
-// long before the tile's PV, so the key loads hide behind the softmax.  Warp 0 streams the
-// queries and keys, warp 2 the values, warp 1 issues the MMAs (PV of tile n, then QK of tile
-// n + 2), warps 3-6 run the online softmax of query tile A and warps 7-10 that of B, one query
-// row per thread (its TMEM lane).  TMEM per query tile: two 64-column score buffers and a
-// 128-column output (512 columns in all).
-//   QK:  S[128 x 64]  = Q [128 x 192] (q_c | q_R, three 64-column K-major chunks)
+// of their own, three stages each: a key stage is refilled as soon as its QK products are
+// done, long before the tile's PV.  Warp 0 streams the queries and keys, warp 2 the values,
+// warp 1 issues the MMAs (PV of tile n, then QK of tile n + 2), warps 3-6 run the online
+// softmax of query tile A and warps 7-10 that of B, one query row per thread (its TMEM lane).
+// TMEM per query tile: two 64-column score buffers and a 128-column output (512 columns in
+// all).  P goes back into the first 32 columns of its score buffer (bf16 pairs), where the PV
+// MMA reads it as a tensor-memory operand: no shared memory for P, and no wait on the previous
+// PV before it is written (the buffer's last reader, PV of tile n - 2, finished before the
+// scores of tile n were complete).
+//   QK:  S[128 x 64]  = Q [128 x 192] (q_c | q_R, three 64-column K-major chunks in shared memory)
 //                       x K tile [64 x 192] (k | k_R, three K-major chunks)
-//   PV:  O[128 x 128] += P [128 x 64] (bf16, K-major, written by the softmax warps)
+//   PV:  O[128 x 128] += P [128 x 64] (bf16 in TMEM)
 //                       x V tile [64 keys x 128] (MN-major: keys are K, dims are N)
 // The running max moves only when a tile's max exceeds it by more than 8 (log2 units); the
 // output is then rescaled in TMEM before the tile's PV.  Every wait is bounded.
 #pragma once
 #include "ptx.cuh"
+#ifdef MLA_PREFILL_TRACE
+#include <cstdio>
+#endif
 
 namespace mla {
 namespace prefill {
+
+#ifdef MLA_PREFILL_TRACE
+// instrumented builds only: event times (ns from the CTA's start) of CTA (0, 0), printed at its end
+constexpr int kTraceTiles = 24;
+#define PF_TRACE(arr, n, k) \
+    do { if (trace_cta && (n) < kTraceTiles) (arr)[(n) * 4 + (k)] = globaltimer_ns() - trace_t0; } while (0)
+#else
+#define PF_TRACE(arr, n, k) \
+    do { } while (0)
+#endif
 
 constexpr int kQ = 128;        // queries per query tile (MMA M)
 constexpr int kQT = 2;         // query tiles per CTA
@@ -42,13 +58,11 @@ constexpr int kQBytes = 3 * kQChunk;                       // one query tile: q_
 constexpr int kKVBox = kKV * 64 * 2;                       // [64 rows][64] bf16, 8 KB
 constexpr int kKStage = 3 * kKVBox;                        // k 0-63, k 64-127, k_R
 constexpr int kVStage = 2 * kKVBox;                        // v 0-63, v 64-127
-constexpr int kStages = 2;
-constexpr int kPBytes = kQ * kKV * 2;                      // [128 queries][64 keys] bf16
+constexpr int kStages = 3;
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kQT * kQBytes;               // 96 KB
-constexpr int kOffV = kOffK + kStages * kKStage;           // 144 KB
-constexpr int kOffP = kOffV + kStages * kVStage;           // 176 KB
-constexpr int kOffBar = kOffP + kQT * kPBytes;             // 208 KB
+constexpr int kOffV = kOffK + kStages * kKStage;           // 168 KB
+constexpr int kOffBar = kOffV + kStages * kVStage;         // 216 KB
 constexpr int kSmemBytes = kOffBar + 256;
 constexpr uint32_t kTmemCols = 512;                        // per query tile t: S at 256 t + {0, 64}, O at 256 t + 128
 constexpr float kRescaleLog2 = 8.f;
@@ -66,15 +80,24 @@ struct Params {
 enum : int {
     kBarQ = 0,
     kBarKFull = 1,      // [stage]
-    kBarKEmpty = 3,     // [stage]
-    kBarVFull = 5,      // [stage]
-    kBarVEmpty = 7,     // [stage]
-    kBarSFull = 9,      // [tile][buffer]
-    kBarPReady = 13,    // [tile], 128 arrivals
-    kBarPvDone = 15,    // [tile]
-    kBarDone = 17,
-    kBarCount = 18,
+    kBarKEmpty = 4,     // [stage]
+    kBarVFull = 7,      // [stage]
+    kBarVEmpty = 10,    // [stage]
+    kBarSFull = 13,     // [tile][buffer]
+    kBarPReady = 17,    // [tile][buffer], 128 arrivals
+    kBarPvDone = 21,    // [tile]
+    kBarDone = 23,      // every MMA of the CTA has finished
+    kBarCount = 24,
 };
+// Phase bookkeeping.  A barrier waited by parity must never run two phases ahead of its waiter:
+//   S full [t][b]   completes for tiles b, b + 2, ...; QK of tile n + 2 is issued only after the
+//                   MMA thread has seen P of tile n ready, so the softmax is never two behind.
+//   P ready [t][b]  arrives for tiles b, b + 2, ...; the softmax makes P of tile n + 2 only from
+//                   the scores of tile n + 2, which follow the PV of tile n.
+//   PV done [t]     completes for every tile; the softmax waits it (for tile n - 1) only while
+//                   at tile n, after the scores of tile n, whose commit covers the PV of tile
+//                   n - 2, so exactly one phase can be pending.  The final read of O waits on
+//                   kBarDone instead.
 
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_qc, const __grid_constant__ CUtensorMap tm_qr,
@@ -102,7 +125,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_qc, const __grid_cons
 
     if (threadIdx.x == 0) {
         mbar_init(bar(kBarQ, 0), 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kStages; ++s) {
             mbar_init(bar(kBarKFull, s), 1);
             mbar_init(bar(kBarKEmpty, s), 1);
             mbar_init(bar(kBarVFull, s), 1);
@@ -111,7 +134,8 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_qc, const __grid_cons
         for (int t = 0; t < kQT; ++t) {
             mbar_init(bar(kBarSFull, 2 * t), 1);
             mbar_init(bar(kBarSFull, 2 * t + 1), 1);
-            mbar_init(bar(kBarPReady, t), 128);
+            mbar_init(bar(kBarPReady, 2 * t), 128);
+            mbar_init(bar(kBarPReady, 2 * t + 1), 128);
             mbar_init(bar(kBarPvDone, t), 1);
         }
         mbar_init(bar(kBarDone, 0), 1);
@@ -127,6 +151,11 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_qc, const __grid_cons
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
     const WaitCtx w{p.timeout_ns, abort_flag, p.dev_error};
+#ifdef MLA_PREFILL_TRACE
+    const bool trace_cta = blockIdx.x == 0 && blockIdx.y == 0;
+    const uint64_t trace_t0 = globaltimer_ns();
+    uint64_t tr[kTraceTiles * 4] = {};
+#endif
 
     if (warp == 0 || warp == 2) {
         if (lane == 0) {
@@ -145,8 +174,8 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_qc, const __grid_cons
             const int full_id = keys ? kBarKFull : kBarVFull, empty_id = keys ? kBarKEmpty : kBarVEmpty;
             int issued = 0;
             for (int n = 0; n < n_tiles; ++n) {
-                const int s = n & 1;
-                if (n >= 2 && !wait_phase(bar(empty_id, s), ((n - 2) >> 1) & 1, w)) break;
+                const int s = n % kStages;
+                if (n >= kStages && !wait_phase(bar(empty_id, s), (n / kStages - 1) & 1, w)) break;
                 const uint32_t full = bar(full_id, s);
                 const int j0 = n * kKV;
                 if (keys) {
@@ -165,8 +194,8 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_qc, const __grid_cons
             }
             // loads in flight land before the CTA can exit
             if (keys) drain_phase(bar(kBarQ, 0), 0, w.timeout_ns);
-            for (int n = (issued > 2 ? issued - 2 : 0); n < issued; ++n)
-                drain_phase(bar(full_id, n & 1), (n >> 1) & 1, w.timeout_ns);
+            for (int n = (issued > kStages ? issued - kStages : 0); n < issued; ++n)
+                drain_phase(bar(full_id, n % kStages), (n / kStages) & 1, w.timeout_ns);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -174,10 +203,10 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_qc, const __grid_cons
             constexpr uint32_t idesc_pv = idesc_bf16(128, 128, false, true);
             // both query tiles' scores for key tile n; the key stage is released when they finish
             const auto issue_qk = [&](int n) -> bool {
-                const int s = n & 1;
-                if (!wait_phase(bar(kBarKFull, s), (n >> 1) & 1, w)) return false;
+                const int s = n & 1, ks = n % kStages;
+                if (!wait_phase(bar(kBarKFull, ks), (n / kStages) & 1, w)) return false;
                 tc_fence_after();
-                const uint32_t st = sbase + kOffK + s * kKStage;
+                const uint32_t st = sbase + kOffK + ks * kKStage;
 #pragma unroll 1
                 for (int t = 0; t < kQT; ++t) {
 #pragma unroll 1
@@ -191,7 +220,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_qc, const __grid_cons
                     }
                     mma_commit(bar(kBarSFull, 2 * t + s));
                 }
-                mma_commit(bar(kBarKEmpty, s));
+                mma_commit(bar(kBarKEmpty, ks));
                 return true;
             };
             bool ok = wait_phase(bar(kBarQ, 0), 0, w) && (tc_fence_after(), issue_qk(0)) &&
@@ -199,26 +228,36 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_qc, const __grid_cons
             for (int n = 0; ok && n < n_tiles; ++n) {
                 // PV of tile n for both query tiles, then the scores of tile n + 2 into the freed
                 // score buffers
-                if (!(ok = wait_phase(bar(kBarVFull, n & 1), (n >> 1) & 1, w))) break;
-                const uint32_t vt = sbase + kOffV + (n & 1) * kVStage;
+                const int vs = n % kStages;
+                if (!(ok = wait_phase(bar(kBarVFull, vs), (n / kStages) & 1, w))) break;
+                PF_TRACE(tr, n, 0);
+                const uint32_t vt = sbase + kOffV + vs * kVStage;
 #pragma unroll 1
                 for (int t = 0; t < kQT && ok; ++t) {
-                    if (!(ok = wait_phase(bar(kBarPReady, t), n & 1, w))) break;
+                    if (!(ok = wait_phase(bar(kBarPReady, 2 * t + (n & 1)), (n >> 1) & 1, w))) break;
+                    PF_TRACE(tr, n, 1 + t);
                     tc_fence_after();
-                    const uint32_t pt = sbase + kOffP + t * kPBytes;
+                    const uint32_t pt = tmem + 256 * t + (n & 1) * kKV;  // P in its score buffer
 #pragma unroll
                     for (int k = 0; k < kKV / 16; ++k) {
-                        const uint64_t a = smem_desc(pt + 32 * k, 16, 1024);
                         const uint64_t b = smem_desc(vt + 2048 * k, 8192, 1024);
-                        mma_ss(tmem + 256 * t + 128, a, b, idesc_pv, (n | k) != 0 ? 1u : 0u);
+                        mma_ts(tmem + 256 * t + 128, pt + 8 * k, b, idesc_pv, (n | k) != 0 ? 1u : 0u);
                     }
                     mma_commit(bar(kBarPvDone, t));
                 }
                 if (!ok) break;
-                mma_commit(bar(kBarVEmpty, n & 1));
+                mma_commit(bar(kBarVEmpty, vs));
                 if (n + 2 < n_tiles && !(ok = issue_qk(n + 2))) break;
+                PF_TRACE(tr, n, 3);
             }
             mma_commit(bar(kBarDone, 0));  // arrives when every MMA issued here has finished
+#ifdef MLA_PREFILL_TRACE
+            if (trace_cta)
+                for (int n = 0; n < kTraceTiles && n < n_tiles; ++n)
+                    printf("mma %2d v %7llu pA %7llu pB %7llu qk+2 %7llu\n", n, (unsigned long long)tr[4 * n],
+                           (unsigned long long)tr[4 * n + 1], (unsigned long long)tr[4 * n + 2],
+                           (unsigned long long)tr[4 * n + 3]);
+#endif
         }
     } else {
         // softmax of query tile t: warp (3..10) & 3 selects the TMEM lane quarter, one row per thread
@@ -227,12 +266,12 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_qc, const __grid_cons
         const int qpos = min(first_pos + i, p.seq_len - 1);
         const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
         const uint32_t t_s = tmem + lane_base + 256 * t, t_o = t_s + 128;
-        uint8_t* prow = smem + kOffP + t * kPBytes + row * 128;
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int n = 0; n < n_tiles; ++n) {
             const int s = n & 1;
             if (!(ok = wait_warp(bar(kBarSFull, 2 * t + s), (n >> 1) & 1, w))) break;
+            PF_TRACE(tr, n, 0);
             tc_fence_after();
             uint32_t r[2][32];
             tmem_ld32(t_s + s * kKV, r[0]);
@@ -260,33 +299,35 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_qc, const __grid_cons
                 pk[k] = pack_bf16x2(a, b);
             }
             l = l * f + sum;
-            // the P buffer and the output: the previous tile's PV has finished with both
-            if (n > 0) {
+            if (__any_sync(0xffffffffu, grow)) {
+                // rescale O once the previous tile's PV has finished with it; every lane of the
+                // warp takes part (factor 1 where the max stayed)
                 if (!(ok = wait_warp(bar(kBarPvDone, t), (n - 1) & 1, w))) break;
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, grow)) {
-                    // rescale O; every lane of the warp takes part (factor 1 where the max stayed)
 #pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t o[32];
-                        tmem_ld32(t_o + 32 * c, o);
-                        tmem_wait_ld();
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(t_o + 32 * c, o);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
-                        tmem_st32(t_o + 32 * c, o);
-                    }
-                    tmem_wait_st();
+                    for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
+                    tmem_st32(t_o + 32 * c, o);
                 }
             }
-#pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8)
-                *reinterpret_cast<uint4*>(prow + ((c8 ^ (row & 7)) << 4)) =
-                    make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
-            fence_proxy_async_cta();  // the P tile is read by the tensor core (async proxy)
+            PF_TRACE(tr, n, 1);
+            tmem_st32(t_s + s * kKV, pk);  // P over the scores it was made from
+            tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(kBarPReady, t));
+            mbar_arrive(bar(kBarPReady, 2 * t + s));
+            PF_TRACE(tr, n, 2);
         }
-        if (ok && wait_warp(bar(kBarPvDone, t), (n_tiles - 1) & 1, w)) {
+#ifdef MLA_PREFILL_TRACE
+        if (trace_cta && lane == 0 && (warp == kSoftmaxWarp0 || warp == kSoftmaxWarp0 + 4))
+            for (int n = 0; n < kTraceTiles && n < n_tiles; ++n)
+                printf("smx t%d %2d s %7llu computed %7llu arrived %7llu\n", t, n, (unsigned long long)tr[4 * n],
+                       (unsigned long long)tr[4 * n + 1], (unsigned long long)tr[4 * n + 2]);
+#endif
+        if (ok && wait_warp(bar(kBarDone, 0), 0, w)) {
             tc_fence_after();
             const float inv = 1.f / l;
             __nv_bfloat16* dst = p.out + ((int64_t)i * 128 + h) * 128;
