@@ -348,7 +348,7 @@ MLA_API mla_status mla_decode_paged_static_ws(const mla_plan_info* info, const v
  *   out[t,h,:] = sum_j softmax_j((q_c[t,h] . k_h[j] + q_R[t,h] . k_R[j]) * softmax_scale) v_h[j].
  * Steps, all on `stream`: the sequence's rows gathered into bf16 (dequantised for FP8 and
  * NVFP4 caches, as mla_gather_kv), k_h and v_h for all heads (tcgen05 GEMMs), then a causal
- * attention kernel (2 x 128 queries x 1 head per CTA sharing 64-key tiles, online softmax).
+ * attention kernel (2 x 128 queries x 1 head per CTA sharing 128-key tiles, online softmax).
  *   kv_dtype, kv_pool, kv_scale, kr_pool, num_pool_pages   the cache, as mla_gather_kv
  *   block_table_row  device int32 [max_pages]: the sequence's pages (ceil(seq_len/64) <= max_pages)
  *   q_c, q_r         device bf16 [chunk_len][128][128] / [chunk_len][128][64]

@@ -542,13 +542,14 @@ extern "C" mla_status mla_prefill_decompressed(mla_kv_dtype kv_dtype, const void
     const cuuint64_t qr_dims[3] = {64, 128, (cuuint64_t)chunk_len};
     const cuuint64_t qr_str[2] = {64 * 2, 128 * 64 * 2};
     const cuuint32_t q_box[3] = {64, 1, 128};
-    // k and v head-major [128 heads][S][128]: boxes of 64 dims x 64 keys of one head
+    // k and v head-major [128 heads][S][128]: boxes of 64 dims x one key tile of one head
+    constexpr cuuint32_t kKeys = mla::prefill::kKV;
     const cuuint64_t k_dims[3] = {128, (cuuint64_t)seq_len, 128};
     const cuuint64_t k_str[2] = {128 * 2, (cuuint64_t)seq_len * 128 * 2};
-    const cuuint32_t k_box[3] = {64, 64, 1};
+    const cuuint32_t k_box[3] = {64, kKeys, 1};
     const cuuint64_t r_dims[2] = {576, (cuuint64_t)seq_len};
     const cuuint64_t r_str[1] = {576 * 2};
-    const cuuint32_t r_box[2] = {64, 64};
+    const cuuint32_t r_box[2] = {64, kKeys};
     if (!make_map_bf16(&tm_qc, q_c, 3, qc_dims, qc_str, q_box) || !make_map_bf16(&tm_qr, q_r, 3, qr_dims, qr_str, q_box) ||
         !make_map_bf16(&tm_k, k, 3, k_dims, k_str, k_box) || !make_map_bf16(&tm_kr, rows, 2, r_dims, r_str, r_box) ||
         !make_map_bf16(&tm_v, v, 3, k_dims, k_str, k_box))

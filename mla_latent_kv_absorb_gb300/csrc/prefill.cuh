@@ -11,24 +11,24 @@
 // v [128][S][128] (head-major); k_R comes from the gathered cache rows [S][576] (columns
 // 512..575).
 //
-// One CTA = two tiles of 128 queries (A and B) of one head, sharing every 64-key tile, so 40 KB
-// of keys and values feed twice the MMA work (the per-SM TMA ingress, not the tensor core, set
-// the pace with one query tile).  Keys (k and k_R, 24 KB a tile) and values (16 KB) have rings
-// of their own, three stages each: a key stage is refilled as soon as its QK products are
-// done, long before the tile's PV.  Warp 0 streams the queries and keys, warp 2 the values,
-// warp 1 issues the MMAs (PV of tile n, then QK of tile n + 2), warps 3-6 run the online
-// softmax of query tile A and warps 7-10 that of B, one query row per thread (its TMEM lane).
-// TMEM per query tile: two 64-column score buffers and a 128-column output (512 columns in
-// all).  P goes back into the first 32 columns of its score buffer (bf16 pairs), where the PV
-// MMA reads it as a tensor-memory operand: no shared memory for P, and no wait on the previous
-// PV before it is written (the buffer's last reader, PV of tile n - 2, finished before the
-// scores of tile n were complete).
-//   QK:  S[128 x 64]  = Q [128 x 192] (q_c | q_R, three 64-column K-major chunks in shared memory)
-//                       x K tile [64 x 192] (k | k_R, three K-major chunks)
-//   PV:  O[128 x 128] += P [128 x 64] (bf16 in TMEM)
-//                       x V tile [64 keys x 128] (MN-major: keys are K, dims are N)
-// The running max moves only when a tile's max exceeds it by more than 8 (log2 units); the
-// output is then rescaled in TMEM before the tile's PV.  Every wait is bounded.
+// One CTA = two tiles of 128 queries (A and B) of one head, sharing every 128-key tile, so the
+// key and value bytes feed twice the MMA work (the per-SM TMA ingress, not the tensor core, set
+// the pace with one query tile).  The tensor core's cost is per instruction up to N = 256, so
+// the key tile is 128 wide: each QK instruction is M = 128 queries x N = 128 keys.  TMEM per
+// query tile: one 128-column score buffer and a 128-column output (512 columns in all); the
+// softmax writes P (bf16 pairs) back over the first 64 columns of its scores, where the PV MMA
+// reads it as a tensor-memory operand.  With one score buffer per query tile the two tiles
+// alternate: the MMA order per key tile n is PV_A(n), QK_A(n+1), PV_B(n), QK_B(n+1), so while
+// one tile's softmax runs the tensor core works on the other tile's products.
+//   QK:  S[128 x 128] = Q [128 x 192] (q_c | q_R, three 64-column K-major chunks in shared memory)
+//                       x K tile [128 x 192] (k | k_R, three K-major chunks)
+//   PV:  O[128 x 128] += P [128 x 128] (bf16 in TMEM)
+//                       x V tile [128 keys x 128] (MN-major: keys are K, dims are N)
+// Warp 0 streams the queries and keys (two stages), warp 2 the values (one stage: a value tile
+// is needed only after the next key tile's QK products), warp 1 issues the MMAs, warps 3-6 and
+// 7-10 run the online softmax of tiles A and B, one query row per thread (its TMEM lane).  The
+// running max moves only when a tile's max exceeds it by more than 8 (log2 units); the output
+// is then rescaled in TMEM before the tile's PV.  Every wait is bounded.
 #pragma once
 #include "ptx.cuh"
 #ifdef MLA_PREFILL_TRACE
@@ -50,21 +50,21 @@ constexpr int kTraceTiles = 24;
 
 constexpr int kQ = 128;        // queries per query tile (MMA M)
 constexpr int kQT = 2;         // query tiles per CTA
-constexpr int kKV = 64;        // keys per key/value tile
+constexpr int kKV = 128;       // keys per key/value tile (QK MMA N)
 constexpr int kThreads = 32 * (3 + 4 * kQT);  // warps 0, 2 TMA, warp 1 MMA + TMEM, 4 softmax warps per query tile
 constexpr int kSoftmaxWarp0 = 3;
 constexpr int kQChunk = kQ * 64 * 2;                       // [128 rows][64] bf16, 16 KB
 constexpr int kQBytes = 3 * kQChunk;                       // one query tile: q_c 0-63, q_c 64-127, q_R
-constexpr int kKVBox = kKV * 64 * 2;                       // [64 rows][64] bf16, 8 KB
+constexpr int kKVBox = kKV * 64 * 2;                       // [128 rows][64] bf16, 16 KB
 constexpr int kKStage = 3 * kKVBox;                        // k 0-63, k 64-127, k_R
 constexpr int kVStage = 2 * kKVBox;                        // v 0-63, v 64-127
-constexpr int kStages = 3;
+constexpr int kKStages = 2;
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kQT * kQBytes;               // 96 KB
-constexpr int kOffV = kOffK + kStages * kKStage;           // 168 KB
-constexpr int kOffBar = kOffV + kStages * kVStage;         // 216 KB
+constexpr int kOffV = kOffK + kKStages * kKStage;          // 192 KB
+constexpr int kOffBar = kOffV + kVStage;                   // 224 KB
 constexpr int kSmemBytes = kOffBar + 256;
-constexpr uint32_t kTmemCols = 512;                        // per query tile t: S at 256 t + {0, 64}, O at 256 t + 128
+constexpr uint32_t kTmemCols = 512;                        // per query tile t: S at 256 t, O at 256 t + 128
 constexpr float kRescaleLog2 = 8.f;
 
 struct Params {
@@ -80,24 +80,23 @@ struct Params {
 enum : int {
     kBarQ = 0,
     kBarKFull = 1,      // [stage]
-    kBarKEmpty = 4,     // [stage]
-    kBarVFull = 7,      // [stage]
-    kBarVEmpty = 10,    // [stage]
-    kBarSFull = 13,     // [tile][buffer]
-    kBarPReady = 17,    // [tile][buffer], 128 arrivals
-    kBarPvDone = 21,    // [tile]
-    kBarDone = 23,      // every MMA of the CTA has finished
-    kBarCount = 24,
+    kBarKEmpty = 3,     // [stage]
+    kBarVFull = 5,
+    kBarVEmpty = 6,
+    kBarSFull = 7,      // [tile]
+    kBarPReady = 9,     // [tile], 128 arrivals
+    kBarDone = 11,      // every MMA of the CTA has finished
+    kBarCount = 12,
 };
 // Phase bookkeeping.  A barrier waited by parity must never run two phases ahead of its waiter:
-//   S full [t][b]   completes for tiles b, b + 2, ...; QK of tile n + 2 is issued only after the
-//                   MMA thread has seen P of tile n ready, so the softmax is never two behind.
-//   P ready [t][b]  arrives for tiles b, b + 2, ...; the softmax makes P of tile n + 2 only from
-//                   the scores of tile n + 2, which follow the PV of tile n.
-//   PV done [t]     completes for every tile; the softmax waits it (for tile n - 1) only while
-//                   at tile n, after the scores of tile n, whose commit covers the PV of tile
-//                   n - 2, so exactly one phase can be pending.  The final read of O waits on
-//                   kBarDone instead.
+//   S full [t]   completes once per key tile; QK_t(n + 1) is issued only after the MMA thread has
+//                seen P_t(n) ready, i.e. after the softmax finished tile n.
+//   P ready [t]  arrives once per key tile; P_t(n + 1) needs S_t(n + 1), issued after PV_t(n),
+//                i.e. after the MMA thread waited for P_t(n).
+//   K, V rings   each stage is refilled only after its consumer's commit, waited in order.
+// The rescale of O at tile n needs PV_t(n - 1) finished: S_t(n) complete implies it (QK_t(n) was
+// issued after PV_t(n - 1) and a commit covers every earlier MMA of the thread).  The final read
+// of O waits on kBarDone.
 
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_qc, const __grid_constant__ CUtensorMap tm_qr,
@@ -125,18 +124,15 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_qc, const __grid_cons
 
     if (threadIdx.x == 0) {
         mbar_init(bar(kBarQ, 0), 1);
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kKStages; ++s) {
             mbar_init(bar(kBarKFull, s), 1);
             mbar_init(bar(kBarKEmpty, s), 1);
-            mbar_init(bar(kBarVFull, s), 1);
-            mbar_init(bar(kBarVEmpty, s), 1);
         }
+        mbar_init(bar(kBarVFull, 0), 1);
+        mbar_init(bar(kBarVEmpty, 0), 1);
         for (int t = 0; t < kQT; ++t) {
-            mbar_init(bar(kBarSFull, 2 * t), 1);
-            mbar_init(bar(kBarSFull, 2 * t + 1), 1);
-            mbar_init(bar(kBarPReady, 2 * t), 128);
-            mbar_init(bar(kBarPReady, 2 * t + 1), 128);
-            mbar_init(bar(kBarPvDone, t), 1);
+            mbar_init(bar(kBarSFull, t), 1);
+            mbar_init(bar(kBarPReady, t), 128);
         }
         mbar_init(bar(kBarDone, 0), 1);
         *abort_flag = 0;
@@ -162,6 +158,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_qc, const __grid_cons
             // warp 0: the queries, then the key tiles; warp 2: the value tiles
             const uint64_t pol = l2_policy_evict_last();  // the head's other query tiles re-read them
             const bool keys = warp == 0;
+            const int stages = keys ? kKStages : 1;
             if (keys) {
                 mbar_arrive_expect_tx(bar(kBarQ, 0), kQT * kQBytes);
                 for (int t = 0; t < kQT; ++t) {
@@ -174,8 +171,8 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_qc, const __grid_cons
             const int full_id = keys ? kBarKFull : kBarVFull, empty_id = keys ? kBarKEmpty : kBarVEmpty;
             int issued = 0;
             for (int n = 0; n < n_tiles; ++n) {
-                const int s = n % kStages;
-                if (n >= kStages && !wait_phase(bar(empty_id, s), (n / kStages - 1) & 1, w)) break;
+                const int s = n % stages;
+                if (n >= stages && !wait_phase(bar(empty_id, s), (n / stages - 1) & 1, w)) break;
                 const uint32_t full = bar(full_id, s);
                 const int j0 = n * kKV;
                 if (keys) {
@@ -185,7 +182,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_qc, const __grid_cons
                     tma_load_3d(st + kKVBox, &tm_k, full, 64, j0, h, pol);
                     tma_load_2d(st + 2 * kKVBox, &tm_kr, full, 512, j0, pol);
                 } else {
-                    const uint32_t st = sbase + kOffV + s * kVStage;
+                    const uint32_t st = sbase + kOffV;
                     mbar_arrive_expect_tx(full, kVStage);
                     tma_load_3d(st, &tm_v, full, 0, j0, h, pol);
                     tma_load_3d(st + kKVBox, &tm_v, full, 64, j0, h, pol);
@@ -194,67 +191,66 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_qc, const __grid_cons
             }
             // loads in flight land before the CTA can exit
             if (keys) drain_phase(bar(kBarQ, 0), 0, w.timeout_ns);
-            for (int n = (issued > kStages ? issued - kStages : 0); n < issued; ++n)
-                drain_phase(bar(full_id, n % kStages), (n / kStages) & 1, w.timeout_ns);
+            for (int n = (issued > stages ? issued - stages : 0); n < issued; ++n)
+                drain_phase(bar(full_id, n % stages), (n / stages) & 1, w.timeout_ns);
         }
     } else if (warp == 1) {
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16(128, kKV, false, false);
             constexpr uint32_t idesc_pv = idesc_bf16(128, 128, false, true);
-            // both query tiles' scores for key tile n; the key stage is released when they finish
-            const auto issue_qk = [&](int n) -> bool {
-                const int s = n & 1, ks = n % kStages;
-                if (!wait_phase(bar(kBarKFull, ks), (n / kStages) & 1, w)) return false;
+            // the scores of query tile t for key tile n (its key stage has landed)
+            const auto issue_qk = [&](int t, int n) {
+                const uint32_t st = sbase + kOffK + (n % kKStages) * kKStage;
+#pragma unroll 1
+                for (int c = 0; c < 3; ++c) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint64_t a = smem_desc(sbase + kOffQ + t * kQBytes + c * kQChunk + 32 * k, 16, 1024);
+                        const uint64_t b = smem_desc(st + c * kKVBox + 32 * k, 16, 1024);
+                        mma_ss(tmem + 256 * t, a, b, idesc_qk, (c | k) != 0 ? 1u : 0u);
+                    }
+                }
+                mma_commit(bar(kBarSFull, t));
+            };
+            // PV of query tile t for key tile n: P from its score buffer, V from the value stage
+            const auto issue_pv = [&](int t, int n) {
+                const uint32_t pt = tmem + 256 * t;
+#pragma unroll
+                for (int k = 0; k < kKV / 16; ++k) {
+                    const uint64_t b = smem_desc(sbase + kOffV + 2048 * k, kKVBox, 1024);
+                    mma_ts(tmem + 256 * t + 128, pt + 8 * k, b, idesc_pv, (n | k) != 0 ? 1u : 0u);
+                }
+            };
+            bool ok = wait_phase(bar(kBarQ, 0), 0, w) && wait_phase(bar(kBarKFull, 0), 0, w);
+            if (ok) {
                 tc_fence_after();
-                const uint32_t st = sbase + kOffK + ks * kKStage;
+                for (int t = 0; t < kQT; ++t) issue_qk(t, 0);
+                mma_commit(bar(kBarKEmpty, 0));
+            }
+            for (int n = 0; ok && n < n_tiles; ++n) {
+                const bool more = n + 1 < n_tiles;
+                if (!(ok = wait_phase(bar(kBarVFull, 0), n & 1, w))) break;
+                if (more && !(ok = wait_phase(bar(kBarKFull, (n + 1) % kKStages), ((n + 1) / kKStages) & 1, w)))
+                    break;
+                PF_TRACE(tr, n, 0);
 #pragma unroll 1
                 for (int t = 0; t < kQT; ++t) {
-#pragma unroll 1
-                    for (int c = 0; c < 3; ++c) {
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const uint64_t a = smem_desc(sbase + kOffQ + t * kQBytes + c * kQChunk + 32 * k, 16, 1024);
-                            const uint64_t b = smem_desc(st + c * kKVBox + 32 * k, 16, 1024);
-                            mma_ss(tmem + 256 * t + s * kKV, a, b, idesc_qk, (c | k) != 0 ? 1u : 0u);
-                        }
-                    }
-                    mma_commit(bar(kBarSFull, 2 * t + s));
-                }
-                mma_commit(bar(kBarKEmpty, ks));
-                return true;
-            };
-            bool ok = wait_phase(bar(kBarQ, 0), 0, w) && (tc_fence_after(), issue_qk(0)) &&
-                      (n_tiles < 2 || issue_qk(1));
-            for (int n = 0; ok && n < n_tiles; ++n) {
-                // PV of tile n for both query tiles, then the scores of tile n + 2 into the freed
-                // score buffers
-                const int vs = n % kStages;
-                if (!(ok = wait_phase(bar(kBarVFull, vs), (n / kStages) & 1, w))) break;
-                PF_TRACE(tr, n, 0);
-                const uint32_t vt = sbase + kOffV + vs * kVStage;
-#pragma unroll 1
-                for (int t = 0; t < kQT && ok; ++t) {
-                    if (!(ok = wait_phase(bar(kBarPReady, 2 * t + (n & 1)), (n >> 1) & 1, w))) break;
+                    if (!(ok = wait_phase(bar(kBarPReady, t), n & 1, w))) break;
                     PF_TRACE(tr, n, 1 + t);
                     tc_fence_after();
-                    const uint32_t pt = tmem + 256 * t + (n & 1) * kKV;  // P in its score buffer
-#pragma unroll
-                    for (int k = 0; k < kKV / 16; ++k) {
-                        const uint64_t b = smem_desc(vt + 2048 * k, 8192, 1024);
-                        mma_ts(tmem + 256 * t + 128, pt + 8 * k, b, idesc_pv, (n | k) != 0 ? 1u : 0u);
-                    }
-                    mma_commit(bar(kBarPvDone, t));
+                    issue_pv(t, n);
+                    if (t == kQT - 1) mma_commit(bar(kBarVEmpty, 0));
+                    if (more) issue_qk(t, n + 1);  // into the score buffer PV_t(n) has just read
                 }
                 if (!ok) break;
-                mma_commit(bar(kBarVEmpty, vs));
-                if (n + 2 < n_tiles && !(ok = issue_qk(n + 2))) break;
+                if (more) mma_commit(bar(kBarKEmpty, (n + 1) % kKStages));
                 PF_TRACE(tr, n, 3);
             }
             mma_commit(bar(kBarDone, 0));  // arrives when every MMA issued here has finished
 #ifdef MLA_PREFILL_TRACE
             if (trace_cta)
                 for (int n = 0; n < kTraceTiles && n < n_tiles; ++n)
-                    printf("mma %2d v %7llu pA %7llu pB %7llu qk+2 %7llu\n", n, (unsigned long long)tr[4 * n],
+                    printf("mma %2d kv %7llu pA %7llu pB %7llu end %7llu\n", n, (unsigned long long)tr[4 * n],
                            (unsigned long long)tr[4 * n + 1], (unsigned long long)tr[4 * n + 2],
                            (unsigned long long)tr[4 * n + 3]);
 #endif
@@ -269,41 +265,28 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_qc, const __grid_cons
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int n = 0; n < n_tiles; ++n) {
-            const int s = n & 1;
-            if (!(ok = wait_warp(bar(kBarSFull, 2 * t + s), (n >> 1) & 1, w))) break;
+            if (!(ok = wait_warp(bar(kBarSFull, t), n & 1, w))) break;
             PF_TRACE(tr, n, 0);
             tc_fence_after();
-            uint32_t r[2][32];
-            tmem_ld32(t_s + s * kKV, r[0]);
-            tmem_ld32(t_s + s * kKV + 32, r[1]);
-            tmem_wait_ld();
             const int j0 = n * kKV;
-            float x[64];
+            // pass 1: the tile's row max (keys past the query's position masked)
             float mt = -INFINITY;
+#pragma unroll 1
+            for (int c = 0; c < kKV / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(t_s + 32 * c, r);
+                tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                const float v = __uint_as_float(r[c >> 5][c & 31]) * p.scale_log2;
-                x[c] = j0 + c <= qpos ? v : -INFINITY;
-                mt = fmaxf(mt, x[c]);
+                for (int k = 0; k < 32; ++k)
+                    if (j0 + 32 * c + k <= qpos) mt = fmaxf(mt, __uint_as_float(r[k]) * p.scale_log2);
             }
             // the running max: set by the first tile, moved later only by more than the threshold
             const bool grow = n > 0 && mt > m + kRescaleLog2;
             const float f = grow ? ex2_approx(m - mt) : 1.f;
             if (n == 0 || grow) m = mt;
-            float sum = 0.f;
-            uint32_t pk[32];
-#pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                const float a = ex2_approx(x[2 * k] - m), b = ex2_approx(x[2 * k + 1] - m);
-                sum += a + b;
-                pk[k] = pack_bf16x2(a, b);
-            }
-            l = l * f + sum;
             if (__any_sync(0xffffffffu, grow)) {
-                // rescale O once the previous tile's PV has finished with it; every lane of the
-                // warp takes part (factor 1 where the max stayed)
-                if (!(ok = wait_warp(bar(kBarPvDone, t), (n - 1) & 1, w))) break;
-                tc_fence_after();
+                // rescale O (the previous tile's PV has finished: see the phase notes); every lane
+                // of the warp takes part, factor 1 where the max stayed
 #pragma unroll 1
                 for (int c = 0; c < 4; ++c) {
                     uint32_t o[32];
@@ -314,11 +297,30 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_qc, const __grid_cons
                     tmem_st32(t_o + 32 * c, o);
                 }
             }
-            PF_TRACE(tr, n, 1);
-            tmem_st32(t_s + s * kKV, pk);  // P over the scores it was made from
+            // pass 2: P = 2^(s - m) in bf16 pairs over the first 64 columns of the scores (the P
+            // of chunk c lands on columns already read)
+            float sum = 0.f;
+#pragma unroll 1
+            for (int c = 0; c < kKV / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(t_s + 32 * c, r);
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const int j = j0 + 32 * c + 2 * k;
+                    const float a = j <= qpos ? ex2_approx(__uint_as_float(r[2 * k]) * p.scale_log2 - m) : 0.f;
+                    const float b = j + 1 <= qpos ? ex2_approx(__uint_as_float(r[2 * k + 1]) * p.scale_log2 - m) : 0.f;
+                    sum += a + b;
+                    pk[k] = pack_bf16x2(a, b);
+                }
+                tmem_st16(t_s + 16 * c, pk);
+            }
+            l = l * f + sum;
             tmem_wait_st();
+            PF_TRACE(tr, n, 1);
             tc_fence_before();
-            mbar_arrive(bar(kBarPReady, 2 * t + s));
+            mbar_arrive(bar(kBarPReady, t));
             PF_TRACE(tr, n, 2);
         }
 #ifdef MLA_PREFILL_TRACE
