@@ -26,7 +26,11 @@
 //                       x V tile [128 keys x 128] (MN-major: keys are K, dims are N)
 // Warp 0 streams the queries and keys (two stages), warp 2 the values (one stage: a value tile
 // is needed only after the next key tile's QK products), warp 1 issues the MMAs, warps 3-6 and
-// 7-10 run the online softmax of tiles A and B, one query row per thread (its TMEM lane).  The
+// 7-10 run the online softmax of tiles A and B, one query row per thread (its TMEM lane).
+// Every warp has exactly one role.  (Measured alternatives: 96-key tiles with two value stages,
+// 6.7 ms on the bench chunk, and one ring of two 48 KB slots shared by keys and values, 6.4 ms,
+// both slower than this layout's 5.8 ms: the wider QK instruction matters more than hiding the
+// value load.)  The
 // running max moves only when a tile's max exceeds it by more than 8 (log2 units); the output
 // is then rescaled in TMEM before the tile's PV.  Every wait is bounded.
 #pragma once
@@ -255,7 +259,7 @@ prefill_attn_kernel(const __grid_constant__ CUtensorMap tm_qc, const __grid_cons
                            (unsigned long long)tr[4 * n + 3]);
 #endif
         }
-    } else {
+    } else if (warp >= kSoftmaxWarp0 && warp < kSoftmaxWarp0 + 4 * kQT) {
         // softmax of query tile t: warp (3..10) & 3 selects the TMEM lane quarter, one row per thread
         const int t = (warp - kSoftmaxWarp0) >> 2;
         const int q4 = warp & 3, row = 32 * q4 + lane, i = i0 + kQ * t + row;
