@@ -71,3 +71,40 @@ def test_multi_query_host_paths_match_device_path():
     assert graphed._host_graph is not None
     assert one_call.device_error() == 0 and graphed.device_error() == 0
     assert torch.equal(got1, want) and torch.equal(got2, want)
+
+
+@pytest.mark.parametrize("fused_absorb,fused_tail", [(True, False), (False, True), (True, True)])
+def test_multi_query_through_the_fused_calls(fused_absorb, fused_tail):
+    """The fused absorb (decode prologue) and the fused merge + projection take the same query
+    rows: bit-identical to the separate kernels."""
+    q = 3
+    inp = _mq_inputs([2500, 64 * 7 + 3, 700], q, seed=960)
+    q_c, q_r, w_uk, w_uv, kv, bt = binding.inputs_to_device(inp, DEV)
+    mk = lambda **f: binding.DecodeStep(inp.seq_lens, w_uk=w_uk, w_uv=w_uv, block_table=bt, min_pages_per_split=2,
+                                        queries_per_seq=q, **kv, **f)
+    want = mk().run(q_c, q_r).clone()
+    step = mk(fused_absorb=fused_absorb, fused_tail=fused_tail)
+    got = step.run(q_c, q_r).clone()
+    torch.cuda.synchronize()
+    assert step.device_error() == 0 and step.info.num_combine > 0
+    assert torch.equal(got, want)
+
+
+def test_multi_query_static_workspace_matches():
+    """The no-allocation decode entry point takes the query rows too (same plan, same bits)."""
+    q = 2
+    inp = _mq_inputs([3000, 900], q, seed=970)
+    q_c, q_r, w_uk, w_uv, kv, bt = binding.inputs_to_device(inp, DEV)
+    step = binding.DecodeStep(inp.seq_lens, w_uk=w_uk, w_uv=w_uv, block_table=bt, min_pages_per_split=2,
+                              queries_per_seq=q, **kv)
+    step.run(q_c, q_r)
+    torch.cuda.synchronize()
+    assert step.info.num_partials <= binding.MLA_STATIC_WS_MAX_PARTIALS
+    o2 = torch.empty_like(step.o_lat)
+    l2 = torch.empty_like(step.lse)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    binding.mla_decode_paged_static_ws(step.info, step.plan_dev, step.q_abs, q_r, kv_pool=kv["kv_pool"],
+                                       block_table=bt, o_lat=o2, lse=l2, dev_error=err)
+    torch.cuda.synchronize()
+    assert binding.mla_read_device_error(err) == 0
+    assert torch.equal(o2, step.o_lat) and torch.equal(l2, step.lse)
