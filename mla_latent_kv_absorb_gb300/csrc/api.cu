@@ -210,7 +210,7 @@ mla_status launch_decode_fp8(const mla_plan_info* info, const void* plan_dev, co
                              void* workspace, void* o_lat, float* lse, uint32_t* dev_error, void* stream)
 {
     if (!aligned16(kr_pool) || (reinterpret_cast<uintptr_t>(kv_scale) & 3u)) return MLA_ERR_ALIGNMENT;
-    CUtensorMap tm_c8, tm_kr;
+    CUtensorMap tm_c8, tm_kr, tm_q;
     const cuuint64_t c_dims[3] = {512, 64, (cuuint64_t)num_pool_pages};
     const cuuint64_t c_strides[2] = {512, 64 * 512};
     const cuuint32_t c_box[3] = {128, 64, 1};
@@ -221,6 +221,11 @@ mla_status launch_decode_fp8(const mla_plan_info* info, const void* plan_dev, co
                   c_box) ||
         !make_map_bf16(&tm_kr, kr_pool, 3, r_dims, r_strides, r_box))
         return MLA_ERR_CUDA;
+    // q_abs as [batch * 128 rows][512], boxes of 128 rows (one query row's heads) x 64 dims
+    const cuuint64_t q_dims[2] = {512, (cuuint64_t)info->batch * 128};
+    const cuuint64_t q_str[1] = {512 * 2};
+    const cuuint32_t q_box[2] = {64, 128};
+    if (!make_map_bf16(&tm_q, q_abs, 2, q_dims, q_str, q_box)) return MLA_ERR_CUDA;
 
     mla::decode_fp8::Params p;
     p.plan = static_cast<const int32_t*>(plan_dev);
@@ -247,7 +252,7 @@ mla_status launch_decode_fp8(const mla_plan_info* info, const void* plan_dev, co
 
     if (!set_smem(mla::decode_fp8::decode_fp8_kernel, mla::decode_fp8::kSmemBytes)) return MLA_ERR_CUDA;
     return launch_pdl(mla::decode_fp8::decode_fp8_kernel, dim3(2 * info->num_clusters), dim3(mla::decode_fp8::kThreads),
-                      mla::decode_fp8::kSmemBytes, static_cast<cudaStream_t>(stream), tm_c8, tm_kr, p);
+                      mla::decode_fp8::kSmemBytes, static_cast<cudaStream_t>(stream), tm_c8, tm_kr, tm_q, p);
 }
 
 // Host checks shared by the decode entry points (nothing is launched when one fails).

@@ -31,7 +31,10 @@
 //   rank 0, the score CTA: q_hi and q_lo in TMEM (128 columns each, four e4m3 per 32-bit
 //     column), the scores of four pages in the other 256 columns.  Per four-page group the four
 //     128-column boxes of c8 (8 KB per page, 32 KB per K-chunk) stream through a three-slot
-//     ring, and the k_R boxes (8 KB per page) through a buffer of their own.  Eight softmax warps, the shipper and tracker as in
+//     ring, and the k_R boxes (8 KB per page) through a buffer of their own.  An item's bf16
+//     q_abs rows go through the same ring ahead of its pages (four entries of two 64-dim boxes);
+//     the MMA thread copies them into the score columns (tcgen05.cp) and the softmax warps turn
+//     them into the e4m3 pair, so the query costs coalesced TMA traffic and no register file.  Eight softmax warps, the shipper and tracker as in
 //     the bf16 kernel; warp 11 turns k_R into k_R / sigma and writes the per-token factors the
 //     softmax needs (sigma * scale * log2(e), sigma * g).
 //   rank 1, the value CTA: O in TMEM (512 columns), four 32 KB c8 page stages, PV from P~;
@@ -43,6 +46,8 @@
 //   kr_full / kr_empty    k_R / sigma is in place (warp 11) / the MMA has read it (commit)
 //   sig_ready             counter: groups whose token factors are written (warp 11)
 //   p_ready[4]            the value CTA's P~ of a message is written (its four converter warps)
+//   q_raw                 the item's bf16 query is in the score columns (the MMA thread's commit
+//                         after its copies; waited by the softmax warps)
 #pragma once
 #include "decode.cuh"
 
@@ -66,6 +71,7 @@ constexpr int kKrWarp = 11;                       // score CTA: k_R / sigma, tok
 constexpr int kAckWarp = 6;                       // value CTA: message acknowledgements
 constexpr int kPConvWarp0 = 7;                    // value CTA: warps 7-10 turn P into P~ (e4m3 pair)
 constexpr int kChunkStages = 3;                   // score CTA: c8 K-chunk ring
+constexpr int kQueryEntries = 4;                  // ring entries carrying an item's q_abs (two 16 KB boxes each)
 constexpr int kValueStages = 4;
 constexpr int kMaxStages = 4;
 constexpr int kStagingSlots = 4;
@@ -120,7 +126,8 @@ enum Bar : int {
     kKrFull = kKrLanded + 1,
     kKrEmpty = kKrFull + 1,
     kPReady0 = kKrEmpty + 1,
-    kNumBars = kPReady0 + kMsgSlots
+    kQRaw = kPReady0 + kMsgSlots,
+    kNumBars = kQRaw + 1
 };
 
 constexpr int kOffTmemHolder = kOffBars + 8 * kNumBars;
@@ -289,18 +296,40 @@ __device__ __forceinline__ void value_producer(const CUtensorMap* tm_c8, const P
 // Score CTA: chunk j of a four-page group holds c8 box j (128 columns) of the group's pages in
 // rows 0-63, 64-127, 128-191, 192-255, through a three-slot ring; the k_R box has a buffer of
 // its own that warp 11 fills (see kr_convert).
-__device__ __forceinline__ void score_producer(const CUtensorMap* tm_c8, const Params& p, int item_begin,
-                                               int item_end, int items_off, uint32_t sbase, uint32_t bars,
-                                               const dev::WaitCtx& w, int lane)
+__device__ __forceinline__ void score_producer(const CUtensorMap* tm_c8, const CUtensorMap* tm_q, const Params& p,
+                                               int item_begin, int item_end, int items_off, uint32_t sbase,
+                                               uint32_t bars, const dev::WaitCtx& w, int lane)
 {
     using namespace dev;
     const uint64_t policy = l2_policy_evict_last();  // the value CTA reads these pages next
-    if (lane == 0) tma_prefetch_desc(tm_c8);
+    if (lane == 0) {
+        tma_prefetch_desc(tm_c8);
+        tma_prefetch_desc(tm_q);
+    }
     int s = 0, phase = 0, c = 0;
     bool ok = true;
     for (int i = item_begin; i < item_end && ok; ++i) {
         const Item it = load_item(p.plan, items_off, i);
         const int32_t* bt = p.block_table + (int64_t)it.table_row * p.max_pages;
+        if (lane == 0) {
+            // the item's q_abs rows (128 heads x 512 dims) as four ring entries of two 64-dim
+            // boxes each, ahead of its pages; the softmax warps read and release them
+            if (i == item_begin) griddep_wait();  // q_abs comes from the kernel launched before
+            for (int j = 0; j < kQueryEntries && ok; ++j, ++c) {
+                if (c >= kChunkStages) ok = wait_phase_ool(bars + 8 * (kEmpty0 + s), phase - 1, w);
+                if (!ok) break;
+                const uint32_t full = bars + 8 * (kFull0 + s);
+                const uint32_t dst = sbase + kOffChunks + s * kChunkBytes;
+                mbar_arrive_expect_tx(full, kChunkBytes);
+                tma_load_2d(dst, tm_q, full, 128 * j, 128 * it.seq, policy);
+                tma_load_2d(dst + kChunkBytes / 2, tm_q, full, 128 * j + 64, 128 * it.seq, policy);
+                if (++s == kChunkStages) {
+                    s = 0;
+                    ++phase;
+                }
+            }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
         for (int pg0 = it.page_begin; pg0 < it.page_end && ok; pg0 += 32) {
             const int n = min(32, it.page_end - pg0);  // a multiple of 4 unless it ends the item
             int page = 0;
@@ -364,21 +393,31 @@ __device__ __forceinline__ void kr_convert(const CUtensorMap* tm_kr, const Param
     for (int i = item_begin; i < item_end; ++i) {
         const Item it = load_item(p.plan, items_off, i);
         const int32_t* bt = p.block_table + (int64_t)it.table_row * p.max_pages;
-        // largest scale over the item's tokens: lane k takes pages k, k + 32, ...
+        // largest scale over the item's tokens: lane k takes pages k, k + 32, ...; a page's
+        // sixteen scale loads are in flight together, and the next page id is loaded before them,
+        // so each page costs one memory round trip
+        const auto page_at = [&](int pg) {
+            return (pg < it.page_end && pg < p.max_pages) ? __ldg(bt + pg) : -1;
+        };
         float smax = 0.f;
+        int page = page_at(it.page_begin + lane);
         for (int pg = it.page_begin + lane; pg < it.page_end; pg += 32) {
-            const int page = pg < p.max_pages ? __ldg(bt + pg) : -1;
-            if (page < 0 || page >= p.num_pool_pages) continue;  // reported by the producers
-            const int valid = min(64, it.seq_len - 64 * pg);
-            const float4* sc = reinterpret_cast<const float4*>(p.kv_scale + (int64_t)page * 64);
-#pragma unroll 4
-            for (int v = 0; v < 16; ++v) {
-                const float4 x = __ldg(sc + v);
-                if (4 * v + 0 < valid) smax = fmaxf(smax, x.x);
-                if (4 * v + 1 < valid) smax = fmaxf(smax, x.y);
-                if (4 * v + 2 < valid) smax = fmaxf(smax, x.z);
-                if (4 * v + 3 < valid) smax = fmaxf(smax, x.w);
+            const int next = page_at(pg + 32);
+            if (page >= 0 && page < p.num_pool_pages) {  // a bad id is reported by the producers
+                const int valid = min(64, it.seq_len - 64 * pg);
+                const float4* sc = reinterpret_cast<const float4*>(p.kv_scale + (int64_t)page * 64);
+                float4 x[16];
+#pragma unroll
+                for (int v = 0; v < 16; ++v) x[v] = __ldg(sc + v);
+#pragma unroll
+                for (int v = 0; v < 16; ++v) {
+                    if (4 * v + 0 < valid) smax = fmaxf(smax, x[v].x);
+                    if (4 * v + 1 < valid) smax = fmaxf(smax, x[v].y);
+                    if (4 * v + 2 < valid) smax = fmaxf(smax, x[v].z);
+                    if (4 * v + 3 < valid) smax = fmaxf(smax, x[v].w);
+                }
             }
+            page = next;
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
@@ -483,6 +522,28 @@ __device__ __forceinline__ void score_mma(const Params& p, int item_begin, int i
     int s = 0, phase = 0, G = 0, n_item = 0;
     for (int i = item_begin; i < item_end; ++i, ++n_item) {
         const Item it = load_item(p.plan, items_off, i);
+        // The item's bf16 query rows into the score columns (free once the softmax has read the
+        // previous item's last scores): dims 64 k .. 64 k + 63 -> columns 32 k .. 32 k + 31 of lane
+        // h for head h; the softmax warps turn them into the e4m3 pair (q_ready).
+        if (n_item > 0 && !wait_phase_ool(bars + 8 * kSFree0, G - 1, w)) goto out;
+#pragma unroll 1
+        for (int j = 0; j < kQueryEntries; ++j) {
+            if (!wait_phase_ool(full0 + 8 * s, phase, w)) goto out;
+            tc_fence_after();
+            const uint64_t src = smem_desc(sbase + kOffChunks + s * kChunkBytes, 16, 1024);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4)
+                    tmem_cp_128x256b(d + 64 * j + 32 * h + 8 * k4,
+                                     src + (uint64_t)(h * ((kChunkBytes / 2) >> 4) + 2 * k4));
+            mma_commit(empty0 + 8 * s);
+            if (++s == kChunkStages) {
+                s = 0;
+                ++phase;
+            }
+        }
+        mma_commit(bars + 8 * kQRaw);
         if (!wait_phase_ool(bars + 8 * kQReady, n_item, w)) goto out;
         tc_fence_after();
         for (int pg = it.page_begin; pg < it.page_end; pg += kGroupPages, ++G) {
@@ -528,48 +589,62 @@ out:
     drain_phase(bars + 8 * kDrain, 0, w.timeout_ns);
 }
 
-// The query of row `row` (both softmax sets of the row compute the same 2^e): the row's largest
-// magnitude sets e (bf16 magnitudes order as their 15-bit patterns); set k converts q_abs dims
-// 256k..256k+255, times 2^e, into the e4m3 pair and writes it to TMEM columns 64k.. of q_hi and
-// of q_lo in lane `row`; set 0 writes q_R 2^e (exact) to row `row` of the K-major,
-// 128-byte-swizzled q_R tile.  Returns 2^-e.
-__device__ __noinline__ float load_query(const Params& p, int seq, int row, int set, uint32_t taddr,
-                                        uint8_t* qr_smem)
+// The query of row `row`: the MMA thread has copied the item's bf16 q_abs rows into the score
+// columns (column k of lane h: dims 2k, 2k + 1 of head h; commit on q_raw).  Set k reads its
+// dims 256k..256k+255 (columns 128k..128k+127) twice: once for the largest magnitude, which the
+// sets agree on through `mx_xchg` (one word per row and set) and which sets e (bf16 magnitudes
+// order as their 15-bit patterns), and once to convert them, times 2^e, into the e4m3 pair in
+// TMEM columns 64k.. of q_hi and of q_lo.  Set 0 writes q_R 2^e (exact) to row `row` of the
+// K-major, 128-byte-swizzled q_R tile.  *r_h = 2^-e.  Both sets reach the barrier, so a failed
+// wait makes both return false.
+__device__ __noinline__ bool load_query(const Params& p, int seq, int row, int set, int n_item, uint32_t bars,
+                                        uint32_t taddr, uint8_t* qr_smem, uint32_t* mx_xchg, const dev::WaitCtx& w,
+                                        float* r_h)
 {
     using namespace dev;
-    const uint4* qrow = reinterpret_cast<const uint4*>(p.q_abs + ((int64_t)seq * 128 + row) * 512);
-    uint32_t mx = 0;
-#pragma unroll 4
-    for (int v = 0; v < 64; ++v) {
-        const uint4 x = __ldg(qrow + v);
-        const uint32_t a = max(max(x.x & 0x7FFFu, (x.x >> 16) & 0x7FFFu), max(x.y & 0x7FFFu, (x.y >> 16) & 0x7FFFu));
-        const uint32_t b = max(max(x.z & 0x7FFFu, (x.z >> 16) & 0x7FFFu), max(x.w & 0x7FFFu, (x.w >> 16) & 0x7FFFu));
-        mx = max(mx, max(a, b));
+    const uint32_t raw = taddr + kSCol + 128 * set;
+    uint4 qrv[8];  // set 0: q_R of the row, loaded while the query copies land
+    if (set == 0) {
+        const uint4* qr = reinterpret_cast<const uint4*>(p.q_r + ((int64_t)seq * 128 + row) * 64);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) qrv[v] = __ldg(qr + v);
     }
+    const bool ok = wait_warp_ool(bars + 8 * kQRaw, n_item, w);
+    uint32_t mx = 0;
+    if (ok) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int j = 0; j < 4; ++j) {
+            uint32_t r[32];
+            tmem_ld32(raw + 32 * j, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) mx = max(mx, max(r[k] & 0x7FFFu, (r[k] >> 16) & 0x7FFFu));
+        }
+    }
+    mx_xchg[set * 128 + row] = mx;
+    if (named_barrier_or(kSoftmaxBarrier, 256, !ok || *w.abort)) return false;
+    mx = max(mx_xchg[row], mx_xchg[128 + row]);
     // max |q| in [2^E, 2^(E+1)) with E = exponent field - 127; 2^(7-E) maps it into [128, 256)
     const int e = (mx == 0) ? 0 : max(-64, min(64, 7 - ((int)(mx >> 7) - 127)));
     const float sc = exp2i(e);
-    const uint4* qa = qrow + 32 * set;
 #pragma unroll 1
-    for (int c2 = 0; c2 < 2; ++c2) {  // 128 dims -> 32 TMEM columns of q_hi and of q_lo
-        uint32_t hi[32], lo[32];
+    for (int j = 0; j < 4; ++j) {  // 64 dims -> 16 TMEM columns of q_hi and of q_lo
+        uint32_t r[32], hi[16], lo[16];
+        tmem_ld32(raw + 32 * j, r);
+        tmem_wait_ld();
 #pragma unroll
-        for (int v = 0; v < 16; ++v) {
-            const uint4 x = __ldg(qa + 16 * c2 + v);
-            split_e4m3x4(bf16_lo(x.x) * sc, bf16_hi(x.x) * sc, bf16_lo(x.y) * sc, bf16_hi(x.y) * sc, hi[2 * v],
-                         lo[2 * v]);
-            split_e4m3x4(bf16_lo(x.z) * sc, bf16_hi(x.z) * sc, bf16_lo(x.w) * sc, bf16_hi(x.w) * sc, hi[2 * v + 1],
-                         lo[2 * v + 1]);
-        }
-        tmem_st32(taddr + kQHiCol + 64 * set + 32 * c2, hi);
-        tmem_st32(taddr + kQLoCol + 64 * set + 32 * c2, lo);
+        for (int v = 0; v < 16; ++v)
+            split_e4m3x4(bf16_lo(r[2 * v]) * sc, bf16_hi(r[2 * v]) * sc, bf16_lo(r[2 * v + 1]) * sc,
+                         bf16_hi(r[2 * v + 1]) * sc, hi[v], lo[v]);
+        tmem_st16(taddr + kQHiCol + 64 * set + 16 * j, hi);
+        tmem_st16(taddr + kQLoCol + 64 * set + 16 * j, lo);
     }
     if (set == 0) {
-        const uint4* qr = reinterpret_cast<const uint4*>(p.q_r + ((int64_t)seq * 128 + row) * 64);
         uint8_t* dst = qr_smem + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
-            uint4 x = __ldg(qr + v);
+            uint4 x = qrv[v];
             x.x = pack_bf16x2(bf16_lo(x.x) * sc, bf16_hi(x.x) * sc);
             x.y = pack_bf16x2(bf16_lo(x.y) * sc, bf16_hi(x.y) * sc);
             x.z = pack_bf16x2(bf16_lo(x.z) * sc, bf16_hi(x.z) * sc);
@@ -579,7 +654,8 @@ __device__ __noinline__ float load_query(const Params& p, int seq, int row, int 
         fence_proxy_async_cta();  // read by the MMA (async proxy)
     }
     tmem_wait_st();
-    return exp2i(-e);
+    *r_h = exp2i(-e);
+    return true;
 }
 
 // Row max of one page of raw scores in registers, in log2 units before the row factor:
@@ -710,11 +786,17 @@ __device__ __forceinline__ void score_softmax(const Params& p, int item_begin, i
     const uint32_t* freed = reinterpret_cast<const uint32_t*>(smem + kOffStgFreed);
     const uint32_t* sig_ready = reinterpret_cast<const uint32_t*>(smem + kOffSigReady);
     float* xchg = reinterpret_cast<float*>(smem + kOffXchg);  // [slot 2][kind 2: max, l][set 2][128]
-    griddep_wait();  // q_abs comes from the kernel launched before this one
     int g = 0, G = 0;  // pages (messages) and four-page groups
-    for (int i = item_begin; i < item_end; ++i) {
+    for (int i = item_begin, n_item = 0; i < item_end; ++i, ++n_item) {
         const Item it = load_item(p.plan, items_off, i);
-        const float r_h = load_query(p, it.seq, row, set, tmem + lane_off, smem + kOffQR);
+        // The exchange slot of the query maxima: the group-max slot that the next group does not
+        // use.  Group G - 1 (the previous item's last group, which also ran the l barrier) read it
+        // before every softmax thread passed that barrier; group G + 1 writes it only after the
+        // first barrier of group G, behind every thread's read here.  (Every item has a page.)
+        float r_h;
+        if (!load_query(p, it.seq, row, set, n_item, bars, tmem + lane_off, smem + kOffQR,
+                        reinterpret_cast<uint32_t*>(xchg + ((G + 1) & 1) * 2 * 2 * 128), w, &r_h))
+            return;
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bars + 8 * kQReady);
@@ -730,9 +812,10 @@ __device__ __forceinline__ void score_softmax(const Params& p, int item_begin, i
             bool ok = wait_warp_ool(bars + 8 * kSFull0, G, w);
             if (lane == 0 && warp == 2) MLA_EV(4, G);
             // One page of scores in registers at a time (a second one would spill into local
-            // memory, which the shared-memory carve-out leaves little L1 for): the first page
-            // stays, the second is read once for its max and again after the first page's P,
-            // and the score buffer is freed after that second read.
+            // memory, which the shared-memory carve-out leaves little L1 for): the second page is
+            // read first, for its max only, then the first page, which stays; the second is read
+            // again after the first page's P, and the score buffer is freed after that read.
+            // (One loop body reads both pages: the code stays small in the instruction cache.)
             uint32_t sr[64];
             const uint32_t scol = tmem + lane_off + kSCol + 128 * set;
             const int t0 = pg + 2 * set;
@@ -741,17 +824,12 @@ __device__ __forceinline__ void score_softmax(const Params& p, int item_begin, i
             if (ok) ok = wait_freed(sig_ready, (uint32_t)(G + 1), w);  // this group's token factors
             if (ok) {
                 tc_fence_after();
-                if (n_mine > 1) {  // the second page: max only
-                    tmem_ld32(scol + 64, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-                    tmem_ld32(scol + 96, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+#pragma unroll 1
+                for (int j = n_mine - 1; j >= 0; --j) {
+                    tmem_ld32(scol + 64 * j, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+                    tmem_ld32(scol + 64 * j + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
                     tmem_wait_ld();
-                    mx = page_scale_max(sr, sig + 64 * (2 * set + 1), valid1);
-                }
-                if (n_mine > 0) {
-                    tmem_ld32(scol, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-                    tmem_ld32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-                    tmem_wait_ld();
-                    mx = fmaxf(mx, page_scale_max(sr, sig + 64 * (2 * set), valid0));
+                    mx = fmaxf(mx, page_scale_max(sr, sig + 64 * (2 * set + j), j ? valid1 : valid0));
                 }
                 if (n_mine < 2) {  // nothing left to read: the next group's QK may start
                     tc_fence_before();
@@ -1048,7 +1126,7 @@ done:
 // 12 warps: each SM sub-partition holds three, and its 16K registers allow 3 x 32 x 168.
 __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
 decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_c8, const __grid_constant__ CUtensorMap tm_kr,
-                  const Params p)
+                  const __grid_constant__ CUtensorMap tm_q, const Params p)
 {
     using namespace dev;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -1079,6 +1157,7 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_c8, const __grid_consta
             mbar_init(bars + 8 * (kCopied0 + b), 1);       // the message landed in the value CTA
         }
         mbar_init(bars + 8 * kQReady, 8);                  // one arrive per softmax warp
+        mbar_init(bars + 8 * kQRaw, 1);                    // the MMA thread's commit after the query copies
         for (int s = 0; s < kStagingSlots; ++s) mbar_init(bars + 8 * (kStgReady0 + s), 4);  // one set's warps
         mbar_init(bars + 8 * kKrLanded, 1);
         mbar_init(bars + 8 * kKrFull, 1);   // warp 11: the group's k_R / sigma is in place
@@ -1113,7 +1192,7 @@ decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_c8, const __grid_consta
         const int item_end = cluster < n_clusters ? p.plan[cl_off + cluster + 1] : 0;
         if (rank == 0) {
             if (warp == 0)
-                score_producer(&tm_c8, p, item_begin, item_end, items_off, sbase, bars, w, lane);
+                score_producer(&tm_c8, &tm_q, p, item_begin, item_end, items_off, sbase, bars, w, lane);
             else if (warp == 1) {
                 if (lane == 0) score_mma(p, item_begin, item_end, items_off, sbase, bars, tmem, w);
             } else if (warp >= 2 && warp < 10)
