@@ -8,12 +8,16 @@
 // Scores.  s[h,t] = scale * (q_abs[h] . c_t + q_R[h] . k_R[t])
 //                 = scale * sigma_t * 2^-e_h * (q~[h] . c8_t + q_R[h] 2^e_h . k_R[t] / sigma_t)
 // where q~[h] = q_abs[h] * 2^e_h, the power of two 2^e_h putting row h's largest magnitude in
-// [128, 256).  q~ is held as a pair of e4m3 matrices q_hi = e4m3(q~), q_lo = e4m3(q~ - q_hi),
-// exact to about 2^-8 relative wherever |q~| >= 1/4; QK runs one e4m3 MMA for each, which at
+// [128, 256).  q~ is held as a pair of e4m3 matrices q_hi = e4m3(q~), q_lo = e4m3(q~ - q_hi).
+// A bf16 value has eight significant bits; rounding it to four leaves a residual that is a
+// multiple of its last bit and at most eight of them, which four bits hold, so q_hi + q_lo = q~
+// exactly wherever |q~| >= 1/4 (below, within 2^-10); QK runs one e4m3 MMA for each, which at
 // twice the bf16 rate costs the tensor time of one bf16 MMA.  A converter warp divides each
 // page's k_R rows by sigma_t in shared memory (bf16x2 fused multiply-adds by a two-part 1/sigma,
-// one rounding), so that the RoPE MMA
-// (bf16, q_R 2^e_h) accumulates into the same fp32 scores; the softmax then scales column t
+// one rounding), so that the RoPE MMA (bf16, q_R 2^e_h) accumulates into the same fp32 scores.
+// That rounding, 2^-9 relative per element, is the path's main score noise (a power-of-two
+// sigma_t makes it exact; a second bf16 part would need 32 KB of shared memory or 256 TMEM
+// columns that the layout below does not have).  The softmax then scales column t
 // by sigma_t and row h by 2^-e_h.
 //
 // Output.  o[h] = sum_t p[h,t] sigma_t c8_t / l[h].  The PV operand is P~ = p * sigma_t * g,
