@@ -29,7 +29,7 @@ def _sync_err(step_or_err):
 
 # ------------------------------------------------------------------------------------ absorb
 
-@pytest.mark.parametrize("batch", [1, 16, 128, 130])
+@pytest.mark.parametrize("batch", [1, 16, 17, 128, 130, 256, 257])
 def test_absorb_q(batch):
     inp = synth.make_inputs([1] * batch, seed=100 + batch)
     q_abs = torch.empty(batch, 128, 512, dtype=torch.bfloat16, device=DEV)
@@ -41,7 +41,7 @@ def test_absorb_q(batch):
 
 # ------------------------------------------------------------------------------------ out-proj
 
-@pytest.mark.parametrize("batch", [1, 16, 129])
+@pytest.mark.parametrize("batch", [1, 16, 33, 129, 256, 300])
 def test_out_proj(batch):
     inp = synth.make_inputs([1] * batch, seed=200 + batch)
     g = torch.Generator().manual_seed(batch)
