@@ -141,3 +141,28 @@ def test_recorded_traffic_only_for_the_current_source(tmp_path, monkeypatch):
     rec["kernel_hash"] = "0" * 16  # taken on another version of the kernel
     path.write_text(json.dumps([rec]))
     assert bench.recorded_traffic("decode_bf16_kernel", "b16_s65536", 1000) is None
+
+
+def test_recorded_traffic_close_to_algorithmic_bytes():
+    """Structural self-check on the committed ncu records: each decode kernel's measured DRAM
+    traffic for one launch is within 5 % of the bytes the algorithm must move (every cached token
+    once, the queries in, the latent outputs out): nothing is read twice."""
+    import json
+
+    import bench
+
+    class Fake:
+        def __init__(self, kv_dtype, lens):
+            self.kv_dtype, self.seq_lens, self.queries_per_seq = kv_dtype, np.asarray(lens, np.int32), 1
+            self.batch, self.num_tokens, self.rows = len(lens), int(sum(lens)), len(lens)
+
+    shapes = {"b16_s65536": ("bf16", [65536] * 16), "b128_s8192_fp8": ("fp8_e4m3", [8192] * 128)}
+    with open(bench.TRAFFIC_PATH) as f:
+        records = json.load(f)
+    assert {r["workload"] for r in records} == set(shapes)
+    for r in records:
+        dtype, lens = shapes[r["workload"]]
+        algorithmic = bench.workload_accounting(Fake(dtype, lens))["decode_bytes"]
+        ratio = r["dram_bytes_per_launch"] / algorithmic
+        assert 0.95 <= ratio <= 1.05, (r["kernel"], ratio)
+        assert r["dram_bytes_per_launch"] == r["dram_bytes_read"] + r["dram_bytes_write"]
