@@ -166,3 +166,22 @@ def test_recorded_traffic_close_to_algorithmic_bytes():
         ratio = r["dram_bytes_per_launch"] / algorithmic
         assert 0.95 <= ratio <= 1.05, (r["kernel"], ratio)
         assert r["dram_bytes_per_launch"] == r["dram_bytes_read"] + r["dram_bytes_write"]
+
+
+def test_reference_arm_under_torchrun_two_ranks():
+    """The reference arm launched the way the driver launches N > 1 (torchrun, two ranks on this
+    host): rank 0 alone times the oracle and prints one JSON line, the other rank exits 0 without
+    work."""
+    import json
+    import subprocess
+
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2", "--master-addr",
+           "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus",
+           "2", "--steps", "1", "--warmup", "3", "--workload", "b1_s2048"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout[-2000:]
+    res = json.loads(lines[0])
+    assert res["impl"] == "reference" and res["n_gpus"] == 2 and res["value"] > 0
