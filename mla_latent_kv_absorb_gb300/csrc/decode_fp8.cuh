@@ -461,10 +461,13 @@ __device__ __forceinline__ void kr_convert(const CUtensorMap* tm_kr, const Param
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const int t = lane + 32 * k, q = k >> 1;
-                const bool valid = q < npg && pages[q] >= 0 && 64 * (pg + q) + (t & 63) < it.seq_len;
+                const bool in_seq = q < npg && 64 * (pg + q) + (t & 63) < it.seq_len;
+                const bool valid = in_seq && pages[q] >= 0;
                 // a zero scale (a zero latent row) enters the score side as 2^-64, so that k_R /
-                // sigma stays finite and sigma (q . c8 + q_R . k_R / sigma) is still q_R . k_R
-                sig[t] = valid ? fmaxf(sigma[k], 5.421011e-20f) * p.scale_log2 : 0.f;
+                // sigma stays finite and sigma (q . c8 + q_R . k_R / sigma) is still q_R . k_R;
+                // a slot past the sequence end gets NaN, which the softmax's maximum skips
+                // (fmaxf returns the other operand), so the maximum needs no mask
+                sig[t] = valid ? fmaxf(sigma[k], 5.421011e-20f) * p.scale_log2 : (in_seq ? 0.f : __int_as_float(0x7fc00000));
                 sig[256 + t] = valid ? sigma[k] * g : 0.f;
             }
             if (lane == 0) sig[512] = g;
@@ -664,18 +667,19 @@ __device__ __noinline__ bool load_query(const Params& p, int seq, int row, int s
 
 // Row max of one page of raw scores in registers, in log2 units before the row factor:
 // max_t S[t] * sig_s[t] (sig_s = sigma_t * scale * log2(e)) over the slots before the sequence
-// end (the raw score past it may be NaN).  The scores stay untouched in their registers.
-__device__ __forceinline__ float page_scale_max(const uint32_t (&sr)[64], const float* sig_s, int valid)
+// end: past it sig_s is NaN, so the product is NaN whatever the raw score, and fmaxf skips it.
+// The scores stay untouched in their registers.
+__device__ __forceinline__ float page_scale_max(const uint32_t (&sr)[64], const float* sig_s)
 {
     float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
     for (int v = 0; v < 16; ++v) {
         const float4 f = *reinterpret_cast<const float4*>(sig_s + 4 * v);
         const int j = 4 * v;
-        m4[0] = fmaxf(m4[0], j + 0 < valid ? __uint_as_float(sr[j + 0]) * f.x : -INFINITY);
-        m4[1] = fmaxf(m4[1], j + 1 < valid ? __uint_as_float(sr[j + 1]) * f.y : -INFINITY);
-        m4[2] = fmaxf(m4[2], j + 2 < valid ? __uint_as_float(sr[j + 2]) * f.z : -INFINITY);
-        m4[3] = fmaxf(m4[3], j + 3 < valid ? __uint_as_float(sr[j + 3]) * f.w : -INFINITY);
+        m4[0] = fmaxf(m4[0], __uint_as_float(sr[j + 0]) * f.x);
+        m4[1] = fmaxf(m4[1], __uint_as_float(sr[j + 1]) * f.y);
+        m4[2] = fmaxf(m4[2], __uint_as_float(sr[j + 2]) * f.z);
+        m4[3] = fmaxf(m4[3], __uint_as_float(sr[j + 3]) * f.w);
     }
     return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
 }
@@ -684,8 +688,8 @@ __device__ __forceinline__ float page_scale_max(const uint32_t (&sr)[64], const 
 // into this thread's row of the swizzled staging tile (16-byte chunk c of the row goes to chunk
 // c ^ (row & 7)), the layout of the bf16 kernel.  The value CTA scales it by sigma_t g and
 // splits it into the e4m3 pair.  Returns the row sum of p.
-__device__ __forceinline__ float page_softmax(const uint32_t (&sr)[64], const float* sig_s, int valid, float r_h,
-                                              float m_used, uint8_t* stage_row, int row)
+__device__ __forceinline__ float page_softmax(const uint32_t (&sr)[64], const float* sig_s, float r_h, float m_used,
+                                              uint8_t* stage_row, int row)
 {
     using namespace dev;
     float l4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -698,10 +702,10 @@ __device__ __forceinline__ float page_softmax(const uint32_t (&sr)[64], const fl
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int j = 8 * c + 2 * q;
-            float p0 = ex2_approx(fmaf(__uint_as_float(sr[j]) * fs[2 * q], r_h, -m_used));
-            float p1 = ex2_approx(fmaf(__uint_as_float(sr[j + 1]) * fs[2 * q + 1], r_h, -m_used));
-            p0 = j < valid ? p0 : 0.f;
-            p1 = j + 1 < valid ? p1 : 0.f;
+            // past the sequence end sig_s is NaN: fmaxf(NaN, -inf) = -inf and 2^-inf = 0
+            const float p0 = ex2_approx(fmaxf(fmaf(__uint_as_float(sr[j]) * fs[2 * q], r_h, -m_used), -INFINITY));
+            const float p1 =
+                ex2_approx(fmaxf(fmaf(__uint_as_float(sr[j + 1]) * fs[2 * q + 1], r_h, -m_used), -INFINITY));
             pk[q] = pack_bf16x2(p0, p1);
             l4[(2 * q) & 3] += p0;
             l4[(2 * q + 1) & 3] += p1;
@@ -833,7 +837,7 @@ __device__ __forceinline__ void score_softmax(const Params& p, int item_begin, i
                     tmem_ld32(scol + 64 * j, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
                     tmem_ld32(scol + 64 * j + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
                     tmem_wait_ld();
-                    mx = fmaxf(mx, page_scale_max(sr, sig + 64 * (2 * set + j), j ? valid1 : valid0));
+                    mx = fmaxf(mx, page_scale_max(sr, sig + 64 * (2 * set + j)));
                 }
                 if (n_mine < 2) {  // nothing left to read: the next group's QK may start
                     tc_fence_before();
@@ -874,7 +878,7 @@ __device__ __forceinline__ void score_softmax(const Params& p, int item_begin, i
                 const int slot = gg % kStagingSlots;
                 if (gg >= kStagingSlots) ok = wait_freed(freed, (uint32_t)(gg - kStagingSlots + 1), w);
                 if (!ok) break;
-                l_mine += page_softmax(sr, sig + 64 * (2 * set + j), j ? valid1 : valid0, r_h, m_used,
+                l_mine += page_softmax(sr, sig + 64 * (2 * set + j), r_h, m_used,
                                        smem + kOffScoreStaging + slot * kPBytes + p_row_off, row);
                 const float f_page = (set == 0 && j == 0) ? factor : 1.f;  // O rescale precedes page 0
                 if (t0 + j == it.page_end - 1)
