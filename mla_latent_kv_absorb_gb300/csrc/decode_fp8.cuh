@@ -665,47 +665,49 @@ __device__ __noinline__ bool load_query(const Params& p, int seq, int row, int s
     return true;
 }
 
-// Row max of one page of raw scores in registers, in log2 units before the row factor:
-// max_t S[t] * sig_s[t] (sig_s = sigma_t * scale * log2(e)) over the slots before the sequence
-// end: past it sig_s is NaN, so the product is NaN whatever the raw score, and fmaxf skips it.
-// The scores stay untouched in their registers.
-__device__ __forceinline__ float page_scale_max(const uint32_t (&sr)[64], const float* sig_s)
+// Scales one page of raw scores in registers in place, y[t] = S[t] * sig_s[t] (sig_s = sigma_t *
+// scale * log2(e): log2 units before the row factor), and returns their row max over the slots
+// before the sequence end: past it sig_s is NaN, so y is NaN whatever the raw score, and fmaxf
+// skips it.
+__device__ __forceinline__ float page_scale_max(uint32_t (&sr)[64], const float* sig_s)
 {
     float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
     for (int v = 0; v < 16; ++v) {
         const float4 f = *reinterpret_cast<const float4*>(sig_s + 4 * v);
         const int j = 4 * v;
-        m4[0] = fmaxf(m4[0], __uint_as_float(sr[j + 0]) * f.x);
-        m4[1] = fmaxf(m4[1], __uint_as_float(sr[j + 1]) * f.y);
-        m4[2] = fmaxf(m4[2], __uint_as_float(sr[j + 2]) * f.z);
-        m4[3] = fmaxf(m4[3], __uint_as_float(sr[j + 3]) * f.w);
+        const float y0 = __uint_as_float(sr[j + 0]) * f.x, y1 = __uint_as_float(sr[j + 1]) * f.y;
+        const float y2 = __uint_as_float(sr[j + 2]) * f.z, y3 = __uint_as_float(sr[j + 3]) * f.w;
+        sr[j + 0] = __float_as_uint(y0);
+        sr[j + 1] = __float_as_uint(y1);
+        sr[j + 2] = __float_as_uint(y2);
+        sr[j + 3] = __float_as_uint(y3);
+        m4[0] = fmaxf(m4[0], y0);
+        m4[1] = fmaxf(m4[1], y1);
+        m4[2] = fmaxf(m4[2], y2);
+        m4[3] = fmaxf(m4[3], y3);
     }
     return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
 }
 
-// Softmax of one page: p = 2^(S sig_s[t] 2^-e - m) (0 past the sequence end), written as bf16
-// into this thread's row of the swizzled staging tile (16-byte chunk c of the row goes to chunk
-// c ^ (row & 7)), the layout of the bf16 kernel.  The value CTA scales it by sigma_t g and
-// splits it into the e4m3 pair.  Returns the row sum of p.
-__device__ __forceinline__ float page_softmax(const uint32_t (&sr)[64], const float* sig_s, float r_h, float m_used,
-                                              uint8_t* stage_row, int row)
+// Softmax of one page scaled by page_scale_max: p = 2^(y[t] 2^-e - m) (0 past the sequence end),
+// written as bf16 into this thread's row of the swizzled staging tile (16-byte chunk c of the row
+// goes to chunk c ^ (row & 7)), the layout of the bf16 kernel.  The value CTA scales it by
+// sigma_t g and splits it into the e4m3 pair.  Returns the row sum of p.
+__device__ __forceinline__ float page_softmax(const uint32_t (&sr)[64], float r_h, float m_used, uint8_t* stage_row,
+                                              int row)
 {
     using namespace dev;
     float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-        const float4 f0 = *reinterpret_cast<const float4*>(sig_s + 8 * c);
-        const float4 f1 = *reinterpret_cast<const float4*>(sig_s + 8 * c + 4);
-        const float fs[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
         uint32_t pk[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int j = 8 * c + 2 * q;
-            // past the sequence end sig_s is NaN: fmaxf(NaN, -inf) = -inf and 2^-inf = 0
-            const float p0 = ex2_approx(fmaxf(fmaf(__uint_as_float(sr[j]) * fs[2 * q], r_h, -m_used), -INFINITY));
-            const float p1 =
-                ex2_approx(fmaxf(fmaf(__uint_as_float(sr[j + 1]) * fs[2 * q + 1], r_h, -m_used), -INFINITY));
+            // past the sequence end y is NaN: fmaxf(NaN, -inf) = -inf and 2^-inf = 0
+            const float p0 = ex2_approx(fmaxf(fmaf(__uint_as_float(sr[j]), r_h, -m_used), -INFINITY));
+            const float p1 = ex2_approx(fmaxf(fmaf(__uint_as_float(sr[j + 1]), r_h, -m_used), -INFINITY));
             pk[q] = pack_bf16x2(p0, p1);
             l4[(2 * q) & 3] += p0;
             l4[(2 * q + 1) & 3] += p1;
@@ -873,13 +875,13 @@ __device__ __forceinline__ void score_softmax(const Params& p, int item_begin, i
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bars + 8 * kSFree0);
+                    page_scale_max(sr, sig + 64 * (2 * set + 1));  // scaled again (its max is known)
                 }
                 const int gg = g + 2 * set + j;
                 const int slot = gg % kStagingSlots;
                 if (gg >= kStagingSlots) ok = wait_freed(freed, (uint32_t)(gg - kStagingSlots + 1), w);
                 if (!ok) break;
-                l_mine += page_softmax(sr, sig + 64 * (2 * set + j), r_h, m_used,
-                                       smem + kOffScoreStaging + slot * kPBytes + p_row_off, row);
+                l_mine += page_softmax(sr, r_h, m_used, smem + kOffScoreStaging + slot * kPBytes + p_row_off, row);
                 const float f_page = (set == 0 && j == 0) ? factor : 1.f;  // O rescale precedes page 0
                 if (t0 + j == it.page_end - 1)
                     hold_last = true;
