@@ -566,19 +566,26 @@ __device__ __forceinline__ void load_query_rope(const Params& p, int seq, int ro
     fence_proxy_async_cta();  // read by the MMA (async proxy)
 }
 
-// Softmax of one page held in registers: masks slots past the sequence end, p = 2^(s * scale *
-// log2(e) - m) (one FMA and one MUFU.EX2 per score), and writes P as bf16 straight into this
-// thread's row of the swizzled staging tile (16-byte chunk c of the row goes to chunk c ^ (row
-// & 7)).  Returns the row sum of p.
-__device__ __forceinline__ float page_softmax(uint32_t (&sr)[64], int valid, float scale_log2, float m_used,
-                                              uint8_t* stage_row, int row)
+// Slots past the sequence end read as -infinity (the raw score there may be anything, NaN
+// included): then the page maximum skips them and their p is 2^-inf = 0.  Only a sequence's
+// last page has such slots.
+__device__ __forceinline__ void page_mask(uint32_t (&sr)[64], int valid)
 {
-    using namespace dev;
     if (valid < 64) {
 #pragma unroll
         for (int j = 0; j < 64; ++j)
             if (j >= valid) sr[j] = __float_as_uint(-INFINITY);
     }
+}
+
+// Softmax of one page held in registers (masked by page_mask): p = 2^(s * scale * log2(e) - m)
+// (one FMA and one MUFU.EX2 per score), and writes P as bf16 straight into this thread's row of
+// the swizzled staging tile (16-byte chunk c of the row goes to chunk c ^ (row & 7)).  Returns
+// the row sum of p.
+__device__ __forceinline__ float page_softmax(const uint32_t (&sr)[64], float scale_log2, float m_used,
+                                              uint8_t* stage_row, int row)
+{
+    using namespace dev;
     float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
@@ -597,21 +604,14 @@ __device__ __forceinline__ float page_softmax(uint32_t (&sr)[64], int valid, flo
     return ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
 }
 
-// Row max of a page's raw scores (slots past the sequence end excluded), 8-way tree.
-__device__ __forceinline__ float page_max(const uint32_t (&sr)[64], int valid)
+// Row max of a page's raw scores (masked by page_mask), 8-way tree.
+__device__ __forceinline__ float page_max(const uint32_t (&sr)[64])
 {
     float m8[8];
-    if (valid >= 64) {  // every page but a sequence's last: no masking
 #pragma unroll
-        for (int a = 0; a < 8; ++a) m8[a] = __uint_as_float(sr[a]);
+    for (int a = 0; a < 8; ++a) m8[a] = __uint_as_float(sr[a]);
 #pragma unroll
-        for (int j = 8; j < 64; ++j) m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(sr[j]));
-    } else {
-#pragma unroll
-        for (int a = 0; a < 8; ++a) m8[a] = (a < valid) ? __uint_as_float(sr[a]) : -INFINITY;
-#pragma unroll
-        for (int j = 8; j < 64; ++j) m8[j & 7] = fmaxf(m8[j & 7], (j < valid) ? __uint_as_float(sr[j]) : -INFINITY);
-    }
+    for (int j = 8; j < 64; ++j) m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(sr[j]));
     return fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
 }
 
@@ -759,8 +759,14 @@ __device__ __forceinline__ void score_softmax(const Params& p, int item_begin, i
                 if (lane == 0) mbar_arrive(bars + 8 * kSFree0);  // the next group's QK may start
                 if (lane == 0 && warp == 2) MLA_EV(5, G);
                 MLA_TRACE_ADD(14, MLA_TRACE_NOW() - tc0);
-                if (n_mine > 0) mx = page_max(sr[0], valid0);
-                if (n_mine > 1) mx = fmaxf(mx, page_max(sr[1], valid1));
+                if (n_mine > 0) {
+                    page_mask(sr[0], valid0);
+                    mx = page_max(sr[0]);
+                }
+                if (n_mine > 1) {
+                    page_mask(sr[1], valid1);
+                    mx = fmaxf(mx, page_max(sr[1]));
+                }
             }
             MLA_TRACE_ADD(11, MLA_TRACE_NOW() - tc0);
 
@@ -789,8 +795,8 @@ __device__ __forceinline__ void score_softmax(const Params& p, int item_begin, i
                     ok = MLA_TIMED(8, wait_freed(freed, (uint32_t)(gg - kStagingSlots + 1), w));
                 if (!ok) break;
                 [[maybe_unused]] const long long tw0 = MLA_TRACE_NOW();
-                l_mine += page_softmax(sr[j], j ? valid1 : valid0, p.scale_log2, m_used,
-                                       smem + kOffScoreStaging + slot * kPBytes + p_row_off, row);
+                l_mine += page_softmax(sr[j], p.scale_log2, m_used, smem + kOffScoreStaging + slot * kPBytes + p_row_off,
+                                       row);
                 const float f_page = (set == 0 && j == 0) ? factor : 1.f;  // O rescale precedes page 0
                 if (t0 + j == it.page_end - 1)
                     hold_last = true;
