@@ -785,17 +785,23 @@ __device__ __forceinline__ void score_softmax(const Params& p, int item_begin, i
             // P of my pages goes into staging slot (message % 4), free once the value CTA has
             // consumed the message four before; every page but the item's last is handed to the
             // shipper at once, the last waits for 1/l below
+            // (one loop body for both pages, the code small in the instruction cache: the second
+            // page moves into the first one's registers)
             bool hold_last = false;
-#pragma unroll
+#pragma unroll 1
             for (int j = 0; j < 2; ++j) {
                 if (j >= n_mine || !ok) break;
+                if (j == 1) {
+#pragma unroll
+                    for (int k = 0; k < 64; ++k) sr[0][k] = sr[1][k];
+                }
                 const int gg = g + 2 * set + j;
                 const int slot = gg % kStagingSlots;
                 if (gg >= kStagingSlots)
                     ok = MLA_TIMED(8, wait_freed(freed, (uint32_t)(gg - kStagingSlots + 1), w));
                 if (!ok) break;
                 [[maybe_unused]] const long long tw0 = MLA_TRACE_NOW();
-                l_mine += page_softmax(sr[j], p.scale_log2, m_used, smem + kOffScoreStaging + slot * kPBytes + p_row_off,
+                l_mine += page_softmax(sr[0], p.scale_log2, m_used, smem + kOffScoreStaging + slot * kPBytes + p_row_off,
                                        row);
                 const float f_page = (set == 0 && j == 0) ? factor : 1.f;  // O rescale precedes page 0
                 if (t0 + j == it.page_end - 1)
